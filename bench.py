@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Benchmark of one 3DGS training step (projection, binning + sort, fused
+forward/backward rasterization, compaction + VJP, deferred Adam) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config medium] [--impl gpu|reference]
+
+Prints ONE JSON line (rank 0).  The metric is Gaussian-pixel evaluations per
+second (forward evaluations up to each pixel's stop, plus backward evaluations
+up to each pixel's last composited entry) over the whole step, with the fused
+raster kernel's own time, its roofline fraction, the end-to-end number through
+the public API from pinned host memory, and the CPU oracle timed on a bounded
+sample.  Under torchrun (N > 1) every rank trains its own replica of the
+workload (the step has no cross-GPU exchange on one node here); the value is
+the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "fused raster fwd+bwd Gaussian-pixel evals/s and ms/iter at 1 GB300; % of roofline"
+UNIT = "Gaussian-pixel evals/s"
+
+WORKLOADS = {
+    "tiny": "tiny: 1,000 Gaussians, RGB, one 64x64 view",
+    "small": "small: 100,000 Gaussians, RGB, one 1280x720 view",
+    "medium": "medium: 1,000,000 Gaussians in 64 clusters, SH degree 3, one 1920x1080 view, fx=fy=1400",
+    "large": "large: 11,200,000 Gaussians, SH degree 3, one 4096x2160 view, fx=fy=3000",
+    "batched": "batched: 20,000,000 Gaussians, SH degree 3, 16 views 1920x1080, gradients summed",
+}
+
+# Algorithmic FP32 work of the fused raster kernel, in flops (fma = 2), per unit:
+#   forward, every evaluated entry: d = p - mean (2), power (8), portable exp (21: scale 1,
+#     reduction 2 fma, Horner 7 fma, 2^k scaling 2), alpha = o * G (1)         -> 32
+#   forward, every composited entry: T(1-alpha) (2), alpha T (1), colour += c w (6) -> 9
+#   backward, every entry up to the pixel's last: power + exp + alpha again     -> 32
+#   backward, every composited entry: 1-alpha, reciprocal, T_i, w (4), dL/dc (3),
+#     <g,c> and <g,S> (10), dL/dalpha (3), S += c w (6), dL/do, dL/dpower (2),
+#     dL/dconic (7), dL/dmean2d (6)                                             -> 41
+FLOPS_FWD_EVAL, FLOPS_FWD_COMP, FLOPS_BWD_EVAL, FLOPS_BWD_COMP = 32, 9, 32, 41
+# The same work with exp counted as one special-function op (and the reciprocal as one):
+FLOPS_FWD_EVAL_SFU, FLOPS_BWD_EVAL_SFU, FLOPS_BWD_COMP_SFU = 11, 11, 39
+SMS, FP32_LANES, SFU_LANES = 152, 128, 16
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "measured"
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+    except OSError:
+        mp, src = {}, "fallback"
+    mhz = float(mp.get("sm_max_mhz", 2070.0))
+    return dict(src=src, sm_max_mhz=mhz, hbm_gbs=float(mp.get("hbm_gbs", 6800.0)),
+                fp32_tflops=SMS * FP32_LANES * 2 * mhz * 1e6 / 1e12,
+                sfu_tops=SMS * SFU_LANES * mhz * 1e6 / 1e12)
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for p in ("differentiable_rasterizer_gb300/csrc/raster.cu", "differentiable_rasterizer_gb300/csrc/gs_common.cuh"):
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_from_profile():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it matches the source."""
+    path = os.path.join(ROOT, "profiles", "raster_fused_medium_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except OSError:
+        return None
+    return d.get("dram_bytes_per_launch") if d.get("source_sha256") == source_sha() else None
+
+
+# ----------------------------------------------------------------------------- clocks
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def start_clock_sampler(path, gpu_index):
+    try:
+        f = open(path, "w")
+        p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + CLOCK_QUERY, "--format=csv",
+                              "-lms", "200"], stdout=f, stderr=subprocess.DEVNULL)
+        return p, f
+    except (OSError, FileNotFoundError):
+        return None, None
+
+
+def stop_clock_sampler(handle, path):
+    p, f = handle
+    if p is None:
+        return None
+    p.terminate()
+    try:
+        p.wait(timeout=5)
+    except subprocess.TimeoutExpired:
+        p.kill()
+    f.close()
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    with open(path) as fh:
+        for line in fh:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9 or parts[0] == "index":
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) sample
+def band_camera(cam, rows):
+    """The same camera restricted to `rows` image rows around the centre (identical pixels)."""
+    from differentiable_rasterizer_gb300 import scenes
+    rows = min(rows, cam.height)
+    y0 = (cam.height - rows) // 2
+    return scenes.Camera(cam.R, cam.t, cam.fx, cam.fy, cam.cx, cam.cy - y0, cam.width, rows), y0
+
+
+def oracle_sample_step(sc, targets, rows, state, t):
+    """One oracle training step (O1..O12) on a band of `rows` rows of every view."""
+    import oracle
+    from differentiable_rasterizer_gb300 import scenes
+    cams, tg = [], []
+    for v, cam in enumerate(sc.cameras):
+        bc, y0 = band_camera(cam, rows)
+        cams.append(bc)
+        tg.append(targets[v][:, y0:y0 + bc.height, :])
+    sub = scenes.Scene(sc.name, sc.params, sc.sh_degree, cams, "given", None, None, sc.lr, sc.opts)
+    lr_rows = scenes.lr_rows(sc.lr, sc.sh_degree)
+    t0 = time.perf_counter()
+    out = oracle.train_step(sub, np.stack(tg), state, t, lr_rows, scenes.ADAM_BETAS, scenes.ADAM_EPS)
+    dt = time.perf_counter() - t0
+    ev = sum(v["render"]["e_fwd"] + v["render"]["e_bwd"] for v in out["views"])
+    return ev, dt
+
+
+def cpu_targets_band(sc, rows):
+    """Targets on the band only, rendered by the oracle from the perturbed scene."""
+    import oracle
+    if sc.target_kind == "uniform":
+        return sc.target_uniform
+    out = []
+    for cam in sc.cameras:
+        bc, y0 = band_camera(cam, rows)
+        pr = oracle.project(sc.perturbed_params, sc.sh_degree, bc, sc.opts)
+        img = oracle.render(pr, bc, sc.opts)["image"]
+        full = np.zeros((3, cam.height, cam.width), np.float32)
+        full[:, y0:y0 + bc.height] = img
+        out.append(full)
+    return np.stack(out)
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on bounded samples of the same workload."""
+    from differentiable_rasterizer_gb300 import scenes
+    import oracle
+    oracle.build()
+    sc = scenes.make_scene(args.config)
+    rows = args.ref_rows
+    targets = cpu_targets_band(sc, rows)
+    state = dict(params=sc.params.copy(), m=np.zeros_like(sc.params), v=np.zeros_like(sc.params),
+                 last_step=np.zeros(sc.n, np.int32))
+    for w in range(args.warmup):
+        oracle_sample_step(sc, targets, rows, state, w + 1)
+    ev_tot, t_tot = 0, 0.0
+    for k in range(args.steps):
+        ev, dt = oracle_sample_step(sc, targets, rows, state, args.warmup + k + 1)
+        ev_tot += ev
+        t_tot += dt
+    val = ev_tot / t_tot
+    sample = f"{rows} central image rows of every view (full projection of all Gaussians, band render, VJP, " \
+             f"compaction, deferred Adam) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded)", "config": {"workload": WORKLOADS[args.config], "sample": sample},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from differentiable_rasterizer_gb300 import build as gs_build, pipeline, scenes
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    gs_build.build()
+
+    sc = scenes.make_scene(args.config)
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda")
+    pert = torch.from_numpy(sc.perturbed_params).cuda()
+    target = tr.render(pert).clone()     # training target: render of the perturbed scene
+    del pert
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        tr.t += 1
+        if ev is not None:
+            ev[0].record(stream)
+        tr.project()
+        if ev is not None:
+            ev[1].record(stream)
+        tr.bin_sort()
+        if ev is not None:
+            ev[2].record(stream)
+        tr.raster(target)
+        if ev is not None:
+            ev[3].record(stream)
+        tr.compact()
+        if ev is not None:
+            ev[4].record(stream)
+        tr.adam(tr.t)
+        if ev is not None:
+            ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else f"/tmp/bench_clocks_r{rank}.csv"
+    sampler = start_clock_sampler(clock_path, local)
+    time.sleep(0.5)
+    tr.eval_counts.zero_()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = stop_clock_sampler(sampler, clock_path)
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in evs])
+    counts = tr.eval_counts.cpu().numpy().astype(np.float64)
+    e_fwd, e_bwd, e_comp = counts / args.steps
+    evals_per_step = e_fwd + e_bwd
+    raster_ms = float(stage_ms[:, 2].mean())
+
+    # ---- end to end through the public API: pinned host target in, loss out, every step
+    target_host = target.cpu().pin_memory()
+    loss_host = torch.empty(tr.V, dtype=torch.float64).pin_memory()
+    target_dev = torch.empty_like(target)
+    tr.eval_counts.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(args.steps):
+        tr.train_step_host(target_host, target_dev, loss_host)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_evals = float(tr.eval_counts.cpu().numpy()[:2].sum())
+
+    times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = times.tolist()
+    value = world * evals_per_step * args.steps / (total_ms / 1e3)
+    e2e_value = world * e2e_evals / (e2e_ms / 1e3)
+
+    pk = peaks()
+    flops = (e_fwd * FLOPS_FWD_EVAL + e_comp * FLOPS_FWD_COMP + e_bwd * FLOPS_BWD_EVAL + e_comp * FLOPS_BWD_COMP)
+    achieved = flops / (raster_ms / 1e3) / 1e12
+    # exp counted as one special-function op: the bound is the slower of the FP32 and SFU pipes
+    flops_a = e_fwd * FLOPS_FWD_EVAL_SFU + e_comp * FLOPS_FWD_COMP + e_bwd * FLOPS_BWD_EVAL_SFU + e_comp * FLOPS_BWD_COMP_SFU
+    sfu_ops = e_fwd + e_bwd + e_comp
+    t_bound_a = max(flops_a / (pk["fp32_tflops"] * 1e12), sfu_ops / (pk["sfu_tops"] * 1e12))
+    roofline = {"bound": "alu", "achieved": achieved, "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["fp32_tflops"], "traffic": traffic_from_profile(),
+                "kernel": "raster_fused_kernel<true>",
+                "peak_basis": f"152 SMs x 128 FP32 lanes x 2 (fma) x {pk['sm_max_mhz']:.0f} MHz (sm_max_mhz, {pk['src']})",
+                "work": "flops per launch = 32 E_fwd + 9 E_comp + 32 E_bwd + 41 E_comp (portable exp as its 21 flops)",
+                "frac_exp_as_sfu_op": t_bound_a / (raster_ms / 1e3)}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; target = render of "
+            "the scene with means perturbed by N(0, 0.01))",
+            "config": {"workload": WORKLOADS[args.config], "n_gaussians": sc.n, "views": sc.n_views,
+                       "resolution": [sc.cameras[0].width, sc.cameras[0].height], "sh_degree": sc.sh_degree,
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "l2": "inputs larger than L2: each step streams params, Adam state and grads "
+                             f"({4 * sc.params.size * 4 / 1e9:.2f} GB) through HBM"},
+            "evals_per_step": {"e_fwd": e_fwd, "e_bwd": e_bwd, "e_comp": e_comp},
+            "instances": tr.n_instances,
+            "fused_raster": {"ms": raster_ms, "evals_per_s": evals_per_step / (raster_ms / 1e3)},
+            "stage_ms": dict(zip(["project", "bin_sort", "raster_fused", "grad_compact", "adam_deferred"],
+                                 [float(x) for x in stage_ms.mean(0)])),
+            "roofline": roofline,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(target.numel() * 4),
+                    "d2h_bytes_per_step": int(tr.V * 8)},
+            "gpu_launches": int(tr.kernel_launches_per_step() * args.steps),
+            "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sc, args)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(sc, args):
+    """The oracle timed on a bounded sample (a band of rows) of the same workload, one core."""
+    rows = args.cpu_rows
+    targets = cpu_targets_band(sc, rows)
+    state = dict(params=sc.params.copy(), m=np.zeros_like(sc.params), v=np.zeros_like(sc.params),
+                 last_step=np.zeros(sc.n, np.int32))
+    ev, dt = oracle_sample_step(sc, targets, rows, state, 1)
+    return {"value": ev / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
+            "sample": f"one oracle training step on {rows} central image rows of each view "
+                      f"(all {sc.n} Gaussians projected; band render, L1, gradients, VJP, compaction, "
+                      f"deferred Adam), {int(ev)} evaluations; host has {os.cpu_count()} cores"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="medium", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=270)
+    ap.add_argument("--ref-rows", type=int, default=68)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+        return
+    run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,144 @@
+// compact.cu -- gs_grad_compact: sparse-gradient compaction ("encoder") and
+// aggregation ("decoder") for one GPU (ByteSplat, English abstract: zero partial
+// gradients eliminated; encoder/decoder kernels compact the remaining records
+// and aggregate them directly at their owner).
+//
+//   per view v: idx[v] = ascending list of Gaussians with touched[v][g] != 0
+//   union:      idx[V] = ascending list of Gaussians touched in any view
+//   decode:     for each Gaussian of the union, the projection VJP of every
+//               touching view is summed in view order in registers and added to
+//               the dense gradient with one read-modify-write; the consumed
+//               grad2d / touched entries are cleared.
+// With one owner (this GPU) no record leaves the device, so the "send" of the
+// encoded list is the list itself.
+#include "gs_common.cuh"
+#include "project_math.cuh"
+#include "scan.cuh"
+
+namespace gs {
+
+__global__ void union_kernel(const uint8_t* __restrict__ touched, int64_t n, int n_views, uint8_t* __restrict__ u)
+{
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n) return;
+    uint8_t any = 0;
+    for (int v = 0; v < n_views; ++v) any |= touched[(size_t)v * n + g];
+    u[g] = any ? 1 : 0;
+}
+
+struct VjpArgs {
+    float* grad2d;
+    uint8_t* touched;
+    const float* params;
+    int64_t n;
+    float near_z, lowpass;
+    int32_t tiles_x, tiles_y;
+    const uint32_t* idx_union;
+    const int64_t* n_union;
+    float* grads;
+};
+
+template <int DEG>
+__global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= *a.n_union) return;
+    const int64_t g = a.idx_union[i];
+    GaussParams<DEG> gp;
+    gp.load(a.params, a.n, g);
+    constexpr int P = GaussParams<DEG>::kRows;
+    float grad[P];
+#pragma unroll
+    for (int r = 0; r < P; ++r) grad[r] = 0.0f;
+    for (int v = 0; v < cs.n_views; ++v) {
+        const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
+        if (!a.touched[o]) continue;
+        ProjOut po;
+        ProjInter it;
+        if (project_one<DEG>(gp, cs.cam[v], a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, &it)) {
+            float4* src = reinterpret_cast<float4*>(a.grad2d + o * GS_GRAD2D_STRIDE);
+            const float4 x0 = src[0], x1 = src[1], x2 = src[2];
+            const float g2[9] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x};
+            vjp_one<DEG>(gp, cs.cam[v], it, po.clamp, g2, grad);
+            const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            src[0] = z; src[1] = z; src[2] = z;
+        }
+        a.touched[o] = 0;
+    }
+#pragma unroll
+    for (int r = 0; r < P; ++r) {
+        float* dst = a.grads + (size_t)r * a.n + g;
+        *dst = *dst + grad[r];
+    }
+}
+
+struct CompactWs {
+    size_t sums, flags, bytes;
+};
+
+inline CompactWs compact_ws(int64_t n)
+{
+    CompactWs L;
+    size_t o = 0;
+    L.sums = o;  o = (o + scan_ws_bytes(n) + 255) & ~(size_t)255;
+    L.flags = o; o = (o + (size_t)n + 255) & ~(size_t)255;
+    L.bytes = o;
+    return L;
+}
+
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const float* params, int64_t n,
+                                     int32_t sh_degree, const gs_camera* cams, int32_t n_views,
+                                     const gs_render_opts* opts, uint32_t* idx, int64_t* n_idx, float* grads,
+                                     void* ws, size_t* ws_bytes, void* stream)
+{
+    if (!ws_bytes || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
+    const CompactWs L = compact_ws(n);
+    if (!ws) {
+        *ws_bytes = L.bytes;
+        return GS_OK;
+    }
+    if (*ws_bytes < L.bytes) return GS_ERR_INVALID_ARG;
+    if (!opts || !n_idx) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!grad2d || !touched || !params || !idx || !grads)) return GS_ERR_INVALID_ARG;
+    if (param_rows(sh_degree) < 0 || !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    gs_status st = check_views(cams, n_views);
+    if (st != GS_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* w = (char*)ws;
+    unsigned long long* sums = (unsigned long long*)(w + L.sums);
+    uint8_t* flags = (uint8_t*)(w + L.flags);
+    unsigned long long* counts = reinterpret_cast<unsigned long long*>(n_idx);
+    for (int v = 0; v < n_views; ++v)
+        GS_CUDA_TRY((scan_launch<uint8_t, true>(touched + (size_t)v * n, n, idx + (size_t)v * n, sums, counts + v, s)));
+    if (n > 0) {
+        union_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(touched, n, n_views, flags);
+        GS_LAUNCH_CHECK();
+    }
+    GS_CUDA_TRY((scan_launch<uint8_t, true>(flags, n, idx + (size_t)n_views * n, sums, counts + n_views, s)));
+    if (n == 0) return GS_OK;
+    VjpArgs a;
+    a.grad2d = grad2d;
+    a.touched = touched;
+    a.params = params;
+    a.n = n;
+    a.near_z = opts->near_z;
+    a.lowpass = opts->lowpass;
+    a.tiles_x = tiles_x_of(cams[0].width);
+    a.tiles_y = tiles_y_of(cams[0].height);
+    a.idx_union = idx + (size_t)n_views * n;
+    a.n_union = n_idx + n_views;
+    a.grads = grads;
+    const CamSet cs = make_camset(cams, n_views);
+    const int threads = 128;
+    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    if (sh_degree == 0)
+        vjp_kernel<0><<<blocks, threads, 0, s>>>(a, cs);
+    else
+        vjp_kernel<3><<<blocks, threads, 0, s>>>(a, cs);
+    GS_LAUNCH_CHECK();
+    return GS_OK;
+}

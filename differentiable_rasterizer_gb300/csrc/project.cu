@@ -1,0 +1,88 @@
+// project.cu -- gs_project: EWA projection of every Gaussian into every view.
+//
+// One thread per Gaussian reads its parameters once (coalesced SoA rows) and
+// loops over the views, so a batch of V views costs one pass over the
+// parameters instead of V (Grendel, abstract: batched multi-view training).
+// Culling follows GS-Scale's frustum-culling step (abstract), done on the GPU.
+// The arithmetic order is fixed (see gs.h) so the cull / rect decisions are
+// reproducible bit for bit on a CPU.
+#include "gs_common.cuh"
+#include "project_math.cuh"
+
+namespace gs {
+
+struct ProjectArgs {
+    const float* params;
+    int64_t n;
+    int32_t sh_degree;
+    float near_z, lowpass;
+    int32_t tiles_x, tiles_y;
+    float4* rec;
+    float* depth;
+    ushort4* rect;
+    uint32_t* tiles_touched;
+};
+
+template <int DEG>
+__global__ void __launch_bounds__(128) project_kernel(ProjectArgs a, CamSet cs)
+{
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= a.n) return;
+    GaussParams<DEG> gp;
+    gp.load(a.params, a.n, g);
+    for (int v = 0; v < cs.n_views; ++v) {
+        const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
+        ProjOut po;
+        const bool vis = project_one<DEG>(gp, cs.cam[v], a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, nullptr);
+        if (!vis) {
+            a.tiles_touched[o] = 0u;
+            continue;
+        }
+        float4* r = a.rec + o * 3;
+        r[0] = make_float4(po.mx, po.my, -0.5f * po.cA, po.cB);
+        r[1] = make_float4(-0.5f * po.cC, po.opacity, po.col[0], po.col[1]);
+        r[2] = make_float4(po.col[2], po.depth, 0.0f, 0.0f);
+        a.depth[o] = po.depth;
+        a.rect[o] = make_ushort4((unsigned short)po.x0, (unsigned short)po.y0, (unsigned short)po.x1,
+                                 (unsigned short)po.y1);
+        a.tiles_touched[o] = (uint32_t)((po.x1 - po.x0) * (po.y1 - po.y0));
+    }
+}
+
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, const gs_camera* cams,
+                                int32_t n_views, const gs_render_opts* opts, const gs_proj* out, void* stream)
+{
+    if (!opts || !out || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
+    if (param_rows(sh_degree) < 0) return GS_ERR_INVALID_ARG;
+    gs_status st = check_views(cams, n_views);
+    if (st != GS_OK) return st;
+    if (n == 0) return GS_OK;
+    if (!params || !out->rec || !out->depth || !out->rect || !out->tiles_touched || !aligned16(out->rec))
+        return GS_ERR_INVALID_ARG;
+    ProjectArgs a;
+    a.params = params;
+    a.n = n;
+    a.sh_degree = sh_degree;
+    a.near_z = opts->near_z;
+    a.lowpass = opts->lowpass;
+    a.tiles_x = tiles_x_of(cams[0].width);
+    a.tiles_y = tiles_y_of(cams[0].height);
+    a.rec = reinterpret_cast<float4*>(out->rec);
+    a.depth = out->depth;
+    a.rect = reinterpret_cast<ushort4*>(out->rect);
+    a.tiles_touched = out->tiles_touched;
+    const CamSet cs = make_camset(cams, n_views);
+    const int threads = 128;
+    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (sh_degree == 0)
+        project_kernel<0><<<blocks, threads, 0, s>>>(a, cs);
+    else
+        project_kernel<3><<<blocks, threads, 0, s>>>(a, cs);
+    GS_LAUNCH_CHECK();
+    return GS_OK;
+}

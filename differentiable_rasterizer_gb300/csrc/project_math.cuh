@@ -1,0 +1,303 @@
+// project_math.cuh -- per-Gaussian projection and its vector-Jacobian product.
+//
+// project_one() evaluates, in a fixed IEEE operation order:
+//   activation   s = exp(log_scale), q^ = q / |q|, R(q^), M = R diag(s), Sigma = M M^T,
+//                o = 1 / (1 + exp(-logit))
+//   view         t = R_cam mu + t_cam, culled unless t_z > near_z
+//   EWA          J = [[fx/tz, 0, -fx tx/tz^2], [0, fy/tz, -fy ty/tz^2]],
+//                T = J R_cam, Sigma2D = T Sigma T^T + lowpass I, mean2d = (fx tx/tz + cx, fy ty/tz + cy)
+//   conic        det = a c - b^2 (> 0), conic = (c, -b, a) / det
+//   radius       mid = (a + c)/2, lambda_max = mid + sqrt(max(0, mid^2 - det)), r = ceil(3 sqrt(lambda_max))
+//   tile rect    floor((m - r)/16) .. floor((m + r)/16) per axis, clipped; empty -> culled
+//   colour       degree 0: rgb; degree 3: max(0, sum_k coef_k Y_k(unit(mu - C_cam)) + 1/2)
+// and vjp_one() is its reverse-mode derivative (fp32, fma allowed).
+#pragma once
+
+#include "gs_common.cuh"
+
+namespace gs {
+
+template <int DEG>
+struct GaussParams {
+    static constexpr int kCol = DEG == 0 ? 3 : 48;
+    static constexpr int kRows = 11 + kCol;
+    float mu[3], ls[3], q[4], logit;
+    float col[kCol];   // degree 3: col[3k + c] = coefficient k, channel c
+    __device__ __forceinline__ void load(const float* __restrict__ P, int64_t n, int64_t g)
+    {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) mu[i] = __ldg(P + (size_t)i * n + g);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) ls[i] = __ldg(P + (size_t)(3 + i) * n + g);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __ldg(P + (size_t)(6 + i) * n + g);
+        logit = __ldg(P + (size_t)10 * n + g);
+#pragma unroll
+        for (int i = 0; i < kCol; ++i) col[i] = __ldg(P + (size_t)(11 + i) * n + g);
+    }
+};
+
+struct ProjOut {
+    float mx, my, cA, cB, cC, opacity, col[3], depth;
+    int x0, y0, x1, y1;
+    uint32_t clamp;   // bit c: colour channel c clamped at 0
+};
+
+// Forward intermediates kept for the VJP.
+struct ProjInter {
+    float t[3], s[3], qn, qh[4], R[9], M[9], S[9], T0[3], T1[3];
+    float a, b, c, det;
+    float dir[3], nv;
+    float o;
+};
+
+template <int DEG>
+__device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs_camera& cam, float near_z,
+                                            float lowpass, int tiles_x, int tiles_y, ProjOut& out, ProjInter* it)
+{
+    const float* W = cam.R;
+    float t[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        t[i] = ((W[3 * i + 0] * gp.mu[0] + W[3 * i + 1] * gp.mu[1]) + W[3 * i + 2] * gp.mu[2]) + cam.t[i];
+    if (!(t[2] > near_z)) return false;
+    float s[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) s[j] = pexp(gp.ls[j]);
+    const float q0 = gp.q[0], q1 = gp.q[1], q2 = gp.q[2], q3 = gp.q[3];
+    const float qn = sqrtf(((q0 * q0 + q1 * q1) + q2 * q2) + q3 * q3);
+    if (!(qn > 0.0f)) return false;
+    const float w = q0 / qn, x = q1 / qn, y = q2 / qn, z = q3 / qn;
+    const float xx = x * x, yy = y * y, zz = z * z, xy = x * y, xz = x * z, yz = y * z;
+    const float wx = w * x, wy = w * y, wz = w * z;
+    float R[9];
+    R[0] = 1.0f - 2.0f * (yy + zz); R[1] = 2.0f * (xy - wz);        R[2] = 2.0f * (xz + wy);
+    R[3] = 2.0f * (xy + wz);        R[4] = 1.0f - 2.0f * (xx + zz); R[5] = 2.0f * (yz - wx);
+    R[6] = 2.0f * (xz - wy);        R[7] = 2.0f * (yz + wx);        R[8] = 1.0f - 2.0f * (xx + yy);
+    float M[9];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) M[3 * i + j] = R[3 * i + j] * s[j];
+    float S[9];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            S[3 * i + j] = (M[3 * i + 0] * M[3 * j + 0] + M[3 * i + 1] * M[3 * j + 1]) + M[3 * i + 2] * M[3 * j + 2];
+    const float fx = cam.fx, fy = cam.fy;
+    const float tz2 = t[2] * t[2];
+    const float j00 = fx / t[2], j11 = fy / t[2];
+    const float j02 = -(fx * t[0]) / tz2, j12 = -(fy * t[1]) / tz2;
+    float T0[3], T1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        T0[k] = j00 * W[0 + k] + j02 * W[6 + k];
+        T1[k] = j11 * W[3 + k] + j12 * W[6 + k];
+    }
+    float u[3], v[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        u[k] = (T0[0] * S[0 + k] + T0[1] * S[3 + k]) + T0[2] * S[6 + k];
+        v[k] = (T1[0] * S[0 + k] + T1[1] * S[3 + k]) + T1[2] * S[6 + k];
+    }
+    const float a = ((u[0] * T0[0] + u[1] * T0[1]) + u[2] * T0[2]) + lowpass;
+    const float b = (u[0] * T1[0] + u[1] * T1[1]) + u[2] * T1[2];
+    const float c = ((v[0] * T1[0] + v[1] * T1[1]) + v[2] * T1[2]) + lowpass;
+    const float mx = (fx * t[0]) / t[2] + cam.cx;
+    const float my = (fy * t[1]) / t[2] + cam.cy;
+    const float det = a * c - b * b;
+    if (!(det > 0.0f)) return false;
+    const float cA = c / det, cB = (-b) / det, cC = a / det;
+    const float mid = 0.5f * (a + c);
+    float disc = mid * mid - det;
+    if (disc < 0.0f) disc = 0.0f;
+    const float lmax = mid + sqrtf(disc);
+    const float r = ceilf(3.0f * sqrtf(lmax));
+    if (!(isfinite(mx) && isfinite(my) && isfinite(r) && isfinite(cA) && isfinite(cB) && isfinite(cC))) return false;
+    float fx0 = floorf((mx - r) * 0.0625f), fx1 = floorf((mx + r) * 0.0625f) + 1.0f;
+    float fy0 = floorf((my - r) * 0.0625f), fy1 = floorf((my + r) * 0.0625f) + 1.0f;
+    if (fx0 < 0.0f) fx0 = 0.0f;
+    if (fy0 < 0.0f) fy0 = 0.0f;
+    if (fx1 > (float)tiles_x) fx1 = (float)tiles_x;
+    if (fy1 > (float)tiles_y) fy1 = (float)tiles_y;
+    if (!(fx0 < fx1 && fy0 < fy1)) return false;
+    const float o = 1.0f / (1.0f + pexp(-gp.logit));
+    float col[3];
+    uint32_t cm = 0;
+    float dir[3] = {0.0f, 0.0f, 0.0f}, nv = 0.0f;
+    if (DEG == 0) {
+        col[0] = gp.col[0]; col[1] = gp.col[1]; col[2] = gp.col[2];
+    } else {
+        float cc[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cc[j] = -((W[0 + j] * cam.t[0] + W[3 + j] * cam.t[1]) + W[6 + j] * cam.t[2]);
+        const float dv0 = gp.mu[0] - cc[0], dv1 = gp.mu[1] - cc[1], dv2 = gp.mu[2] - cc[2];
+        nv = sqrtf((dv0 * dv0 + dv1 * dv1) + dv2 * dv2);
+        dir[0] = dv0 / nv; dir[1] = dv1 / nv; dir[2] = dv2 / nv;
+        float Y[16];
+        sh_basis(dir[0], dir[1], dir[2], Y);
+#pragma unroll
+        for (int ch = 0; ch < 3; ++ch) {
+            float acc = gp.col[ch] * Y[0];
+#pragma unroll
+            for (int k = 1; k < 16; ++k) acc = acc + gp.col[(3 * k + ch) % GaussParams<DEG>::kCol] * Y[k];
+            acc = acc + 0.5f;
+            if (acc < 0.0f) { acc = 0.0f; cm |= 1u << ch; }
+            col[ch] = acc;
+        }
+    }
+    if (!(isfinite(o) && isfinite(col[0]) && isfinite(col[1]) && isfinite(col[2]))) return false;
+    out.mx = mx; out.my = my; out.cA = cA; out.cB = cB; out.cC = cC; out.opacity = o;
+    out.col[0] = col[0]; out.col[1] = col[1]; out.col[2] = col[2];
+    out.depth = t[2];
+    out.x0 = (int)fx0; out.y0 = (int)fy0; out.x1 = (int)fx1; out.y1 = (int)fy1;
+    out.clamp = cm;
+    if (it) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) { it->t[i] = t[i]; it->s[i] = s[i]; it->dir[i] = dir[i]; it->T0[i] = T0[i]; it->T1[i] = T1[i]; }
+        it->qn = qn; it->qh[0] = w; it->qh[1] = x; it->qh[2] = y; it->qh[3] = z;
+#pragma unroll
+        for (int i = 0; i < 9; ++i) { it->R[i] = R[i]; it->M[i] = M[i]; it->S[i] = S[i]; }
+        it->a = a; it->b = b; it->c = c; it->det = det; it->nv = nv; it->o = o;
+    }
+    return true;
+}
+
+// d loss / d params of one (Gaussian, view) given d loss / d (mean2d, conic, opacity, colour).
+// g2: mx, my, A, B, C, o, r, g, b.  grad[] is accumulated (+=), rows as in the parameter buffer.
+template <int DEG>
+__device__ __forceinline__ void vjp_one(const GaussParams<DEG>& gp, const gs_camera& cam, const ProjInter& it,
+                                        uint32_t clamp, const float g2[9], float* grad)
+{
+    const float* W = cam.R;
+    const float fx = cam.fx, fy = cam.fy;
+    const float a = it.a, b = it.b, c = it.c;
+    const float id = 1.0f / it.det;
+    // conic (A, B, C) = (c, -b, a) / det
+    const float gA = g2[2], gB = g2[3], gC = g2[4];
+    const float g_id = __fmaf_rn(gA, c, __fmaf_rn(-gB, b, gC * a));
+    const float g_det = -g_id * id * id;
+    const float ga = __fmaf_rn(gC, id, g_det * c);
+    const float gc = __fmaf_rn(gA, id, g_det * a);
+    const float gb = __fmaf_rn(-gB, id, g_det * (-2.0f * b));
+    // a = T0 S T0^T + l, b = T0 S T1^T, c = T1 S T1^T + l
+    float ST0[3], ST1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        ST0[k] = __fmaf_rn(it.S[3 * k], it.T0[0], __fmaf_rn(it.S[3 * k + 1], it.T0[1], it.S[3 * k + 2] * it.T0[2]));
+        ST1[k] = __fmaf_rn(it.S[3 * k], it.T1[0], __fmaf_rn(it.S[3 * k + 1], it.T1[1], it.S[3 * k + 2] * it.T1[2]));
+    }
+    float gT0[3], gT1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        gT0[k] = __fmaf_rn(2.0f * ga, ST0[k], gb * ST1[k]);
+        gT1[k] = __fmaf_rn(gb, ST0[k], 2.0f * gc * ST1[k]);
+    }
+    float Gs[9];
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+        for (int l = 0; l < 3; ++l)
+            Gs[3 * k + l] = __fmaf_rn(ga * it.T0[k], it.T0[l],
+                                      __fmaf_rn(0.5f * gb, __fmaf_rn(it.T0[k], it.T1[l], it.T1[k] * it.T0[l]),
+                                                gc * it.T1[k] * it.T1[l]));
+    // Sigma = M M^T: dM = 2 Gs M
+    float gR[9], gs[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const float gM = 2.0f * __fmaf_rn(Gs[3 * i], it.M[j], __fmaf_rn(Gs[3 * i + 1], it.M[3 + j], Gs[3 * i + 2] * it.M[6 + j]));
+            gR[3 * i + j] = gM * it.s[j];
+            gs[j] = __fmaf_rn(gM, it.R[3 * i + j], gs[j]);
+        }
+    const float w = it.qh[0], x = it.qh[1], y = it.qh[2], z = it.qh[3];
+    const float gw = 2.0f * (-z * gR[1] + y * gR[2] + z * gR[3] - x * gR[5] - y * gR[6] + x * gR[7]);
+    const float gx = 2.0f * (y * gR[1] + z * gR[2] + y * gR[3] - 2.0f * x * gR[4] - w * gR[5] + z * gR[6] + w * gR[7] - 2.0f * x * gR[8]);
+    const float gy = 2.0f * (-2.0f * y * gR[0] + x * gR[1] + w * gR[2] + x * gR[3] + z * gR[5] - w * gR[6] + z * gR[7] - 2.0f * y * gR[8]);
+    const float gz = 2.0f * (-2.0f * z * gR[0] - w * gR[1] + x * gR[2] + w * gR[3] - 2.0f * z * gR[4] + y * gR[5] + x * gR[6] + y * gR[7]);
+    const float dotq = w * gw + x * gx + y * gy + z * gz;
+    const float iqn = 1.0f / it.qn;
+    // T = J W
+    float gj00 = 0.0f, gj02 = 0.0f, gj11 = 0.0f, gj12 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        gj00 = __fmaf_rn(gT0[k], W[k], gj00);
+        gj02 = __fmaf_rn(gT0[k], W[6 + k], gj02);
+        gj11 = __fmaf_rn(gT1[k], W[3 + k], gj11);
+        gj12 = __fmaf_rn(gT1[k], W[6 + k], gj12);
+    }
+    const float tx = it.t[0], ty = it.t[1], tz = it.t[2];
+    const float itz = 1.0f / tz, itz2 = itz * itz, itz3 = itz2 * itz;
+    const float gmx = g2[0], gmy = g2[1];
+    float gt[3];
+    gt[0] = gj02 * (-fx * itz2) + gmx * (fx * itz);
+    gt[1] = gj12 * (-fy * itz2) + gmy * (fy * itz);
+    gt[2] = gj00 * (-fx * itz2) + gj02 * (2.0f * fx * tx * itz3) + gj11 * (-fy * itz2) + gj12 * (2.0f * fy * ty * itz3)
+          + gmx * (-fx * tx * itz2) + gmy * (-fy * ty * itz2);
+    float gmu[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) gmu[j] = __fmaf_rn(W[j], gt[0], __fmaf_rn(W[3 + j], gt[1], W[6 + j] * gt[2]));
+    if (DEG == 0) {
+        grad[11] += g2[6];
+        grad[12] += g2[7];
+        grad[13] += g2[8];
+    } else {
+        const float X = it.dir[0], Yv = it.dir[1], Z = it.dir[2];
+        float Y[16];
+        sh_basis(X, Yv, Z, Y);
+        // gradient of each basis polynomial w.r.t. (x, y, z)
+        const float XX = X * X, YY = Yv * Yv, ZZ = Z * Z;
+        float dY[16][3];
+        dY[0][0] = 0.0f; dY[0][1] = 0.0f; dY[0][2] = 0.0f;
+        dY[1][0] = 0.0f; dY[1][1] = SH::K1; dY[1][2] = 0.0f;
+        dY[2][0] = 0.0f; dY[2][1] = 0.0f; dY[2][2] = SH::K1;
+        dY[3][0] = SH::K1; dY[3][1] = 0.0f; dY[3][2] = 0.0f;
+        dY[4][0] = SH::K2 * Yv; dY[4][1] = SH::K2 * X; dY[4][2] = 0.0f;
+        dY[5][0] = 0.0f; dY[5][1] = SH::K2 * Z; dY[5][2] = SH::K2 * Yv;
+        dY[6][0] = -2.0f * SH::K3 * X; dY[6][1] = -2.0f * SH::K3 * Yv; dY[6][2] = 4.0f * SH::K3 * Z;
+        dY[7][0] = SH::K2 * Z; dY[7][1] = 0.0f; dY[7][2] = SH::K2 * X;
+        dY[8][0] = 2.0f * SH::K4 * X; dY[8][1] = -2.0f * SH::K4 * Yv; dY[8][2] = 0.0f;
+        dY[9][0] = 6.0f * SH::K5 * X * Yv; dY[9][1] = SH::K5 * (3.0f * XX - 3.0f * YY); dY[9][2] = 0.0f;
+        dY[10][0] = SH::K6 * Yv * Z; dY[10][1] = SH::K6 * X * Z; dY[10][2] = SH::K6 * X * Yv;
+        dY[11][0] = -2.0f * SH::K7 * X * Yv; dY[11][1] = SH::K7 * (4.0f * ZZ - XX - 3.0f * YY); dY[11][2] = 8.0f * SH::K7 * Yv * Z;
+        dY[12][0] = -6.0f * SH::K8 * X * Z; dY[12][1] = -6.0f * SH::K8 * Yv * Z; dY[12][2] = SH::K8 * (6.0f * ZZ - 3.0f * XX - 3.0f * YY);
+        dY[13][0] = SH::K7 * (4.0f * ZZ - 3.0f * XX - YY); dY[13][1] = -2.0f * SH::K7 * X * Yv; dY[13][2] = 8.0f * SH::K7 * X * Z;
+        dY[14][0] = 2.0f * SH::K9 * X * Z; dY[14][1] = -2.0f * SH::K9 * Yv * Z; dY[14][2] = SH::K9 * (XX - YY);
+        dY[15][0] = SH::K5 * (3.0f * XX - 3.0f * YY); dY[15][1] = -6.0f * SH::K5 * X * Yv; dY[15][2] = 0.0f;
+        float gd0 = 0.0f, gd1 = 0.0f, gd2 = 0.0f;
+#pragma unroll
+        for (int ch = 0; ch < 3; ++ch) {
+            if (clamp & (1u << ch)) continue;
+            const float gcol = g2[6 + ch];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int row = 11 + 3 * k + ch;
+                grad[row] = __fmaf_rn(gcol, Y[k], grad[row]);
+                const float kc = gcol * gp.col[(3 * k + ch) % GaussParams<DEG>::kCol];
+                gd0 = __fmaf_rn(kc, dY[k][0], gd0);
+                gd1 = __fmaf_rn(kc, dY[k][1], gd1);
+                gd2 = __fmaf_rn(kc, dY[k][2], gd2);
+            }
+        }
+        const float dd = X * gd0 + Yv * gd1 + Z * gd2;
+        const float inv = 1.0f / it.nv;
+        gmu[0] += (gd0 - X * dd) * inv;
+        gmu[1] += (gd1 - Yv * dd) * inv;
+        gmu[2] += (gd2 - Z * dd) * inv;
+    }
+    grad[10] += g2[5] * it.o * (1.0f - it.o);
+    grad[0] += gmu[0];
+    grad[1] += gmu[1];
+    grad[2] += gmu[2];
+    grad[3] += gs[0] * it.s[0];
+    grad[4] += gs[1] * it.s[1];
+    grad[5] += gs[2] * it.s[2];
+    grad[6] += (gw - w * dotq) * iqn;
+    grad[7] += (gx - x * dotq) * iqn;
+    grad[8] += (gy - y * dotq) * iqn;
+    grad[9] += (gz - z * dotq) * iqn;
+}
+
+}  // namespace gs

@@ -1,0 +1,177 @@
+"""One training step of the tile-based 3DGS rasterizer on one GPU.
+
+``GaussianTrainer`` owns the device buffers (torch tensors used as plain device
+memory) and calls the five C-ABI entry points in order on one stream:
+
+    gs_project -> gs_bin_sort -> gs_raster_fused_fwd_bwd -> gs_grad_compact -> gs_adam_deferred
+
+Buffer layout in HBM (fp32 unless stated):
+    params, grads, adam_m, adam_v   [P, n]           P = 14 (RGB) or 59 (SH degree 3)
+    last_step                       [n] int32
+    rec                             [V, n, 12]       3 float4 per (view, Gaussian)
+    depth, tiles_touched, rect      [V, n], [V, n], [V, n, 4] uint16
+    keys, ids                       [capacity] u64, u32 (sorted instances)
+    ranges                          [V * tiles, 2] u32
+    image                           [V, 3, H, W];  loss [V] fp64
+    grad2d                          [V, n, 12]  (kept all-zero between steps)
+    touched                         [V, n] u8   (kept all-zero between steps)
+    idx, n_idx                      [V + 1, n] u32, [V + 1] int64 (per-view lists + union)
+The sizes follow the workload: nothing is allocated per step once the instance
+capacity has been reached (it grows by 25 % headroom when a step needs more).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import abi
+
+
+class GaussianTrainer:
+    def __init__(self, params: np.ndarray | torch.Tensor, sh_degree: int, cameras, opts: dict, lr,
+                 betas=(0.9, 0.999), eps=1e-8, device="cuda", capacity: int | None = None):
+        self.device = torch.device(device)
+        self.sh_degree = sh_degree
+        self.P = abi.gs_param_rows(sh_degree)
+        p = torch.as_tensor(params, dtype=torch.float32)
+        assert p.shape[0] == self.P, (p.shape, self.P)
+        self.n = int(p.shape[1])
+        self.V = len(cameras)
+        self.W, self.H = cameras[0].width, cameras[0].height
+        self.tiles = abi.gs_num_tiles(self.W, self.H)
+        self.cams = abi.cameras(cameras)
+        self.opts = abi.render_opts(opts)
+        self.lr = tuple(float(x) for x in lr)
+        self.betas = betas
+        self.eps = eps
+        self.t = 0
+        dev = self.device
+        n, V = self.n, self.V
+        self.params = p.to(dev).contiguous()
+        self.grads = torch.zeros_like(self.params)
+        self.adam_m = torch.zeros_like(self.params)
+        self.adam_v = torch.zeros_like(self.params)
+        self.last_step = torch.zeros(n, dtype=torch.int32, device=dev)
+        self.rec = torch.empty((V, n, 12), dtype=torch.float32, device=dev)
+        self.depth = torch.empty((V, n), dtype=torch.float32, device=dev)
+        self.rect = torch.empty((V, n, 4), dtype=torch.int16, device=dev)
+        self.tiles_touched = torch.empty((V, n), dtype=torch.int32, device=dev)
+        self.ranges = torch.empty((V * self.tiles, 2), dtype=torch.int32, device=dev)
+        self.image = torch.empty((V, 3, self.H, self.W), dtype=torch.float32, device=dev)
+        self.loss = torch.zeros(V, dtype=torch.float64, device=dev)
+        self.grad2d = torch.zeros((V, n, abi.GS_GRAD2D_STRIDE), dtype=torch.float32, device=dev)
+        self.touched = torch.zeros((V, n), dtype=torch.uint8, device=dev)
+        self.idx = torch.empty((V + 1, n), dtype=torch.int32, device=dev)
+        self.n_idx = torch.zeros(V + 1, dtype=torch.int64, device=dev)
+        self.eval_counts = torch.zeros(3, dtype=torch.int64, device=dev)
+        self.compact_ws = torch.empty(abi.gs_grad_compact_ws_bytes(n), dtype=torch.uint8, device=dev)
+        self.proj = abi.proj_struct(self.rec.data_ptr(), self.depth.data_ptr(), self.rect.data_ptr(),
+                                    self.tiles_touched.data_ptr())
+        self.capacity = 0
+        self.n_instances = 0
+        self._alloc_instances(capacity if capacity is not None else max(1024, 4 * n * V // 8))
+
+    # ------------------------------------------------------------------ buffers
+    def _alloc_instances(self, capacity: int):
+        capacity = int(min(capacity, 2 ** 32 - 1))
+        self.capacity = capacity
+        self.keys = torch.empty(capacity, dtype=torch.int64, device=self.device)
+        self.ids = torch.empty(capacity, dtype=torch.int32, device=self.device)
+        nbytes = abi.gs_bin_sort_ws_bytes(self.n, self.V, self.W, self.H, capacity)
+        self.sort_ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+
+    def kernel_launches_per_step(self) -> int:
+        """Kernels the library launches for one train_step (its launch structure:
+        projection 1; bin/sort: offsets scan 3, emit 1, per radix pass histogram 1 +
+        scan 3 + scatter 1, ranges 1; fused raster 1; compaction: 3 per view-list scan,
+        union 1, union scan 3, VJP 1; Adam 1).  Memsets and copies are not kernels."""
+        V, n = self.V, self.n
+        ntile_ids = V * self.tiles
+        bits = 32 + max(1, int(ntile_ids - 1).bit_length())
+        npass = (bits + 7) // 8
+        sort = (3 if n * V else 0) + ((1 + 5 * npass + 1) if self.n_instances else 0)
+        compact = (3 * V + 1 + 3 + 1) if n else 0
+        return (1 if n else 0) + sort + 1 + compact + (1 if n else 0)
+
+    def stream_handle(self):
+        return torch.cuda.current_stream(self.device).cuda_stream
+
+    # ------------------------------------------------------------------ stages
+    def project(self, params=None):
+        params = self.params if params is None else params
+        abi.gs_project(params.data_ptr(), self.n, self.sh_degree, self.cams, self.V, self.opts, self.proj,
+                       self.stream_handle())
+
+    def bin_sort(self):
+        while True:
+            st, cnt = abi.gs_bin_sort(self.proj, self.n, self.V, self.W, self.H, self.capacity, self.keys.data_ptr(),
+                                      self.ids.data_ptr(), self.ranges.data_ptr(), self.sort_ws.data_ptr(),
+                                      self.sort_ws.numel(), self.stream_handle())
+            self.n_instances = cnt
+            if st == abi.GS_OK:
+                return cnt
+            self._alloc_instances(int(math.ceil(cnt * 1.25)) + 1024)
+
+    def raster(self, target=None, count_evals=True):
+        abi.gs_raster_fused_fwd_bwd(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,
+                                    self.opts, target.data_ptr() if target is not None else None,
+                                    self.image.data_ptr(), self.loss.data_ptr(), self.grad2d.data_ptr(),
+                                    self.touched.data_ptr(), self.eval_counts.data_ptr() if count_evals else None,
+                                    self.stream_handle())
+
+    def compact(self):
+        abi.gs_grad_compact(self.grad2d.data_ptr(), self.touched.data_ptr(), self.params.data_ptr(), self.n,
+                            self.sh_degree, self.cams, self.V, self.opts, self.idx.data_ptr(), self.n_idx.data_ptr(),
+                            self.grads.data_ptr(), self.compact_ws.data_ptr(), self.compact_ws.numel(),
+                            self.stream_handle())
+
+    def adam(self, t, flush=False):
+        union = self.idx[self.V]
+        abi.gs_adam_deferred(self.params.data_ptr(), self.grads.data_ptr(), self.adam_m.data_ptr(),
+                             self.adam_v.data_ptr(), self.last_step.data_ptr(), self.n, self.sh_degree,
+                             union.data_ptr(), self.n_idx[self.V:].data_ptr(), t, self.lr, self.betas[0],
+                             self.betas[1], self.eps, flush, self.stream_handle())
+
+    # ------------------------------------------------------------------ steps
+    def train_step(self, target: torch.Tensor, count_evals=True):
+        """One full step (device-resident target [V, 3, H, W]); returns the loss tensor (device)."""
+        self.t += 1
+        self.project()
+        self.bin_sort()
+        self.raster(target, count_evals)
+        self.compact()
+        self.adam(self.t)
+        return self.loss
+
+    def train_step_host(self, target_host: torch.Tensor, target_dev: torch.Tensor, loss_host: torch.Tensor):
+        """End-to-end step from pinned host memory: copy the target in, step, copy the loss out."""
+        target_dev.copy_(target_host, non_blocking=True)
+        self.train_step(target_dev)
+        loss_host.copy_(self.loss, non_blocking=True)
+        return loss_host
+
+    def render(self, params=None) -> torch.Tensor:
+        """Forward only (no loss, gradients or touched flags); returns the image tensor."""
+        self.project(params)
+        self.bin_sort()
+        self.raster(None, count_evals=False)
+        return self.image
+
+    def flush(self):
+        """Bring every Gaussian's optimizer state to the current step (before reading params)."""
+        if self.t > 0:
+            self.adam(self.t, flush=True)
+
+    def state_dict(self):
+        self.flush()
+        return dict(params=self.params.clone(), m=self.adam_m.clone(), v=self.adam_v.clone(),
+                    last_step=self.last_step.clone(), t=self.t)
+
+    def load_state_dict(self, sd):
+        self.params.copy_(sd["params"])
+        self.adam_m.copy_(sd["m"])
+        self.adam_v.copy_(sd["v"])
+        self.last_step.copy_(sd["last_step"])
+        self.t = int(sd["t"])

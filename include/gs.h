@@ -1,0 +1,210 @@
+/*
+ * gs.h -- C ABI of the GB300 (sm_103a) 3D Gaussian Splatting training step.
+ *
+ * One training step is five calls on one CUDA stream:
+ *
+ *   gs_project               EWA projection, culling, colour (per Gaussian x view)
+ *   gs_bin_sort              16x16 tile binning with (tile, depth) keys + LSD radix sort
+ *   gs_raster_fused_fwd_bwd  forward compositing, L1 loss and backward in ONE kernel
+ *   gs_grad_compact          touched-set compaction, projection VJP, scatter-add
+ *   gs_adam_deferred         Adam on the touched Gaussians only, with catch-up
+ *
+ * Method sources (pages, by title and section):
+ *   ByteSplat: Efficient Distributed 3DGS Training via Intra- and Inter-GPU
+ *     Communication Reduction -- English abstract: forward and backward
+ *     rasterization fused into a single kernel that keeps intermediate results
+ *     on chip; zero partial gradients eliminated, the remaining records compacted
+ *     by an encoder and aggregated by a decoder.
+ *   On Scaling Up 3D Gaussian Splatting Training (Grendel) -- abstract: batched
+ *     training over multiple views, sqrt(batch size) hyper-parameter scaling;
+ *     method-details section: L1 loss.
+ *   GS-Scale: Unlocking Large-Scale 3DGS Training via Host Offloading --
+ *     abstract: frustum culling; deferred optimizer update that avoids memory
+ *     traffic for Gaussians with zero gradients.
+ * The rasterizer arithmetic is the standard tile-based 3DGS one: EWA projection
+ * to a 2D conic and radius, alpha = min(0.99, o * exp(-1/2 d^T Sigma2D^-1 d)),
+ * alpha < 1/255 skipped, compositing stops once T < 1e-4.
+ *
+ * Conventions for every call
+ *   - Returns gs_status; nothing is thrown across the ABI.
+ *   - All array pointers are DEVICE pointers owned by the caller unless the
+ *     argument says "host".  The library allocates no device memory and keeps no
+ *     state between calls; calls that need scratch take (ws, ws_bytes): pass
+ *     ws == NULL to query the size into *ws_bytes.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  gs_bin_sort is the only call that synchronises the host
+ *     (it reads the instance count back to size the sort).
+ *   - Arithmetic is fp32 (fp64 for the loss sum).  The forward decisions (cull,
+ *     tile rect, alpha skip, transmittance stop) are computed with IEEE-rounded
+ *     + - * / sqrt, no contraction, and one portable exp (Cody-Waite reduction,
+ *     degree-7 Taylor polynomial in Horner form with fma, exact 2^k scaling),
+ *     so they are reproducible bit for bit by a CPU implementation.
+ *   - Sizes: n <= 2^31 - 1 Gaussians, n_views <= GS_MAX_VIEWS, all views share
+ *     one resolution, instance count < 2^32.
+ *   - Thread-compatible: no hidden globals; concurrent calls on different
+ *     buffers are safe.
+ *
+ * Parameter buffer ([P][n] fp32, row-major, one row per scalar parameter):
+ *   rows 0-2 mean (world), 3-5 log-scale, 6-9 quaternion (w, x, y, z; any norm),
+ *   10 opacity logit, colour: degree 0 -> rows 11-13 RGB (P = 14);
+ *   degree 3 -> SH coefficient k (0..15, k = l^2 + l + m, real orthonormal basis
+ *   without Condon-Shortley phase), channel c at row 11 + 3k + c (P = 59);
+ *   colour = max(0, sum_k coef_k Y_k(dir) + 0.5), dir = unit(mean - camera centre).
+ */
+#ifndef GS_H
+#define GS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GS_API __attribute__((visibility("default")))
+#else
+#define GS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gs_status {
+    GS_OK = 0,
+    GS_ERR_INVALID_ARG = 1, /* a pointer, size or option is out of range          */
+    GS_ERR_CAPACITY = 2,    /* instance buffers too small; needed count reported  */
+    GS_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed        */
+    GS_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out                 */
+    GS_ERR_DEVICE = 5       /* a kernel reported an error through the device word */
+} gs_status;
+
+#define GS_TILE 16          /* tile edge in pixels                                */
+#define GS_MAX_VIEWS 32     /* views per call (cameras are passed by value)       */
+#define GS_REC_FLOAT4 3     /* float4 per projected record                        */
+#define GS_GRAD2D_STRIDE 12 /* floats per (view, Gaussian) in grad2d              */
+
+/* Pinhole camera.  World -> camera: x_c = R x_w + t (R row-major).  Camera looks
+ * along +z, image x right, y down; pixel (i, j) has its centre at (i + .5, j + .5);
+ * u = fx * x_c / z_c + cx,  v = fy * y_c / z_c + cy. */
+typedef struct gs_camera {
+    float R[9];
+    float t[3];
+    float fx, fy, cx, cy;
+    int32_t width, height;
+} gs_camera;
+
+/* Render options.  Defaults: near_z 0.2, lowpass 0.3 (px^2 added to the 2D
+ * covariance diagonal), alpha_min 1/255 (skip below), alpha_max 0.99 (clamp),
+ * t_min 1e-4 (stop once T falls below it; the Gaussian that crosses is
+ * composited unless exclude_crossing = 1), bg = background colour. */
+typedef struct gs_render_opts {
+    float near_z, lowpass, alpha_min, alpha_max, t_min;
+    float bg[3];
+    int32_t exclude_crossing;
+    int32_t reserved;
+} gs_render_opts;
+
+/* Per-view projected records, caller-allocated, each [n_views][n]:
+ *   rec            3 float4 per (view, Gaussian), 16-byte aligned:
+ *                  {mx, my, -A/2, B}, {-C/2, opacity, r, g}, {b, depth, 0, 0}
+ *                  (mean in pixels, conic (A, B, C) = Sigma2D^-1, depth = z_c);
+ *                  written only for visible Gaussians
+ *   depth          float z_c (written only for visible Gaussians)
+ *   rect           4 x uint16 tile bounds x0, y0, x1, y1, half-open, clipped
+ *                  to the grid (written only for visible Gaussians)
+ *   tiles_touched  (x1 - x0) * (y1 - y0), 0 = culled (always written)
+ */
+typedef struct gs_proj {
+    float* rec;
+    float* depth;
+    uint16_t* rect;
+    uint32_t* tiles_touched;
+} gs_proj;
+
+/* EWA projection of every Gaussian into every view (one pass over params).
+ * Cull: z_c <= near_z, non-finite values, zero quaternion, det(Sigma2D) <= 0,
+ * or an empty tile rect.  Radius = ceil(3 sqrt(lambda_max(Sigma2D))); rect =
+ * tiles floor((m -/+ r)/16).  Opacity = sigmoid(logit).
+ * params: [P][n]; cams/opts: HOST; out: device arrays described above.
+ * Errors: INVALID_ARG for NULL pointers, n < 0, n_views outside 1..GS_MAX_VIEWS,
+ * sh_degree not 0 or 3, differing view sizes; CUDA on launch failure. */
+GS_API gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, const gs_camera* cams, int32_t n_views,
+                     const gs_render_opts* opts, const gs_proj* out, void* stream);
+
+/* Tile binning and sort.  Every visible (view v, Gaussian g) emits one instance
+ * per tile of its rect with key = ((v * tiles + tile) << 32) | bits(depth) and
+ * value g; instances are sorted by key (LSD radix over the 32 depth bits and the
+ * bits of v * tiles + tile), stably, so equal keys keep ascending g.
+ * keys, ids: [capacity] outputs (sorted); tile_ranges: [n_views * tiles][2]
+ * uint32 [start, end) into the sorted arrays (start == end: empty tile).
+ * n_instances: HOST out, set even when the capacity is too small.
+ * ws / ws_bytes: scratch (ws == NULL: query).  Synchronises the host once.
+ * Errors: CAPACITY if n_instances > capacity (outputs untouched);
+ * INVALID_ARG for bad sizes or a too small workspace. */
+GS_API gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views, int32_t width, int32_t height,
+                      int64_t capacity, uint64_t* keys, uint32_t* ids, uint32_t* tile_ranges,
+                      int64_t* n_instances, void* ws, size_t* ws_bytes, void* stream);
+
+/* Fused forward + backward rasterization: one CTA per 16x16 tile (256 threads,
+ * one pixel each).  Forward: front-to-back over the tile's sorted list, skip
+ * power > 0 or alpha < alpha_min, C += c * alpha * T, T *= 1 - alpha, stop at
+ * T < t_min; C += T * bg.  The per-pixel T, colour and last index stay in
+ * registers.  With a target: L1 loss per view, mean over 3*H*W values, summed in
+ * fp64, and its gradient sign(C - target) / (3HW) on chip; backward walks the
+ * same list back to front (transmittance recovered by division) and
+ * accumulates per-Gaussian gradients with warp reductions and one atomic per
+ * warp and component.
+ * target: [V][3][H][W] or NULL (forward only: no loss, gradients or touched).
+ * image: [V][3][H][W] out.  loss: [V] fp64 out (overwritten).
+ * grad2d: [V][n][GS_GRAD2D_STRIDE] accumulated (+=): d/d mean2d (x, y),
+ *   d/d conic (A, B, C), d/d opacity, d/d colour (r, g, b), 3 pad floats.
+ * touched: [V][n] u8 set to 1 for every Gaussian composited at least once.
+ *   grad2d and touched must be zero on entry; gs_grad_compact returns them to
+ *   zero, so a step loop needs to clear them only once.
+ * eval_counts: NULL or [3] u64 accumulated (+=): E_fwd = list entries evaluated
+ *   up to the stop (skipped ones included), E_bwd = sum of (last index + 1),
+ *   E_comp = entries composited (alpha >= alpha_min and not stopped).
+ * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
+GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges, const uint32_t* ids,
+                                  const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
+                                  const float* target, float* image, double* loss, float* grad2d, uint8_t* touched,
+                                  uint64_t* eval_counts, void* stream);
+
+/* Sparse-gradient compaction ("encoder") and aggregation ("decoder"):
+ * per view, idx[v] = ascending list of touched Gaussians, n_idx[v] its length;
+ * idx[n_views] / n_idx[n_views] = the union over views.  For every Gaussian of
+ * the union the projection VJP of each touching view is summed in view order
+ * and added to grads (one read-modify-write per Gaussian).  grad2d and touched
+ * are cleared for the entries consumed.
+ * idx: [(n_views + 1) * n] u32 out; n_idx: [n_views + 1] int64 DEVICE out.
+ * grads: [P][n] fp32 accumulated (+=).  cams/opts: HOST, as given to gs_project.
+ * Errors: INVALID_ARG for bad pointers, sizes or a too small workspace. */
+GS_API gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const float* params, int64_t n, int32_t sh_degree,
+                          const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
+                          uint32_t* idx, int64_t* n_idx, float* grads, void* ws, size_t* ws_bytes, void* stream);
+
+/* Deferred Adam (dense-equivalent).  For every listed Gaussian g with
+ * s = last_step[g] < t: the skipped zero-gradient steps j = s+1 .. t-1 are
+ * replayed, then step t uses grads; last_step[g] = t and grads[:, g] = 0.
+ * One step: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+ *           p -= lr * ((m / bc1) / (sqrt(v / bc2) + eps)),
+ * bc = 1 - beta^j with beta^j by binary exponentiation in fp64, rounded to fp32.
+ * flush = 1: every Gaussian with last_step < t is brought to step t with zero
+ *   gradients (idx, n_idx, grads unused) -- call before reading or saving params.
+ * params, grads, m, v: [P][n]; last_step: [n] int32 (0 = never stepped).
+ * idx: [>= *n_idx] u32, n_idx: DEVICE int64.  lr: HOST [5] per group (mean,
+ * log-scale, quaternion, opacity, colour).  t >= 1.
+ * Errors: INVALID_ARG for bad pointers or t < 1. */
+GS_API gs_status gs_adam_deferred(float* params, float* grads, float* m, float* v, int32_t* last_step, int64_t n,
+                           int32_t sh_degree, const uint32_t* idx, const int64_t* n_idx, int32_t t, const float* lr,
+                           float beta1, float beta2, float eps, int32_t flush, void* stream);
+
+/* Static helpers (no device work). */
+GS_API const char* gs_error_string(gs_status s);
+GS_API int32_t gs_param_rows(int32_t sh_degree);                     /* 14, 59, or -1 */
+GS_API int64_t gs_num_tiles(int32_t width, int32_t height);          /* ceil(W/16) * ceil(H/16) */
+GS_API const char* gs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_H */

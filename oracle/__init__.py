@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 
 import numpy as np
@@ -21,6 +22,10 @@ _SRC = os.path.join(_HERE, "gs_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "libgs_oracle.so")
 
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wno-unused-function"]
+# fmaf() is correctly rounded by definition; on x86-64 let it be the FMA instruction
+# instead of libm's software emulation (same results, much faster).  aarch64 has it natively.
+if platform.machine() in ("x86_64", "AMD64"):
+    CFLAGS += ["-mfma"]
 
 
 def build(force: bool = False) -> str:
@@ -141,7 +146,7 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
     loss = np.zeros(1, np.float64)
     g2 = np.zeros((n, 9), np.float64) if (grads and target is not None) else None
     touched = np.zeros(n, np.uint8)
-    counts = np.zeros(2, np.int64)
+    counts = np.zeros(3, np.int64)
     last = np.zeros(H * W, np.int32) if want_last else None
     sig = np.zeros(1, np.uint64) if want_sig else None
     tgt = np.ascontiguousarray(np.asarray(target, dt)) if target is not None else None
@@ -150,7 +155,7 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
                                                   _ptr(counts), _ptr(last), _ptr(sig))
     assert rc == 0
     out = dict(image=img, loss=float(loss[0]) if target is not None else None, grad2d=g2, touched=touched,
-               e_fwd=int(counts[0]), e_bwd=int(counts[1]))
+               e_fwd=int(counts[0]), e_bwd=int(counts[1]), e_comp=int(counts[2]))
     if want_last:
         out["last"] = last.reshape(H, W)
     if want_sig:

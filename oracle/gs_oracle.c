@@ -85,7 +85,7 @@ static float pow2i_f(int e) /* 2^e for e in [-126, 127], built from the exponent
     return v.f;
 }
 
-float oracle_pexp_f32(float x)
+static float pexp32(float x)
 {
     if (x != x) return x;
     if (x < -104.0f) x = -104.0f;
@@ -97,10 +97,14 @@ float oracle_pexp_f32(float x)
     float k = rintf(x * log2e);
     float r = fmaf(-k, ln2_hi, x);
     r = fmaf(-k, ln2_lo, r);
-    /* Taylor coefficients 1/j!, j = 0..7 */
-    float c[8];
-    double f = 1.0;
-    for (int j = 0; j < 8; ++j) { if (j > 0) f *= (double)j; c[j] = (float)(1.0 / f); }
+    /* Taylor coefficients 1/j!, j = 0..7, rounded to fp32 once */
+    static float c[8];
+    static int ready = 0;
+    if (!ready) {
+        double f = 1.0;
+        for (int j = 0; j < 8; ++j) { if (j > 0) f *= (double)j; c[j] = (float)(1.0 / f); }
+        ready = 1;
+    }
     float p = c[7];
     for (int j = 6; j >= 0; --j) p = fmaf(p, r, c[j]);
     int ki = (int)k;
@@ -108,7 +112,9 @@ float oracle_pexp_f32(float x)
     int k2 = ki - k1;
     return (p * pow2i_f(k1)) * pow2i_f(k2);
 }
-#define PEXP(x) oracle_pexp_f32(x)
+
+float oracle_pexp_f32(float x) { return pexp32(x); }
+#define PEXP(x) pexp32(x)
 #else
 #define PEXP(x) exp(x)
 #endif
@@ -461,7 +467,8 @@ static uint64_t fnv(uint64_t h, uint64_t v)
  * target == NULL: forward only (no loss, no gradients).
  * grad2d: [n][9] fp64 accumulated (+=): d mean2d x, y; d conic A, B, C; d opacity; d colour r, g, b.
  * touched: [n] set to 1 for every Gaussian composited at least once.
- * counts: E_fwd (entries evaluated up to the stop, skipped ones included), E_bwd (sum of last+1).
+ * counts: E_fwd (entries evaluated up to the stop, skipped ones included), E_bwd (sum of last+1),
+ *         E_comp (entries composited).
  * last_idx: [H*W] list position of the last composited entry (-1 if none), or NULL.
  * sig: decision signature (hash of every discrete decision), or NULL.
  */
@@ -487,7 +494,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
     /* dL/dC = sign(C - target) / (3HW) [reading: L1 = mean absolute error over pixels and channels] */
     const REAL inv3hw = (REAL)(1.0 / (3.0 * (double)HW));
     double lsum = 0.0;
-    int64_t efwd = 0, ebwd = 0;
+    int64_t efwd = 0, ebwd = 0, ecomp = 0;
     uint64_t h = 1469598103934665603ull;
     if (sig)
         for (int64_t g = 0; g < n; ++g) {
@@ -536,6 +543,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
             for (int ch = 0; ch < 3; ++ch) C[ch] = C[ch] + T * op.bg[ch];
             efwd += nev;
             ebwd += last + 1;
+            ecomp += ncomp;
             if (last_idx) last_idx[(int64_t)py * width + px] = (int32_t)last;
             for (int ch = 0; ch < 3; ++ch) image[ch * HW + (int64_t)py * width + px] = C[ch];
             if (sig) {
@@ -583,7 +591,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
         }
     }
     if (loss) *loss = lsum / (3.0 * (double)HW);
-    if (counts) { counts[0] = efwd; counts[1] = ebwd; }
+    if (counts) { counts[0] = efwd; counts[1] = ebwd; counts[2] = ecomp; }
     if (sig) *sig = h;
     free(comp);
     free(buf);

@@ -1,0 +1,182 @@
+"""Stage-by-stage parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Test infrastructure: imported by the GPU tests and by the smoke check only.
+Every comparison feeds both sides the same seeded inputs; expected values come
+from the oracle alone.
+
+Bars (the method's statement): tile lists, sort order and compacted index sets
+bit-exact; images within 1e-5 absolute; gradients within relative 2e-3 with an
+absolute floor of 1e-6.  Projection records, evaluation counts and the touched
+set are compared bit for bit as well, since the forward decisions are
+specified to be reproducible (IEEE operations in a fixed order and one
+portable exp on both sides).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from differentiable_rasterizer_gb300 import pipeline, scenes
+
+IMG_ATOL = 1e-5
+GRAD_RTOL = 2e-3
+GRAD_ATOL = 1e-6
+
+
+def oracle_targets(sc, prec="f32"):
+    """Targets [V,3,H,W]: the scene's uniform noise, or the oracle's render of the perturbed scene."""
+    if sc.target_kind == "uniform":
+        return np.ascontiguousarray(sc.target_uniform, np.float32)
+    out = []
+    for cam in sc.cameras:
+        pr = oracle.project(sc.perturbed_params, sc.sh_degree, cam, sc.opts, prec)
+        out.append(oracle.render(pr, cam, sc.opts, prec=prec)["image"])
+    return np.ascontiguousarray(np.stack(out), np.float32)
+
+
+def bits(a):
+    a = np.ascontiguousarray(a)
+    return a.view(np.uint32) if a.dtype == np.float32 else a.view(np.uint64)
+
+
+def grad_report(gpu, ref, rtol=GRAD_RTOL, atol=GRAD_ATOL):
+    """(ok, stats) for |gpu - ref| <= atol + rtol |ref| elementwise."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(gpu - ref)
+    ok = err <= atol + rtol * np.abs(ref)
+    scale = np.abs(ref).max() if ref.size else 0.0
+    big = np.abs(ref) > 1e-3 * scale
+    rel_big = (err[big] / np.abs(ref[big])).max() if big.any() else 0.0
+    return bool(ok.all()), dict(n=int(ref.size), bad=int((~ok).sum()), max_abs_err=float(err.max(initial=0.0)),
+                                max_abs_ref=float(scale), max_rel_err_significant=float(rel_big),
+                                n_significant=int(big.sum()))
+
+
+def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print):
+    """Runs one full step stage by stage on the GPU and checks every stage against the oracle.
+
+    Returns a dict of statistics; raises AssertionError on any mismatch."""
+    stats = {}
+    if targets is None:
+        targets = oracle_targets(sc)
+    V, n = sc.n_views, sc.n
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device=device)
+    tgt_dev = torch.from_numpy(targets).to(device)
+    P = sc.params.shape[0]
+
+    # --- A1 projection: records bit-exact
+    tr.project()
+    torch.cuda.synchronize()
+    rec = tr.rec.cpu().numpy()
+    tt = tr.tiles_touched.cpu().numpy().view(np.uint32)
+    rect = tr.rect.cpu().numpy().view(np.uint16)
+    depth = tr.depth.cpu().numpy()
+    oprojs = []
+    for v, cam in enumerate(sc.cameras):
+        pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
+        oprojs.append(pr)
+        vis = pr["visible"].astype(bool)
+        assert np.array_equal(tt[v] > 0, vis), f"view {v}: visibility differs at {np.flatnonzero((tt[v] > 0) != vis)[:10]}"
+        o = pr["rec"][vis]
+        exp = np.stack([o[:, 0], o[:, 1], np.float32(-0.5) * o[:, 2], o[:, 3], np.float32(-0.5) * o[:, 4], o[:, 5],
+                        o[:, 6], o[:, 7], o[:, 8], o[:, 9]], 1).astype(np.float32)
+        got = rec[v][vis][:, :10]
+        diff = np.flatnonzero((bits(got) != bits(exp)).any(1))
+        assert diff.size == 0, f"view {v}: projection records differ for {diff.size} Gaussians, e.g. " \
+                               f"{np.flatnonzero(vis)[diff[:3]]}: gpu {got[diff[:1]]} oracle {exp[diff[:1]]}"
+        assert np.array_equal(rect[v][vis].astype(np.int32), pr["rect"][vis])
+        area = (pr["rect"][vis, 2] - pr["rect"][vis, 0]) * (pr["rect"][vis, 3] - pr["rect"][vis, 1])
+        assert np.array_equal(tt[v][vis], area.astype(np.uint32))
+        assert np.array_equal(bits(depth[v][vis]), bits(o[:, 9]))
+    stats["visible"] = [int((tt[v] > 0).sum()) for v in range(V)]
+
+    # --- A2 binning + sort: keys, ids and ranges bit-exact
+    N = tr.bin_sort()
+    torch.cuda.synchronize()
+    keys = tr.keys[:N].cpu().numpy().view(np.uint64)
+    ids = tr.ids[:N].cpu().numpy().view(np.uint32)
+    ranges = tr.ranges.cpu().numpy().view(np.uint32).reshape(V, -1, 2)
+    tiles = tr.tiles
+    base = 0
+    for v, cam in enumerate(sc.cameras):
+        off, oids = oracle.tile_lists(oprojs[v], cam)
+        m = oids.size
+        assert np.array_equal(ids[base:base + m], oids.astype(np.uint32)), f"view {v}: sorted ids differ"
+        tile_of = np.repeat(np.arange(tiles, dtype=np.uint64), np.diff(off).astype(np.int64))
+        dbits = bits(oprojs[v]["rec"][oids, 9]).astype(np.uint64)
+        exp_keys = ((np.uint64(v * tiles) + tile_of) << np.uint64(32)) | dbits
+        assert np.array_equal(keys[base:base + m], exp_keys), f"view {v}: sorted keys differ"
+        assert np.array_equal(ranges[v][:, 0], (off[:-1] + base).astype(np.uint32)), f"view {v}: range starts"
+        assert np.array_equal(ranges[v][:, 1], (off[1:] + base).astype(np.uint32)), f"view {v}: range ends"
+        base += m
+    assert base == N
+    stats["instances"] = int(N)
+
+    # --- A3 fused raster: image, loss, counts, touched, per-Gaussian 2D gradients
+    tr.eval_counts.zero_()
+    tr.raster(tgt_dev)
+    torch.cuda.synchronize()
+    img = tr.image.cpu().numpy()
+    loss = tr.loss.cpu().numpy()
+    g2d = tr.grad2d.cpu().numpy()[..., :9].copy()
+    touched = tr.touched.cpu().numpy().copy()
+    counts = tr.eval_counts.cpu().numpy()
+    efwd = ebwd = ecomp = 0
+    orend = []
+    for v, cam in enumerate(sc.cameras):
+        out = oracle.render(oprojs[v], cam, sc.opts, target=targets[v])
+        orend.append(out)
+        d = np.abs(img[v].astype(np.float64) - out["image"])
+        stats.setdefault("img_max_abs_err", []).append(float(d.max()))
+        stats.setdefault("img_exact_frac", []).append(float((bits(img[v]) == bits(out["image"])).mean()))
+        assert d.max() <= IMG_ATOL, f"view {v}: image max abs err {d.max()}"
+        assert abs(loss[v] - out["loss"]) <= 1e-9 * max(1.0, abs(out["loss"])), (loss[v], out["loss"])
+        assert np.array_equal(touched[v], out["touched"]), f"view {v}: touched sets differ"
+        ok, st = grad_report(g2d[v][out["touched"] > 0], out["grad2d"][out["touched"] > 0])
+        stats.setdefault("grad2d", []).append(st)
+        assert ok, f"view {v}: grad2d out of tolerance {st}"
+        efwd += out["e_fwd"]
+        ebwd += out["e_bwd"]
+        ecomp += out["e_comp"]
+    assert int(counts[0]) == efwd and int(counts[1]) == ebwd and int(counts[2]) == ecomp, (counts, efwd, ebwd, ecomp)
+    stats["e_fwd"], stats["e_bwd"], stats["e_comp"] = efwd, ebwd, ecomp
+
+    # --- A4 compaction + VJP + scatter-add
+    tr.compact()
+    torch.cuda.synchronize()
+    idx = tr.idx.cpu().numpy().view(np.uint32)
+    n_idx = tr.n_idx.cpu().numpy()
+    ref_grads = np.zeros((P, n), np.float64)
+    for v, cam in enumerate(sc.cameras):
+        exp_idx = oracle.compact(orend[v]["touched"])
+        assert n_idx[v] == exp_idx.size and np.array_equal(idx[v][:n_idx[v]], exp_idx), f"view {v}: compacted list"
+        oracle.vjp(sc.params, sc.sh_degree, cam, sc.opts, orend[v]["grad2d"], orend[v]["touched"],
+                   oprojs[v]["clamp"], ref_grads)
+    union = oracle.compact(np.any(np.stack([o["touched"] for o in orend]), 0).astype(np.uint8))
+    assert n_idx[V] == union.size and np.array_equal(idx[V][:n_idx[V]], union), "union list"
+    grads = tr.grads.cpu().numpy()
+    ok, st = grad_report(grads, ref_grads)
+    stats["grads"] = st
+    assert ok, f"dense gradients out of tolerance {st}"
+    assert not tr.grad2d.any().item() and not tr.touched.any().item(), "grad2d / touched not cleared"
+
+    # --- A5 deferred Adam, fed the GPU's gradients: bit-exact with the oracle
+    if check_adam:
+        p_o = sc.params.copy()
+        m_o = np.zeros_like(p_o)
+        v_o = np.zeros_like(p_o)
+        last_o = np.zeros(n, np.int32)
+        g_o = grads.astype(np.float32).copy()
+        lr_rows = scenes.lr_rows(sc.lr, sc.sh_degree)
+        oracle.adam_deferred(p_o, m_o, v_o, g_o, last_o, lr_rows, union, 1, tr.betas[0], tr.betas[1], tr.eps)
+        tr.adam(1)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(tr.params.cpu().numpy()), bits(p_o)), "Adam params"
+        assert np.array_equal(bits(tr.adam_m.cpu().numpy()), bits(m_o)), "Adam m"
+        assert np.array_equal(bits(tr.adam_v.cpu().numpy()), bits(v_o)), "Adam v"
+        assert np.array_equal(tr.last_step.cpu().numpy(), last_o), "last_step"
+        assert not tr.grads.any().item(), "grads not cleared"
+    log(f"[parity] {sc.name}: {stats}")
+    return stats

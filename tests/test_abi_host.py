@@ -1,0 +1,90 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it builds, loads, exports
+every entry point that include/gs.h declares, answers workspace queries, and
+rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from differentiable_rasterizer_gb300 import build, abi
+    build.build()
+    return abi.lib()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "gs.h")).read()
+    return sorted(set(re.findall(r"GS_API\s+[\w\s\*]*?\b(gs_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    syms = _declared_symbols()
+    for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_static_helpers(L):
+    from differentiable_rasterizer_gb300 import abi
+    assert abi.gs_param_rows(0) == 14 and abi.gs_param_rows(3) == 59 and abi.gs_param_rows(2) == -1
+    assert abi.gs_num_tiles(1920, 1080) == 120 * 68
+    assert abi.gs_num_tiles(64, 64) == 16
+    assert "sm_103a" in abi.gs_version()
+    assert L.gs_error_string(2) == b"instance capacity too small"
+
+
+def test_workspace_queries(L):
+    from differentiable_rasterizer_gb300 import abi
+    a = abi.gs_bin_sort_ws_bytes(1000, 1, 64, 64, 4000)
+    b = abi.gs_bin_sort_ws_bytes(1000, 1, 64, 64, 400000)
+    assert 0 < a < b and a % 256 == 0
+    assert abi.gs_grad_compact_ws_bytes(10 ** 6) >= 10 ** 6   # union flags
+    assert abi.gs_grad_compact_ws_bytes(0) >= 0
+
+
+def test_invalid_arguments_are_rejected_on_the_host(L):
+    from differentiable_rasterizer_gb300 import abi, scenes
+    sc = scenes.make_scene("tiny")
+    cams = abi.cameras(sc.cameras)
+    opts = abi.render_opts(sc.opts)
+    proj = abi.GsProj(16, 16, 16, 16)
+    # NULL params / bad degree / bad view count
+    assert L.gs_project(None, 10, 0, cams, 1, ctypes.byref(opts), ctypes.byref(proj), None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_project(16, 10, 2, cams, 1, ctypes.byref(opts), ctypes.byref(proj), None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_project(16, 10, 0, cams, 0, ctypes.byref(opts), ctypes.byref(proj), None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_project(16, 10, 0, cams, 33, ctypes.byref(opts), ctypes.byref(proj), None) == abi.GS_ERR_INVALID_ARG
+    # mixed resolutions
+    two = abi.cameras([sc.cameras[0], scenes.Camera(sc.cameras[0].R, sc.cameras[0].t, 64, 64, 32, 32, 64, 32)])
+    assert L.gs_project(16, 10, 0, two, 2, ctypes.byref(opts), ctypes.byref(proj), None) == abi.GS_ERR_INVALID_ARG
+    # misaligned record buffer
+    bad = abi.GsProj(20, 16, 16, 16)
+    assert L.gs_project(16, 10, 0, cams, 1, ctypes.byref(opts), ctypes.byref(bad), None) == abi.GS_ERR_INVALID_ARG
+    # workspace too small
+    cnt = ctypes.c_int64(0)
+    sz = ctypes.c_size_t(8)
+    assert L.gs_bin_sort(ctypes.byref(proj), 10, 1, 64, 64, 100, 16, 16, 16, ctypes.byref(cnt), 16,
+                         ctypes.byref(sz), None) == abi.GS_ERR_INVALID_ARG
+    # Adam: t must be >= 1
+    lr = (ctypes.c_float * 5)(1, 1, 1, 1, 1)
+    assert L.gs_adam_deferred(16, 16, 16, 16, 16, 10, 0, 16, 16, 0, lr, ctypes.c_float(0.9), ctypes.c_float(0.999),
+                              ctypes.c_float(1e-8), 0, None) == abi.GS_ERR_INVALID_ARG
+    # raster with a target but no gradient buffers
+    assert L.gs_raster_fused_fwd_bwd(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None, None,
+                                     None, None, None) == abi.GS_ERR_INVALID_ARG
+
+
+def test_binding_raises_without_the_library(tmp_path, monkeypatch):
+    from differentiable_rasterizer_gb300 import abi
+    monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="CUDA library missing"):
+        abi.lib()

@@ -1,0 +1,170 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, stage by
+stage, on seeded inputs (tiny, ragged, dense, multi-view, degree-3, small,
+medium), plus edge cases (no Gaussians, everything culled, instance capacity
+growth), the deferred Adam with catch-up and flush, and several training steps."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from differentiable_rasterizer_gb300 import pipeline, scenes
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from differentiable_rasterizer_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _variant(sc, **kw):
+    sc.opts = dict(sc.opts, **kw)
+    return sc
+
+
+def test_tiny():
+    parity.run_stage_parity(scenes.make_scene("tiny"))
+
+
+def test_tiny_exclude_crossing_and_background():
+    parity.run_stage_parity(_variant(scenes.make_scene("tiny"), exclude_crossing=1, bg=(0.25, 0.5, 0.75)))
+
+
+def test_ragged_resolution_partial_tiles():
+    sc = scenes.make_scene("tiny")
+    cam = sc.cameras[0]
+    sc.cameras = [scenes.Camera(cam.R, cam.t, 64.0, 64.0, 35.0, 22.5, 70, 45)]
+    sc.target_uniform = np.random.default_rng(9).uniform(0, 1, (1, 3, 45, 70)).astype(np.float32)
+    parity.run_stage_parity(sc)
+
+
+def test_dense_lists_span_several_chunks_and_stop_early():
+    """~4000 large, fairly opaque Gaussians on 64x64: tile lists longer than one
+    shared-memory chunk, many pixels reach T < 1e-4 mid-list."""
+    sc = scenes.random_small_scene(21, n=4000, width=64, height=64, sh_degree=0, log_lo=-3.0, log_hi=-1.8,
+                                   logit_mu=1.0, spread=1.2)
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] > 16 * 600
+    assert st["e_fwd"] < st["instances"] * 256   # early stops happened
+
+
+def test_multi_view_small_reduced():
+    sc = scenes.make_scene("small", n=20000)
+    base = sc.cameras[0]
+    cams = []
+    for k, ang in enumerate((-0.15, 0.0, 0.2)):
+        c, s = math.cos(ang), math.sin(ang)
+        R = np.array([[c, 0, s], [0, 1, 0], [-s, 0, c]], np.float32)
+        cams.append(scenes.Camera(R, np.array([0.3 * k, 0, 0.5], np.float32), 250.0, 250.0, 160.0, 90.0, 320, 180))
+    sc.cameras = cams
+    parity.run_stage_parity(sc)
+
+
+def test_degree3_medium_recipe_reduced():
+    sc = scenes.make_scene("medium", n=60000)
+    c = sc.cameras[0]
+    sc.cameras = [scenes.Camera(c.R, c.t, 350.0, 350.0, 240.0, 135.0, 480, 270)]
+    parity.run_stage_parity(sc)
+
+
+def test_small_full():
+    parity.run_stage_parity(scenes.make_scene("small"))
+
+
+@pytest.mark.slow
+def test_medium_full():
+    parity.run_stage_parity(scenes.make_scene("medium"))
+
+
+def test_no_gaussians_and_all_culled():
+    sc = scenes.make_scene("tiny", n=1)
+    sc.params = sc.params[:, :0].copy()
+    tr = pipeline.GaussianTrainer(sc.params, 0, sc.cameras, _variant(sc, bg=(0.1, 0.2, 0.3)).opts, sc.lr)
+    tgt = torch.zeros((1, 3, 64, 64), device="cuda")
+    tr.train_step(tgt)
+    torch.cuda.synchronize()
+    img = tr.image.cpu().numpy()
+    assert np.allclose(img[0, 0], 0.1) and np.allclose(img[0, 2], 0.3)
+    assert tr.n_instances == 0
+    # everything behind the camera
+    sc = scenes.make_scene("tiny")
+    sc.params[2] = -3.0
+    tr = pipeline.GaussianTrainer(sc.params, 0, sc.cameras, sc.opts, sc.lr)
+    tr.train_step(torch.from_numpy(sc.target_uniform).cuda())
+    torch.cuda.synchronize()
+    assert tr.n_instances == 0 and tr.n_idx.cpu().numpy().sum() == 0
+    assert np.array_equal(tr.params.cpu().numpy(), sc.params)
+
+
+def test_capacity_growth_retries():
+    sc = scenes.make_scene("tiny")
+    tr = pipeline.GaussianTrainer(sc.params, 0, sc.cameras, sc.opts, sc.lr, capacity=16)
+    tr.project()
+    cnt = tr.bin_sort()
+    assert tr.capacity >= cnt > 16
+    off, ids = oracle.tile_lists(oracle.project(sc.params, 0, sc.cameras[0], sc.opts), sc.cameras[0])
+    assert cnt == ids.size
+    assert np.array_equal(tr.ids[:cnt].cpu().numpy().view(np.uint32), ids.astype(np.uint32))
+
+
+def test_adam_deferred_catch_up_and_flush_bitexact():
+    rng = np.random.default_rng(5)
+    n, sh = 5000, 3
+    P = scenes.PARAM_ROWS[sh]
+    p0 = rng.standard_normal((P, n)).astype(np.float32)
+    lr = (1e-3, 2e-3, 3e-3, 4e-2, 5e-3)
+    lr_rows = scenes.lr_rows(lr, sh)
+    cams = scenes.make_scene("tiny").cameras
+    tr = pipeline.GaussianTrainer(p0, sh, cams, dict(scenes.DEFAULT_OPTS), lr)
+    po, mo, vo = p0.copy(), np.zeros_like(p0), np.zeros_like(p0)
+    lo = np.zeros(n, np.int32)
+    for t in range(1, 9):
+        mask = rng.uniform(size=n) < (0.02 if t < 6 else 0.5)
+        idx = np.flatnonzero(mask).astype(np.uint32)
+        g = (rng.standard_normal((P, n)) * mask).astype(np.float32)
+        tr.grads.copy_(torch.from_numpy(g))
+        tr.idx[tr.V, :idx.size].copy_(torch.from_numpy(idx.view(np.int32)))
+        tr.n_idx[tr.V] = idx.size
+        tr.adam(t)
+        go = g.copy()
+        oracle.adam_deferred(po, mo, vo, go, lo, lr_rows, idx, t, 0.9, 0.999, 1e-8)
+    torch.cuda.synchronize()
+    assert np.array_equal(parity.bits(tr.params.cpu().numpy()), parity.bits(po))
+    assert np.array_equal(parity.bits(tr.adam_m.cpu().numpy()), parity.bits(mo))
+    assert np.array_equal(tr.last_step.cpu().numpy(), lo)
+    tr.adam(8, flush=True)
+    oracle.adam_deferred(po, mo, vo, go, lo, lr_rows, None, 8, 0.9, 0.999, 1e-8, flush=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(parity.bits(tr.params.cpu().numpy()), parity.bits(po))
+    assert np.array_equal(parity.bits(tr.adam_v.cpu().numpy()), parity.bits(vo))
+    assert (tr.last_step.cpu().numpy() == 8).all()
+
+
+def test_three_training_steps_track_the_oracle():
+    """Step t+1 checked against the oracle started from the GPU's state after step t."""
+    sc = scenes.make_scene("small", n=20000)
+    c = sc.cameras[0]
+    sc.cameras = [scenes.Camera(c.R, c.t, 250.0, 250.0, 160.0, 90.0, 320, 180)]
+    targets = parity.oracle_targets(sc)
+    tr = pipeline.GaussianTrainer(sc.params, 0, sc.cameras, sc.opts, sc.lr)
+    tgt = torch.from_numpy(targets).cuda()
+    for step in range(3):
+        p_before = tr.params.cpu().numpy()
+        tr.train_step(tgt)
+        torch.cuda.synchronize()
+        pr = oracle.project(p_before, 0, sc.cameras[0], sc.opts)
+        out = oracle.render(pr, sc.cameras[0], sc.opts, target=targets[0])
+        assert np.abs(tr.image.cpu().numpy()[0] - out["image"]).max() <= parity.IMG_ATOL
+        assert abs(tr.loss.item() - out["loss"]) <= 1e-9
+        assert tr.last_step.cpu().numpy().max() == step + 1
+    # deferred state equals dense after a flush: every Gaussian reaches step 3
+    tr.flush()
+    torch.cuda.synchronize()
+    assert (tr.last_step.cpu().numpy() == 3).all()
