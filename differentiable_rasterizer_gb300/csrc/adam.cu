@@ -3,9 +3,9 @@
 // unnecessary memory accesses for Gaussians with zero gradients"), made exactly
 // equal to dense Adam by replaying the skipped zero-gradient steps first.
 //
-// One thread per listed Gaussian walks its parameter rows (coalesced across the
-// warp when the list is dense).  The bias corrections of the current step are
-// computed once per block; replayed steps compute their own.  A row whose
+// One thread per (parameter row, listed Gaussian), coalesced across the warp when
+// the list is dense.  The bias corrections of the current step are computed once
+// per block; replayed steps compute their own.  A row whose
 // moments are both +0 is left as is during replay: a zero-gradient step from a
 // zero state changes nothing, bit for bit.
 #include "gs_common.cuh"
@@ -24,11 +24,11 @@ __device__ __forceinline__ double powi_binary(double b, int e)
 }
 
 struct AdamArgs {
-    float* params;
-    float* grads;
-    float* m;
-    float* v;
-    int32_t* last_step;
+    float* __restrict__ params;
+    float* __restrict__ grads;
+    float* __restrict__ m;
+    float* __restrict__ v;
+    int32_t* __restrict__ last_step;
     int64_t n;
     int32_t rows;
     const uint32_t* idx;
@@ -52,6 +52,9 @@ __device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, 
     v = vn;
 }
 
+// One thread per (parameter row, listed Gaussian): every thread does its own
+// 4 loads and 4 stores, so the whole list streams through HBM at full width.
+// last_step is only read here; stamp_kernel writes it afterwards.
 __global__ void __launch_bounds__(256) adam_deferred_kernel(AdamArgs a)
 {
     __shared__ float s_bc[2];
@@ -62,28 +65,35 @@ __global__ void __launch_bounds__(256) adam_deferred_kernel(AdamArgs a)
     __syncthreads();
     const float bc1t = s_bc[0], bc2t = s_bc[1];
     const int64_t count = a.flush ? a.n : *a.n_idx;
+    const int r = blockIdx.y;
+    const float lr = a.lr[row_group(r)];
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t g = a.flush ? i : (int64_t)a.idx[i];
         const int s = a.last_step[g];
         if (s >= a.t) continue;
-        for (int r = 0; r < a.rows; ++r) {
-            const size_t e = (size_t)r * a.n + g;
-            float p = a.params[e], m = a.m[e], v = a.v[e];
-            const float lr = a.lr[row_group(r)];
-            for (int j = s + 1; j < a.t; ++j) {
-                if (__float_as_uint(m) == 0u && __float_as_uint(v) == 0u) break;   // zero state: replay is a no-op
-                const float bc1 = (float)(1.0 - powi_binary((double)a.b1, j));
-                const float bc2 = (float)(1.0 - powi_binary((double)a.b2, j));
-                adam_one(p, m, v, 0.0f, lr, a.b1, a.b2, a.eps, bc1, bc2);
-            }
-            const float gr = a.flush ? 0.0f : a.grads[e];
-            adam_one(p, m, v, gr, lr, a.b1, a.b2, a.eps, bc1t, bc2t);
-            a.params[e] = p;
-            a.m[e] = m;
-            a.v[e] = v;
-            if (!a.flush) a.grads[e] = 0.0f;
+        const size_t e = (size_t)r * a.n + g;
+        float p = a.params[e], m = a.m[e], v = a.v[e];
+        const float gr = a.flush ? 0.0f : a.grads[e];
+        for (int j = s + 1; j < a.t; ++j) {
+            if (__float_as_uint(m) == 0u && __float_as_uint(v) == 0u) break;   // zero state: replay is a no-op
+            const float bc1 = (float)(1.0 - powi_binary((double)a.b1, j));
+            const float bc2 = (float)(1.0 - powi_binary((double)a.b2, j));
+            adam_one(p, m, v, 0.0f, lr, a.b1, a.b2, a.eps, bc1, bc2);
         }
-        a.last_step[g] = a.t;
+        adam_one(p, m, v, gr, lr, a.b1, a.b2, a.eps, bc1t, bc2t);
+        a.params[e] = p;
+        a.m[e] = m;
+        a.v[e] = v;
+        if (!a.flush) a.grads[e] = 0.0f;
+    }
+}
+
+__global__ void __launch_bounds__(256) stamp_kernel(AdamArgs a)
+{
+    const int64_t count = a.flush ? a.n : *a.n_idx;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = a.flush ? i : (int64_t)a.idx[i];
+        if (a.last_step[g] < a.t) a.last_step[g] = a.t;
     }
 }
 
@@ -119,11 +129,18 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     int dev = 0, sms = 0;
     GS_CUDA_TRY(cudaGetDevice(&dev));
     GS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    // The list length lives on the device: size the grid for n and let threads
+    // beyond the list exit (grid-stride beyond 8 resident blocks per SM).
     const int threads = 256;
-    int64_t blocks = (n + threads - 1) / threads;
-    const int64_t cap = (int64_t)sms * 8;
-    if (blocks > cap) blocks = cap;
-    adam_deferred_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(a);
+    int64_t bx = (n + threads - 1) / threads;
+    const int64_t cap = ((int64_t)sms * 8 + rows - 1) / rows;
+    if (bx > cap) bx = cap;
+    cudaStream_t s = (cudaStream_t)stream;
+    adam_deferred_kernel<<<dim3((unsigned)bx, (unsigned)rows), threads, 0, s>>>(a);
+    GS_LAUNCH_CHECK();
+    int64_t bs = (n + threads - 1) / threads;
+    if (bs > (int64_t)sms * 8) bs = (int64_t)sms * 8;
+    stamp_kernel<<<(unsigned)bs, threads, 0, s>>>(a);
     GS_LAUNCH_CHECK();
     return GS_OK;
 }

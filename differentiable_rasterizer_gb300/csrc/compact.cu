@@ -27,15 +27,15 @@ __global__ void union_kernel(const uint8_t* __restrict__ touched, int64_t n, int
 }
 
 struct VjpArgs {
-    float* grad2d;
-    uint8_t* touched;
-    const float* params;
+    float* __restrict__ grad2d;
+    uint8_t* __restrict__ touched;
+    const float* __restrict__ params;
     int64_t n;
     float near_z, lowpass;
     int32_t tiles_x, tiles_y;
-    const uint32_t* idx_union;
-    const int64_t* n_union;
-    float* grads;
+    const uint32_t* __restrict__ idx_union;
+    const int64_t* __restrict__ n_union;
+    float* __restrict__ grads;
 };
 
 template <int DEG>
@@ -47,9 +47,12 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
     GaussParams<DEG> gp;
     gp.load(a.params, a.n, g);
     constexpr int P = GaussParams<DEG>::kRows;
+    // Current gradient values are loaded up front with the parameters, so the
+    // final write-back is a run of independent stores rather than P dependent
+    // read-modify-writes.
     float grad[P];
 #pragma unroll
-    for (int r = 0; r < P; ++r) grad[r] = 0.0f;
+    for (int r = 0; r < P; ++r) grad[r] = a.grads[(size_t)r * a.n + g];
     for (int v = 0; v < cs.n_views; ++v) {
         const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
         if (!a.touched[o]) continue;
@@ -66,10 +69,7 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
         a.touched[o] = 0;
     }
 #pragma unroll
-    for (int r = 0; r < P; ++r) {
-        float* dst = a.grads + (size_t)r * a.n + g;
-        *dst = *dst + grad[r];
-    }
+    for (int r = 0; r < P; ++r) a.grads[(size_t)r * a.n + g] = grad[r];
 }
 
 struct CompactWs {

@@ -15,7 +15,7 @@ struct ProjectArgs {
     const float* params;
     int64_t n;
     int32_t sh_degree;
-    float near_z, lowpass;
+    float near_z, lowpass, alpha_min;
     int32_t tiles_x, tiles_y;
     float4* rec;
     float* depth;
@@ -41,7 +41,10 @@ __global__ void __launch_bounds__(128) project_kernel(ProjectArgs a, CamSet cs)
         float4* r = a.rec + o * 3;
         r[0] = make_float4(po.mx, po.my, -0.5f * po.cA, po.cB);
         r[1] = make_float4(-0.5f * po.cC, po.opacity, po.col[0], po.col[1]);
-        r[2] = make_float4(po.col[2], po.depth, 0.0f, 0.0f);
+        // Rasterizer cut: a pixel with power < tau has alpha < alpha_min for sure
+        // (o * exp(tau) <= 0.99 alpha_min, with slack for logf and pexp rounding).
+        const float tau = po.opacity >= a.alpha_min ? logf(a.alpha_min / po.opacity) - 0.01f : INFINITY;
+        r[2] = make_float4(po.col[2], po.depth, tau, 0.0f);
         a.depth[o] = po.depth;
         a.rect[o] = make_ushort4((unsigned short)po.x0, (unsigned short)po.y0, (unsigned short)po.x1,
                                  (unsigned short)po.y1);
@@ -56,7 +59,7 @@ using namespace gs;
 extern "C" gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, const gs_camera* cams,
                                 int32_t n_views, const gs_render_opts* opts, const gs_proj* out, void* stream)
 {
-    if (!opts || !out || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
+    if (!opts_ok(opts) || !out || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
     if (param_rows(sh_degree) < 0) return GS_ERR_INVALID_ARG;
     gs_status st = check_views(cams, n_views);
     if (st != GS_OK) return st;
@@ -69,6 +72,7 @@ extern "C" gs_status gs_project(const float* params, int64_t n, int32_t sh_degre
     a.sh_degree = sh_degree;
     a.near_z = opts->near_z;
     a.lowpass = opts->lowpass;
+    a.alpha_min = opts->alpha_min;
     a.tiles_x = tiles_x_of(cams[0].width);
     a.tiles_y = tiles_y_of(cams[0].height);
     a.rec = reinterpret_cast<float4*>(out->rec);

@@ -31,6 +31,7 @@ struct RasterArgs {
     int64_t n;
     int32_t W, H, tiles_x, tiles, n_views;
     float alpha_min, alpha_max, t_min, bg0, bg1, bg2, inv3hw;
+    double inv3hw_d;   // 1 / (3 H W) for the loss mean
     int32_t exclude_crossing;
 };
 
@@ -41,10 +42,38 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Sums eight values over the warp with a butterfly that halves the live values
+// at each of the first three stages (each lane sends the half its partner
+// keeps): 4 + 2 + 1 + 1 + 1 shuffles instead of 8 x 5.  Afterwards every lane L
+// holds the full sum of value (L >> 2) & 7.
+__device__ __forceinline__ float warp_reduce8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                              float v7, int lane)
+{
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float a0 = (h16 ? v4 : v0) + __shfl_xor_sync(0xffffffffu, h16 ? v0 : v4, 16);
+    float a1 = (h16 ? v5 : v1) + __shfl_xor_sync(0xffffffffu, h16 ? v1 : v5, 16);
+    float a2 = (h16 ? v6 : v2) + __shfl_xor_sync(0xffffffffu, h16 ? v2 : v6, 16);
+    float a3 = (h16 ? v7 : v3) + __shfl_xor_sync(0xffffffffu, h16 ? v3 : v7, 16);
+    float b0 = (h8 ? a2 : a0) + __shfl_xor_sync(0xffffffffu, h8 ? a0 : a2, 8);
+    float b1 = (h8 ? a3 : a1) + __shfl_xor_sync(0xffffffffu, h8 ? a1 : a3, 8);
+    float c0 = (h4 ? b1 : b0) + __shfl_xor_sync(0xffffffffu, h4 ? b0 : b1, 4);
+    c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
+    c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
+    return c0;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 template <bool kBackward>
 __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a)
 {
-    __shared__ float4 s_r0[kChunk], s_r1[kChunk], s_r2[kChunk];
+    __shared__ float4 s_r0[kChunk], s_r1[kChunk];
+    __shared__ float2 s_r2[kChunk];   // (blue, tau)
     __shared__ uint32_t s_id[kChunk];
     __shared__ double s_red_d[kTileThreads / 32];
     __shared__ unsigned long long s_red_u[3][kTileThreads / 32];
@@ -64,52 +93,60 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const int len = (int)(range.y - range.x);
     const float4* __restrict__ recv = a.rec + (size_t)v * (size_t)a.n * 3;
 
-    // ------------------------------------------------------------- forward
-    float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
-    int last = -1, nev = 0, ncomp = 0;
-    bool done = !inside;
-    int resident = -1;   // chunk currently in shared memory
-    const int nchunks = (len + kChunk - 1) / kChunk;
-    for (int c = 0; c < nchunks; ++c) {
-        if (__syncthreads_and(done)) break;
-        const int base = c * kChunk;
+    auto stage = [&](int base) {
         const int k = base + threadIdx.x;
         if (k < len) {
             const uint32_t g = __ldg(a.ids + lo + k);
             const float4* r = recv + (size_t)g * 3;
             s_r0[threadIdx.x] = __ldg(r);
             s_r1[threadIdx.x] = __ldg(r + 1);
-            s_r2[threadIdx.x] = __ldg(r + 2);
+            const float4 r2 = __ldg(r + 2);
+            s_r2[threadIdx.x] = make_float2(r2.x, r2.z);
             s_id[threadIdx.x] = g;
         }
+    };
+
+    // ------------------------------------------------------------- forward
+    float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
+    int last = -1, ncomp = 0;
+    int stop = -1;                      // list index where this pixel stopped, -1 if it never did
+    bool done = !inside;
+    int resident = -1;                  // chunk currently in shared memory
+    const int nchunks = (len + kChunk - 1) / kChunk;
+    for (int c = 0; c < nchunks; ++c) {
+        if (__syncthreads_and(done)) break;
+        const int base = c * kChunk;
+        stage(base);
         resident = c;
         __syncthreads();
         const int cnt = min(kChunk, len - base);
         if (!done) {
             for (int j = 0; j < cnt; ++j) {
-                ++nev;
                 const float4 r0 = s_r0[j];
                 const float dx = pxf - r0.x, dy = pyf - r0.y;
                 const float4 r1 = s_r1[j];
                 // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
                 const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                if (power > 0.0f) continue;
-                const float araw = r1.y * pexp(power);
+                const float2 r2 = s_r2[j];
+                // power > 0 is skipped by definition; power < tau has alpha < alpha_min
+                if (power > 0.0f || power < r2.y) continue;
+                const float araw = r1.y * pexp_neg(power);
                 const float alpha = fminf(a.alpha_max, araw);
                 if (alpha < a.alpha_min) continue;
                 const float Tn = T * (1.0f - alpha);
-                if (a.exclude_crossing && Tn < a.t_min) { done = true; break; }
+                if (a.exclude_crossing && Tn < a.t_min) { done = true; stop = base + j; break; }
                 const float wgt = alpha * T;
                 C0 = C0 + r1.z * wgt;
                 C1 = C1 + r1.w * wgt;
-                C2 = C2 + s_r2[j].x * wgt;
+                C2 = C2 + r2.x * wgt;
                 T = Tn;
                 last = base + j;
                 ++ncomp;
-                if (!a.exclude_crossing && T < a.t_min) { done = true; break; }
+                if (!a.exclude_crossing && T < a.t_min) { done = true; stop = base + j; break; }
             }
         }
     }
+    const int nev = inside ? (stop >= 0 ? stop + 1 : len) : 0;
     C0 = C0 + T * a.bg0;
     C1 = C1 + T * a.bg1;
     C2 = C2 + T * a.bg2;
@@ -132,6 +169,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         }
     }
     // block reductions: loss, evaluation counts, last composited index
+    int warp_last;
     {
         unsigned long long ef = (unsigned long long)nev, eb = (unsigned long long)(last + 1);
         unsigned long long ec = (unsigned long long)ncomp;
@@ -144,6 +182,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             ec += __shfl_xor_sync(0xffffffffu, ec, o);
             ml = max(ml, __shfl_xor_sync(0xffffffffu, ml, o));
         }
+        warp_last = ml;
         if (lane == 0) {
             s_red_d[warp] = lsum;
             s_red_u[0][warp] = ef;
@@ -164,7 +203,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             ec += s_red_u[2][w];
             max_last = max(max_last, s_max_last[w]);
         }
-        if (kBackward && ls != 0.0) atomicAdd(a.loss + v, ls);
+        if (kBackward && ls != 0.0) atomicAdd(a.loss + v, ls * a.inv3hw_d);
         if (a.counts) {
             atomicAdd(a.counts, ef);
             atomicAdd(a.counts + 1, eb);
@@ -182,82 +221,69 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     float Tcur = T;
     float* __restrict__ g2v = a.grad2d + (size_t)v * (size_t)a.n * GS_GRAD2D_STRIDE;
     uint8_t* __restrict__ touchv = a.touched + (size_t)v * (size_t)a.n;
+    const int red_slot = (lane >> 2) & 7;   // component this lane holds after warp_reduce8
     for (int c = max_last / kChunk; c >= 0; --c) {
         const int base = c * kChunk;
         if (c != resident) {
             __syncthreads();   // every thread is done reading the resident chunk
-            const int k = base + threadIdx.x;
-            if (k < len) {
-                const uint32_t g = __ldg(a.ids + lo + k);
-                const float4* r = recv + (size_t)g * 3;
-                s_r0[threadIdx.x] = __ldg(r);
-                s_r1[threadIdx.x] = __ldg(r + 1);
-                s_r2[threadIdx.x] = __ldg(r + 2);
-                s_id[threadIdx.x] = g;
-            }
+            stage(base);
             resident = c;
             __syncthreads();
         }
-        const int jtop = min(kChunk - 1, max_last - base);
+        // this warp has nothing composited beyond warp_last
+        const int jtop = min(kChunk - 1, warp_last - base);
         for (int j = jtop; j >= 0; --j) {
             const int i = base + j;
             float gm0 = 0.0f, gm1 = 0.0f, gA = 0.0f, gB = 0.0f, gC = 0.0f, go = 0.0f;
             float gr = 0.0f, gg = 0.0f, gb = 0.0f;
             bool contrib = false;
-            if (i <= last) {
-                const float4 r0 = s_r0[j];
-                const float dx = pxf - r0.x, dy = pyf - r0.y;
-                const float4 r1 = s_r1[j];
-                const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                if (power <= 0.0f) {
-                    const float G = pexp(power);
-                    const float araw = r1.y * G;
-                    const float alpha = fminf(a.alpha_max, araw);
-                    if (alpha >= a.alpha_min) {
-                        contrib = true;
-                        const float cb = s_r2[j].x;
-                        const float oma = 1.0f - alpha;
-                        const float inv_oma = __frcp_rn(oma);
-                        const float Ti = Tcur * inv_oma;
-                        const float wgt = alpha * Ti;
-                        gr = g0 * wgt;
-                        gg = g1 * wgt;
-                        gb = g2c * wgt;
-                        const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
-                        const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
-                        const float dalpha = __fmaf_rn(Ti, dotc, -dots * inv_oma);
-                        S0 = __fmaf_rn(r1.z, wgt, S0);
-                        S1 = __fmaf_rn(r1.w, wgt, S1);
-                        S2 = __fmaf_rn(cb, wgt, S2);
-                        Tcur = Ti;
-                        if (araw <= a.alpha_max) {
-                            go = dalpha * G;
-                            const float dp = dalpha * alpha;
-                            // d power / d(A, B, C) = (-dx^2/2, -dx dy, -dy^2/2);
-                            // d power / d mean2d = (A dx + B dy, B dx + C dy), A = -2 r0.z, C = -2 r1.x
-                            const float dxdy = dx * dy;
-                            gA = -0.5f * dp * dx * dx;
-                            gB = -dp * dxdy;
-                            gC = -0.5f * dp * dy * dy;
-                            gm0 = dp * __fmaf_rn(-2.0f * r0.z, dx, r0.w * dy);
-                            gm1 = dp * __fmaf_rn(r0.w, dx, -2.0f * r1.x * dy);
-                        }
+            const float4 r0 = s_r0[j];
+            const float dx = pxf - r0.x, dy = pyf - r0.y;
+            const float4 r1 = s_r1[j];
+            const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+            const float2 r2 = s_r2[j];
+            if (i <= last && power <= 0.0f && power >= r2.y) {
+                const float G = pexp_neg(power);
+                const float araw = r1.y * G;
+                const float alpha = fminf(a.alpha_max, araw);
+                if (alpha >= a.alpha_min) {
+                    contrib = true;
+                    const float oma = 1.0f - alpha;
+                    const float inv_oma = rcp_approx(oma);
+                    const float Ti = Tcur * inv_oma;
+                    const float wgt = alpha * Ti;
+                    gr = g0 * wgt;
+                    gg = g1 * wgt;
+                    gb = g2c * wgt;
+                    const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * r2.x));
+                    const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
+                    const float dalpha = __fmaf_rn(Ti, dotc, -dots * inv_oma);
+                    S0 = __fmaf_rn(r1.z, wgt, S0);
+                    S1 = __fmaf_rn(r1.w, wgt, S1);
+                    S2 = __fmaf_rn(r2.x, wgt, S2);
+                    Tcur = Ti;
+                    if (araw <= a.alpha_max) {
+                        go = dalpha * G;
+                        const float dp = dalpha * alpha;
+                        // d power / d(A, B, C) = (-dx^2/2, -dx dy, -dy^2/2);
+                        // d power / d mean2d = (A dx + B dy, B dx + C dy), A = -2 r0.z, C = -2 r1.x
+                        const float hdp = -0.5f * dp;
+                        gA = hdp * dx * dx;
+                        gB = -dp * (dx * dy);
+                        gC = hdp * dy * dy;
+                        gm0 = dp * __fmaf_rn(-2.0f * r0.z, dx, r0.w * dy);
+                        gm1 = dp * __fmaf_rn(r0.w, dx, -2.0f * r1.x * dy);
                     }
                 }
             }
             if (__any_sync(0xffffffffu, contrib)) {
-                gm0 = warp_sum(gm0); gm1 = warp_sum(gm1);
-                gA = warp_sum(gA); gB = warp_sum(gB); gC = warp_sum(gC);
-                go = warp_sum(go);
-                gr = warp_sum(gr); gg = warp_sum(gg); gb = warp_sum(gb);
-                if (lane == 0) {
-                    const uint32_t gid = s_id[j];
-                    float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
-                    atomicAdd(reinterpret_cast<float4*>(dst), make_float4(gm0, gm1, gA, gB));
-                    atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(gC, go, gr, gg));
-                    atomicAdd(dst + 8, gb);
-                    touchv[gid] = 1;
-                }
+                const float s8 = warp_reduce8(gm0, gm1, gA, gB, gC, go, gr, gg, lane);
+                const float sb = warp_sum(gb);
+                const uint32_t gid = s_id[j];
+                float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
+                if ((lane & 3) == 0) atomicAdd(dst + red_slot, s8);
+                if (lane == 1) atomicAdd(dst + 8, sb);
+                if (lane == 2) touchv[gid] = 1;
             }
         }
     }
@@ -273,7 +299,7 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
                                              double* loss, float* grad2d, uint8_t* touched, uint64_t* eval_counts,
                                              void* stream)
 {
-    if (!proj || !tile_ranges || !opts || !image || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
+    if (!proj || !tile_ranges || !opts_ok(opts) || !image || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
     gs_status st = check_views(cams, n_views);
     if (st != GS_OK) return st;
     if (target && (!loss || (n > 0 && (!grad2d || !touched)))) return GS_ERR_INVALID_ARG;
@@ -302,7 +328,8 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
     a.bg0 = opts->bg[0];
     a.bg1 = opts->bg[1];
     a.bg2 = opts->bg[2];
-    a.inv3hw = (float)(1.0 / (3.0 * (double)W * (double)H));
+    a.inv3hw_d = 1.0 / (3.0 * (double)W * (double)H);
+    a.inv3hw = (float)a.inv3hw_d;
     a.exclude_crossing = opts->exclude_crossing ? 1 : 0;
     cudaStream_t s = (cudaStream_t)stream;
     const long long grid = (long long)a.tiles * n_views;

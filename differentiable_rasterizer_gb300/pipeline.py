@@ -86,14 +86,14 @@ class GaussianTrainer:
         """Kernels the library launches for one train_step (its launch structure:
         projection 1; bin/sort: offsets scan 3, emit 1, per radix pass histogram 1 +
         scan 3 + scatter 1, ranges 1; fused raster 1; compaction: 3 per view-list scan,
-        union 1, union scan 3, VJP 1; Adam 1).  Memsets and copies are not kernels."""
+        union 1, union scan 3, VJP 1; Adam 2).  Memsets and copies are not kernels."""
         V, n = self.V, self.n
         ntile_ids = V * self.tiles
         bits = 32 + max(1, int(ntile_ids - 1).bit_length())
         npass = (bits + 7) // 8
         sort = (3 if n * V else 0) + ((1 + 5 * npass + 1) if self.n_instances else 0)
         compact = (3 * V + 1 + 3 + 1) if n else 0
-        return (1 if n else 0) + sort + 1 + compact + (1 if n else 0)
+        return (1 if n else 0) + sort + 1 + compact + (2 if n else 0)
 
     def stream_handle(self):
         return torch.cuda.current_stream(self.device).cuda_stream

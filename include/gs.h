@@ -94,7 +94,9 @@ typedef struct gs_camera {
 /* Render options.  Defaults: near_z 0.2, lowpass 0.3 (px^2 added to the 2D
  * covariance diagonal), alpha_min 1/255 (skip below), alpha_max 0.99 (clamp),
  * t_min 1e-4 (stop once T falls below it; the Gaussian that crosses is
- * composited unless exclude_crossing = 1), bg = background colour. */
+ * composited unless exclude_crossing = 1), bg = background colour.
+ * Valid ranges (else GS_ERR_INVALID_ARG): 1e-30 <= alpha_min <= alpha_max < 1,
+ * alpha_max > 0, t_min >= 0, near_z > 0, lowpass >= 0. */
 typedef struct gs_render_opts {
     float near_z, lowpass, alpha_min, alpha_max, t_min;
     float bg[3];
@@ -104,8 +106,10 @@ typedef struct gs_render_opts {
 
 /* Per-view projected records, caller-allocated, each [n_views][n]:
  *   rec            3 float4 per (view, Gaussian), 16-byte aligned:
- *                  {mx, my, -A/2, B}, {-C/2, opacity, r, g}, {b, depth, 0, 0}
- *                  (mean in pixels, conic (A, B, C) = Sigma2D^-1, depth = z_c);
+ *                  {mx, my, -A/2, B}, {-C/2, opacity, r, g}, {b, depth, tau, 0}
+ *                  (mean in pixels, conic (A, B, C) = Sigma2D^-1, depth = z_c,
+ *                  tau = ln(alpha_min / opacity) - 0.01: any pixel with power
+ *                  below tau has alpha < alpha_min, +inf if opacity < alpha_min);
  *                  written only for visible Gaussians
  *   depth          float z_c (written only for visible Gaussians)
  *   rect           4 x uint16 tile bounds x0, y0, x1, y1, half-open, clipped
