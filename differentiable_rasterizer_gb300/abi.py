@@ -181,3 +181,15 @@ def gs_num_tiles(width, height) -> int:
 
 def gs_version() -> str:
     return lib().gs_version().decode()
+
+
+def gs_grad_compact_static(grad2d, touched, params, n, sh_degree, cams, n_views, opts, idx, n_idx, grads, stream):
+    """gs_grad_compact for callers that cannot allocate device memory: its scratch is a
+    fixed array inside the library (at most GS_COMPACT_STATIC_MAX_N Gaussians)."""
+    L = lib()
+    f = L.gs_grad_compact_static
+    if f.argtypes is None:
+        f.argtypes = [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P]
+        f.restype = ctypes.c_int
+    _check("gs_grad_compact_static", f(grad2d, touched, params, n, sh_degree, cams, n_views, ctypes.byref(opts), idx,
+                                       n_idx, grads, stream))

@@ -142,3 +142,63 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
     GS_LAUNCH_CHECK();
     return GS_OK;
 }
+
+// ---------------------------------------------------------------------------
+// gs_grad_compact_static: the same compaction + VJP + scatter-add for callers
+// that cannot allocate device memory at step time -- for example code embedded
+// in a host application that owns all device memory and offers no allocator,
+// or a deployment that fixes its memory budget at start-up and forbids any
+// cudaMalloc afterwards.  Its scratch is a file-scope device array sized for
+// GS_COMPACT_STATIC_MAX_N Gaussians, held by every GPU that loads this library
+// until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kAlign256(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr int64_t kStaticMaxN = GS_COMPACT_STATIC_MAX_N;
+// block sums of the scans (one u64 per 4096 items, plus the total) and the union flags
+constexpr size_t kStaticScratchBytes =
+    kAlign256((size_t)((kStaticMaxN + 4095) / 4096 + 1) * sizeof(unsigned long long)) + kAlign256((size_t)kStaticMaxN);
+
+__device__ __align__(256) unsigned char g_compact_scratch[kStaticScratchBytes];
+
+// Device address of g_compact_scratch per device ordinal.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device, with that device current, and cached.
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mutex;
+
+gs_status static_scratch(void** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GS_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GS_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_compact_scratch) != cudaSuccess || !p) return GS_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return GS_OK;
+}
+
+}  // namespace
+
+extern "C" gs_status gs_grad_compact_static(float* grad2d, uint8_t* touched, const float* params, int64_t n,
+                                            int32_t sh_degree, const gs_camera* cams, int32_t n_views,
+                                            const gs_render_opts* opts, uint32_t* idx, int64_t* n_idx, float* grads,
+                                            void* stream)
+{
+    if (n < 0 || n > kStaticMaxN) return GS_ERR_INVALID_ARG;
+    if (gs::compact_ws(n).bytes > kStaticScratchBytes) return GS_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const gs_status st = static_scratch(&scratch);
+    if (st != GS_OK) return st;
+    size_t bytes = kStaticScratchBytes;
+    return gs_grad_compact(grad2d, touched, params, n, sh_degree, cams, n_views, opts, idx, n_idx, grads, scratch,
+                           &bytes, stream);
+}

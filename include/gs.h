@@ -185,6 +185,31 @@ GS_API gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const float* p
                           const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
                           uint32_t* idx, int64_t* n_idx, float* grads, void* ws, size_t* ws_bytes, void* stream);
 
+/* Maximum Gaussian count of gs_grad_compact_static (its scratch: ~4.2 MB per GPU). */
+#define GS_COMPACT_STATIC_MAX_N (1 << 22)
+
+/* gs_grad_compact without a workspace argument, for callers that cannot
+ * allocate device memory while they run -- e.g. code embedded in a host
+ * application that owns all GPU memory and exposes no allocator, or a
+ * deployment that fixes its memory budget at start-up.  The pages have no
+ * counterpart; this is an interface convenience of this library.
+ * Scratch lives in one file-scope device array of this library (about 4.2 MB,
+ * sized for GS_COMPACT_STATIC_MAX_N Gaussians), which every GPU that loads the
+ * library keeps until the process exits.  The call allocates nothing (no
+ * cudaMalloc/cudaFree, no allocating library routine).
+ * Same arguments, outputs and errors as gs_grad_compact, minus (ws, ws_bytes);
+ * n > GS_COMPACT_STATIC_MAX_N returns GS_ERR_INVALID_ARG.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array: calls
+ * whose work overlaps on the GPU (other streams, other threads) race on it and
+ * must be serialised by the caller.  Nothing in it needs to start at zero; it
+ * keeps whatever the last call left there. */
+GS_API gs_status gs_grad_compact_static(float* grad2d, uint8_t* touched, const float* params, int64_t n,
+                                        int32_t sh_degree, const gs_camera* cams, int32_t n_views,
+                                        const gs_render_opts* opts, uint32_t* idx, int64_t* n_idx, float* grads,
+                                        void* stream);
+
 /* Deferred Adam (dense-equivalent).  For every listed Gaussian g with
  * s = last_step[g] < t: the skipped zero-gradient steps j = s+1 .. t-1 are
  * replayed, then step t uses grads; last_step[g] = t and grads[:, g] = 0.
