@@ -3,16 +3,19 @@
 // unnecessary memory accesses for Gaussians with zero gradients"), made exactly
 // equal to dense Adam by replaying the skipped zero-gradient steps first.
 //
-// One thread per (parameter row, listed Gaussian), coalesced across the warp when
-// the list is dense.  The bias corrections of the current step are computed once
-// per block; replayed steps compute their own.  A row whose
-// moments are both +0 is left as is during replay: a zero-gradient step from a
-// zero state changes nothing, bit for bit.
+// One thread per (listed Gaussian, group of 4 parameter rows): the loads of all
+// its rows are issued before any arithmetic, and consecutive threads touch
+// consecutive Gaussians of a row (coalesced when the list is dense).  The bias
+// corrections of the current step come from the host (the same fp64 binary
+// exponentiation as the device code, so the same values); replayed steps
+// compute their own.  A row whose moments are both +0 skips the replay: a
+// zero-gradient step from a zero state changes nothing, bit for bit.
+// last_step is only read by the update kernel; stamp_kernel writes it after.
 #include "gs_common.cuh"
 
 namespace gs {
 
-__device__ __forceinline__ double powi_binary(double b, int e)
+__host__ __device__ __forceinline__ double powi_binary(double b, int e)
 {
     double r = 1.0;
     while (e > 0) {
@@ -36,8 +39,11 @@ struct AdamArgs {
     int32_t t;
     float lr[5];
     float b1, b2, eps;
+    float bc1t, bc2t;   // bias corrections of step t
     int32_t flush;
 };
+
+constexpr int kRowsPerThread = 4;
 
 __device__ __forceinline__ int row_group(int r) { return r < 3 ? 0 : (r < 6 ? 1 : (r < 10 ? 2 : (r == 10 ? 3 : 4))); }
 
@@ -52,38 +58,43 @@ __device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, 
     v = vn;
 }
 
-// One thread per (parameter row, listed Gaussian): every thread does its own
-// 4 loads and 4 stores, so the whole list streams through HBM at full width.
-// last_step is only read here; stamp_kernel writes it afterwards.
 __global__ void __launch_bounds__(256) adam_deferred_kernel(AdamArgs a)
 {
-    __shared__ float s_bc[2];
-    if (threadIdx.x == 0) {
-        s_bc[0] = (float)(1.0 - powi_binary((double)a.b1, a.t));
-        s_bc[1] = (float)(1.0 - powi_binary((double)a.b2, a.t));
-    }
-    __syncthreads();
-    const float bc1t = s_bc[0], bc2t = s_bc[1];
     const int64_t count = a.flush ? a.n : *a.n_idx;
-    const int r = blockIdx.y;
-    const float lr = a.lr[row_group(r)];
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t g = a.flush ? i : (int64_t)a.idx[i];
-        const int s = a.last_step[g];
-        if (s >= a.t) continue;
-        const size_t e = (size_t)r * a.n + g;
-        float p = a.params[e], m = a.m[e], v = a.v[e];
-        const float gr = a.flush ? 0.0f : a.grads[e];
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    const int64_t g = a.flush ? i : (int64_t)a.idx[i];
+    const int s = a.last_step[g];
+    if (s >= a.t) return;
+    const int r0 = blockIdx.y * kRowsPerThread;
+    float p[kRowsPerThread], m[kRowsPerThread], v[kRowsPerThread], gr[kRowsPerThread];
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) {
+        const int r = r0 + k;
+        if (r < a.rows) {
+            const size_t e = (size_t)r * a.n + g;
+            p[k] = a.params[e];
+            m[k] = a.m[e];
+            v[k] = a.v[e];
+            gr[k] = a.flush ? 0.0f : a.grads[e];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) {
+        const int r = r0 + k;
+        if (r >= a.rows) break;
+        const float lr = a.lr[row_group(r)];
         for (int j = s + 1; j < a.t; ++j) {
-            if (__float_as_uint(m) == 0u && __float_as_uint(v) == 0u) break;   // zero state: replay is a no-op
+            if (__float_as_uint(m[k]) == 0u && __float_as_uint(v[k]) == 0u) break;   // zero state: replay is a no-op
             const float bc1 = (float)(1.0 - powi_binary((double)a.b1, j));
             const float bc2 = (float)(1.0 - powi_binary((double)a.b2, j));
-            adam_one(p, m, v, 0.0f, lr, a.b1, a.b2, a.eps, bc1, bc2);
+            adam_one(p[k], m[k], v[k], 0.0f, lr, a.b1, a.b2, a.eps, bc1, bc2);
         }
-        adam_one(p, m, v, gr, lr, a.b1, a.b2, a.eps, bc1t, bc2t);
-        a.params[e] = p;
-        a.m[e] = m;
-        a.v[e] = v;
+        adam_one(p[k], m[k], v[k], gr[k], lr, a.b1, a.b2, a.eps, a.bc1t, a.bc2t);
+        const size_t e = (size_t)r * a.n + g;
+        a.params[e] = p[k];
+        a.m[e] = m[k];
+        a.v[e] = v[k];
         if (!a.flush) a.grads[e] = 0.0f;
     }
 }
@@ -125,18 +136,19 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     a.b1 = beta1;
     a.b2 = beta2;
     a.eps = eps;
+    a.bc1t = (float)(1.0 - powi_binary((double)beta1, t));
+    a.bc2t = (float)(1.0 - powi_binary((double)beta2, t));
     a.flush = flush ? 1 : 0;
     int dev = 0, sms = 0;
     GS_CUDA_TRY(cudaGetDevice(&dev));
     GS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    // The list length lives on the device: size the grid for n and let threads
-    // beyond the list exit (grid-stride beyond 8 resident blocks per SM).
+    // The list length lives on the device: the grid covers n entries and threads
+    // beyond the list return at once.
     const int threads = 256;
-    int64_t bx = (n + threads - 1) / threads;
-    const int64_t cap = ((int64_t)sms * 8 + rows - 1) / rows;
-    if (bx > cap) bx = cap;
+    const int64_t bx = (n + threads - 1) / threads;
+    const unsigned by = (unsigned)((rows + kRowsPerThread - 1) / kRowsPerThread);
     cudaStream_t s = (cudaStream_t)stream;
-    adam_deferred_kernel<<<dim3((unsigned)bx, (unsigned)rows), threads, 0, s>>>(a);
+    adam_deferred_kernel<<<dim3((unsigned)bx, by), threads, 0, s>>>(a);
     GS_LAUNCH_CHECK();
     int64_t bs = (n + threads - 1) / threads;
     if (bs > (int64_t)sms * 8) bs = (int64_t)sms * 8;

@@ -23,6 +23,47 @@ struct ProjectArgs {
     uint32_t* tiles_touched;
 };
 
+// Where a pixel can pass the alpha test, for the rasterizer's culling.
+//  tau: a pixel whose power is below tau has alpha < alpha_min for certain
+//       (o * exp(tau) <= 0.99 alpha_min; the 0.01 covers logf and exp rounding).
+//  hx, hy: half-extents of a box around the mean outside which the rasterizer's
+//       fp32 power is below tau.  With M = [[A, B], [B, C]] and
+//       P(e) = -1/2 e^T M e, the kernel's rounded power is at most
+//       P + 16u Q(e) (u = 2^-24, Q = the sum of the absolute terms), and
+//       Q <= -P (1 + 2|B| / lambda_min(M)) = -P kappa; so power >= tau needs
+//       e^T M e <= K = -2 tau / (1 - 16u kappa), whose bounding box is
+//       |e_x| <= sqrt(K C / det M), |e_y| <= sqrt(K A / det M).  det M is
+//       formed with Kahan's two-product correction; the box is widened by a
+//       relative 1e-4 and by an absolute slack that covers the rounding of the
+//       comparisons at the mean's magnitude.  hx = hy = -1: no pixel passes;
+//       +inf: no useful bound (badly conditioned conic).
+__device__ __forceinline__ void alpha_support(const ProjOut& po, float alpha_min, float& tau, float& hx, float& hy)
+{
+    if (!(po.opacity >= alpha_min)) {
+        tau = INFINITY;
+        hx = hy = -1.0f;
+        return;
+    }
+    tau = logf(alpha_min / po.opacity) - 0.01f;
+    const float A = po.cA, B = po.cB, C = po.cC;
+    const float bb = B * B;
+    const float bb_err = __fmaf_rn(B, B, -bb);             // exact error of B*B
+    const float det = __fmaf_rn(A, C, -bb) - bb_err;       // Kahan: A C - B^2 to ~1 ulp
+    const float mid = 0.5f * (A + C);
+    const float lmax = mid + sqrtf(fmaxf(mid * mid - det, 0.0f));
+    const float lmin = det / lmax;
+    const float kappa = 1.01f * (1.0f + 2.0f * fabsf(B) / lmin) + 0.01f;
+    const float eps = 16.0f * 0x1.0p-24f * kappa;
+    if (!(det > 0.0f) || !(lmin > 0.0f) || !(eps < 0.5f)) {
+        hx = hy = INFINITY;
+        return;
+    }
+    const float K = -2.0f * tau / (1.0f - eps);
+    hx = sqrtf(K * C / det) * 1.0001f + 1e-3f + fabsf(po.mx) * 0x1.0p-18f;
+    hy = sqrtf(K * A / det) * 1.0001f + 1e-3f + fabsf(po.my) * 0x1.0p-18f;
+    if (!(hx >= 0.0f) || !(hy >= 0.0f)) hx = hy = INFINITY;
+}
+
 template <int DEG>
 __global__ void __launch_bounds__(128) project_kernel(ProjectArgs a, CamSet cs)
 {
@@ -41,10 +82,9 @@ __global__ void __launch_bounds__(128) project_kernel(ProjectArgs a, CamSet cs)
         float4* r = a.rec + o * 3;
         r[0] = make_float4(po.mx, po.my, -0.5f * po.cA, po.cB);
         r[1] = make_float4(-0.5f * po.cC, po.opacity, po.col[0], po.col[1]);
-        // Rasterizer cut: a pixel with power < tau has alpha < alpha_min for sure
-        // (o * exp(tau) <= 0.99 alpha_min, with slack for logf and pexp rounding).
-        const float tau = po.opacity >= a.alpha_min ? logf(a.alpha_min / po.opacity) - 0.01f : INFINITY;
-        r[2] = make_float4(po.col[2], po.depth, tau, 0.0f);
+        float tau, hx, hy;
+        alpha_support(po, a.alpha_min, tau, hx, hy);
+        r[2] = make_float4(po.col[2], tau, hx, hy);
         a.depth[o] = po.depth;
         a.rect[o] = make_ushort4((unsigned short)po.x0, (unsigned short)po.y0, (unsigned short)po.x1,
                                  (unsigned short)po.y1);

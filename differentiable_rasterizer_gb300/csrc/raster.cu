@@ -3,20 +3,39 @@
 // forward rasterization and backward rasterization into a single GPU kernel,
 // retaining intermediate results on-chip").
 //
-// One CTA per 16x16 tile, one thread per pixel.  The tile's sorted list is
-// staged through shared memory in chunks of kChunk records (gathered through
-// the instance ids).  Per pixel the transmittance T, the colour, the index of
-// the last composited entry and dL/dC never leave registers; the target pixel
-// is read once.  Backward walks the list back to front, recovering T_i by
-// division, and reduces each Gaussian's 9 gradient components over the warp
-// before one atomic per warp and component.  If the part of the list that any
-// pixel composited fits in the last staged chunk, backward reads no records
-// from memory at all.
+// One CTA per 16x16 tile; thread t owns pixel (t % 16, t / 16).  The tile's
+// sorted list is staged through shared memory in chunks of kChunk records
+// (gathered through the instance ids).  Each chunk is handled in two phases:
+//
+//  pairs      Gaussian-parallel: a warp takes one staged Gaussian and its lanes
+//             sweep the pixels of the Gaussian's alpha-support box inside the
+//             tile (the box comes from gs_project and provably contains every
+//             pixel whose fp32 power can reach the per-Gaussian cut tau); every
+//             pixel whose alpha passes sets bit j in its 256-bit row.
+//  composite  pixel-parallel: each pixel walks its set bits in list order and
+//             composites them, with T, the colour, the stop index and dL/dC in
+//             registers.
+//
+// Entries that do not pass are skipped by definition, so the image, stop index
+// and evaluation counts are those of walking every list entry.  The entries a
+// pixel composited are exactly its passing bits up to its last index, so
+// backward needs no per-pixel list: each pixel walks those bits back to front
+// (T recovered by division, the colour behind accumulated), adds its 9 gradient
+// terms into per-Gaussian shared-memory accumulators, and each chunk's sums go
+// to global memory with one vector atomic per Gaussian per tile.  Chunks that
+// are no longer resident are restaged and their bits recomputed.
+//
+// All decisions use the same fp32 operations in the same order as the CPU
+// definition (see gs_common.cuh); boxes, tau and bits only avoid work whose
+// outcome is already known.
 #include "gs_common.cuh"
 
 namespace gs {
 
-constexpr int kChunk = 256;   // records per shared-memory stage
+constexpr int kChunk = 256;      // records per shared-memory stage
+constexpr int kWords = kChunk / 32;
+constexpr int kWarps = kTileThreads / 32;
+constexpr int kQueue = 1024;     // backward queue entries per warp and chunk
 
 struct RasterArgs {
     const float4* __restrict__ rec;     // [V][n][3]
@@ -31,36 +50,9 @@ struct RasterArgs {
     int64_t n;
     int32_t W, H, tiles_x, tiles, n_views;
     float alpha_min, alpha_max, t_min, bg0, bg1, bg2, inv3hw;
-    double inv3hw_d;   // 1 / (3 H W) for the loss mean
+    double inv3hw_d;                    // 1 / (3 H W) for the loss mean
     int32_t exclude_crossing;
 };
-
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Sums eight values over the warp with a butterfly that halves the live values
-// at each of the first three stages (each lane sends the half its partner
-// keeps): 4 + 2 + 1 + 1 + 1 shuffles instead of 8 x 5.  Afterwards every lane L
-// holds the full sum of value (L >> 2) & 7.
-__device__ __forceinline__ float warp_reduce8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
-                                              float v7, int lane)
-{
-    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
-    float a0 = (h16 ? v4 : v0) + __shfl_xor_sync(0xffffffffu, h16 ? v0 : v4, 16);
-    float a1 = (h16 ? v5 : v1) + __shfl_xor_sync(0xffffffffu, h16 ? v1 : v5, 16);
-    float a2 = (h16 ? v6 : v2) + __shfl_xor_sync(0xffffffffu, h16 ? v2 : v6, 16);
-    float a3 = (h16 ? v7 : v3) + __shfl_xor_sync(0xffffffffu, h16 ? v3 : v7, 16);
-    float b0 = (h8 ? a2 : a0) + __shfl_xor_sync(0xffffffffu, h8 ? a0 : a2, 8);
-    float b1 = (h8 ? a3 : a1) + __shfl_xor_sync(0xffffffffu, h8 ? a1 : a3, 8);
-    float c0 = (h4 ? b1 : b0) + __shfl_xor_sync(0xffffffffu, h4 ? b0 : b1, 4);
-    c0 += __shfl_xor_sync(0xffffffffu, c0, 2);
-    c0 += __shfl_xor_sync(0xffffffffu, c0, 1);
-    return c0;
-}
 
 __device__ __forceinline__ float rcp_approx(float x)
 {
@@ -69,42 +61,181 @@ __device__ __forceinline__ float rcp_approx(float x)
     return r;
 }
 
+// Pixels of the tile at (ox, oy) whose centres lie in the box |x - mx| <= hx,
+// |y - my| <= hy, as half-open column/row ranges packed x0 | x1<<8 | y0<<16 | y1<<24
+// (0: none).
+__device__ __forceinline__ uint32_t tile_box(float mx, float my, float hx, float hy, int ox, int oy)
+{
+    if (!(hx >= 0.0f && hy >= 0.0f)) return 0u;
+    const float fx0 = fmaxf(ceilf(mx - hx - (float)ox - 0.5f), 0.0f);
+    const float fx1 = fminf(floorf(mx + hx - (float)ox - 0.5f) + 1.0f, (float)kTile);
+    const float fy0 = fmaxf(ceilf(my - hy - (float)oy - 0.5f), 0.0f);
+    const float fy1 = fminf(floorf(my + hy - (float)oy - 0.5f) + 1.0f, (float)kTile);
+    if (!(fx0 < fx1 && fy0 < fy1)) return 0u;
+    return (uint32_t)fx0 | ((uint32_t)fx1 << 8) | ((uint32_t)fy0 << 16) | ((uint32_t)fy1 << 24);
+}
+
+// Gradient terms of one composited entry (9: mean2d x y, conic A B C, opacity,
+// colour r g b) given dL/dC (g0..g2), the colour behind it (S, updated) and the
+// transmittance after it (Tcur, updated to the one before it).
+struct EntryGrad {
+    float gm0, gm1, gA, gB, gC, go, gr, gg, gb;
+};
+
+__device__ __forceinline__ EntryGrad entry_grad(const float4 r0, const float4 r1, float cb, float dx, float dy, float G,
+                                                float araw, float alpha, float alpha_max, float g0, float g1, float g2c,
+                                                float& S0, float& S1, float& S2, float& Tcur)
+{
+    EntryGrad e;
+    const float oma = 1.0f - alpha;
+    const float inv_oma = rcp_approx(oma);
+    const float Ti = Tcur * inv_oma;
+    const float wgt = alpha * Ti;
+    e.gr = g0 * wgt;
+    e.gg = g1 * wgt;
+    e.gb = g2c * wgt;
+    const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
+    const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
+    const float dalpha = __fmaf_rn(Ti, dotc, -dots * inv_oma);
+    S0 = __fmaf_rn(r1.z, wgt, S0);
+    S1 = __fmaf_rn(r1.w, wgt, S1);
+    S2 = __fmaf_rn(cb, wgt, S2);
+    Tcur = Ti;
+    if (araw <= alpha_max) {
+        e.go = dalpha * G;
+        const float dp = dalpha * alpha;
+        // d power / d(A, B, C) = (-dx^2/2, -dx dy, -dy^2/2);
+        // d power / d mean2d = (A dx + B dy, B dx + C dy), A = -2 r0.z, C = -2 r1.x
+        const float hdp = -0.5f * dp;
+        e.gA = hdp * dx * dx;
+        e.gB = -dp * (dx * dy);
+        e.gC = hdp * dy * dy;
+        e.gm0 = dp * __fmaf_rn(-2.0f * r0.z, dx, r0.w * dy);
+        e.gm1 = dp * __fmaf_rn(r0.w, dx, -2.0f * r1.x * dy);
+    } else {
+        e.go = e.gA = e.gB = e.gC = e.gm0 = e.gm1 = 0.0f;
+    }
+    return e;
+}
+
+// Gradient terms of one composited entry from its transmittance before it (Ti),
+// the colour composited behind it (S0..S2) and 1 / (1 - alpha) (rc).
+__device__ __forceinline__ EntryGrad entry_grad_at(const float4 r0, const float4 r1, float cb, float dx, float dy,
+                                                   float G, float araw, float alpha, float alpha_max, float g0,
+                                                   float g1, float g2c, float Ti, float S0, float S1, float S2,
+                                                   float rc)
+{
+    EntryGrad e;
+    const float wgt = alpha * Ti;
+    e.gr = g0 * wgt;
+    e.gg = g1 * wgt;
+    e.gb = g2c * wgt;
+    const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
+    const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
+    const float dalpha = __fmaf_rn(Ti, dotc, -dots * rc);
+    if (araw <= alpha_max) {
+        e.go = dalpha * G;
+        const float dp = dalpha * alpha;
+        const float hdp = -0.5f * dp;
+        e.gA = hdp * dx * dx;
+        e.gB = -dp * (dx * dy);
+        e.gC = hdp * dy * dy;
+        e.gm0 = dp * __fmaf_rn(-2.0f * r0.z, dx, r0.w * dy);
+        e.gm1 = dp * __fmaf_rn(r0.w, dx, -2.0f * r1.x * dy);
+    } else {
+        e.go = e.gA = e.gB = e.gC = e.gm0 = e.gm1 = 0.0f;
+    }
+    return e;
+}
+
 template <bool kBackward>
 __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a)
 {
     __shared__ float4 s_r0[kChunk], s_r1[kChunk];
-    __shared__ float2 s_r2[kChunk];   // (blue, tau)
+    __shared__ float2 s_r2[kChunk];                 // (blue, tau)
     __shared__ uint32_t s_id[kChunk];
-    __shared__ double s_red_d[kTileThreads / 32];
-    __shared__ unsigned long long s_red_u[3][kTileThreads / 32];
-    __shared__ int s_max_last[kTileThreads / 32];
+    __shared__ uint32_t s_box[kChunk];              // tile_box of each staged Gaussian
+    __shared__ uint32_t s_bits[kWords][kTileThreads];   // bit j of pixel p: entry j passes at p
+    __shared__ uint32_t s_skip[kWarps];             // pixels that need no more pairs
+    __shared__ float s_acc[kBackward ? 9 : 1][kChunk];
+    __shared__ uint8_t s_hit[kBackward ? kChunk : 1];
+    __shared__ uint16_t s_q[kBackward ? kWarps : 1][kBackward ? kQueue : 1];   // (owner lane << 8) | entry
+    __shared__ double s_red_d[kWarps];
+    __shared__ unsigned long long s_red_u[3][kWarps];
+    __shared__ int s_max_last[kWarps];
 
     const int tile_lin = blockIdx.x;                 // v * tiles + tile
     const int v = tile_lin / a.tiles;
     const int tile = tile_lin - v * a.tiles;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int px = tx * kTile + (threadIdx.x & (kTile - 1));
-    const int py = ty * kTile + (threadIdx.x / kTile);
+    const int ox = tx * kTile, oy = ty * kTile;
+    const int px = ox + (threadIdx.x & (kTile - 1));
+    const int py = oy + (threadIdx.x / kTile);
     const bool inside = px < a.W && py < a.H;
     const float pxf = (float)px + 0.5f, pyf = (float)py + 0.5f;
     const uint2 range = a.ranges[tile_lin];
     const int lo = (int)range.x;
     const int len = (int)(range.y - range.x);
     const float4* __restrict__ recv = a.rec + (size_t)v * (size_t)a.n * 3;
+    const float alpha_min = a.alpha_min, alpha_max = a.alpha_max;
 
+    // Stage chunk records, their boxes, and clear this pixel's bit row.
     auto stage = [&](int base) {
         const int k = base + threadIdx.x;
+        uint32_t box = 0u;
         if (k < len) {
             const uint32_t g = __ldg(a.ids + lo + k);
             const float4* r = recv + (size_t)g * 3;
-            s_r0[threadIdx.x] = __ldg(r);
+            const float4 r0 = __ldg(r);
+            s_r0[threadIdx.x] = r0;
             s_r1[threadIdx.x] = __ldg(r + 1);
             const float4 r2 = __ldg(r + 2);
-            s_r2[threadIdx.x] = make_float2(r2.x, r2.z);
+            s_r2[threadIdx.x] = make_float2(r2.x, r2.y);
             s_id[threadIdx.x] = g;
+            box = tile_box(r0.x, r0.y, r2.z, r2.w, ox, oy);
+        }
+        s_box[threadIdx.x] = box;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) s_bits[w][threadIdx.x] = 0u;
+    };
+    // Pair phase: warp-per-Gaussian sweep of each box, setting pass bits.
+    auto pairs = [&](int cnt) {
+        for (int j = warp; j < cnt; j += kWarps) {
+            const uint32_t box = s_box[j];
+            const int bx0 = box & 0xff, bw = (int)((box >> 8) & 0xff) - bx0;
+            const int by0 = (box >> 16) & 0xff, bh = (int)(box >> 24) - by0;
+            if (box == 0u) continue;
+            const int area = bw * bh;
+            const float4 r0 = s_r0[j];
+            const float4 r1 = s_r1[j];
+            const float tau = s_r2[j].y;
+            const float inv_w = 1.0f / (float)bw;
+            const uint32_t bit = 1u << (j & 31);
+            for (int q = lane; q < area; q += 32) {
+                const int ly = (int)(((float)q + 0.5f) * inv_w);   // exact: q < 256, bw <= 16
+                const int lx = q - ly * bw;
+                const int ix = bx0 + lx, iy = by0 + ly;
+                const int p = iy * kTile + ix;
+                if ((s_skip[p >> 5] >> (p & 31)) & 1u) continue;
+                const float dx = ((float)(ox + ix) + 0.5f) - r0.x;
+                const float dy = ((float)(oy + iy) + 0.5f) - r0.y;
+                // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
+                const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+                // power > 0 is skipped by definition; power < tau has alpha < alpha_min
+                if (power > 0.0f || power < tau) continue;
+                const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
+                if (alpha < alpha_min) continue;
+                atomicOr(&s_bits[j >> 5][p], bit);
+            }
         }
     };
+
+    if (kBackward) {
+#pragma unroll
+        for (int k = 0; k < 9; ++k) s_acc[k][threadIdx.x] = 0.0f;
+        s_hit[threadIdx.x] = 0;
+    }
 
     // ------------------------------------------------------------- forward
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
@@ -116,33 +247,36 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     for (int c = 0; c < nchunks; ++c) {
         if (__syncthreads_and(done)) break;
         const int base = c * kChunk;
+        const uint32_t skip = __ballot_sync(0xffffffffu, done);
+        if (lane == 0) s_skip[warp] = skip;
         stage(base);
         resident = c;
         __syncthreads();
         const int cnt = min(kChunk, len - base);
+        pairs(cnt);
+        __syncthreads();
         if (!done) {
-            for (int j = 0; j < cnt; ++j) {
-                const float4 r0 = s_r0[j];
-                const float dx = pxf - r0.x, dy = pyf - r0.y;
-                const float4 r1 = s_r1[j];
-                // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
-                const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                const float2 r2 = s_r2[j];
-                // power > 0 is skipped by definition; power < tau has alpha < alpha_min
-                if (power > 0.0f || power < r2.y) continue;
-                const float araw = r1.y * pexp_neg(power);
-                const float alpha = fminf(a.alpha_max, araw);
-                if (alpha < a.alpha_min) continue;
-                const float Tn = T * (1.0f - alpha);
-                if (a.exclude_crossing && Tn < a.t_min) { done = true; stop = base + j; break; }
-                const float wgt = alpha * T;
-                C0 = C0 + r1.z * wgt;
-                C1 = C1 + r1.w * wgt;
-                C2 = C2 + r2.x * wgt;
-                T = Tn;
-                last = base + j;
-                ++ncomp;
-                if (!a.exclude_crossing && T < a.t_min) { done = true; stop = base + j; break; }
+            for (int w = 0; w < kWords && !done; ++w) {
+                uint32_t word = s_bits[w][threadIdx.x];
+                while (word) {
+                    const int j = (w << 5) | (__ffs(word) - 1);
+                    word &= word - 1u;
+                    const float4 r0 = s_r0[j];
+                    const float dx = pxf - r0.x, dy = pyf - r0.y;
+                    const float4 r1 = s_r1[j];
+                    const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+                    const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
+                    const float Tn = T * (1.0f - alpha);
+                    if (a.exclude_crossing && Tn < a.t_min) { done = true; stop = base + j; break; }
+                    const float wgt = alpha * T;
+                    C0 = C0 + r1.z * wgt;
+                    C1 = C1 + r1.w * wgt;
+                    C2 = C2 + s_r2[j].x * wgt;
+                    T = Tn;
+                    last = base + j;
+                    ++ncomp;
+                    if (!a.exclude_crossing && T < a.t_min) { done = true; stop = base + j; break; }
+                }
             }
         }
     }
@@ -169,7 +303,6 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         }
     }
     // block reductions: loss, evaluation counts, last composited index
-    int warp_last;
     {
         unsigned long long ef = (unsigned long long)nev, eb = (unsigned long long)(last + 1);
         unsigned long long ec = (unsigned long long)ncomp;
@@ -182,7 +315,6 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             ec += __shfl_xor_sync(0xffffffffu, ec, o);
             ml = max(ml, __shfl_xor_sync(0xffffffffu, ml, o));
         }
-        warp_last = ml;
         if (lane == 0) {
             s_red_d[warp] = lsum;
             s_red_u[0][warp] = ef;
@@ -192,16 +324,16 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         }
     }
     __syncthreads();
-    int max_last = -1;
     if (threadIdx.x == 0) {
         double ls = 0.0;
         unsigned long long ef = 0, eb = 0, ec = 0;
-        for (int w = 0; w < kTileThreads / 32; ++w) {
+        int ml = -1;
+        for (int w = 0; w < kWarps; ++w) {
             ls += s_red_d[w];
             ef += s_red_u[0][w];
             eb += s_red_u[1][w];
             ec += s_red_u[2][w];
-            max_last = max(max_last, s_max_last[w]);
+            ml = max(ml, s_max_last[w]);
         }
         if (kBackward && ls != 0.0) atomicAdd(a.loss + v, ls * a.inv3hw_d);
         if (a.counts) {
@@ -209,11 +341,11 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             atomicAdd(a.counts + 1, eb);
             atomicAdd(a.counts + 2, ec);
         }
-        s_max_last[0] = max_last;
+        s_max_last[0] = ml;
     }
     if (!kBackward) return;
     __syncthreads();
-    max_last = s_max_last[0];
+    const int max_last = s_max_last[0];
     if (max_last < 0) return;
 
     // ------------------------------------------------------------- backward
@@ -221,70 +353,195 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     float Tcur = T;
     float* __restrict__ g2v = a.grad2d + (size_t)v * (size_t)a.n * GS_GRAD2D_STRIDE;
     uint8_t* __restrict__ touchv = a.touched + (size_t)v * (size_t)a.n;
-    const int red_slot = (lane >> 2) & 7;   // component this lane holds after warp_reduce8
     for (int c = max_last / kChunk; c >= 0; --c) {
         const int base = c * kChunk;
         if (c != resident) {
-            __syncthreads();   // every thread is done reading the resident chunk
+            __syncthreads();   // the previous chunk's records and sums are no longer read
+            const uint32_t skip = __ballot_sync(0xffffffffu, last < base);
+            if (lane == 0) s_skip[warp] = skip;
             stage(base);
             resident = c;
             __syncthreads();
+            pairs(min(kChunk, len - base));
+            __syncthreads();
         }
-        // this warp has nothing composited beyond warp_last
-        const int jtop = min(kChunk - 1, warp_last - base);
-        for (int j = jtop; j >= 0; --j) {
-            const int i = base + j;
-            float gm0 = 0.0f, gm1 = 0.0f, gA = 0.0f, gB = 0.0f, gC = 0.0f, go = 0.0f;
-            float gr = 0.0f, gg = 0.0f, gb = 0.0f;
-            bool contrib = false;
-            const float4 r0 = s_r0[j];
-            const float dx = pxf - r0.x, dy = pyf - r0.y;
-            const float4 r1 = s_r1[j];
-            const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-            const float2 r2 = s_r2[j];
-            if (i <= last && power <= 0.0f && power >= r2.y) {
-                const float G = pexp_neg(power);
-                const float araw = r1.y * G;
-                const float alpha = fminf(a.alpha_max, araw);
-                if (alpha >= a.alpha_min) {
-                    contrib = true;
-                    const float oma = 1.0f - alpha;
-                    const float inv_oma = rcp_approx(oma);
-                    const float Ti = Tcur * inv_oma;
-                    const float wgt = alpha * Ti;
-                    gr = g0 * wgt;
-                    gg = g1 * wgt;
-                    gb = g2c * wgt;
-                    const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * r2.x));
-                    const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
-                    const float dalpha = __fmaf_rn(Ti, dotc, -dots * inv_oma);
-                    S0 = __fmaf_rn(r1.z, wgt, S0);
-                    S1 = __fmaf_rn(r1.w, wgt, S1);
-                    S2 = __fmaf_rn(r2.x, wgt, S2);
-                    Tcur = Ti;
-                    if (araw <= a.alpha_max) {
-                        go = dalpha * G;
-                        const float dp = dalpha * alpha;
-                        // d power / d(A, B, C) = (-dx^2/2, -dx dy, -dy^2/2);
-                        // d power / d mean2d = (A dx + B dy, B dx + C dy), A = -2 r0.z, C = -2 r1.x
-                        const float hdp = -0.5f * dp;
-                        gA = hdp * dx * dx;
-                        gB = -dp * (dx * dy);
-                        gC = hdp * dy * dy;
-                        gm0 = dp * __fmaf_rn(-2.0f * r0.z, dx, r0.w * dy);
-                        gm1 = dp * __fmaf_rn(r0.w, dx, -2.0f * r1.x * dy);
+        // This pixel's composited entries in the chunk: its passing bits up to last.
+        const int lim = last - base;
+        uint32_t words[kWords];
+        int nmine = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            const int top = lim - (w << 5);
+            uint32_t word = top >= 0 ? s_bits[w][threadIdx.x] : 0u;
+            if (top >= 0 && top < 31) word &= (2u << top) - 1u;
+            words[w] = word;
+            nmine += __popc(word);
+        }
+        int incl = nmine;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        const int myoff = incl - nmine;                       // my segment in the warp's queue
+        const int nq = __shfl_sync(0xffffffffu, incl, 31);
+        if (nq > kQueue) {
+            // Rare overflow: walk my own entries one by one, newest first.
+            for (int w = kWords - 1; w >= 0; --w) {
+                uint32_t word = words[w];
+                while (word) {
+                    const int b = 31 - __clz(word);
+                    word &= ~(1u << b);
+                    const int j = (w << 5) | b;
+                    const float4 r0 = s_r0[j];
+                    const float dx = pxf - r0.x, dy = pyf - r0.y;
+                    const float4 r1 = s_r1[j];
+                    const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+                    const float G = pexp_neg(power);
+                    const float araw = r1.y * G;
+                    const float alpha = fminf(alpha_max, araw);
+                    const EntryGrad e = entry_grad(r0, r1, s_r2[j].x, dx, dy, G, araw, alpha, alpha_max, g0, g1, g2c,
+                                                   S0, S1, S2, Tcur);
+                    atomicAdd(&s_acc[0][j], e.gm0);
+                    atomicAdd(&s_acc[1][j], e.gm1);
+                    atomicAdd(&s_acc[2][j], e.gA);
+                    atomicAdd(&s_acc[3][j], e.gB);
+                    atomicAdd(&s_acc[4][j], e.gC);
+                    atomicAdd(&s_acc[5][j], e.go);
+                    atomicAdd(&s_acc[6][j], e.gr);
+                    atomicAdd(&s_acc[7][j], e.gg);
+                    atomicAdd(&s_acc[8][j], e.gb);
+                    s_hit[j] = 1;
+                }
+            }
+        } else if (nq > 0) {
+            // Queue the warp's entries grouped by pixel, newest first, then process
+            // them 32 at a time: T before each entry is a segmented product of
+            // 1/(1 - alpha) from the pixel's current T, the colour behind it a
+            // segmented exclusive sum of c * w from the pixel's current S.
+            uint16_t* q = s_q[warp];
+            {
+                int k = myoff;
+#pragma unroll
+                for (int w = kWords - 1; w >= 0; --w) {
+                    uint32_t word = words[w];
+                    while (word) {
+                        const int b = 31 - __clz(word);
+                        word &= ~(1u << b);
+                        q[k++] = (uint16_t)((lane << 8) | (w << 5) | b);
                     }
                 }
             }
-            if (__any_sync(0xffffffffu, contrib)) {
-                const float s8 = warp_reduce8(gm0, gm1, gA, gB, gC, go, gr, gg, lane);
-                const float sb = warp_sum(gb);
-                const uint32_t gid = s_id[j];
-                float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
-                if ((lane & 3) == 0) atomicAdd(dst + red_slot, s8);
-                if (lane == 1) atomicAdd(dst + 8, sb);
-                if (lane == 2) touchv[gid] = 1;
+            __syncwarp();
+            const int myend = myoff + nmine;
+            for (int r = 0; r < nq; r += 32) {
+                const int qi = r + lane;
+                const bool valid = qi < nq;
+                const uint32_t ent = valid ? (uint32_t)q[qi] : 0u;
+                const int owner = (int)(ent >> 8);
+                const int j = (int)(ent & 0xffu);
+                const int own_off = __shfl_sync(0xffffffffu, myoff, owner);
+                const float Tst = __shfl_sync(0xffffffffu, Tcur, owner);
+                const float Ss0 = __shfl_sync(0xffffffffu, S0, owner);
+                const float Ss1 = __shfl_sync(0xffffffffu, S1, owner);
+                const float Ss2 = __shfl_sync(0xffffffffu, S2, owner);
+                const float go0 = __shfl_sync(0xffffffffu, g0, owner);
+                const float go1 = __shfl_sync(0xffffffffu, g1, owner);
+                const float go2 = __shfl_sync(0xffffffffu, g2c, owner);
+                const int pidx = warp * 32 + owner;
+                const float pxo = (float)(ox + (pidx & (kTile - 1))) + 0.5f;
+                const float pyo = (float)(oy + pidx / kTile) + 0.5f;
+                float4 r0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), r1 = r0;
+                float cb = 0.0f, dx = 0.0f, dy = 0.0f, G = 0.0f, araw = 0.0f, alpha = 0.0f;
+                if (valid) {
+                    r0 = s_r0[j];
+                    r1 = s_r1[j];
+                    cb = s_r2[j].x;
+                    dx = pxo - r0.x;
+                    dy = pyo - r0.y;
+                    const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+                    G = pexp_neg(power);
+                    araw = r1.y * G;
+                    alpha = fminf(alpha_max, araw);
+                }
+                const float rc = rcp_approx(1.0f - alpha);
+                // segmented inclusive product (T) and sums (colour behind)
+                bool hd = !valid || lane == 0 || qi == own_off;
+                float P = rc;
+                float x0 = r1.z * alpha, x1 = r1.w * alpha, x2 = cb * alpha;   // c * alpha, times T below
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const float Pu = __shfl_up_sync(0xffffffffu, P, d);
+                    const bool hu = __shfl_up_sync(0xffffffffu, (int)hd, d) != 0;
+                    if (lane >= d) {
+                        if (!hd) P = Pu * P;
+                        hd = hd || hu;
+                    }
+                }
+                const float Tb = Tst * P;             // transmittance before this entry
+                x0 *= Tb;
+                x1 *= Tb;
+                x2 *= Tb;
+                float y0 = x0, y1 = x1, y2 = x2;
+                hd = !valid || lane == 0 || qi == own_off;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const float u0 = __shfl_up_sync(0xffffffffu, y0, d);
+                    const float u1 = __shfl_up_sync(0xffffffffu, y1, d);
+                    const float u2 = __shfl_up_sync(0xffffffffu, y2, d);
+                    const bool hu = __shfl_up_sync(0xffffffffu, (int)hd, d) != 0;
+                    if (lane >= d) {
+                        if (!hd) {
+                            y0 += u0;
+                            y1 += u1;
+                            y2 += u2;
+                        }
+                        hd = hd || hu;
+                    }
+                }
+                if (valid) {
+                    const EntryGrad e = entry_grad_at(r0, r1, cb, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb,
+                                                      Ss0 + (y0 - x0), Ss1 + (y1 - x1), Ss2 + (y2 - x2), rc);
+                    atomicAdd(&s_acc[0][j], e.gm0);
+                    atomicAdd(&s_acc[1][j], e.gm1);
+                    atomicAdd(&s_acc[2][j], e.gA);
+                    atomicAdd(&s_acc[3][j], e.gB);
+                    atomicAdd(&s_acc[4][j], e.gC);
+                    atomicAdd(&s_acc[5][j], e.go);
+                    atomicAdd(&s_acc[6][j], e.gr);
+                    atomicAdd(&s_acc[7][j], e.gg);
+                    atomicAdd(&s_acc[8][j], e.gb);
+                    s_hit[j] = 1;
+                }
+                // carry each pixel's T and S past the part of its segment in this round
+                const int seg_lo = max(myoff, r), seg_hi = min(myend, r + 32);
+                const int k = seg_hi - 1 - r;
+                const int src = k < 0 ? 0 : (k > 31 ? 31 : k);
+                const float Tk = __shfl_sync(0xffffffffu, Tb, src);
+                const float Y0 = __shfl_sync(0xffffffffu, y0, src);
+                const float Y1 = __shfl_sync(0xffffffffu, y1, src);
+                const float Y2 = __shfl_sync(0xffffffffu, y2, src);
+                if (seg_lo < seg_hi) {
+                    Tcur = Tk;
+                    S0 += Y0;
+                    S1 += Y1;
+                    S2 += Y2;
+                }
             }
+            __syncwarp();
+        }
+        __syncthreads();
+        // this chunk's per-Gaussian sums go out once per tile
+        const int j = threadIdx.x;
+        if (s_hit[j]) {
+            float* dst = g2v + (size_t)s_id[j] * GS_GRAD2D_STRIDE;
+            atomicAdd(reinterpret_cast<float4*>(dst), make_float4(s_acc[0][j], s_acc[1][j], s_acc[2][j], s_acc[3][j]));
+            atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(s_acc[4][j], s_acc[5][j], s_acc[6][j], s_acc[7][j]));
+            atomicAdd(dst + 8, s_acc[8][j]);
+            touchv[s_id[j]] = 1;
+#pragma unroll
+            for (int k = 0; k < 9; ++k) s_acc[k][j] = 0.0f;
+            s_hit[j] = 0;
         }
     }
 }

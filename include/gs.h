@@ -106,10 +106,13 @@ typedef struct gs_render_opts {
 
 /* Per-view projected records, caller-allocated, each [n_views][n]:
  *   rec            3 float4 per (view, Gaussian), 16-byte aligned:
- *                  {mx, my, -A/2, B}, {-C/2, opacity, r, g}, {b, depth, tau, 0}
- *                  (mean in pixels, conic (A, B, C) = Sigma2D^-1, depth = z_c,
+ *                  {mx, my, -A/2, B}, {-C/2, opacity, r, g}, {b, tau, hx, hy}
+ *                  (mean in pixels, conic (A, B, C) = Sigma2D^-1;
  *                  tau = ln(alpha_min / opacity) - 0.01: any pixel with power
- *                  below tau has alpha < alpha_min, +inf if opacity < alpha_min);
+ *                  below tau has alpha < alpha_min, +inf if opacity < alpha_min;
+ *                  hx, hy: half-extents of a box around the mean outside which
+ *                  the rasterizer's fp32 power is below tau, -1 if no pixel can
+ *                  pass, +inf if no bound is available);
  *                  written only for visible Gaussians
  *   depth          float z_c (written only for visible Gaussians)
  *   rect           4 x uint16 tile bounds x0, y0, x1, y1, half-open, clipped

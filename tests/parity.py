@@ -81,8 +81,8 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
         assert np.array_equal(tt[v] > 0, vis), f"view {v}: visibility differs at {np.flatnonzero((tt[v] > 0) != vis)[:10]}"
         o = pr["rec"][vis]
         exp = np.stack([o[:, 0], o[:, 1], np.float32(-0.5) * o[:, 2], o[:, 3], np.float32(-0.5) * o[:, 4], o[:, 5],
-                        o[:, 6], o[:, 7], o[:, 8], o[:, 9]], 1).astype(np.float32)
-        got = rec[v][vis][:, :10]
+                        o[:, 6], o[:, 7], o[:, 8]], 1).astype(np.float32)
+        got = rec[v][vis][:, :9]
         diff = np.flatnonzero((bits(got) != bits(exp)).any(1))
         assert diff.size == 0, f"view {v}: projection records differ for {diff.size} Gaussians, e.g. " \
                                f"{np.flatnonzero(vis)[diff[:3]]}: gpu {got[diff[:1]]} oracle {exp[diff[:1]]}"
