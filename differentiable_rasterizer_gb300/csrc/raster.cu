@@ -35,7 +35,7 @@ namespace gs {
 constexpr int kChunk = 256;      // records per shared-memory stage
 constexpr int kWords = kChunk / 32;
 constexpr int kWarps = kTileThreads / 32;
-constexpr int kQueue = 1024;     // backward queue entries per warp and chunk
+constexpr int kQueue = 256;      // queue window (entries) per warp
 
 struct RasterArgs {
     const float4* __restrict__ rec;     // [V][n][3]
@@ -76,47 +76,10 @@ __device__ __forceinline__ uint32_t tile_box(float mx, float my, float hx, float
 }
 
 // Gradient terms of one composited entry (9: mean2d x y, conic A B C, opacity,
-// colour r g b) given dL/dC (g0..g2), the colour behind it (S, updated) and the
-// transmittance after it (Tcur, updated to the one before it).
+// colour r g b).
 struct EntryGrad {
     float gm0, gm1, gA, gB, gC, go, gr, gg, gb;
 };
-
-__device__ __forceinline__ EntryGrad entry_grad(const float4 r0, const float4 r1, float cb, float dx, float dy, float G,
-                                                float araw, float alpha, float alpha_max, float g0, float g1, float g2c,
-                                                float& S0, float& S1, float& S2, float& Tcur)
-{
-    EntryGrad e;
-    const float oma = 1.0f - alpha;
-    const float inv_oma = rcp_approx(oma);
-    const float Ti = Tcur * inv_oma;
-    const float wgt = alpha * Ti;
-    e.gr = g0 * wgt;
-    e.gg = g1 * wgt;
-    e.gb = g2c * wgt;
-    const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
-    const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
-    const float dalpha = __fmaf_rn(Ti, dotc, -dots * inv_oma);
-    S0 = __fmaf_rn(r1.z, wgt, S0);
-    S1 = __fmaf_rn(r1.w, wgt, S1);
-    S2 = __fmaf_rn(cb, wgt, S2);
-    Tcur = Ti;
-    if (araw <= alpha_max) {
-        e.go = dalpha * G;
-        const float dp = dalpha * alpha;
-        // d power / d(A, B, C) = (-dx^2/2, -dx dy, -dy^2/2);
-        // d power / d mean2d = (A dx + B dy, B dx + C dy), A = -2 r0.z, C = -2 r1.x
-        const float hdp = -0.5f * dp;
-        e.gA = hdp * dx * dx;
-        e.gB = -dp * (dx * dy);
-        e.gC = hdp * dy * dy;
-        e.gm0 = dp * __fmaf_rn(-2.0f * r0.z, dx, r0.w * dy);
-        e.gm1 = dp * __fmaf_rn(r0.w, dx, -2.0f * r1.x * dy);
-    } else {
-        e.go = e.gA = e.gB = e.gC = e.gm0 = e.gm1 = 0.0f;
-    }
-    return e;
-}
 
 // Gradient terms of one composited entry from its transmittance before it (Ti),
 // the colour composited behind it (S0..S2) and 1 / (1 - alpha) (rc).
@@ -157,9 +120,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     __shared__ uint32_t s_box[kChunk];              // tile_box of each staged Gaussian
     __shared__ uint32_t s_bits[kWords][kTileThreads];   // bit j of pixel p: entry j passes at p
     __shared__ uint32_t s_skip[kWarps];             // pixels that need no more pairs
-    __shared__ float s_acc[kBackward ? 9 : 1][kChunk];
-    __shared__ uint8_t s_hit[kBackward ? kChunk : 1];
-    __shared__ uint16_t s_q[kBackward ? kWarps : 1][kBackward ? kQueue : 1];   // (owner lane << 8) | entry
+    __shared__ uint16_t s_q[kWarps][kQueue];        // (owner lane << 8) | entry, grouped by pixel
     __shared__ double s_red_d[kWarps];
     __shared__ unsigned long long s_red_u[3][kWarps];
     __shared__ int s_max_last[kWarps];
@@ -231,11 +192,48 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         }
     };
 
-    if (kBackward) {
+    // Queue window: this lane's entries (bits in `words`, in list order when
+    // ascending, newest first otherwise) whose position in the warp's queue
+    // (myoff + rank) falls in [wb, wb + kQueue), written grouped by pixel.
+    uint16_t* const q = s_q[warp];
+    auto fill_window = [&](const uint32_t (&words)[kWords], bool ascending, int myoff, int nmine, int wb) {
+        const int k0 = max(wb - myoff, 0), k1 = min(wb + kQueue - myoff, nmine);
+        if (k0 >= k1) return;
+        int k = 0;
 #pragma unroll
-        for (int k = 0; k < 9; ++k) s_acc[k][threadIdx.x] = 0.0f;
-        s_hit[threadIdx.x] = 0;
-    }
+        for (int i = 0; i < kWords; ++i) {
+            const int w = ascending ? i : kWords - 1 - i;
+            uint32_t word = words[w];
+            while (word && k < k1) {
+                const int b = ascending ? (__ffs(word) - 1) : (31 - __clz(word));
+                word &= ~(1u << b);
+                if (k >= k0) q[myoff + k - wb] = (uint16_t)((lane << 8) | (w << 5) | b);
+                ++k;
+            }
+        }
+    };
+    // This lane's entry bits (passing, up to lim), their count, the warp prefix;
+    // returns the warp total.
+    auto gather = [&](uint32_t (&words)[kWords], int lim, int& myoff, int& nmine) {
+        nmine = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            const int top = lim - (w << 5);
+            uint32_t word = top >= 0 ? s_bits[w][threadIdx.x] : 0u;
+            if (top >= 0 && top < 31) word &= (2u << top) - 1u;
+            words[w] = word;
+            nmine += __popc(word);
+        }
+        int incl = nmine;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        myoff = incl - nmine;
+        return __shfl_sync(0xffffffffu, incl, 31);
+    };
+
 
     // ------------------------------------------------------------- forward
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
@@ -255,6 +253,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         const int cnt = min(kChunk, len - base);
         pairs(cnt);
         __syncthreads();
+        // Composite: each pixel applies its passing entries in list order.
         if (!done) {
             for (int w = 0; w < kWords && !done; ++w) {
                 uint32_t word = s_bits[w][threadIdx.x];
@@ -365,79 +364,23 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             pairs(min(kChunk, len - base));
             __syncthreads();
         }
-        // This pixel's composited entries in the chunk: its passing bits up to last.
-        const int lim = last - base;
+        // This pixel's composited entries in the chunk are its passing bits up to
+        // last.  The warp queues them grouped by pixel, newest first, and handles
+        // them 32 at a time: T before each entry is a segmented product of
+        // 1/(1 - alpha) from the pixel's current T, the colour behind it a
+        // segmented exclusive sum of c * w from the pixel's current S.
         uint32_t words[kWords];
-        int nmine = 0;
-#pragma unroll
-        for (int w = 0; w < kWords; ++w) {
-            const int top = lim - (w << 5);
-            uint32_t word = top >= 0 ? s_bits[w][threadIdx.x] : 0u;
-            if (top >= 0 && top < 31) word &= (2u << top) - 1u;
-            words[w] = word;
-            nmine += __popc(word);
-        }
-        int incl = nmine;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
-        }
-        const int myoff = incl - nmine;                       // my segment in the warp's queue
-        const int nq = __shfl_sync(0xffffffffu, incl, 31);
-        if (nq > kQueue) {
-            // Rare overflow: walk my own entries one by one, newest first.
-            for (int w = kWords - 1; w >= 0; --w) {
-                uint32_t word = words[w];
-                while (word) {
-                    const int b = 31 - __clz(word);
-                    word &= ~(1u << b);
-                    const int j = (w << 5) | b;
-                    const float4 r0 = s_r0[j];
-                    const float dx = pxf - r0.x, dy = pyf - r0.y;
-                    const float4 r1 = s_r1[j];
-                    const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                    const float G = pexp_neg(power);
-                    const float araw = r1.y * G;
-                    const float alpha = fminf(alpha_max, araw);
-                    const EntryGrad e = entry_grad(r0, r1, s_r2[j].x, dx, dy, G, araw, alpha, alpha_max, g0, g1, g2c,
-                                                   S0, S1, S2, Tcur);
-                    atomicAdd(&s_acc[0][j], e.gm0);
-                    atomicAdd(&s_acc[1][j], e.gm1);
-                    atomicAdd(&s_acc[2][j], e.gA);
-                    atomicAdd(&s_acc[3][j], e.gB);
-                    atomicAdd(&s_acc[4][j], e.gC);
-                    atomicAdd(&s_acc[5][j], e.go);
-                    atomicAdd(&s_acc[6][j], e.gr);
-                    atomicAdd(&s_acc[7][j], e.gg);
-                    atomicAdd(&s_acc[8][j], e.gb);
-                    s_hit[j] = 1;
-                }
-            }
-        } else if (nq > 0) {
-            // Queue the warp's entries grouped by pixel, newest first, then process
-            // them 32 at a time: T before each entry is a segmented product of
-            // 1/(1 - alpha) from the pixel's current T, the colour behind it a
-            // segmented exclusive sum of c * w from the pixel's current S.
-            uint16_t* q = s_q[warp];
-            {
-                int k = myoff;
-#pragma unroll
-                for (int w = kWords - 1; w >= 0; --w) {
-                    uint32_t word = words[w];
-                    while (word) {
-                        const int b = 31 - __clz(word);
-                        word &= ~(1u << b);
-                        q[k++] = (uint16_t)((lane << 8) | (w << 5) | b);
-                    }
-                }
-            }
+        int myoff, nmine;
+        const int nq = gather(words, last - base, myoff, nmine);
+        const int myend = myoff + nmine;
+        for (int wb = 0; wb < nq; wb += kQueue) {
+            fill_window(words, false, myoff, nmine, wb);
             __syncwarp();
-            const int myend = myoff + nmine;
-            for (int r = 0; r < nq; r += 32) {
+            const int wend = min(nq, wb + kQueue);
+            for (int r = wb; r < wend; r += 32) {
                 const int qi = r + lane;
-                const bool valid = qi < nq;
-                const uint32_t ent = valid ? (uint32_t)q[qi] : 0u;
+                const bool valid = qi < wend;
+                const uint32_t ent = valid ? (uint32_t)q[qi - wb] : 0u;
                 const int owner = (int)(ent >> 8);
                 const int j = (int)(ent & 0xffu);
                 const int own_off = __shfl_sync(0xffffffffu, myoff, owner);
@@ -502,16 +445,12 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 if (valid) {
                     const EntryGrad e = entry_grad_at(r0, r1, cb, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb,
                                                       Ss0 + (y0 - x0), Ss1 + (y1 - x1), Ss2 + (y2 - x2), rc);
-                    atomicAdd(&s_acc[0][j], e.gm0);
-                    atomicAdd(&s_acc[1][j], e.gm1);
-                    atomicAdd(&s_acc[2][j], e.gA);
-                    atomicAdd(&s_acc[3][j], e.gB);
-                    atomicAdd(&s_acc[4][j], e.gC);
-                    atomicAdd(&s_acc[5][j], e.go);
-                    atomicAdd(&s_acc[6][j], e.gr);
-                    atomicAdd(&s_acc[7][j], e.gg);
-                    atomicAdd(&s_acc[8][j], e.gb);
-                    s_hit[j] = 1;
+                    const uint32_t gid = s_id[j];
+                    float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
+                    atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
+                    atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
+                    atomicAdd(dst + 8, e.gb);
+                    touchv[gid] = 1;
                 }
                 // carry each pixel's T and S past the part of its segment in this round
                 const int seg_lo = max(myoff, r), seg_hi = min(myend, r + 32);
@@ -529,19 +468,6 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 }
             }
             __syncwarp();
-        }
-        __syncthreads();
-        // this chunk's per-Gaussian sums go out once per tile
-        const int j = threadIdx.x;
-        if (s_hit[j]) {
-            float* dst = g2v + (size_t)s_id[j] * GS_GRAD2D_STRIDE;
-            atomicAdd(reinterpret_cast<float4*>(dst), make_float4(s_acc[0][j], s_acc[1][j], s_acc[2][j], s_acc[3][j]));
-            atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(s_acc[4][j], s_acc[5][j], s_acc[6][j], s_acc[7][j]));
-            atomicAdd(dst + 8, s_acc[8][j]);
-            touchv[s_id[j]] = 1;
-#pragma unroll
-            for (int k = 0; k < 9; ++k) s_acc[k][j] = 0.0f;
-            s_hit[j] = 0;
         }
     }
 }
