@@ -1,17 +1,22 @@
-// binsort.cu -- gs_bin_sort: 16x16 tile binning with (tile, depth) keys and an
-// LSD radix sort, then per-tile ranges of the sorted instance list.
+// binsort.cu -- gs_bin_sort: 16x16 tile binning with (tile, depth) keys and a
+// sort, then per-tile ranges of the sorted instance list.
 //
-//   1. exclusive scan of tiles_touched over [V][n] -> instance offsets, total;
-//   2. total read back to the host (the step's one host synchronisation);
-//   3. emit: (view, Gaussian) writes key = ((v*tiles + tile) << 32) | bits(depth),
-//      value = Gaussian index, for the tiles of its rect in row-major order;
-//   4. LSD radix sort over the 32 depth bits and the bits of v*tiles + tile,
-//      8-bit digits, each pass = block digit histograms -> scan -> stable scatter
-//      (ranks within a warp from __match_any_sync, warps in order), so equal keys
-//      keep emission order (ascending Gaussian index within a view);
-//   5. tile ranges [start, end) from the sorted keys.
-// The pass count decides which buffer the emit writes, so the last pass always
-// lands in the caller's arrays.
+// Per-tile path (the normal case):
+//   1. count instances per (view, tile) with atomics;
+//   2. exclusive scan of the counts = the start of every tile's bucket;
+//   3. one pass over the buckets: instance total, largest bucket, list of buckets
+//      larger than a shared-memory block sort holds; scatter cursors;
+//   4. the totals go to the host (the step's one host synchronisation);
+//   5. scatter: every visible (view, Gaussian) appends (depth bits << 32 | index)
+//      to the bucket of each tile of its rect (atomic cursor, any order);
+//   6. one CTA per bucket sorts it by (depth bits, index) in shared memory
+//      (bitonic) and writes key = ((v*tiles + tile) << 32) | depth bits, value =
+//      index, and the tile's range.
+// The result equals a stable sort by (tile, depth) of instances emitted in
+// (view, Gaussian) order: within a bucket the index breaks depth ties.
+// Buckets over kBigCap instances use the LSD radix path instead: scan of
+// tiles_touched, emit, 8-bit LSD passes (block digit histograms -> scan ->
+// stable scatter with ranks from __match_any_sync), ranges from the sorted keys.
 #include "gs_common.cuh"
 #include "scan.cuh"
 
@@ -129,14 +134,125 @@ __global__ void tile_ranges_kernel(const uint64_t* __restrict__ keys, int64_t N,
     if (i == N - 1 || (uint32_t)(keys[i + 1] >> 32) != t) ranges[t].y = (uint32_t)(i + 1);
 }
 
+constexpr int kSmallCap = 2048;    // bucket sizes sorted by the 256-thread kernel (16 KB)
+constexpr int kBigCap = 16384;     // bucket sizes sorted by the 1024-thread kernel (128 KB)
+
+__global__ void count_tiles_kernel(const uint32_t* __restrict__ touched_cnt, const ushort4* __restrict__ rect,
+                                   int64_t n, int64_t total_vn, int tiles_x, int tiles, uint32_t* __restrict__ cnt)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total_vn || touched_cnt[i] == 0) return;
+    const int64_t v = i / n;
+    const ushort4 r = rect[i];
+    uint32_t* c = cnt + v * tiles;
+    for (int ty = r.y; ty < r.w; ++ty)
+        for (int tx = r.x; tx < r.z; ++tx) atomicAdd(c + ty * tiles_x + tx, 1u);
+}
+
+// stats[0] = largest bucket, stats[1] = number of buckets over kSmallCap
+__global__ void bucket_stats_kernel(const uint32_t* __restrict__ cnt, const uint32_t* __restrict__ off, int64_t nb,
+                                    uint32_t* __restrict__ cursor, unsigned int* __restrict__ stats,
+                                    uint32_t* __restrict__ big_list)
+{
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nb) return;
+    const uint32_t c = cnt[t];
+    cursor[t] = off[t];
+    if (c == 0) return;
+    atomicMax(stats, c);
+    if (c > (uint32_t)kSmallCap) big_list[atomicAdd(stats + 1, 1u)] = (uint32_t)t;
+}
+
+__global__ void scatter_tiles_kernel(const uint32_t* __restrict__ touched_cnt, const ushort4* __restrict__ rect,
+                                     const float* __restrict__ depth, int64_t n, int64_t total_vn, int tiles_x,
+                                     int tiles, uint32_t* __restrict__ cursor, uint64_t* __restrict__ tmp)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total_vn || touched_cnt[i] == 0) return;
+    const int64_t v = i / n;
+    const uint32_t g = (uint32_t)(i - v * n);
+    const ushort4 r = rect[i];
+    const uint64_t key = ((uint64_t)__float_as_uint(depth[i]) << 32) | g;
+    uint32_t* cur = cursor + v * tiles;
+    for (int ty = r.y; ty < r.w; ++ty)
+        for (int tx = r.x; tx < r.z; ++tx) tmp[atomicAdd(cur + ty * tiles_x + tx, 1u)] = key;
+}
+
+// Bitonic sort of s[0, P) ascending (P a power of two), all threads of the block.
+__device__ __forceinline__ void block_bitonic(uint64_t* s, int P)
+{
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < P; i += blockDim.x) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const uint64_t x = s[i], y = s[ixj];
+                    const bool up = (i & k) == 0;
+                    if ((x > y) == up) {
+                        s[i] = y;
+                        s[ixj] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ void sort_bucket(uint64_t* s, uint32_t t, const uint32_t* __restrict__ cnt,
+                                            const uint32_t* __restrict__ off, const uint64_t* __restrict__ tmp,
+                                            uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
+{
+    const int c = (int)cnt[t];
+    const uint32_t o = off[t];
+    int P = 1;
+    while (P < c) P <<= 1;
+    for (int i = threadIdx.x; i < P; i += blockDim.x) s[i] = i < c ? tmp[o + i] : ~0ull;
+    __syncthreads();
+    block_bitonic(s, P);
+    const uint64_t hi = (uint64_t)t << 32;
+    for (int i = threadIdx.x; i < c; i += blockDim.x) {
+        const uint64_t k = s[i];
+        keys[o + i] = hi | (k >> 32);
+        ids[o + i] = (uint32_t)k;
+    }
+}
+
+// One 256-thread CTA per bucket: writes every bucket's range, sorts buckets of
+// at most kSmallCap instances.
+__global__ void __launch_bounds__(256) sort_small_kernel(const uint32_t* __restrict__ cnt,
+                                                         const uint32_t* __restrict__ off,
+                                                         const uint64_t* __restrict__ tmp, uint64_t* __restrict__ keys,
+                                                         uint32_t* __restrict__ ids, uint2* __restrict__ ranges)
+{
+    __shared__ uint64_t s[kSmallCap];
+    const uint32_t t = blockIdx.x;
+    const uint32_t c = cnt[t];
+    if (threadIdx.x == 0) ranges[t] = make_uint2(off[t], off[t] + c);
+    if (c == 0 || c > (uint32_t)kSmallCap) return;
+    sort_bucket(s, t, cnt, off, tmp, keys, ids);
+}
+
+// One 1024-thread CTA per listed bucket of kSmallCap < size <= kBigCap.
+__global__ void __launch_bounds__(1024) sort_big_kernel(const uint32_t* __restrict__ big_list,
+                                                        const uint32_t* __restrict__ cnt,
+                                                        const uint32_t* __restrict__ off,
+                                                        const uint64_t* __restrict__ tmp, uint64_t* __restrict__ keys,
+                                                        uint32_t* __restrict__ ids)
+{
+    extern __shared__ uint64_t s_big[];
+    sort_bucket(s_big, big_list[blockIdx.x], cnt, off, tmp, keys, ids);
+}
+
 // Aligned bump layout of the workspace.
 struct WsLayout {
-    size_t scan_sums, offsets, totals, alt_keys, alt_ids, hist, hist_sums, bytes;
+    size_t scan_sums, offsets, totals, alt_keys, alt_ids, hist, hist_sums;
+    size_t tile_cnt, tile_off, cursor, tile_sums, stats, big_list, bytes;
 };
 
 inline size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-inline WsLayout ws_layout(int64_t vn, int64_t capacity)
+inline WsLayout ws_layout(int64_t vn, int64_t capacity, int64_t ntile_ids)
 {
     WsLayout L;
     size_t o = 0;
@@ -148,6 +264,12 @@ inline WsLayout ws_layout(int64_t vn, int64_t capacity)
     const int64_t nb = (capacity + kSortItems - 1) / kSortItems;
     L.hist = o;      o = align_up(o + sizeof(uint32_t) * 256 * (size_t)nb);
     L.hist_sums = o; o = align_up(o + scan_ws_bytes(256 * nb));
+    L.tile_cnt = o;  o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
+    L.tile_off = o;  o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
+    L.cursor = o;    o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
+    L.tile_sums = o; o = align_up(o + scan_ws_bytes(ntile_ids));
+    L.stats = o;     o = align_up(o + 4 * sizeof(unsigned int));
+    L.big_list = o;  o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
     L.bytes = o;
     return L;
 }
@@ -171,7 +293,11 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (width <= 0 || height <= 0 || width > 65535 * kTile || height > 65535 * kTile) return GS_ERR_INVALID_ARG;
     if (capacity < 0 || capacity > (int64_t)UINT32_MAX) return GS_ERR_INVALID_ARG;
     const int64_t vn = n * (int64_t)n_views;
-    const WsLayout L = ws_layout(vn, capacity);
+    const int tiles_x = tiles_x_of(width);
+    const int64_t tiles = (int64_t)tiles_x * tiles_y_of(height);
+    const int64_t ntile_ids = tiles * n_views;
+    if (ntile_ids > (int64_t)INT32_MAX) return GS_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(vn, capacity, ntile_ids);
     if (!ws) {
         *ws_bytes = L.bytes;
         return GS_OK;
@@ -180,10 +306,6 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (!proj || !tile_ranges || !n_instances) return GS_ERR_INVALID_ARG;
     if (n > 0 && (!proj->depth || !proj->rect || !proj->tiles_touched)) return GS_ERR_INVALID_ARG;
     if (capacity > 0 && (!keys || !ids)) return GS_ERR_INVALID_ARG;
-    const int tiles_x = tiles_x_of(width);
-    const int64_t tiles = (int64_t)tiles_x * tiles_y_of(height);
-    const int64_t ntile_ids = tiles * n_views;
-    if (ntile_ids > (int64_t)UINT32_MAX) return GS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     char* w = (char*)ws;
     unsigned long long* scan_sums = (unsigned long long*)(w + L.scan_sums);
@@ -193,17 +315,61 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     uint32_t* alt_ids = (uint32_t*)(w + L.alt_ids);
     uint32_t* hist = (uint32_t*)(w + L.hist);
     unsigned long long* hist_sums = (unsigned long long*)(w + L.hist_sums);
+    uint32_t* tile_cnt = (uint32_t*)(w + L.tile_cnt);
+    uint32_t* tile_off = (uint32_t*)(w + L.tile_off);
+    uint32_t* cursor = (uint32_t*)(w + L.cursor);
+    unsigned long long* tile_sums = (unsigned long long*)(w + L.tile_sums);
+    unsigned int* stats = (unsigned int*)(w + L.stats);
+    uint32_t* big_list = (uint32_t*)(w + L.big_list);
+    const ushort4* rect4 = reinterpret_cast<const ushort4*>(proj->rect);
+    const int threads = 256;
+    const unsigned gblocks = (unsigned)((vn + threads - 1) / threads);
 
-    // 1-2: offsets and the instance count
-    GS_CUDA_TRY((scan_launch<uint32_t, false>(proj->tiles_touched, vn, offsets, scan_sums, totals, s)));
-    unsigned long long total = 0;
-    GS_CUDA_TRY(cudaMemcpyAsync(&total, totals, sizeof(total), cudaMemcpyDeviceToHost, s));
+    // per-tile path: counts, bucket starts, totals
+    GS_CUDA_TRY(cudaMemsetAsync(tile_cnt, 0, sizeof(uint32_t) * (size_t)ntile_ids, s));
+    GS_CUDA_TRY(cudaMemsetAsync(stats, 0, 4 * sizeof(unsigned int), s));
+    if (vn > 0) {
+        count_tiles_kernel<<<gblocks, threads, 0, s>>>(proj->tiles_touched, rect4, n, vn, tiles_x, (int)tiles,
+                                                        tile_cnt);
+        GS_LAUNCH_CHECK();
+    }
+    GS_CUDA_TRY((scan_launch<uint32_t, false>(tile_cnt, ntile_ids, tile_off, tile_sums, totals, s)));
+    bucket_stats_kernel<<<(unsigned)((ntile_ids + threads - 1) / threads), threads, 0, s>>>(tile_cnt, tile_off,
+                                                                                           ntile_ids, cursor, stats,
+                                                                                           big_list);
+    GS_LAUNCH_CHECK();
+    struct {
+        unsigned long long total;
+        unsigned int st[4];
+    } host;
+    GS_CUDA_TRY(cudaMemcpyAsync(&host.total, totals, sizeof(host.total), cudaMemcpyDeviceToHost, s));
+    GS_CUDA_TRY(cudaMemcpyAsync(host.st, stats, sizeof(host.st), cudaMemcpyDeviceToHost, s));
     GS_CUDA_TRY(cudaStreamSynchronize(s));
-    *n_instances = (int64_t)total;
-    if ((int64_t)total > capacity) return GS_ERR_CAPACITY;
-    const int64_t N = (int64_t)total;
+    *n_instances = (int64_t)host.total;
+    if ((int64_t)host.total > capacity) return GS_ERR_CAPACITY;
+    if (host.total > 0 && host.st[0] <= (unsigned)kBigCap) {
+        scatter_tiles_kernel<<<gblocks, threads, 0, s>>>(proj->tiles_touched, rect4, proj->depth, n, vn, tiles_x,
+                                                          (int)tiles, cursor, alt_keys);
+        GS_LAUNCH_CHECK();
+        sort_small_kernel<<<(unsigned)ntile_ids, 256, 0, s>>>(tile_cnt, tile_off, alt_keys, keys, ids,
+                                                              reinterpret_cast<uint2*>(tile_ranges));
+        GS_LAUNCH_CHECK();
+        if (host.st[1] > 0) {
+            int P = 1;
+            while (P < (int)host.st[0]) P <<= 1;
+            const size_t smem = sizeof(uint64_t) * (size_t)P;
+            GS_CUDA_TRY(cudaFuncSetAttribute(sort_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            sort_big_kernel<<<host.st[1], 1024, smem, s>>>(big_list, tile_cnt, tile_off, alt_keys, keys, ids);
+            GS_LAUNCH_CHECK();
+        }
+        return GS_OK;
+    }
+
+    // LSD radix path (no instances, or a bucket too large for a block sort)
     GS_CUDA_TRY(cudaMemsetAsync(tile_ranges, 0, sizeof(uint32_t) * 2 * (size_t)ntile_ids, s));
+    const int64_t N = (int64_t)host.total;
     if (N == 0) return GS_OK;
+    GS_CUDA_TRY((scan_launch<uint32_t, false>(proj->tiles_touched, vn, offsets, scan_sums, totals + 1, s)));
 
     // passes: 32 depth bits + the tile-id bits, 8-bit digits
     const int bits = 32 + (ntile_ids > 1 ? bit_length((uint64_t)(ntile_ids - 1)) : 1);
@@ -212,15 +378,11 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     uint32_t* vbuf[2] = {ids, alt_ids};
     int cur = (npass & 1) ? 1 : 0;   // the last pass writes buffer 0 (the caller's)
 
-    // 3: emit
-    {
-        const int threads = 256;
-        emit_kernel<<<(unsigned)((vn + threads - 1) / threads), threads, 0, s>>>(
-            proj->tiles_touched, offsets, reinterpret_cast<const ushort4*>(proj->rect), proj->depth, n, vn, tiles_x,
-            (int)tiles, kbuf[cur], vbuf[cur]);
-        GS_LAUNCH_CHECK();
-    }
-    // 4: radix passes
+    // emit
+    emit_kernel<<<gblocks, threads, 0, s>>>(proj->tiles_touched, offsets, rect4, proj->depth, n, vn, tiles_x,
+                                            (int)tiles, kbuf[cur], vbuf[cur]);
+    GS_LAUNCH_CHECK();
+    // radix passes
     const int64_t nb = (N + kSortItems - 1) / kSortItems;
     for (int p = 0; p < npass; ++p) {
         const int shift = 8 * p;
@@ -234,12 +396,9 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
         GS_LAUNCH_CHECK();
         cur ^= 1;
     }
-    // 5: ranges
-    {
-        const int threads = 256;
-        tile_ranges_kernel<<<(unsigned)((N + threads - 1) / threads), threads, 0, s>>>(
-            keys, N, reinterpret_cast<uint2*>(tile_ranges));
-        GS_LAUNCH_CHECK();
-    }
+    // ranges
+    tile_ranges_kernel<<<(unsigned)((N + threads - 1) / threads), threads, 0, s>>>(keys, N,
+                                                                                 reinterpret_cast<uint2*>(tile_ranges));
+    GS_LAUNCH_CHECK();
     return GS_OK;
 }

@@ -55,6 +55,22 @@ def test_dense_lists_span_several_chunks_and_stop_early():
     assert st["e_fwd"] < st["instances"] * 256   # early stops happened
 
 
+def test_sort_bucket_sizes_over_2048_use_the_large_block_sort():
+    """~6000 wide Gaussians on a 32x32 view: 4 tile buckets of ~6000 instances."""
+    sc = scenes.random_small_scene(31, n=6000, width=32, height=32, sh_degree=0, log_lo=-1.5, log_hi=-1.0,
+                                   logit_mu=-2.0, spread=0.6)
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] > 4 * 2048
+
+
+def test_sort_bucket_over_16384_uses_the_radix_path():
+    """20000 Gaussians on one 16x16 tile: a single bucket larger than a block sort holds."""
+    sc = scenes.random_small_scene(32, n=20000, width=16, height=16, sh_degree=0, log_lo=-2.0, log_hi=-1.0,
+                                   logit_mu=-3.0, spread=0.3)
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] > 16384
+
+
 def test_multi_view_small_reduced():
     sc = scenes.make_scene("small", n=20000)
     base = sc.cameras[0]
