@@ -220,9 +220,12 @@ def run_gpu(args):
 
     sc = scenes.make_scene(args.config)
     tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda")
-    pert = torch.from_numpy(sc.perturbed_params).cuda()
-    target = tr.render(pert).clone()     # training target: render of the perturbed scene
-    del pert
+    if sc.target_kind == "uniform":
+        target = torch.from_numpy(sc.target_uniform).cuda()
+    else:
+        pert = torch.from_numpy(sc.perturbed_params).cuda()
+        target = tr.render(pert).clone()     # training target: render of the perturbed scene
+        del pert
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()

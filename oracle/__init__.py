@@ -63,7 +63,8 @@ def _declare(L):
     for s in ("_f32", "_f64"):
         getattr(L, "oracle_project" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_project" + s).restype = _I32
-        getattr(L, "oracle_render" + s).argtypes = [_P, _P, _P, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]
+        getattr(L, "oracle_render" + s).argtypes = [_P, _P, _P, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                    _P]
         getattr(L, "oracle_render" + s).restype = _I32
         getattr(L, "oracle_vjp" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_vjp" + s).restype = _I32
@@ -136,8 +137,10 @@ def project(params, sh_degree, cam, opts, prec="f32"):
     return dict(rec=rec, rect=rect, visible=vis, clamp=clamp)
 
 
-def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_last=False, want_sig=False):
-    """O7..O10 for one view.  target: [3,H,W] or None (forward only)."""
+def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_last=False, want_sig=False,
+           tile_mask=None):
+    """O7..O10 for one view.  target: [3,H,W] or None (forward only).
+    tile_mask: None or [tiles] bool -- render only those tiles (others stay 0)."""
     dt = _dt(prec)
     rec, rect, vis = proj["rec"], proj["rect"], proj["visible"]
     n = rec.shape[0]
@@ -150,9 +153,10 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
     last = np.zeros(H * W, np.int32) if want_last else None
     sig = np.zeros(1, np.uint64) if want_sig else None
     tgt = np.ascontiguousarray(np.asarray(target, dt)) if target is not None else None
+    tm = np.ascontiguousarray(np.asarray(tile_mask, np.uint8)) if tile_mask is not None else None
     rc = getattr(lib(), "oracle_render_" + prec)(_ptr(rec), _ptr(rect), _ptr(vis), n, W, H, _ptr(opts9(opts)), mode,
                                                   _ptr(tgt), _ptr(img), _ptr(loss), _ptr(g2), _ptr(touched),
-                                                  _ptr(counts), _ptr(last), _ptr(sig))
+                                                  _ptr(counts), _ptr(last), _ptr(sig), _ptr(tm))
     assert rc == 0
     out = dict(image=img, loss=float(loss[0]) if target is not None else None, grad2d=g2, touched=touched,
                e_fwd=int(counts[0]), e_bwd=int(counts[1]), e_comp=int(counts[2]))

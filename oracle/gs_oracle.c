@@ -400,7 +400,7 @@ static int64_t list_literal(const REAL* rec, const int32_t* rect, const uint8_t*
 typedef struct { int64_t* off; cand_t* items; } tile_lists_t;
 
 static int build_tile_lists(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
-                            int tiles_x, int tiles_y, tile_lists_t* tl)
+                            int tiles_x, int tiles_y, const uint8_t* tile_mask, tile_lists_t* tl)
 {
     int64_t nt = (int64_t)tiles_x * tiles_y;
     int64_t* cnt = (int64_t*)calloc((size_t)nt + 1, sizeof(int64_t));
@@ -409,7 +409,8 @@ static int build_tile_lists(const REAL* rec, const int32_t* rect, const uint8_t*
         if (!visible[g]) continue;
         const int32_t* rc = rect + 4 * g;
         for (int ty = rc[1]; ty < rc[3]; ++ty)
-            for (int tx = rc[0]; tx < rc[2]; ++tx) cnt[(int64_t)ty * tiles_x + tx + 1]++;
+            for (int tx = rc[0]; tx < rc[2]; ++tx)
+                if (!tile_mask || tile_mask[(int64_t)ty * tiles_x + tx]) cnt[(int64_t)ty * tiles_x + tx + 1]++;
     }
     for (int64_t i = 0; i < nt; ++i) cnt[i + 1] += cnt[i];
     cand_t* items = (cand_t*)malloc(sizeof(cand_t) * (size_t)(cnt[nt] > 0 ? cnt[nt] : 1));
@@ -421,6 +422,7 @@ static int build_tile_lists(const REAL* rec, const int32_t* rect, const uint8_t*
         const int32_t* rc = rect + 4 * g;
         for (int ty = rc[1]; ty < rc[3]; ++ty)
             for (int tx = rc[0]; tx < rc[2]; ++tx) {
+                if (tile_mask && !tile_mask[(int64_t)ty * tiles_x + tx]) continue;
                 int64_t k = fill[(int64_t)ty * tiles_x + tx]++;
                 items[k].depth = rec[10 * g + 9];
                 items[k].g = g;
@@ -441,7 +443,7 @@ int64_t FN(oracle_tile_lists)(const REAL* rec, const int32_t* rect, const uint8_
     int tiles_x = (width + TILE - 1) / TILE, tiles_y = (height + TILE - 1) / TILE;
     int64_t nt = (int64_t)tiles_x * tiles_y;
     tile_lists_t tl;
-    if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, &tl)) return -1;
+    if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, 0, &tl)) return -1;
     int64_t total = tl.off[nt];
     memcpy(offsets, tl.off, sizeof(int64_t) * (size_t)(nt + 1));
     if (ids)
@@ -471,11 +473,14 @@ static uint64_t fnv(uint64_t h, uint64_t v)
  *         E_comp (entries composited).
  * last_idx: [H*W] list position of the last composited entry (-1 if none), or NULL.
  * sig: decision signature (hash of every discrete decision), or NULL.
+ * tile_mask: NULL, or [tiles] u8: only pixels of tiles with a nonzero entry are
+ *   rendered (the rest of image is left untouched and is excluded from the loss,
+ *   the gradients and the counts); used to check large images tile by tile.
  */
 int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
                       int width, int height, const double* opts9, int mode, const REAL* target,
                       REAL* image, double* loss, double* grad2d, uint8_t* touched, int64_t* counts,
-                      int32_t* last_idx, uint64_t* sig)
+                      int32_t* last_idx, uint64_t* sig, const uint8_t* tile_mask)
 {
     opts_t op;
     load_opts(opts9, &op);
@@ -484,7 +489,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
     tile_lists_t tl = {0, 0};
     cand_t* buf = 0;
     if (mode == 1) {
-        if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, &tl)) return -1;
+        if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, tile_mask, &tl)) return -1;
     } else {
         buf = (cand_t*)malloc(sizeof(cand_t) * (size_t)(n > 0 ? n : 1));
         if (!buf) return -1;
@@ -504,6 +509,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
     for (int py = 0; py < height; ++py) {
         for (int px = 0; px < width; ++px) {
             const int tx = px / TILE, ty = py / TILE;
+            if (tile_mask && !tile_mask[(int64_t)ty * tiles_x + tx]) continue;
             const cand_t* list;
             int64_t len;
             if (mode == 1) {

@@ -182,3 +182,114 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
         assert not tr.grads.any().item(), "grads not cleared"
     log(f"[parity] {sc.name}: {stats}")
     return stats
+
+
+def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, device="cuda", log=print):
+    """Parity at full size where the oracle cannot render whole images quickly.
+
+    Per checked view the oracle projects every Gaussian (visibility and records
+    compared for all), builds every tile list (sorted keys/ids/ranges compared for
+    all), and renders a sample of tiles: random ones plus every tile of a sample
+    of Gaussians, so those Gaussians' 2D gradients are complete.  Images are
+    compared on the sampled tiles; the training target of the GPU (its render of
+    the perturbed scene) must equal the oracle's render of the perturbed scene
+    there bit for bit, and the oracle's loss terms use the oracle's own target.
+    Single-view scenes also compare the sampled Gaussians' dense gradients and
+    their Adam update."""
+    rng = np.random.default_rng(seed)
+    V, n = sc.n_views, sc.n
+    views = list(range(V)) if check_views is None else list(check_views)
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device=device)
+    pert = torch.from_numpy(sc.perturbed_params).to(device)
+    target = tr.render(pert).clone()
+    del pert
+    tr.project()
+    torch.cuda.synchronize()
+    tt = tr.tiles_touched.cpu().numpy().view(np.uint32)
+    N = tr.bin_sort()
+    torch.cuda.synchronize()
+    keys = tr.keys[:N].cpu().numpy().view(np.uint64)
+    ids = tr.ids[:N].cpu().numpy().view(np.uint32)
+    ranges = tr.ranges.cpu().numpy().view(np.uint32).reshape(V, -1, 2)
+    tr.eval_counts.zero_()
+    tr.raster(target)
+    torch.cuda.synchronize()
+    img = tr.image.cpu().numpy()
+    tgt_gpu = target.cpu().numpy()
+    stats = dict(instances=int(N), views=views)
+    tiles = tr.tiles
+    tiles_x = (sc.cameras[0].width + 15) // 16
+    sampled_g = {}
+    for v in views:
+        cam = sc.cameras[v]
+        pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
+        vis = pr["visible"].astype(bool)
+        assert np.array_equal(tt[v] > 0, vis), f"view {v}: visibility"
+        rec = tr.rec[v][torch.from_numpy(np.flatnonzero(vis)).to(device)].cpu().numpy()
+        o = pr["rec"][vis]
+        exp = np.stack([o[:, 0], o[:, 1], np.float32(-0.5) * o[:, 2], o[:, 3], np.float32(-0.5) * o[:, 4], o[:, 5],
+                        o[:, 6], o[:, 7], o[:, 8]], 1).astype(np.float32)
+        assert np.array_equal(bits(rec[:, :9]), bits(exp)), f"view {v}: projection records"
+        off, oids = oracle.tile_lists(pr, cam)
+        base = int(ranges[v][:, 0][np.diff(off) > 0].min()) if off[-1] else 0
+        m = oids.size
+        assert np.array_equal(ids[base:base + m], oids.astype(np.uint32)), f"view {v}: sorted ids"
+        tile_of = np.repeat(np.arange(tiles, dtype=np.uint64), np.diff(off).astype(np.int64))
+        dbits = bits(pr["rec"][oids, 9]).astype(np.uint64)
+        assert np.array_equal(keys[base:base + m], ((np.uint64(v * tiles) + tile_of) << np.uint64(32)) | dbits)
+        full = np.diff(off) > 0
+        assert np.array_equal(ranges[v][full, 0], (off[:-1][full] + base).astype(np.uint32)), f"view {v}: ranges"
+        # sampled tiles: random ones + all tiles of sampled Gaussians with small rects
+        rect = pr["rect"]
+        area = (rect[:, 2] - rect[:, 0]) * (rect[:, 3] - rect[:, 1])
+        cand = np.flatnonzero(vis & (area <= 4))
+        gs = rng.choice(cand, min(n_gauss, cand.size), replace=False)
+        mask = np.zeros(tiles, bool)
+        mask[rng.choice(tiles, n_tiles, replace=False)] = True
+        for g in gs:
+            for ty in range(rect[g, 1], rect[g, 3]):
+                mask[ty * tiles_x + rect[g, 0]:ty * tiles_x + rect[g, 2]] = True
+        prp = oracle.project(sc.perturbed_params, sc.sh_degree, cam, sc.opts)
+        otgt = oracle.render(prp, cam, sc.opts, tile_mask=mask)["image"]
+        H, W = cam.height, cam.width
+        pix = np.repeat(np.repeat(mask.reshape(-1, tiles_x), 16, 0), 16, 1)[:H, :W]
+        assert np.array_equal(bits(tgt_gpu[v][:, pix]), bits(otgt[:, pix])), f"view {v}: target render"
+        out = oracle.render(pr, cam, sc.opts, target=otgt, tile_mask=mask)
+        d = np.abs(img[v][:, pix].astype(np.float64) - out["image"][:, pix])
+        assert d.max() <= IMG_ATOL, f"view {v}: image max abs err {d.max()}"
+        g2d = tr.grad2d[v][torch.from_numpy(gs).to(device)].cpu().numpy()[:, :9]
+        tch = tr.touched[v][torch.from_numpy(gs).to(device)].cpu().numpy()
+        assert np.array_equal(tch, out["touched"][gs]), f"view {v}: touched (sampled)"
+        ok, st = grad_report(g2d, out["grad2d"][gs])
+        assert ok, f"view {v}: grad2d (sampled) {st}"
+        stats.setdefault("grad2d", []).append(st)
+        stats.setdefault("sampled_pixels", []).append(int(pix.sum()))
+        sampled_g[v] = (gs, out["grad2d"][gs], out["touched"][gs], pr["clamp"][gs])
+    if V == 1:
+        gs, g2, tch, clamp = sampled_g[0]
+        tr.compact()
+        torch.cuda.synchronize()
+        sub = np.ascontiguousarray(sc.params[:, gs])
+        ref = oracle.vjp(sub, sc.sh_degree, sc.cameras[0], sc.opts, g2, tch, clamp)
+        got = tr.grads[:, torch.from_numpy(gs).to(device)].cpu().numpy()
+        ok, st = grad_report(got, ref)
+        assert ok, f"dense gradients (sampled) {st}"
+        stats["grads"] = st
+        # Adam for the sampled Gaussians, fed the GPU's gradients
+        p_o = sub.copy()
+        m_o = np.zeros_like(p_o)
+        v_o = np.zeros_like(p_o)
+        last_o = np.zeros(gs.size, np.int32)
+        sel = np.flatnonzero(tch).astype(np.uint32)
+        g_o = got.astype(np.float32).copy()
+        oracle.adam_deferred(p_o, m_o, v_o, g_o, last_o, scenes.lr_rows(sc.lr, sc.sh_degree), sel, 1,
+                             tr.betas[0], tr.betas[1], tr.eps)
+        tr.adam(1)
+        torch.cuda.synchronize()
+        idx = torch.from_numpy(gs).to(device)
+        assert np.array_equal(bits(tr.params[:, idx].cpu().numpy()), bits(p_o)), "Adam params (sampled)"
+        assert np.array_equal(bits(tr.adam_m[:, idx].cpu().numpy()), bits(m_o)), "Adam m (sampled)"
+    log(f"[sampled parity] {sc.name}: {stats}")
+    del tr
+    torch.cuda.empty_cache()
+    return stats

@@ -199,3 +199,21 @@ def test_gradient_of_a_culled_or_untouched_gaussian_is_zero():
     p[2, 0] = -1.0   # behind the camera
     g = _analytic(p, sc)
     assert np.all(g[:, 0] == 0)
+
+
+def test_tile_masked_render_equals_full_render_on_those_tiles():
+    sc = scenes.make_scene("small", n=5000)
+    cam = scenes.Camera(sc.cameras[0].R, sc.cameras[0].t, 250.0, 250.0, 160.0, 90.0, 320, 180)
+    pr = oracle.project(sc.params, 0, cam, sc.opts)
+    tgt = np.random.default_rng(2).uniform(0, 1, (3, 180, 320)).astype(np.float32)
+    full = oracle.render(pr, cam, sc.opts, target=tgt)
+    tiles = 20 * 12
+    mask = np.zeros(tiles, bool)
+    mask[np.random.default_rng(3).choice(tiles, 40, replace=False)] = True
+    part = oracle.render(pr, cam, sc.opts, target=tgt, tile_mask=mask)
+    pix = np.repeat(np.repeat(mask.reshape(12, 20), 16, 0), 16, 1)[:180, :320]
+    assert np.array_equal(part["image"][:, pix], full["image"][:, pix])
+    assert not part["image"][:, ~pix].any()
+    allm = oracle.render(pr, cam, sc.opts, target=tgt, tile_mask=np.ones(tiles, bool))
+    assert np.array_equal(allm["grad2d"], full["grad2d"]) and allm["loss"] == full["loss"]
+    assert (allm["e_fwd"], allm["e_bwd"], allm["e_comp"]) == (full["e_fwd"], full["e_bwd"], full["e_comp"])
