@@ -223,7 +223,7 @@ def run_gpu(args):
     if sc.target_kind == "uniform":
         target = torch.from_numpy(sc.target_uniform).cuda()
     else:
-        pert = torch.from_numpy(sc.perturbed_params).cuda()
+        pert = tr.to_device_layout(sc.perturbed_params)
         target = tr.render(pert).clone()     # training target: render of the perturbed scene
         del pert
     torch.cuda.synchronize()

@@ -23,7 +23,7 @@ GS_REC_FLOAT4 = 3
 GS_GRAD2D_STRIDE = 12
 
 EXPORTS = ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
-           "gs_error_string", "gs_param_rows", "gs_num_tiles", "gs_version")
+           "gs_error_string", "gs_param_rows", "gs_param_stride", "gs_num_tiles", "gs_version")
 
 
 class GsCamera(ctypes.Structure):
@@ -79,6 +79,8 @@ def lib():
         L.gs_error_string.restype = ctypes.c_char_p
         L.gs_param_rows.argtypes = [_I32]
         L.gs_param_rows.restype = _I32
+        L.gs_param_stride.argtypes = [_I32]
+        L.gs_param_stride.restype = _I32
         L.gs_num_tiles.argtypes = [_I32, _I32]
         L.gs_num_tiles.restype = _I64
         L.gs_version.argtypes = []
@@ -173,6 +175,10 @@ def gs_adam_deferred(params, grads, m, v, last_step, n, sh_degree, idx, n_idx, t
 
 def gs_param_rows(sh_degree) -> int:
     return lib().gs_param_rows(sh_degree)
+
+
+def gs_param_stride(sh_degree) -> int:
+    return lib().gs_param_stride(sh_degree)
 
 
 def gs_num_tiles(width, height) -> int:

@@ -16,6 +16,8 @@ extern "C" const char* gs_error_string(gs_status s)
 
 extern "C" int32_t gs_param_rows(int32_t sh_degree) { return gs::param_rows(sh_degree); }
 
+extern "C" int32_t gs_param_stride(int32_t sh_degree) { return gs::param_stride(sh_degree); }
+
 extern "C" int64_t gs_num_tiles(int32_t width, int32_t height)
 {
     if (width <= 0 || height <= 0) return 0;

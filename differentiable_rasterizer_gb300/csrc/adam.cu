@@ -3,9 +3,8 @@
 // unnecessary memory accesses for Gaussians with zero gradients"), made exactly
 // equal to dense Adam by replaying the skipped zero-gradient steps first.
 //
-// One thread per (listed Gaussian, group of 4 parameter rows): the loads of all
-// its rows are issued before any arithmetic, and consecutive threads touch
-// consecutive Gaussians of a row (coalesced when the list is dense).  The bias
+// One thread per (listed Gaussian, float4 chunk of its [stride] parameter
+// block): 16 contiguous bytes of params, m, v and grads per thread.  The bias
 // corrections of the current step come from the host (the same fp64 binary
 // exponentiation as the device code, so the same values); replayed steps
 // compute their own.  A row whose moments are both +0 skips the replay: a
@@ -33,7 +32,7 @@ struct AdamArgs {
     float* __restrict__ v;
     int32_t* __restrict__ last_step;
     int64_t n;
-    int32_t rows;
+    int32_t stride, chunks;
     const uint32_t* idx;
     const int64_t* n_idx;
     int32_t t;
@@ -42,10 +41,6 @@ struct AdamArgs {
     float bc1t, bc2t;   // bias corrections of step t
     int32_t flush;
 };
-
-constexpr int kRowsPerThread = 4;
-
-__device__ __forceinline__ int row_group(int r) { return r < 3 ? 0 : (r < 6 ? 1 : (r < 10 ? 2 : (r == 10 ? 3 : 4))); }
 
 __device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, float lr, float b1, float b2, float eps,
                                          float bc1, float bc2)
@@ -58,45 +53,53 @@ __device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, 
     v = vn;
 }
 
+// Catch up and step one parameter (learning rate lr) of a Gaussian last
+// stepped at s.
+__device__ __forceinline__ void adam_elem(float lr, int s, int t, float b1, float b2, float eps, float bc1t,
+                                          float bc2t, float& p, float& m, float& v, float g)
+{
+    for (int j = s + 1; j < t; ++j) {
+        if (__float_as_uint(m) == 0u && __float_as_uint(v) == 0u) break;   // zero state: replay is a no-op
+        const float bc1 = (float)(1.0 - powi_binary((double)b1, j));
+        const float bc2 = (float)(1.0 - powi_binary((double)b2, j));
+        adam_one(p, m, v, 0.0f, lr, b1, b2, eps, bc1, bc2);
+    }
+    adam_one(p, m, v, g, lr, b1, b2, eps, bc1t, bc2t);
+}
+
+// Learning-rate group of parameter k: mean, log-scale, quaternion, opacity, colour.
+__device__ __forceinline__ float lr_of(const AdamArgs& a, int k)
+{
+    return k < 3 ? a.lr[0] : (k < 6 ? a.lr[1] : (k < 10 ? a.lr[2] : (k == 10 ? a.lr[3] : a.lr[4])));
+}
+
+// One thread per (listed Gaussian, float4 chunk of its parameter block): each
+// thread moves 16 contiguous bytes of params, m, v and grads in and out, so a
+// warp covers whole 256-byte Gaussian blocks whether the list is dense or not.
 __global__ void __launch_bounds__(256) adam_deferred_kernel(AdamArgs a)
 {
     const int64_t count = a.flush ? a.n : *a.n_idx;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= count) return;
-    const int64_t g = a.flush ? i : (int64_t)a.idx[i];
+    const int64_t e = i / a.chunks;
+    if (e >= count) return;
+    const int c = (int)(i - e * a.chunks);
+    const int64_t g = a.flush ? e : (int64_t)a.idx[e];
     const int s = a.last_step[g];
     if (s >= a.t) return;
-    const int r0 = blockIdx.y * kRowsPerThread;
-    float p[kRowsPerThread], m[kRowsPerThread], v[kRowsPerThread], gr[kRowsPerThread];
-#pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-        const int r = r0 + k;
-        if (r < a.rows) {
-            const size_t e = (size_t)r * a.n + g;
-            p[k] = a.params[e];
-            m[k] = a.m[e];
-            v[k] = a.v[e];
-            gr[k] = a.flush ? 0.0f : a.grads[e];
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-        const int r = r0 + k;
-        if (r >= a.rows) break;
-        const float lr = a.lr[row_group(r)];
-        for (int j = s + 1; j < a.t; ++j) {
-            if (__float_as_uint(m[k]) == 0u && __float_as_uint(v[k]) == 0u) break;   // zero state: replay is a no-op
-            const float bc1 = (float)(1.0 - powi_binary((double)a.b1, j));
-            const float bc2 = (float)(1.0 - powi_binary((double)a.b2, j));
-            adam_one(p[k], m[k], v[k], 0.0f, lr, a.b1, a.b2, a.eps, bc1, bc2);
-        }
-        adam_one(p[k], m[k], v[k], gr[k], lr, a.b1, a.b2, a.eps, a.bc1t, a.bc2t);
-        const size_t e = (size_t)r * a.n + g;
-        a.params[e] = p[k];
-        a.m[e] = m[k];
-        a.v[e] = v[k];
-        if (!a.flush) a.grads[e] = 0.0f;
-    }
+    const size_t off = (size_t)g * a.stride + 4 * c;
+    float4 p = *reinterpret_cast<const float4*>(a.params + off);
+    float4 m = *reinterpret_cast<const float4*>(a.m + off);
+    float4 v = *reinterpret_cast<const float4*>(a.v + off);
+    const float4 gr = a.flush ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *reinterpret_cast<const float4*>(a.grads + off);
+    const int k = 4 * c;
+    adam_elem(lr_of(a, k), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.x, m.x, v.x, gr.x);
+    adam_elem(lr_of(a, k + 1), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.y, m.y, v.y, gr.y);
+    adam_elem(lr_of(a, k + 2), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.z, m.z, v.z, gr.z);
+    adam_elem(lr_of(a, k + 3), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.w, m.w, v.w, gr.w);
+    *reinterpret_cast<float4*>(a.params + off) = p;
+    *reinterpret_cast<float4*>(a.m + off) = m;
+    *reinterpret_cast<float4*>(a.v + off) = v;
+    if (!a.flush) *reinterpret_cast<float4*>(a.grads + off) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 }
 
 __global__ void __launch_bounds__(256) stamp_kernel(AdamArgs a)
@@ -121,6 +124,7 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     if (n == 0) return GS_OK;
     if (!params || !m || !v || !last_step) return GS_ERR_INVALID_ARG;
     if (!flush && (!grads || !idx || !n_idx)) return GS_ERR_INVALID_ARG;
+    if (!aligned16(params) || !aligned16(m) || !aligned16(v) || (!flush && !aligned16(grads))) return GS_ERR_INVALID_ARG;
     AdamArgs a;
     a.params = params;
     a.grads = grads;
@@ -128,7 +132,8 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     a.v = v;
     a.last_step = last_step;
     a.n = n;
-    a.rows = rows;
+    a.stride = param_stride(sh_degree);
+    a.chunks = a.stride / 4;
     a.idx = idx;
     a.n_idx = n_idx;
     a.t = t;
@@ -145,10 +150,10 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     // The list length lives on the device: the grid covers n entries and threads
     // beyond the list return at once.
     const int threads = 256;
-    const int64_t bx = (n + threads - 1) / threads;
-    const unsigned by = (unsigned)((rows + kRowsPerThread - 1) / kRowsPerThread);
+    const int64_t bx = (n * a.chunks + threads - 1) / threads;
+    if (bx > INT32_MAX) return GS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    adam_deferred_kernel<<<dim3((unsigned)bx, by), threads, 0, s>>>(a);
+    adam_deferred_kernel<<<(unsigned)bx, threads, 0, s>>>(a);
     GS_LAUNCH_CHECK();
     int64_t bs = (n + threads - 1) / threads;
     if (bs > (int64_t)sms * 8) bs = (int64_t)sms * 8;

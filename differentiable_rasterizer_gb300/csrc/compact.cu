@@ -7,7 +7,8 @@
 //   union:      idx[V] = ascending list of Gaussians touched in any view
 //   decode:     for each Gaussian of the union, the projection VJP of every
 //               touching view is summed in view order in registers and added to
-//               the dense gradient with one read-modify-write; the consumed
+//               the dense gradient with one read-modify-write of the Gaussian's
+//               block ([n][stride] layout, float4 accesses); the consumed
 //               grad2d / touched entries are cleared.
 // With one owner (this GPU) no record leaves the device, so the "send" of the
 // encoded list is the list itself.
@@ -45,14 +46,20 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
     if (i >= *a.n_union) return;
     const int64_t g = a.idx_union[i];
     GaussParams<DEG> gp;
-    gp.load(a.params, a.n, g);
-    constexpr int P = GaussParams<DEG>::kRows;
+    gp.load(a.params, g);
     // Current gradient values are loaded up front with the parameters, so the
-    // final write-back is a run of independent stores rather than P dependent
-    // read-modify-writes.
-    float grad[P];
+    // write-back is a run of independent stores.
+    constexpr int kVec = GaussParams<DEG>::kVec;
+    float4* gdst = reinterpret_cast<float4*>(a.grads + (size_t)g * GaussParams<DEG>::kStride);
+    float grad[kVec * 4];
 #pragma unroll
-    for (int r = 0; r < P; ++r) grad[r] = a.grads[(size_t)r * a.n + g];
+    for (int i = 0; i < kVec; ++i) {
+        const float4 t = gdst[i];
+        grad[4 * i] = t.x;
+        grad[4 * i + 1] = t.y;
+        grad[4 * i + 2] = t.z;
+        grad[4 * i + 3] = t.w;
+    }
     for (int v = 0; v < cs.n_views; ++v) {
         const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
         if (!a.touched[o]) continue;
@@ -69,7 +76,7 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
         a.touched[o] = 0;
     }
 #pragma unroll
-    for (int r = 0; r < P; ++r) a.grads[(size_t)r * a.n + g] = grad[r];
+    for (int i = 0; i < kVec; ++i) gdst[i] = make_float4(grad[4 * i], grad[4 * i + 1], grad[4 * i + 2], grad[4 * i + 3]);
 }
 
 struct CompactWs {
@@ -104,7 +111,8 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
     if (*ws_bytes < L.bytes) return GS_ERR_INVALID_ARG;
     if (!opts || !n_idx) return GS_ERR_INVALID_ARG;
     if (n > 0 && (!grad2d || !touched || !params || !idx || !grads)) return GS_ERR_INVALID_ARG;
-    if (param_rows(sh_degree) < 0 || !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    if (param_rows(sh_degree) < 0 || !aligned16(grad2d) || !aligned16(params) || !aligned16(grads))
+        return GS_ERR_INVALID_ARG;
     gs_status st = check_views(cams, n_views);
     if (st != GS_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;

@@ -140,6 +140,8 @@ struct CamSet {
 #define GS_LAUNCH_CHECK() GS_CUDA_TRY(cudaPeekAtLastError())
 
 inline int param_rows(int sh_degree) { return sh_degree == 0 ? 14 : (sh_degree == 3 ? 59 : -1); }
+// Floats per Gaussian in the parameter, gradient and moment buffers.
+inline int param_stride(int sh_degree) { return sh_degree == 0 ? 16 : (sh_degree == 3 ? 64 : -1); }
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 

@@ -1,6 +1,6 @@
 // project.cu -- gs_project: EWA projection of every Gaussian into every view.
 //
-// One thread per Gaussian reads its parameters once (coalesced SoA rows) and
+// One thread per Gaussian reads its parameter block once (float4 loads) and
 // loops over the views, so a batch of V views costs one pass over the
 // parameters instead of V (Grendel, abstract: batched multi-view training).
 // Culling follows GS-Scale's frustum-culling step (abstract), done on the GPU.
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(128) project_kernel(ProjectArgs a, CamSet cs)
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= a.n) return;
     GaussParams<DEG> gp;
-    gp.load(a.params, a.n, g);
+    gp.load(a.params, g);
     for (int v = 0; v < cs.n_views; ++v) {
         const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
         ProjOut po;
@@ -104,7 +104,8 @@ extern "C" gs_status gs_project(const float* params, int64_t n, int32_t sh_degre
     gs_status st = check_views(cams, n_views);
     if (st != GS_OK) return st;
     if (n == 0) return GS_OK;
-    if (!params || !out->rec || !out->depth || !out->rect || !out->tiles_touched || !aligned16(out->rec))
+    if (!params || !aligned16(params) || !out->rec || !out->depth || !out->rect || !out->tiles_touched ||
+        !aligned16(out->rec))
         return GS_ERR_INVALID_ARG;
     ProjectArgs a;
     a.params = params;

@@ -20,20 +20,33 @@ namespace gs {
 template <int DEG>
 struct GaussParams {
     static constexpr int kCol = DEG == 0 ? 3 : 48;
-    static constexpr int kRows = 11 + kCol;
+    static constexpr int kRows = 11 + kCol;                 // parameters used (P)
+    static constexpr int kStride = DEG == 0 ? 16 : 64;      // floats per Gaussian in memory
+    static constexpr int kVec = (kRows + 3) / 4;            // float4 loads covering P
     float mu[3], ls[3], q[4], logit;
-    float col[kCol];   // degree 3: col[3k + c] = coefficient k, channel c
-    __device__ __forceinline__ void load(const float* __restrict__ P, int64_t n, int64_t g)
+    float col[kCol];   // degree 3: col[3j + c] = coefficient j, channel c
+    // Gaussian g's block of the [n][kStride] parameter buffer, as float4 loads.
+    __device__ __forceinline__ void load(const float* __restrict__ P, int64_t g)
     {
+        const float4* src = reinterpret_cast<const float4*>(P + (size_t)g * kStride);
+        float v[kVec * 4];
 #pragma unroll
-        for (int i = 0; i < 3; ++i) mu[i] = __ldg(P + (size_t)i * n + g);
+        for (int i = 0; i < kVec; ++i) {
+            const float4 t = __ldg(src + i);
+            v[4 * i] = t.x;
+            v[4 * i + 1] = t.y;
+            v[4 * i + 2] = t.z;
+            v[4 * i + 3] = t.w;
+        }
 #pragma unroll
-        for (int i = 0; i < 3; ++i) ls[i] = __ldg(P + (size_t)(3 + i) * n + g);
+        for (int i = 0; i < 3; ++i) mu[i] = v[i];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = __ldg(P + (size_t)(6 + i) * n + g);
-        logit = __ldg(P + (size_t)10 * n + g);
+        for (int i = 0; i < 3; ++i) ls[i] = v[3 + i];
 #pragma unroll
-        for (int i = 0; i < kCol; ++i) col[i] = __ldg(P + (size_t)(11 + i) * n + g);
+        for (int i = 0; i < 4; ++i) q[i] = v[6 + i];
+        logit = v[10];
+#pragma unroll
+        for (int i = 0; i < kCol; ++i) col[i] = v[11 + i];
     }
 };
 

@@ -6,7 +6,8 @@ memory) and calls the five C-ABI entry points in order on one stream:
     gs_project -> gs_bin_sort -> gs_raster_fused_fwd_bwd -> gs_grad_compact -> gs_adam_deferred
 
 Buffer layout in HBM (fp32 unless stated):
-    params, grads, adam_m, adam_v   [P, n]           P = 14 (RGB) or 59 (SH degree 3)
+    params, grads, adam_m, adam_v   [n, stride]      stride = 16 (RGB, P = 14) or 64 (SH 3, P = 59);
+                                                     one aligned block per Gaussian
     last_step                       [n] int32
     rec                             [V, n, 12]       3 float4 per (view, Gaussian)
     depth, tiles_touched, rect      [V, n], [V, n], [V, n, 4] uint16
@@ -35,6 +36,7 @@ class GaussianTrainer:
         self.device = torch.device(device)
         self.sh_degree = sh_degree
         self.P = abi.gs_param_rows(sh_degree)
+        self.stride = abi.gs_param_stride(sh_degree)
         p = torch.as_tensor(params, dtype=torch.float32)
         assert p.shape[0] == self.P, (p.shape, self.P)
         self.n = int(p.shape[1])
@@ -49,7 +51,7 @@ class GaussianTrainer:
         self.t = 0
         dev = self.device
         n, V = self.n, self.V
-        self.params = p.to(dev).contiguous()
+        self.params = self.to_device_layout(p)
         self.grads = torch.zeros_like(self.params)
         self.adam_m = torch.zeros_like(self.params)
         self.adam_v = torch.zeros_like(self.params)
@@ -72,6 +74,18 @@ class GaussianTrainer:
         self.capacity = 0
         self.n_instances = 0
         self._alloc_instances(capacity if capacity is not None else max(1024, 4 * n * V // 8))
+
+    # ------------------------------------------------------------------ layout
+    def to_device_layout(self, rows) -> torch.Tensor:
+        """[P, n] parameter rows (numpy or torch) -> device [n, stride] blocks (padding zero)."""
+        r = torch.as_tensor(rows, dtype=torch.float32)
+        out = torch.zeros((r.shape[1], self.stride), dtype=torch.float32, device=self.device)
+        out[:, :self.P] = r.to(self.device).t()
+        return out
+
+    def rows(self, blocks: torch.Tensor) -> torch.Tensor:
+        """Device [n, stride] blocks -> [P, n] rows (a copy), the generator's layout."""
+        return blocks[:, :self.P].t().contiguous()
 
     # ------------------------------------------------------------------ buffers
     def _alloc_instances(self, capacity: int):

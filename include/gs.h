@@ -44,12 +44,16 @@
  *   - Thread-compatible: no hidden globals; concurrent calls on different
  *     buffers are safe.
  *
- * Parameter buffer ([P][n] fp32, row-major, one row per scalar parameter):
- *   rows 0-2 mean (world), 3-5 log-scale, 6-9 quaternion (w, x, y, z; any norm),
- *   10 opacity logit, colour: degree 0 -> rows 11-13 RGB (P = 14);
- *   degree 3 -> SH coefficient k (0..15, k = l^2 + l + m, real orthonormal basis
- *   without Condon-Shortley phase), channel c at row 11 + 3k + c (P = 59);
- *   colour = max(0, sum_k coef_k Y_k(dir) + 0.5), dir = unit(mean - camera centre).
+ * Parameter buffer ([n][stride] fp32, Gaussian-major: Gaussian g's parameters
+ * are params[g * stride + k], stride = gs_param_stride(sh_degree) = 16 or 64 so
+ * each Gaussian is one aligned 64- or 256-byte block; entries k >= P are padding,
+ * never read by the projection and left as given by the optimizer when zero):
+ *   k 0-2 mean (world), 3-5 log-scale, 6-9 quaternion (w, x, y, z; any norm),
+ *   10 opacity logit, colour: degree 0 -> k 11-13 RGB (P = 14);
+ *   degree 3 -> SH coefficient j (0..15, j = l^2 + l + m, real orthonormal basis
+ *   without Condon-Shortley phase), channel c at k = 11 + 3j + c (P = 59);
+ *   colour = max(0, sum_j coef_j Y_j(dir) + 0.5), dir = unit(mean - camera centre).
+ * Gradients and the Adam moments use the same layout.
  */
 #ifndef GS_H
 #define GS_H
@@ -130,7 +134,7 @@ typedef struct gs_proj {
  * Cull: z_c <= near_z, non-finite values, zero quaternion, det(Sigma2D) <= 0,
  * or an empty tile rect.  Radius = ceil(3 sqrt(lambda_max(Sigma2D))); rect =
  * tiles floor((m -/+ r)/16).  Opacity = sigmoid(logit).
- * params: [P][n]; cams/opts: HOST; out: device arrays described above.
+ * params: [n][stride]; cams/opts: HOST; out: device arrays described above.
  * Errors: INVALID_ARG for NULL pointers, n < 0, n_views outside 1..GS_MAX_VIEWS,
  * sh_degree not 0 or 3, differing view sizes; CUDA on launch failure. */
 GS_API gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, const gs_camera* cams, int32_t n_views,
@@ -182,7 +186,7 @@ GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const u
  * and added to grads (one read-modify-write per Gaussian).  grad2d and touched
  * are cleared for the entries consumed.
  * idx: [(n_views + 1) * n] u32 out; n_idx: [n_views + 1] int64 DEVICE out.
- * grads: [P][n] fp32 accumulated (+=).  cams/opts: HOST, as given to gs_project.
+ * grads: [n][stride] fp32 accumulated (+=).  cams/opts: HOST, as given to gs_project.
  * Errors: INVALID_ARG for bad pointers, sizes or a too small workspace. */
 GS_API gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const float* params, int64_t n, int32_t sh_degree,
                           const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
@@ -221,7 +225,7 @@ GS_API gs_status gs_grad_compact_static(float* grad2d, uint8_t* touched, const f
  * bc = 1 - beta^j with beta^j by binary exponentiation in fp64, rounded to fp32.
  * flush = 1: every Gaussian with last_step < t is brought to step t with zero
  *   gradients (idx, n_idx, grads unused) -- call before reading or saving params.
- * params, grads, m, v: [P][n]; last_step: [n] int32 (0 = never stepped).
+ * params, grads, m, v: [n][stride]; last_step: [n] int32 (0 = never stepped).
  * idx: [>= *n_idx] u32, n_idx: DEVICE int64.  lr: HOST [5] per group (mean,
  * log-scale, quaternion, opacity, colour).  t >= 1.
  * Errors: INVALID_ARG for bad pointers or t < 1. */
@@ -231,7 +235,8 @@ GS_API gs_status gs_adam_deferred(float* params, float* grads, float* m, float* 
 
 /* Static helpers (no device work). */
 GS_API const char* gs_error_string(gs_status s);
-GS_API int32_t gs_param_rows(int32_t sh_degree);                     /* 14, 59, or -1 */
+GS_API int32_t gs_param_rows(int32_t sh_degree);                     /* P: 14, 59, or -1 */
+GS_API int32_t gs_param_stride(int32_t sh_degree);                   /* 16, 64, or -1 */
 GS_API int64_t gs_num_tiles(int32_t width, int32_t height);          /* ceil(W/16) * ceil(H/16) */
 GS_API const char* gs_version(void);
 

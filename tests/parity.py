@@ -158,7 +158,7 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
                    oprojs[v]["clamp"], ref_grads)
     union = oracle.compact(np.any(np.stack([o["touched"] for o in orend]), 0).astype(np.uint8))
     assert n_idx[V] == union.size and np.array_equal(idx[V][:n_idx[V]], union), "union list"
-    grads = tr.grads.cpu().numpy()
+    grads = tr.rows(tr.grads).cpu().numpy()
     ok, st = grad_report(grads, ref_grads)
     stats["grads"] = st
     assert ok, f"dense gradients out of tolerance {st}"
@@ -175,9 +175,9 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
         oracle.adam_deferred(p_o, m_o, v_o, g_o, last_o, lr_rows, union, 1, tr.betas[0], tr.betas[1], tr.eps)
         tr.adam(1)
         torch.cuda.synchronize()
-        assert np.array_equal(bits(tr.params.cpu().numpy()), bits(p_o)), "Adam params"
-        assert np.array_equal(bits(tr.adam_m.cpu().numpy()), bits(m_o)), "Adam m"
-        assert np.array_equal(bits(tr.adam_v.cpu().numpy()), bits(v_o)), "Adam v"
+        assert np.array_equal(bits(tr.rows(tr.params).cpu().numpy()), bits(p_o)), "Adam params"
+        assert np.array_equal(bits(tr.rows(tr.adam_m).cpu().numpy()), bits(m_o)), "Adam m"
+        assert np.array_equal(bits(tr.rows(tr.adam_v).cpu().numpy()), bits(v_o)), "Adam v"
         assert np.array_equal(tr.last_step.cpu().numpy(), last_o), "last_step"
         assert not tr.grads.any().item(), "grads not cleared"
     log(f"[parity] {sc.name}: {stats}")
@@ -200,7 +200,7 @@ def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, de
     V, n = sc.n_views, sc.n
     views = list(range(V)) if check_views is None else list(check_views)
     tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device=device)
-    pert = torch.from_numpy(sc.perturbed_params).to(device)
+    pert = tr.to_device_layout(sc.perturbed_params)
     target = tr.render(pert).clone()
     del pert
     tr.project()
@@ -271,7 +271,7 @@ def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, de
         torch.cuda.synchronize()
         sub = np.ascontiguousarray(sc.params[:, gs])
         ref = oracle.vjp(sub, sc.sh_degree, sc.cameras[0], sc.opts, g2, tch, clamp)
-        got = tr.grads[:, torch.from_numpy(gs).to(device)].cpu().numpy()
+        got = tr.rows(tr.grads)[:, torch.from_numpy(gs).to(device)].cpu().numpy()
         ok, st = grad_report(got, ref)
         assert ok, f"dense gradients (sampled) {st}"
         stats["grads"] = st
@@ -287,8 +287,8 @@ def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, de
         tr.adam(1)
         torch.cuda.synchronize()
         idx = torch.from_numpy(gs).to(device)
-        assert np.array_equal(bits(tr.params[:, idx].cpu().numpy()), bits(p_o)), "Adam params (sampled)"
-        assert np.array_equal(bits(tr.adam_m[:, idx].cpu().numpy()), bits(m_o)), "Adam m (sampled)"
+        assert np.array_equal(bits(tr.rows(tr.params)[:, idx].cpu().numpy()), bits(p_o)), "Adam params (sampled)"
+        assert np.array_equal(bits(tr.rows(tr.adam_m)[:, idx].cpu().numpy()), bits(m_o)), "Adam m (sampled)"
     log(f"[sampled parity] {sc.name}: {stats}")
     del tr
     torch.cuda.empty_cache()

@@ -36,6 +36,7 @@ def test_library_exports_every_declared_symbol(L):
 def test_static_helpers(L):
     from differentiable_rasterizer_gb300 import abi
     assert abi.gs_param_rows(0) == 14 and abi.gs_param_rows(3) == 59 and abi.gs_param_rows(2) == -1
+    assert abi.gs_param_stride(0) == 16 and abi.gs_param_stride(3) == 64 and abi.gs_param_stride(1) == -1
     assert abi.gs_num_tiles(1920, 1080) == 120 * 68
     assert abi.gs_num_tiles(64, 64) == 16
     assert "sm_103a" in abi.gs_version()

@@ -116,7 +116,7 @@ def test_no_gaussians_and_all_culled():
     tr.train_step(torch.from_numpy(sc.target_uniform).cuda())
     torch.cuda.synchronize()
     assert tr.n_instances == 0 and tr.n_idx.cpu().numpy().sum() == 0
-    assert np.array_equal(tr.params.cpu().numpy(), sc.params)
+    assert np.array_equal(tr.rows(tr.params).cpu().numpy(), sc.params)
 
 
 def test_capacity_growth_retries():
@@ -145,21 +145,21 @@ def test_adam_deferred_catch_up_and_flush_bitexact():
         mask = rng.uniform(size=n) < (0.02 if t < 6 else 0.5)
         idx = np.flatnonzero(mask).astype(np.uint32)
         g = (rng.standard_normal((P, n)) * mask).astype(np.float32)
-        tr.grads.copy_(torch.from_numpy(g))
+        tr.grads.copy_(tr.to_device_layout(g))
         tr.idx[tr.V, :idx.size].copy_(torch.from_numpy(idx.view(np.int32)))
         tr.n_idx[tr.V] = idx.size
         tr.adam(t)
         go = g.copy()
         oracle.adam_deferred(po, mo, vo, go, lo, lr_rows, idx, t, 0.9, 0.999, 1e-8)
     torch.cuda.synchronize()
-    assert np.array_equal(parity.bits(tr.params.cpu().numpy()), parity.bits(po))
-    assert np.array_equal(parity.bits(tr.adam_m.cpu().numpy()), parity.bits(mo))
+    assert np.array_equal(parity.bits(tr.rows(tr.params).cpu().numpy()), parity.bits(po))
+    assert np.array_equal(parity.bits(tr.rows(tr.adam_m).cpu().numpy()), parity.bits(mo))
     assert np.array_equal(tr.last_step.cpu().numpy(), lo)
     tr.adam(8, flush=True)
     oracle.adam_deferred(po, mo, vo, go, lo, lr_rows, None, 8, 0.9, 0.999, 1e-8, flush=True)
     torch.cuda.synchronize()
-    assert np.array_equal(parity.bits(tr.params.cpu().numpy()), parity.bits(po))
-    assert np.array_equal(parity.bits(tr.adam_v.cpu().numpy()), parity.bits(vo))
+    assert np.array_equal(parity.bits(tr.rows(tr.params).cpu().numpy()), parity.bits(po))
+    assert np.array_equal(parity.bits(tr.rows(tr.adam_v).cpu().numpy()), parity.bits(vo))
     assert (tr.last_step.cpu().numpy() == 8).all()
 
 
@@ -172,7 +172,7 @@ def test_three_training_steps_track_the_oracle():
     tr = pipeline.GaussianTrainer(sc.params, 0, sc.cameras, sc.opts, sc.lr)
     tgt = torch.from_numpy(targets).cuda()
     for step in range(3):
-        p_before = tr.params.cpu().numpy()
+        p_before = tr.rows(tr.params).cpu().numpy()
         tr.train_step(tgt)
         torch.cuda.synchronize()
         pr = oracle.project(p_before, 0, sc.cameras[0], sc.opts)
