@@ -1,181 +1,280 @@
 // binsort.cu -- gs_bin_sort: 16x16 tile binning with (tile, depth) keys and a
 // sort, then per-tile ranges of the sorted instance list.
 //
-// Per-tile path (the normal case):
-//   1. count instances per (view, tile) with atomics;
-//   2. exclusive scan of the counts = the start of every tile's bucket;
-//   3. one pass over the buckets: instance total, largest bucket, list of buckets
-//      larger than a shared-memory block sort holds; scatter cursors;
-//   4. the totals go to the host (the step's one host synchronisation);
-//   5. scatter: every visible (view, Gaussian) appends (depth bits << 32 | index)
-//      to the bucket of each tile of its rect (atomic cursor, any order);
-//   6. one CTA per bucket sorts it by (depth bits, index) in shared memory
-//      (bitonic) and writes key = ((v*tiles + tile) << 32) | depth bits, value =
-//      index, and the tile's range.
-// The result equals a stable sort by (tile, depth) of instances emitted in
-// (view, Gaussian) order: within a bucket the index breaks depth ties.
-// Buckets over kBigCap instances use the LSD radix path instead: scan of
-// tiles_touched, emit, 8-bit LSD passes (block digit histograms -> scan ->
-// stable scatter with ranks from __match_any_sync), ranges from the sorted keys.
+// The sort by key = ((v * tiles + tile) << 32) | bits(depth), stable in the
+// Gaussian index, is done as a counting sort on the high part followed by a
+// sort of every (view, tile) bucket on (bits(depth), index):
+//
+//   1. count:   block b of view v owns a contiguous range of that view's
+//               Gaussians and counts their instances per tile in shared memory
+//               (native integer atomics); the counts go out tile-major,
+//               cnt[(v * tiles + tile) * B + b];
+//   2. scan:    one exclusive scan of cnt gives, for every (tile, block), where
+//               that block's instances of that tile start in the output;
+//   3. stats:   tile ranges, the instance total, the largest bucket and the lists
+//               of buckets too large for a warp sort; the totals go to the host
+//               (the step's one host synchronisation: capacity check);
+//   4. scatter: the same blocks append (bits(depth) << 32 | g) to their slice of
+//               every bucket through shared-memory cursors (any order);
+//   5. sort:    buckets of <= kWarpCap instances: one warp, bitonic in registers;
+//               <= kRegCap: one CTA, bitonic in registers (long strides through
+//               shared memory); <= kBigCap: one CTA, bitonic in shared memory;
+//               larger: one CTA splits the bucket by key range into kSplit
+//               sub-buckets (counting scatter), sorts the small ones as above and
+//               splits the large ones again (depth first, at most seven levels).
+// Every bucket ends sorted by (bits(depth), g), so the output equals a stable
+// radix sort of instances emitted in (view, Gaussian) order.
 #include "gs_common.cuh"
 #include "scan.cuh"
 
 namespace gs {
 
-constexpr int kSortThreads = 256;
-constexpr int kSortPerThread = 16;
-constexpr int kSortItems = kSortThreads * kSortPerThread;   // one block's tile of keys
-constexpr int kWarps = kSortThreads / 32;
+constexpr int kBinThreads = 1024;          // count / scatter block size
+constexpr int kBinBlocks = 304;            // count / scatter blocks over all views (2 per SM)
+constexpr int kBandTiles = 40960;          // shared-memory tile counters per block (160 KB)
+constexpr int64_t kMaxCounts = 1 << 22;    // cap on (view, tile, block) count entries
+constexpr int kWarpCap = 256;              // bucket sizes sorted by one warp (8 keys per lane)
+constexpr int kRegCap = 2048;              // bucket sizes sorted by one 256-thread CTA in registers
+constexpr int kRegThreads = 256;
+constexpr int kBigCap = 16384;             // bucket sizes sorted by one CTA in shared memory
+constexpr int kSplit = 1024;               // sub-buckets per split of a larger bucket
+constexpr int kStack = 8 * kSplit;         // pending sub-buckets (<= 1023 per level, <= 7 levels)
+constexpr int kSortWarps = 8;              // warps per block of the warp-sort kernel
 
-__global__ void emit_kernel(const uint32_t* __restrict__ touched_cnt, const uint32_t* __restrict__ offsets,
-                            const ushort4* __restrict__ rect, const float* __restrict__ depth, int64_t n,
-                            int64_t total_vn, int tiles_x, int tiles, uint64_t* __restrict__ keys,
-                            uint32_t* __restrict__ ids)
+// Partition of the (view, Gaussian) axis and of the tile rows for count/scatter.
+struct BinGeom {
+    int64_t n;           // Gaussians per view
+    int64_t per_block;   // Gaussians per block
+    int32_t B;           // blocks per view
+    int32_t tiles_x, tiles_y, tiles;
+    int32_t band_rows;   // tile rows per block band
+};
+
+// -------------------------------------------------------------------- count / scatter
+// Block (b, band, v): Gaussians [b * per_block, (b + 1) * per_block) of view v,
+// tile rows [band * band_rows, ...) of that view.
+template <bool kScatter>
+__global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __restrict__ touched_cnt,
+                                                          const ushort4* __restrict__ rect,
+                                                          const float* __restrict__ depth, BinGeom G,
+                                                          uint32_t* __restrict__ cnt, uint64_t* __restrict__ tmp)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= total_vn) return;
-    const uint32_t cnt = touched_cnt[i];
-    if (cnt == 0) return;
-    const int64_t v = i / n;
-    const uint32_t g = (uint32_t)(i - v * n);
-    const ushort4 r = rect[i];
-    const uint64_t dbits = (uint64_t)__float_as_uint(depth[i]);
-    uint32_t off = offsets[i];
-    const uint64_t vbase = (uint64_t)v * (uint64_t)tiles;
-    for (int ty = r.y; ty < r.w; ++ty)
-        for (int tx = r.x; tx < r.z; ++tx) {
-            keys[off] = ((vbase + (uint64_t)(ty * tiles_x + tx)) << 32) | dbits;
-            ids[off] = g;
-            ++off;
+    extern __shared__ uint32_t s_cnt[];
+    const int b = blockIdx.x, band = blockIdx.y, v = blockIdx.z;
+    const int row0 = band * G.band_rows;
+    const int row1 = min(G.tiles_y, row0 + G.band_rows);
+    const int nt = (row1 - row0) * G.tiles_x;
+    const size_t cbase = ((size_t)v * (size_t)G.tiles + (size_t)row0 * (size_t)G.tiles_x) * (size_t)G.B + (size_t)b;
+    // counters (count) or cursors = this block's start in every bucket (scatter)
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) s_cnt[i] = kScatter ? cnt[cbase + (size_t)i * G.B] : 0u;
+    __syncthreads();
+    const int64_t g0 = (int64_t)b * G.per_block;
+    const int64_t g1 = min(G.n, g0 + G.per_block);
+    const size_t vb = (size_t)v * (size_t)G.n;
+    constexpr int U = 4;   // Gaussians in flight per thread
+    for (int64_t gb = g0 + threadIdx.x; gb < g1; gb += (int64_t)U * blockDim.x) {
+        uint32_t tc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t g = gb + (int64_t)u * blockDim.x;
+            tc[u] = g < g1 ? __ldg(touched_cnt + vb + g) : 0u;
         }
-}
-
-__device__ __forceinline__ int64_t sort_item(int it)
-{
-    // warp-striped: warp w owns [w*512, (w+1)*512) of the block tile, 32 consecutive per iteration
-    return (int64_t)blockIdx.x * kSortItems + (int64_t)(threadIdx.x >> 5) * (32 * kSortPerThread) +
-           (int64_t)it * 32 + (threadIdx.x & 31);
-}
-
-__global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(const uint64_t* __restrict__ keys, int64_t N,
-                                                                  int shift, uint32_t mask, uint32_t* __restrict__ hist,
-                                                                  int64_t nb)
-{
-    __shared__ uint32_t s_h[256];
-    s_h[threadIdx.x] = 0;
-    __syncthreads();
+        ushort4 r[U];
+        uint64_t key[U];
 #pragma unroll
-    for (int it = 0; it < kSortPerThread; ++it) {
-        const int64_t i = sort_item(it);
-        if (i < N) atomicAdd(&s_h[(uint32_t)(keys[i] >> shift) & mask], 1u);
-    }
-    __syncthreads();
-    hist[(int64_t)threadIdx.x * nb + blockIdx.x] = s_h[threadIdx.x];   // digit-major
-}
-
-__global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
-    const uint64_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, int64_t N, int shift, uint32_t mask,
-    const uint32_t* __restrict__ offs, int64_t nb, uint64_t* __restrict__ keys_out, uint32_t* __restrict__ vals_out)
-{
-    __shared__ uint32_t s_cnt[kWarps][256];
-    __shared__ uint32_t s_goff[256];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int u = 0; u < U; ++u) {
+            const int64_t g = gb + (int64_t)u * blockDim.x;
+            r[u] = tc[u] ? __ldg(rect + vb + g) : make_ushort4(0, 0, 0, 0);
+            if (kScatter)
+                key[u] = tc[u] ? (((uint64_t)__float_as_uint(__ldg(depth + vb + g)) << 32) | (uint64_t)g) : 0ull;
+        }
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) s_cnt[w][threadIdx.x] = 0;
-    s_goff[threadIdx.x] = offs[(int64_t)threadIdx.x * nb + blockIdx.x];
-    __syncthreads();
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    uint64_t k[kSortPerThread];
-    uint32_t rank[kSortPerThread];
-    uint32_t dig[kSortPerThread];
-#pragma unroll
-    for (int it = 0; it < kSortPerThread; ++it) {
-        const int64_t i = sort_item(it);
-        const bool valid = i < N;
-        k[it] = valid ? keys_in[i] : 0ull;
-        const uint32_t d = valid ? ((uint32_t)(k[it] >> shift) & mask) : 256u;
-        dig[it] = d;
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        const uint32_t before = valid ? s_cnt[warp][d] : 0u;
-        __syncwarp();
-        if (valid && (peers & lt_mask) == 0) s_cnt[warp][d] = before + (uint32_t)__popc(peers);
-        __syncwarp();
-        rank[it] = before + (uint32_t)__popc(peers & lt_mask);
-    }
-    __syncthreads();
-    {   // exclusive scan over warps per digit
-        uint32_t run = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const uint32_t c = s_cnt[w][threadIdx.x];
-            s_cnt[w][threadIdx.x] = run;
-            run += c;
+        for (int u = 0; u < U; ++u) {
+            if (!tc[u]) continue;
+            const int y0 = max((int)r[u].y, row0), y1 = min((int)r[u].w, row1);
+            for (int ty = y0; ty < y1; ++ty) {
+                uint32_t* row = s_cnt + (ty - row0) * G.tiles_x;
+                for (int tx = r[u].x; tx < r[u].z; ++tx) {
+                    const uint32_t pos = atomicAdd(row + tx, 1u);
+                    if (kScatter) tmp[pos] = key[u];
+                }
+            }
         }
     }
+    if (kScatter) return;
     __syncthreads();
-#pragma unroll
-    for (int it = 0; it < kSortPerThread; ++it) {
-        const int64_t i = sort_item(it);
-        if (i < N) {
-            const uint32_t d = dig[it];
-            const uint32_t pos = s_goff[d] + s_cnt[warp][d] + rank[it];
-            keys_out[pos] = k[it];
-            vals_out[pos] = vals_in[i];
-        }
-    }
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) cnt[cbase + (size_t)i * G.B] = s_cnt[i];
 }
 
-__global__ void tile_ranges_kernel(const uint64_t* __restrict__ keys, int64_t N, uint2* __restrict__ ranges)
-{
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= N) return;
-    const uint32_t t = (uint32_t)(keys[i] >> 32);
-    if (i == 0 || (uint32_t)(keys[i - 1] >> 32) != t) ranges[t].x = (uint32_t)i;
-    if (i == N - 1 || (uint32_t)(keys[i + 1] >> 32) != t) ranges[t].y = (uint32_t)(i + 1);
-}
-
-constexpr int kSmallCap = 2048;    // bucket sizes sorted by the 256-thread kernel (16 KB)
-constexpr int kBigCap = 16384;     // bucket sizes sorted by the 1024-thread kernel (128 KB)
-
-__global__ void count_tiles_kernel(const uint32_t* __restrict__ touched_cnt, const ushort4* __restrict__ rect,
-                                   int64_t n, int64_t total_vn, int tiles_x, int tiles, uint32_t* __restrict__ cnt)
-{
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= total_vn || touched_cnt[i] == 0) return;
-    const int64_t v = i / n;
-    const ushort4 r = rect[i];
-    uint32_t* c = cnt + v * tiles;
-    for (int ty = r.y; ty < r.w; ++ty)
-        for (int tx = r.x; tx < r.z; ++tx) atomicAdd(c + ty * tiles_x + tx, 1u);
-}
-
-// stats[0] = largest bucket, stats[1] = number of buckets over kSmallCap
-__global__ void bucket_stats_kernel(const uint32_t* __restrict__ cnt, const uint32_t* __restrict__ off, int64_t nb,
-                                    uint32_t* __restrict__ cursor, unsigned int* __restrict__ stats,
-                                    uint32_t* __restrict__ big_list)
+// Per (view, tile): range [start, end) from the scanned counts; stats[0] =
+// largest bucket, stats[1..3] = number of buckets listed in lists[0][...]
+// (kWarpCap < size <= kRegCap), lists[1][...] (<= kBigCap) and lists[2][...]
+// (larger), each list nb long.
+__global__ void bucket_stats_kernel(const uint32_t* __restrict__ off, int32_t B, int64_t nb,
+                                    const unsigned long long* __restrict__ total, uint2* __restrict__ ranges,
+                                    unsigned int* __restrict__ stats, uint32_t* __restrict__ lists)
 {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= nb) return;
-    const uint32_t c = cnt[t];
-    cursor[t] = off[t];
-    if (c == 0) return;
+    const uint32_t s = off[(size_t)t * B];
+    const uint32_t e = t + 1 < nb ? off[(size_t)(t + 1) * B] : (uint32_t)*total;
+    ranges[t] = make_uint2(s, e);
+    const uint32_t c = e - s;
+    if (c <= (uint32_t)kWarpCap) return;
     atomicMax(stats, c);
-    if (c > (uint32_t)kSmallCap) big_list[atomicAdd(stats + 1, 1u)] = (uint32_t)t;
+    const int cls = c <= (uint32_t)kRegCap ? 0 : (c <= (uint32_t)kBigCap ? 1 : 2);
+    lists[(size_t)cls * nb + atomicAdd(stats + 1 + cls, 1u)] = (uint32_t)t;
 }
 
-__global__ void scatter_tiles_kernel(const uint32_t* __restrict__ touched_cnt, const ushort4* __restrict__ rect,
-                                     const float* __restrict__ depth, int64_t n, int64_t total_vn, int tiles_x,
-                                     int tiles, uint32_t* __restrict__ cursor, uint64_t* __restrict__ tmp)
+// -------------------------------------------------------------------- sorts
+// Sorted keys leave as key = (tile_lin << 32) | bits(depth), value = g.
+__device__ __forceinline__ void emit_sorted(uint64_t k, uint64_t hi, uint64_t* __restrict__ keys,
+                                            uint32_t* __restrict__ ids, size_t pos)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= total_vn || touched_cnt[i] == 0) return;
-    const int64_t v = i / n;
-    const uint32_t g = (uint32_t)(i - v * n);
-    const ushort4 r = rect[i];
-    const uint64_t key = ((uint64_t)__float_as_uint(depth[i]) << 32) | g;
-    uint32_t* cur = cursor + v * tiles;
-    for (int ty = r.y; ty < r.w; ++ty)
-        for (int tx = r.x; tx < r.z; ++tx) tmp[atomicAdd(cur + ty * tiles_x + tx, 1u)] = key;
+    keys[pos] = hi | (k >> 32);
+    ids[pos] = (uint32_t)k;
+}
+
+// Bitonic sort of 32 * E keys held by one warp, lane l owning elements
+// [l * E, (l + 1) * E): strides below E are register swaps, the others lane
+// exchanges.
+template <int E>
+__device__ __forceinline__ void warp_bitonic(uint64_t (&x)[E])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= E) {
+                const int lj = j / E;
+                const bool lower = (lane & lj) == 0;
+#pragma unroll
+                for (int r = 0; r < E; ++r) {
+                    const bool up = (((lane * E + r) & k) == 0);
+                    const uint64_t y = __shfl_xor_sync(0xffffffffu, x[r], lj);
+                    x[r] = (lower == up) ? (y < x[r] ? y : x[r]) : (y > x[r] ? y : x[r]);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < E; ++r) {
+                    if ((r & j) == 0) {
+                        const bool up = (((lane * E + r) & k) == 0);
+                        const uint64_t p = x[r], q = x[r | j];
+                        if ((p > q) == up) {
+                            x[r] = q;
+                            x[r | j] = p;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void warp_sort_e(const uint64_t* __restrict__ src, size_t o, int c, uint64_t hi,
+                                            uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t x[E];
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = lane * E + r;
+        x[r] = i < c ? src[o + i] : ~0ull;
+    }
+    warp_bitonic<E>(x);
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = lane * E + r;
+        if (i < c) emit_sorted(x[r], hi, keys, ids, o + i);
+    }
+}
+
+// One warp sorts src[o, o + c), 0 < c <= kWarpCap, into keys / ids at o.
+__device__ __forceinline__ void warp_sort(const uint64_t* __restrict__ src, size_t o, int c, uint64_t hi,
+                                          uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
+{
+    if (c <= 32) warp_sort_e<1>(src, o, c, hi, keys, ids);
+    else if (c <= 64) warp_sort_e<2>(src, o, c, hi, keys, ids);
+    else if (c <= 128) warp_sort_e<4>(src, o, c, hi, keys, ids);
+    else warp_sort_e<8>(src, o, c, hi, keys, ids);
+}
+
+// Shared-memory slot of element i in a block-sorted array of E keys per thread
+// (one pad word per E keys: blocked and striped accesses stay near conflict free).
+template <int E>
+__device__ __forceinline__ int pad_slot(int i) { return i + i / E; }
+
+// A kRegThreads-thread CTA sorts src[o, o + c), c <= kRegThreads * E: thread t
+// holds elements [t * E, (t + 1) * E) in registers; strides below E are register
+// swaps, strides below 32 E lane exchanges, the rest go through shared memory s
+// (kRegThreads * (E + 1) keys).
+template <int E>
+__device__ __forceinline__ void reg_sort(const uint64_t* __restrict__ src, size_t o, int c, uint64_t hi,
+                                         uint64_t* __restrict__ keys, uint32_t* __restrict__ ids, uint64_t* s)
+{
+    constexpr int P = kRegThreads * E;
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < P; i += kRegThreads) s[pad_slot<E>(i)] = i < c ? src[o + i] : ~0ull;
+    __syncthreads();
+    uint64_t x[E];
+#pragma unroll
+    for (int r = 0; r < E; ++r) x[r] = s[pad_slot<E>(tid * E + r)];
+    __syncthreads();
+#pragma unroll
+    for (int k = 2; k <= P; k <<= 1) {
+        if ((k >> 1) >= 32 * E) {
+#pragma unroll
+            for (int r = 0; r < E; ++r) s[pad_slot<E>(tid * E + r)] = x[r];
+            __syncthreads();
+            for (int j = k >> 1; j >= 32 * E; j >>= 1) {
+                for (int i = tid; i < P; i += kRegThreads) {
+                    const int ixj = i ^ j;
+                    if (ixj > i) {
+                        const uint64_t a = s[pad_slot<E>(i)], b = s[pad_slot<E>(ixj)];
+                        if ((a > b) == ((i & k) == 0)) {
+                            s[pad_slot<E>(i)] = b;
+                            s[pad_slot<E>(ixj)] = a;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+#pragma unroll
+            for (int r = 0; r < E; ++r) x[r] = s[pad_slot<E>(tid * E + r)];
+            __syncthreads();
+        }
+#pragma unroll
+        for (int j = (k >> 1) < 32 * E ? (k >> 1) : 16 * E; j > 0; j >>= 1) {
+            if (j >= E) {
+                const int lj = j / E;
+                const bool lower = (lane & lj) == 0;
+#pragma unroll
+                for (int r = 0; r < E; ++r) {
+                    const bool up = (((tid * E + r) & k) == 0);
+                    const uint64_t y = __shfl_xor_sync(0xffffffffu, x[r], lj);
+                    x[r] = (lower == up) ? (y < x[r] ? y : x[r]) : (y > x[r] ? y : x[r]);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < E; ++r) {
+                    if ((r & j) == 0) {
+                        const bool up = (((tid * E + r) & k) == 0);
+                        const uint64_t p = x[r], q = x[r | j];
+                        if ((p > q) == up) {
+                            x[r] = q;
+                            x[r | j] = p;
+                        }
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < E; ++r) s[pad_slot<E>(tid * E + r)] = x[r];
+    __syncthreads();
+    for (int i = tid; i < c; i += kRegThreads) emit_sorted(s[pad_slot<E>(i)], hi, keys, ids, o + i);
 }
 
 // Bitonic sort of s[0, P) ascending (P a power of two), all threads of the block.
@@ -199,86 +298,246 @@ __device__ __forceinline__ void block_bitonic(uint64_t* s, int P)
     }
 }
 
-__device__ __forceinline__ void sort_bucket(uint64_t* s, uint32_t t, const uint32_t* __restrict__ cnt,
-                                            const uint32_t* __restrict__ off, const uint64_t* __restrict__ tmp,
-                                            uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
+// All threads of the block sort src[o, o + c), c <= kBigCap, through s.
+__device__ __forceinline__ void cta_sort(uint64_t* s, const uint64_t* src, size_t o, int c, uint64_t hi,
+                                         uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
 {
-    const int c = (int)cnt[t];
-    const uint32_t o = off[t];
     int P = 1;
     while (P < c) P <<= 1;
-    for (int i = threadIdx.x; i < P; i += blockDim.x) s[i] = i < c ? tmp[o + i] : ~0ull;
+    for (int i = threadIdx.x; i < P; i += blockDim.x) s[i] = i < c ? src[o + i] : ~0ull;
     __syncthreads();
     block_bitonic(s, P);
-    const uint64_t hi = (uint64_t)t << 32;
-    for (int i = threadIdx.x; i < c; i += blockDim.x) {
-        const uint64_t k = s[i];
-        keys[o + i] = hi | (k >> 32);
-        ids[o + i] = (uint32_t)k;
-    }
+    for (int i = threadIdx.x; i < c; i += blockDim.x) emit_sorted(s[i], hi, keys, ids, o + i);
+    __syncthreads();
 }
 
-// One 256-thread CTA per bucket: writes every bucket's range, sorts buckets of
-// at most kSmallCap instances.
-__global__ void __launch_bounds__(256) sort_small_kernel(const uint32_t* __restrict__ cnt,
-                                                         const uint32_t* __restrict__ off,
-                                                         const uint64_t* __restrict__ tmp, uint64_t* __restrict__ keys,
-                                                         uint32_t* __restrict__ ids, uint2* __restrict__ ranges)
+// Warp w of the block sorts bucket blockIdx.x * kSortWarps + w if it holds
+// 1..kWarpCap instances.
+__global__ void __launch_bounds__(kSortWarps * 32) sort_warp_kernel(const uint2* __restrict__ ranges, int64_t nb,
+                                                                    const uint64_t* __restrict__ tmp,
+                                                                    uint64_t* __restrict__ keys,
+                                                                    uint32_t* __restrict__ ids)
 {
-    __shared__ uint64_t s[kSmallCap];
-    const uint32_t t = blockIdx.x;
-    const uint32_t c = cnt[t];
-    if (threadIdx.x == 0) ranges[t] = make_uint2(off[t], off[t] + c);
-    if (c == 0 || c > (uint32_t)kSmallCap) return;
-    sort_bucket(s, t, cnt, off, tmp, keys, ids);
+    const int64_t t = (int64_t)blockIdx.x * kSortWarps + (threadIdx.x >> 5);
+    if (t >= nb) return;
+    const uint2 r = ranges[t];
+    const int c = (int)(r.y - r.x);
+    if (c == 0 || c > kWarpCap) return;
+    warp_sort(tmp, r.x, c, (uint64_t)t << 32, keys, ids);
 }
 
-// One 1024-thread CTA per listed bucket of kSmallCap < size <= kBigCap.
-__global__ void __launch_bounds__(1024) sort_big_kernel(const uint32_t* __restrict__ big_list,
-                                                        const uint32_t* __restrict__ cnt,
-                                                        const uint32_t* __restrict__ off,
+// One kRegThreads-thread CTA per listed bucket of kWarpCap < size <= kRegCap.
+__global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* __restrict__ list,
+                                                               const uint2* __restrict__ ranges,
+                                                               const uint64_t* __restrict__ tmp,
+                                                               uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
+{
+    __shared__ uint64_t s[kRegThreads * 9];
+    const uint32_t t = list[blockIdx.x];
+    const uint2 r = ranges[t];
+    const int c = (int)(r.y - r.x);
+    const uint64_t hi = (uint64_t)t << 32;
+    if (c <= 2 * kRegThreads) reg_sort<2>(tmp, r.x, c, hi, keys, ids, s);
+    else if (c <= 4 * kRegThreads) reg_sort<4>(tmp, r.x, c, hi, keys, ids, s);
+    else reg_sort<8>(tmp, r.x, c, hi, keys, ids, s);
+}
+
+// One 1024-thread CTA per listed bucket of kRegCap < size <= kBigCap.
+__global__ void __launch_bounds__(1024) sort_mid_kernel(const uint32_t* __restrict__ list,
+                                                        const uint2* __restrict__ ranges,
                                                         const uint64_t* __restrict__ tmp, uint64_t* __restrict__ keys,
                                                         uint32_t* __restrict__ ids)
 {
-    extern __shared__ uint64_t s_big[];
-    sort_bucket(s_big, big_list[blockIdx.x], cnt, off, tmp, keys, ids);
+    extern __shared__ uint64_t s_mid[];
+    const uint32_t t = list[blockIdx.x];
+    const uint2 r = ranges[t];
+    cta_sort(s_mid, tmp, r.x, (int)(r.y - r.x), (uint64_t)t << 32, keys, ids);
+}
+
+// Block-wide min / max of 64-bit values (blockDim.x == 1024).
+__device__ __forceinline__ void block_minmax(uint64_t& lo, uint64_t& hi, uint64_t* s_red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t a = __shfl_xor_sync(0xffffffffu, lo, o);
+        const uint64_t b = __shfl_xor_sync(0xffffffffu, hi, o);
+        lo = a < lo ? a : lo;
+        hi = b > hi ? b : hi;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        s_red[warp] = lo;
+        s_red[32 + warp] = hi;
+    }
+    __syncthreads();
+    lo = s_red[0];
+    hi = s_red[32];
+    for (int w = 1; w < 32; ++w) {
+        lo = s_red[w] < lo ? s_red[w] : lo;
+        hi = s_red[32 + w] > hi ? s_red[32 + w] : hi;
+    }
+    __syncthreads();
+}
+
+// Exclusive scan of s[0, 1024) in place by a 1024-thread block.
+__device__ __forceinline__ void block_scan_1024(uint32_t* s, uint32_t* s_warp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t x = s[threadIdx.x];
+    uint32_t incl = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    uint32_t wpre = 0;
+    for (int w = 0; w < warp; ++w) wpre += s_warp[w];
+    __syncthreads();
+    s[threadIdx.x] = wpre + incl - x;
+    __syncthreads();
+}
+
+// Shared memory of the huge-bucket kernel (dynamic): the block sort area, the
+// pending stack, the sub-bucket counters and cursors.
+struct HugeSmem {
+    uint64_t keys[kBigCap];
+    uint2 stack[kStack];          // (offset, count | in_keys_buffer << 31)
+    uint32_t hist[kSplit];
+    uint32_t cur[kSplit];
+    uint64_t red[64];
+    uint32_t warp_sums[32];
+    int sp;
+};
+
+// One 1024-thread CTA per listed bucket of more than kBigCap instances.  A
+// range is split by uniform slices of its [min, max] key interval:
+// digit(k) = floor((k - min) * s / 2^64) with s = floor((2^64 - 1) / (range + 1))
+// * kSplit (or k - min when the range is below kSplit) is non-decreasing in k
+// and below kSplit, so the sub-buckets in digit order are in key order.  Each
+// level shrinks the key interval by a factor of at least kSplit / 2 and keys are
+// unique within a bucket (below 2^63: depth is finite and positive), so at most
+// seven levels are ever pending and the stack never holds more than
+// 7 * (kSplit - 1) + 1 ranges.
+__global__ void __launch_bounds__(1024) sort_huge_kernel(const uint32_t* __restrict__ list,
+                                                         const uint2* __restrict__ ranges, uint64_t* tmp,
+                                                         uint64_t* keys, uint32_t* __restrict__ ids)
+{
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    HugeSmem& S = *reinterpret_cast<HugeSmem*>(s_raw);
+    const uint32_t t = list[blockIdx.x];
+    const uint2 r0 = ranges[t];
+    const uint64_t hi_key = (uint64_t)t << 32;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        S.stack[0] = make_uint2(r0.x, r0.y - r0.x);
+        S.sp = 1;
+    }
+    __syncthreads();
+    while (S.sp > 0) {
+        const uint2 top = S.stack[S.sp - 1];
+        __syncthreads();
+        if (threadIdx.x == 0) S.sp -= 1;
+        const size_t o = top.x;
+        const uint32_t c = top.y & 0x7fffffffu;
+        const bool in_keys = (top.y >> 31) != 0;
+        const uint64_t* src = in_keys ? keys : tmp;
+        uint64_t* dst = in_keys ? tmp : keys;
+        // key interval of the range
+        uint64_t kmin = ~0ull, kmax = 0ull;
+        for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
+            const uint64_t k = src[o + i];
+            kmin = k < kmin ? k : kmin;
+            kmax = k > kmax ? k : kmax;
+        }
+        block_minmax(kmin, kmax, S.red);
+        const uint64_t range = kmax - kmin;
+        const bool direct = range < (uint64_t)kSplit;
+        const uint64_t scale = direct ? 0ull : (~0ull / (range + 1ull)) * (uint64_t)kSplit;
+        S.hist[threadIdx.x] = 0u;
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
+            const uint64_t d = src[o + i] - kmin;
+            atomicAdd(&S.hist[direct ? (uint32_t)d : (uint32_t)__umul64hi(d, scale)], 1u);
+        }
+        __syncthreads();
+        const uint32_t my_cnt = S.hist[threadIdx.x];
+        block_scan_1024(S.hist, S.warp_sums);   // hist = sub-bucket starts
+        S.cur[threadIdx.x] = S.hist[threadIdx.x];
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
+            const uint64_t k = src[o + i];
+            const uint64_t d = k - kmin;
+            const uint32_t dig = direct ? (uint32_t)d : (uint32_t)__umul64hi(d, scale);
+            dst[o + atomicAdd(&S.cur[dig], 1u)] = k;
+        }
+        __syncthreads();               // every cursor increment is done
+        S.cur[threadIdx.x] = my_cnt;   // sub-bucket sizes
+        __syncthreads();               // dst and the sizes are visible to the whole block
+        // small sub-buckets: one warp each
+        for (int d = warp; d < kSplit; d += 32) {
+            const int sc = (int)S.cur[d];
+            if (sc > 0 && sc <= kWarpCap) warp_sort(dst, o + S.hist[d], sc, hi_key, keys, ids);
+        }
+        // medium sub-buckets: the whole block; large ones are pushed
+        for (int d = 0; d < kSplit; ++d) {
+            const uint32_t sc = S.cur[d];
+            if (sc <= (uint32_t)kWarpCap) continue;
+            if (sc <= (uint32_t)kBigCap) {
+                cta_sort(S.keys, dst, o + S.hist[d], (int)sc, hi_key, keys, ids);
+            } else if (threadIdx.x == 0 && S.sp < kStack) {   // the bound above keeps sp < kStack
+                S.stack[S.sp] = make_uint2((uint32_t)(o + S.hist[d]), sc | (in_keys ? 0u : 0x80000000u));
+                S.sp += 1;
+            }
+        }
+        __syncthreads();
+    }
 }
 
 // Aligned bump layout of the workspace.
 struct WsLayout {
-    size_t scan_sums, offsets, totals, alt_keys, alt_ids, hist, hist_sums;
-    size_t tile_cnt, tile_off, cursor, tile_sums, stats, big_list, bytes;
+    size_t cnt, off, scan_sums, totals, stats, lists, tmp, bytes;
 };
 
 inline size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-inline WsLayout ws_layout(int64_t vn, int64_t capacity, int64_t ntile_ids)
+inline BinGeom bin_geom(int64_t n, int n_views, int tiles_x, int tiles_y)
 {
-    WsLayout L;
-    size_t o = 0;
-    L.scan_sums = o; o = align_up(o + scan_ws_bytes(vn));
-    L.offsets = o;   o = align_up(o + sizeof(uint32_t) * (size_t)vn);
-    L.totals = o;    o = align_up(o + 2 * sizeof(unsigned long long));
-    L.alt_keys = o;  o = align_up(o + sizeof(uint64_t) * (size_t)capacity);
-    L.alt_ids = o;   o = align_up(o + sizeof(uint32_t) * (size_t)capacity);
-    const int64_t nb = (capacity + kSortItems - 1) / kSortItems;
-    L.hist = o;      o = align_up(o + sizeof(uint32_t) * 256 * (size_t)nb);
-    L.hist_sums = o; o = align_up(o + scan_ws_bytes(256 * nb));
-    L.tile_cnt = o;  o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
-    L.tile_off = o;  o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
-    L.cursor = o;    o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
-    L.tile_sums = o; o = align_up(o + scan_ws_bytes(ntile_ids));
-    L.stats = o;     o = align_up(o + 4 * sizeof(unsigned int));
-    L.big_list = o;  o = align_up(o + sizeof(uint32_t) * (size_t)ntile_ids);
-    L.bytes = o;
-    return L;
+    BinGeom G;
+    G.n = n;
+    G.tiles_x = tiles_x;
+    G.tiles_y = tiles_y;
+    G.tiles = tiles_x * tiles_y;
+    const int64_t ntile_ids = (int64_t)G.tiles * n_views;
+    int64_t B = (kBinBlocks + n_views - 1) / n_views;
+    if (B * ntile_ids > kMaxCounts) B = kMaxCounts / ntile_ids;
+    if (B > n) B = n;
+    if (B < 1) B = 1;
+    G.per_block = (n + B - 1) / B;
+    if (G.per_block < 1) G.per_block = 1;
+    G.B = (int32_t)((n + G.per_block - 1) / G.per_block);
+    if (G.B < 1) G.B = 1;
+    G.band_rows = kBandTiles / tiles_x;
+    if (G.band_rows < 1) G.band_rows = 1;
+    if (G.band_rows > tiles_y) G.band_rows = tiles_y;
+    return G;
 }
 
-inline int bit_length(uint64_t x)
+inline WsLayout ws_layout(const BinGeom& G, int64_t ntile_ids, int64_t capacity)
 {
-    int b = 0;
-    while (x) { ++b; x >>= 1; }
-    return b;
+    const int64_t ncnt = ntile_ids * G.B;
+    WsLayout L;
+    size_t o = 0;
+    L.cnt = o;       o = align_up(o + sizeof(uint32_t) * (size_t)ncnt);
+    L.off = o;       o = align_up(o + sizeof(uint32_t) * (size_t)ncnt);
+    L.scan_sums = o; o = align_up(o + scan_ws_bytes(ncnt));
+    L.totals = o;    o = align_up(o + sizeof(unsigned long long));
+    L.stats = o;     o = align_up(o + 4 * sizeof(unsigned int));
+    L.lists = o;     o = align_up(o + 3 * sizeof(uint32_t) * (size_t)ntile_ids);
+    L.tmp = o;       o = align_up(o + sizeof(uint64_t) * (size_t)capacity);
+    L.bytes = o;
+    return L;
 }
 
 }  // namespace gs
@@ -292,12 +551,12 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (!ws_bytes || n < 0 || n > INT32_MAX || n_views < 1 || n_views > GS_MAX_VIEWS) return GS_ERR_INVALID_ARG;
     if (width <= 0 || height <= 0 || width > 65535 * kTile || height > 65535 * kTile) return GS_ERR_INVALID_ARG;
     if (capacity < 0 || capacity > (int64_t)UINT32_MAX) return GS_ERR_INVALID_ARG;
-    const int64_t vn = n * (int64_t)n_views;
-    const int tiles_x = tiles_x_of(width);
-    const int64_t tiles = (int64_t)tiles_x * tiles_y_of(height);
+    const int tiles_x = tiles_x_of(width), tiles_y = tiles_y_of(height);
+    const int64_t tiles = (int64_t)tiles_x * tiles_y;
     const int64_t ntile_ids = tiles * n_views;
-    if (ntile_ids > (int64_t)INT32_MAX) return GS_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(vn, capacity, ntile_ids);
+    if (ntile_ids > (int64_t)INT32_MAX / 2 || tiles_x > kBandTiles) return GS_ERR_INVALID_ARG;
+    const BinGeom G = bin_geom(n, n_views, tiles_x, tiles_y);
+    const WsLayout L = ws_layout(G, ntile_ids, capacity);
     if (!ws) {
         *ws_bytes = L.bytes;
         return GS_OK;
@@ -308,35 +567,33 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (capacity > 0 && (!keys || !ids)) return GS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     char* w = (char*)ws;
+    uint32_t* cnt = (uint32_t*)(w + L.cnt);
+    uint32_t* off = (uint32_t*)(w + L.off);
     unsigned long long* scan_sums = (unsigned long long*)(w + L.scan_sums);
-    uint32_t* offsets = (uint32_t*)(w + L.offsets);
     unsigned long long* totals = (unsigned long long*)(w + L.totals);
-    uint64_t* alt_keys = (uint64_t*)(w + L.alt_keys);
-    uint32_t* alt_ids = (uint32_t*)(w + L.alt_ids);
-    uint32_t* hist = (uint32_t*)(w + L.hist);
-    unsigned long long* hist_sums = (unsigned long long*)(w + L.hist_sums);
-    uint32_t* tile_cnt = (uint32_t*)(w + L.tile_cnt);
-    uint32_t* tile_off = (uint32_t*)(w + L.tile_off);
-    uint32_t* cursor = (uint32_t*)(w + L.cursor);
-    unsigned long long* tile_sums = (unsigned long long*)(w + L.tile_sums);
     unsigned int* stats = (unsigned int*)(w + L.stats);
-    uint32_t* big_list = (uint32_t*)(w + L.big_list);
+    uint32_t* lists = (uint32_t*)(w + L.lists);
+    uint64_t* tmp = (uint64_t*)(w + L.tmp);
+    uint2* ranges = reinterpret_cast<uint2*>(tile_ranges);
     const ushort4* rect4 = reinterpret_cast<const ushort4*>(proj->rect);
-    const int threads = 256;
-    const unsigned gblocks = (unsigned)((vn + threads - 1) / threads);
+    const int64_t ncnt = ntile_ids * G.B;
+    const int bands = (tiles_y + G.band_rows - 1) / G.band_rows;
+    const dim3 bin_grid((unsigned)G.B, (unsigned)bands, (unsigned)n_views);
+    const size_t bin_smem = sizeof(uint32_t) * (size_t)G.band_rows * (size_t)tiles_x;
 
-    // per-tile path: counts, bucket starts, totals
-    GS_CUDA_TRY(cudaMemsetAsync(tile_cnt, 0, sizeof(uint32_t) * (size_t)ntile_ids, s));
     GS_CUDA_TRY(cudaMemsetAsync(stats, 0, 4 * sizeof(unsigned int), s));
-    if (vn > 0) {
-        count_tiles_kernel<<<gblocks, threads, 0, s>>>(proj->tiles_touched, rect4, n, vn, tiles_x, (int)tiles,
-                                                        tile_cnt);
+    if (n > 0) {
+        GS_CUDA_TRY(cudaFuncSetAttribute(bin_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem));
+        bin_kernel<false><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, cnt,
+                                                                   nullptr);
         GS_LAUNCH_CHECK();
+    } else {
+        GS_CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * (size_t)ncnt, s));
     }
-    GS_CUDA_TRY((scan_launch<uint32_t, false>(tile_cnt, ntile_ids, tile_off, tile_sums, totals, s)));
-    bucket_stats_kernel<<<(unsigned)((ntile_ids + threads - 1) / threads), threads, 0, s>>>(tile_cnt, tile_off,
-                                                                                           ntile_ids, cursor, stats,
-                                                                                           big_list);
+    GS_CUDA_TRY((scan_launch<uint32_t, false>(cnt, ncnt, off, scan_sums, totals, s)));
+    const int threads = 256;
+    bucket_stats_kernel<<<(unsigned)((ntile_ids + threads - 1) / threads), threads, 0, s>>>(off, G.B, ntile_ids, totals,
+                                                                                           ranges, stats, lists);
     GS_LAUNCH_CHECK();
     struct {
         unsigned long long total;
@@ -347,58 +604,31 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     GS_CUDA_TRY(cudaStreamSynchronize(s));
     *n_instances = (int64_t)host.total;
     if ((int64_t)host.total > capacity) return GS_ERR_CAPACITY;
-    if (host.total > 0 && host.st[0] <= (unsigned)kBigCap) {
-        scatter_tiles_kernel<<<gblocks, threads, 0, s>>>(proj->tiles_touched, rect4, proj->depth, n, vn, tiles_x,
-                                                          (int)tiles, cursor, alt_keys);
-        GS_LAUNCH_CHECK();
-        sort_small_kernel<<<(unsigned)ntile_ids, 256, 0, s>>>(tile_cnt, tile_off, alt_keys, keys, ids,
-                                                              reinterpret_cast<uint2*>(tile_ranges));
-        GS_LAUNCH_CHECK();
-        if (host.st[1] > 0) {
-            int P = 1;
-            while (P < (int)host.st[0]) P <<= 1;
-            const size_t smem = sizeof(uint64_t) * (size_t)P;
-            GS_CUDA_TRY(cudaFuncSetAttribute(sort_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-            sort_big_kernel<<<host.st[1], 1024, smem, s>>>(big_list, tile_cnt, tile_off, alt_keys, keys, ids);
-            GS_LAUNCH_CHECK();
-        }
-        return GS_OK;
-    }
+    if (host.total == 0) return GS_OK;
 
-    // LSD radix path (no instances, or a bucket too large for a block sort)
-    GS_CUDA_TRY(cudaMemsetAsync(tile_ranges, 0, sizeof(uint32_t) * 2 * (size_t)ntile_ids, s));
-    const int64_t N = (int64_t)host.total;
-    if (N == 0) return GS_OK;
-    GS_CUDA_TRY((scan_launch<uint32_t, false>(proj->tiles_touched, vn, offsets, scan_sums, totals + 1, s)));
-
-    // passes: 32 depth bits + the tile-id bits, 8-bit digits
-    const int bits = 32 + (ntile_ids > 1 ? bit_length((uint64_t)(ntile_ids - 1)) : 1);
-    const int npass = (bits + 7) / 8;
-    uint64_t* kbuf[2] = {keys, alt_keys};
-    uint32_t* vbuf[2] = {ids, alt_ids};
-    int cur = (npass & 1) ? 1 : 0;   // the last pass writes buffer 0 (the caller's)
-
-    // emit
-    emit_kernel<<<gblocks, threads, 0, s>>>(proj->tiles_touched, offsets, rect4, proj->depth, n, vn, tiles_x,
-                                            (int)tiles, kbuf[cur], vbuf[cur]);
+    GS_CUDA_TRY(cudaFuncSetAttribute(bin_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem));
+    bin_kernel<true><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, off, tmp);
     GS_LAUNCH_CHECK();
-    // radix passes
-    const int64_t nb = (N + kSortItems - 1) / kSortItems;
-    for (int p = 0; p < npass; ++p) {
-        const int shift = 8 * p;
-        const int width_bits = min(8, bits - shift);
-        const uint32_t mask = (1u << width_bits) - 1u;
-        radix_hist_kernel<<<(unsigned)nb, kSortThreads, 0, s>>>(kbuf[cur], N, shift, mask, hist, nb);
-        GS_LAUNCH_CHECK();
-        GS_CUDA_TRY((scan_launch<uint32_t, false>(hist, 256 * nb, hist, hist_sums, totals + 1, s)));
-        radix_scatter_kernel<<<(unsigned)nb, kSortThreads, 0, s>>>(kbuf[cur], vbuf[cur], N, shift, mask, hist, nb,
-                                                                    kbuf[cur ^ 1], vbuf[cur ^ 1]);
-        GS_LAUNCH_CHECK();
-        cur ^= 1;
-    }
-    // ranges
-    tile_ranges_kernel<<<(unsigned)((N + threads - 1) / threads), threads, 0, s>>>(keys, N,
-                                                                                 reinterpret_cast<uint2*>(tile_ranges));
+    sort_warp_kernel<<<(unsigned)((ntile_ids + kSortWarps - 1) / kSortWarps), kSortWarps * 32, 0, s>>>(
+        ranges, ntile_ids, tmp, keys, ids);
     GS_LAUNCH_CHECK();
+    if (host.st[1] > 0) {
+        sort_reg_kernel<<<host.st[1], kRegThreads, 0, s>>>(lists, ranges, tmp, keys, ids);
+        GS_LAUNCH_CHECK();
+    }
+    if (host.st[2] > 0) {
+        int P = 1;
+        while (P < (int)min(host.st[0], (unsigned)kBigCap)) P <<= 1;
+        const size_t smem = sizeof(uint64_t) * (size_t)P;
+        GS_CUDA_TRY(cudaFuncSetAttribute(sort_mid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        sort_mid_kernel<<<host.st[2], 1024, smem, s>>>(lists + ntile_ids, ranges, tmp, keys, ids);
+        GS_LAUNCH_CHECK();
+    }
+    if (host.st[3] > 0) {
+        const size_t smem = sizeof(HugeSmem);
+        GS_CUDA_TRY(cudaFuncSetAttribute(sort_huge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        sort_huge_kernel<<<host.st[3], 1024, smem, s>>>(lists + 2 * ntile_ids, ranges, tmp, keys, ids);
+        GS_LAUNCH_CHECK();
+    }
     return GS_OK;
 }

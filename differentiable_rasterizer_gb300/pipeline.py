@@ -98,21 +98,18 @@ class GaussianTrainer:
 
     def kernel_launches_per_step(self) -> int:
         """Kernels the library launches for one train_step, from its launch structure:
-        projection 1; binning: per-tile path count 1, scan 3, bucket stats 1, scatter 1,
-        bucket sort 1 (+1 when a bucket exceeds 2048 instances), or the radix path
-        (scan 3, emit 1, per 8-bit pass 5, ranges 1) when a bucket exceeds 16384;
-        fused raster 1; compaction: 3 per view-list scan, union 1, union scan 3, VJP 1;
-        Adam 2.  Memsets and copies are not kernels.  Reads the last step's ranges."""
+        projection 1; binning: count 1, scan 3, bucket stats 1, then (when there are
+        instances) scatter 1, warp sort 1, and one more sort kernel for each of the
+        size classes 257..2048, 2049..16384 and over 16384 that occurs; fused raster 1;
+        compaction: 3 per view-list scan, union 1, union scan 3, VJP 1; Adam 2.
+        Memsets and copies are not kernels.  Reads the last step's ranges."""
         V, n = self.V, self.n
         r = self.ranges.view(-1, 2).to(torch.int64)
-        biggest = int((r[:, 1] - r[:, 0]).max().item()) if r.numel() else 0
-        if biggest > 16384:
-            ntile_ids = V * self.tiles
-            bits = 32 + max(1, int(ntile_ids - 1).bit_length())
-            npass = (bits + 7) // 8
-            sort = (1 if n * V else 0) + 3 + 1 + ((3 + 1 + 5 * npass + 1) if self.n_instances else 0)
-        else:
-            sort = (1 if n * V else 0) + 3 + 1 + ((3 if biggest > 2048 else 2) if self.n_instances else 0)
+        c = r[:, 1] - r[:, 0]
+        sort = (1 if n * V else 0) + 3 + 1
+        if self.n_instances:
+            sort += 2 + sum(int(((c > lo) & (c <= hi)).any().item())
+                            for lo, hi in ((256, 2048), (2048, 16384), (16384, 1 << 62)))
         compact = (3 * V + 1 + 3 + 1) if n else 0
         return (1 if n else 0) + sort + 1 + compact + (2 if n else 0)
 

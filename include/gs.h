@@ -142,14 +142,16 @@ GS_API gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, c
 
 /* Tile binning and sort.  Every visible (view v, Gaussian g) emits one instance
  * per tile of its rect with key = ((v * tiles + tile) << 32) | bits(depth) and
- * value g; instances are sorted by key (LSD radix over the 32 depth bits and the
- * bits of v * tiles + tile), stably, so equal keys keep ascending g.
+ * value g; instances are sorted by key, stably, so equal keys keep ascending g
+ * (a counting sort on v * tiles + tile, then every (view, tile) bucket sorted on
+ * (bits(depth), g): the same order as an LSD radix sort of the keys).
  * keys, ids: [capacity] outputs (sorted); tile_ranges: [n_views * tiles][2]
  * uint32 [start, end) into the sorted arrays (start == end: empty tile).
  * n_instances: HOST out, set even when the capacity is too small.
  * ws / ws_bytes: scratch (ws == NULL: query).  Synchronises the host once.
  * Errors: CAPACITY if n_instances > capacity (outputs untouched);
- * INVALID_ARG for bad sizes or a too small workspace. */
+ * INVALID_ARG for bad sizes (width above 655360, i.e. more than 40960 tiles in a
+ * row) or a too small workspace. */
 GS_API gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views, int32_t width, int32_t height,
                       int64_t capacity, uint64_t* keys, uint32_t* ids, uint32_t* tile_ranges,
                       int64_t* n_instances, void* ws, size_t* ws_bytes, void* stream);

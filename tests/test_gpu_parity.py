@@ -63,12 +63,44 @@ def test_sort_bucket_sizes_over_2048_use_the_large_block_sort():
     assert st["instances"] > 4 * 2048
 
 
-def test_sort_bucket_over_16384_uses_the_radix_path():
-    """20000 Gaussians on one 16x16 tile: a single bucket larger than a block sort holds."""
+def test_sort_bucket_over_16384_is_split_by_key_range():
+    """20000 Gaussians on one 16x16 tile: a single bucket larger than a block sort
+    holds, split into sub-buckets by key range."""
     sc = scenes.random_small_scene(32, n=20000, width=16, height=16, sh_degree=0, log_lo=-2.0, log_hi=-1.0,
                                    logit_mu=-3.0, spread=0.3)
     st = parity.run_stage_parity(sc)
     assert st["instances"] > 16384
+
+
+def test_sort_split_recursion_on_equal_depths():
+    """40001 Gaussians on one tile: 20000 at depth exactly 2, 10000 at each of the
+    next two float32 values, one at depth 100.  The first split puts the 40000 near
+    ones in one sub-bucket, the second separates the three depths (two sub-buckets
+    of 10000 go to the block sort), the third splits the 20000 of equal depth by
+    index."""
+    n = 40001
+    sc = scenes.random_small_scene(34, n=n, width=16, height=16, sh_degree=0, log_lo=-2.0, log_hi=-1.0,
+                                   logit_mu=-3.0, spread=0.3)
+    z = np.full(n, 2.0, np.float32)
+    z1 = np.nextafter(np.float32(2.0), np.float32(3.0))
+    z[20000:30000] = z1
+    z[30000:40000] = np.nextafter(z1, np.float32(3.0))
+    z[40000] = 100.0
+    sc.params[2] = z[np.random.default_rng(5).permutation(n)]
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] == n
+
+
+def test_wide_view_bins_in_two_tile_row_bands():
+    """An 8192x1296 view has 512 x 81 tiles, more than one block's shared-memory
+    counters hold: the binning runs in two bands of tile rows (80 + 1).  The
+    Gaussians sit across the band boundary."""
+    sc = scenes.random_small_scene(35, n=3000, width=8192, height=1296, sh_degree=0, log_lo=-2.5, log_hi=-1.5,
+                                   spread=1.2)
+    cam = sc.cameras[0]
+    sc.cameras = [scenes.Camera(cam.R, cam.t, 1000.0, 1000.0, 4096.0, 1280.0, 8192, 1296)]
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] > 3000
 
 
 def test_multi_view_small_reduced():
