@@ -3,8 +3,9 @@
 // unnecessary memory accesses for Gaussians with zero gradients"), made exactly
 // equal to dense Adam by replaying the skipped zero-gradient steps first.
 //
-// One thread per (listed Gaussian, float4 chunk of its [stride] parameter
-// block): 16 contiguous bytes of params, m, v and grads per thread.  The bias
+// Work unit: a (listed Gaussian, float4 chunk of its [stride] parameter block)
+// pair, 16 contiguous bytes of params, m, v and grads; a grid of resident
+// blocks strides over the units.  The bias
 // corrections of the current step come from the host (the same fp64 binary
 // exponentiation as the device code, so the same values); replayed steps
 // compute their own.  A row whose moments are both +0 skips the replay: a
@@ -32,7 +33,7 @@ struct AdamArgs {
     float* __restrict__ v;
     int32_t* __restrict__ last_step;
     int64_t n;
-    int32_t stride, chunks;
+    int32_t stride, chunks, chunk_shift;   // chunks = stride / 4 = 1 << chunk_shift
     const uint32_t* idx;
     const int64_t* n_idx;
     int32_t t;
@@ -53,18 +54,13 @@ __device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, 
     v = vn;
 }
 
-// Catch up and step one parameter (learning rate lr) of a Gaussian last
-// stepped at s.
-__device__ __forceinline__ void adam_elem(float lr, int s, int t, float b1, float b2, float eps, float bc1t,
-                                          float bc2t, float& p, float& m, float& v, float g)
+// One replayed zero-gradient step of one parameter; a zero state stays zero
+// (and p unchanged), so it is skipped.
+__device__ __forceinline__ void adam_zero_step(float& p, float& m, float& v, float lr, float b1, float b2, float eps,
+                                               float bc1, float bc2)
 {
-    for (int j = s + 1; j < t; ++j) {
-        if (__float_as_uint(m) == 0u && __float_as_uint(v) == 0u) break;   // zero state: replay is a no-op
-        const float bc1 = (float)(1.0 - powi_binary((double)b1, j));
-        const float bc2 = (float)(1.0 - powi_binary((double)b2, j));
-        adam_one(p, m, v, 0.0f, lr, b1, b2, eps, bc1, bc2);
-    }
-    adam_one(p, m, v, g, lr, b1, b2, eps, bc1t, bc2t);
+    if (__float_as_uint(m) == 0u && __float_as_uint(v) == 0u) return;
+    adam_one(p, m, v, 0.0f, lr, b1, b2, eps, bc1, bc2);
 }
 
 // Learning-rate group of parameter k: mean, log-scale, quaternion, opacity, colour.
@@ -76,30 +72,47 @@ __device__ __forceinline__ float lr_of(const AdamArgs& a, int k)
 // One thread per (listed Gaussian, float4 chunk of its parameter block): each
 // thread moves 16 contiguous bytes of params, m, v and grads in and out, so a
 // warp covers whole 256-byte Gaussian blocks whether the list is dense or not.
-__global__ void __launch_bounds__(256) adam_deferred_kernel(AdamArgs a)
+// Grid-stride over the (listed Gaussian, float4 chunk) units of this step: the
+// list length lives on the device, so the grid is sized for the machine, not
+// the list.  Per unit the loads come in two dependent rounds: the Gaussian
+// index, then its parameter block with last_step.
+__global__ void __launch_bounds__(256, 5) adam_deferred_kernel(AdamArgs a)
 {
     const int64_t count = a.flush ? a.n : *a.n_idx;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t e = i / a.chunks;
-    if (e >= count) return;
-    const int c = (int)(i - e * a.chunks);
-    const int64_t g = a.flush ? e : (int64_t)a.idx[e];
-    const int s = a.last_step[g];
-    if (s >= a.t) return;
-    const size_t off = (size_t)g * a.stride + 4 * c;
-    float4 p = *reinterpret_cast<const float4*>(a.params + off);
-    float4 m = *reinterpret_cast<const float4*>(a.m + off);
-    float4 v = *reinterpret_cast<const float4*>(a.v + off);
-    const float4 gr = a.flush ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *reinterpret_cast<const float4*>(a.grads + off);
-    const int k = 4 * c;
-    adam_elem(lr_of(a, k), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.x, m.x, v.x, gr.x);
-    adam_elem(lr_of(a, k + 1), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.y, m.y, v.y, gr.y);
-    adam_elem(lr_of(a, k + 2), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.z, m.z, v.z, gr.z);
-    adam_elem(lr_of(a, k + 3), s, a.t, a.b1, a.b2, a.eps, a.bc1t, a.bc2t, p.w, m.w, v.w, gr.w);
-    *reinterpret_cast<float4*>(a.params + off) = p;
-    *reinterpret_cast<float4*>(a.m + off) = m;
-    *reinterpret_cast<float4*>(a.v + off) = v;
-    if (!a.flush) *reinterpret_cast<float4*>(a.grads + off) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const int64_t total = count << a.chunk_shift;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = i >> a.chunk_shift;
+        const int c = (int)(i & (a.chunks - 1));
+        const int64_t g = a.flush ? e : (int64_t)__ldg(a.idx + e);
+        const size_t off = (size_t)g * a.stride + 4 * c;
+        float4 p = *reinterpret_cast<const float4*>(a.params + off);
+        float4 m = *reinterpret_cast<const float4*>(a.m + off);
+        float4 v = *reinterpret_cast<const float4*>(a.v + off);
+        const float4 gr =
+            a.flush ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *reinterpret_cast<const float4*>(a.grads + off);
+        const int s = a.last_step[g];
+        if (s >= a.t) continue;
+        const int k = 4 * c;
+        const float l0 = lr_of(a, k), l1 = lr_of(a, k + 1), l2 = lr_of(a, k + 2), l3 = lr_of(a, k + 3);
+        // catch up the zero-gradient steps s+1 .. t-1 (rare: the Gaussian was not
+        // touched in the previous step)
+        for (int j = s + 1; j < a.t; ++j) {
+            const float bc1 = (float)(1.0 - powi_binary((double)a.b1, j));
+            const float bc2 = (float)(1.0 - powi_binary((double)a.b2, j));
+            adam_zero_step(p.x, m.x, v.x, l0, a.b1, a.b2, a.eps, bc1, bc2);
+            adam_zero_step(p.y, m.y, v.y, l1, a.b1, a.b2, a.eps, bc1, bc2);
+            adam_zero_step(p.z, m.z, v.z, l2, a.b1, a.b2, a.eps, bc1, bc2);
+            adam_zero_step(p.w, m.w, v.w, l3, a.b1, a.b2, a.eps, bc1, bc2);
+        }
+        adam_one(p.x, m.x, v.x, gr.x, l0, a.b1, a.b2, a.eps, a.bc1t, a.bc2t);
+        adam_one(p.y, m.y, v.y, gr.y, l1, a.b1, a.b2, a.eps, a.bc1t, a.bc2t);
+        adam_one(p.z, m.z, v.z, gr.z, l2, a.b1, a.b2, a.eps, a.bc1t, a.bc2t);
+        adam_one(p.w, m.w, v.w, gr.w, l3, a.b1, a.b2, a.eps, a.bc1t, a.bc2t);
+        *reinterpret_cast<float4*>(a.params + off) = p;
+        *reinterpret_cast<float4*>(a.m + off) = m;
+        *reinterpret_cast<float4*>(a.v + off) = v;
+        if (!a.flush) *reinterpret_cast<float4*>(a.grads + off) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
 }
 
 __global__ void __launch_bounds__(256) stamp_kernel(AdamArgs a)
@@ -134,6 +147,7 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     a.n = n;
     a.stride = param_stride(sh_degree);
     a.chunks = a.stride / 4;
+    a.chunk_shift = a.chunks == 16 ? 4 : 2;
     a.idx = idx;
     a.n_idx = n_idx;
     a.t = t;
@@ -147,11 +161,11 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
     int dev = 0, sms = 0;
     GS_CUDA_TRY(cudaGetDevice(&dev));
     GS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    // The list length lives on the device: the grid covers n entries and threads
-    // beyond the list return at once.
+    // The list length lives on the device: a grid of resident blocks strides
+    // over it (at most n entries).
     const int threads = 256;
-    const int64_t bx = (n * a.chunks + threads - 1) / threads;
-    if (bx > INT32_MAX) return GS_ERR_INVALID_ARG;
+    int64_t bx = (n * a.chunks + threads - 1) / threads;
+    if (bx > (int64_t)sms * 5) bx = (int64_t)sms * 5;   // 5 resident blocks per SM
     cudaStream_t s = (cudaStream_t)stream;
     adam_deferred_kernel<<<(unsigned)bx, threads, 0, s>>>(a);
     GS_LAUNCH_CHECK();

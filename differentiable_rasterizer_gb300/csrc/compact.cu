@@ -39,12 +39,11 @@ struct VjpArgs {
     float* __restrict__ grads;
 };
 
+// Projection VJP of Gaussian g summed over its touching views, added to its
+// dense gradient block; the consumed grad2d / touched entries are cleared.
 template <int DEG>
-__global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
+__device__ __forceinline__ void vjp_gaussian(const VjpArgs& a, const CamSet& cs, int64_t g)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= *a.n_union) return;
-    const int64_t g = a.idx_union[i];
     GaussParams<DEG> gp;
     gp.load(a.params, g);
     // Current gradient values are loaded up front with the parameters, so the
@@ -77,6 +76,17 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
     }
 #pragma unroll
     for (int i = 0; i < kVec; ++i) gdst[i] = make_float4(grad[4 * i], grad[4 * i + 1], grad[4 * i + 2], grad[4 * i + 3]);
+}
+
+// One thread per Gaussian of the union list; the list length lives on the
+// device, so a grid of resident blocks strides over it.
+template <int DEG>
+__global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
+{
+    const int64_t count = *a.n_union;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+         i += (int64_t)gridDim.x * blockDim.x)
+        vjp_gaussian<DEG>(a, cs, (int64_t)a.idx_union[i]);
 }
 
 struct CompactWs {
@@ -142,11 +152,20 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
     a.grads = grads;
     const CamSet cs = make_camset(cams, n_views);
     const int threads = 128;
-    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    int dev = 0, sms = 0, per_sm = 0;
+    GS_CUDA_TRY(cudaGetDevice(&dev));
+    GS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (sh_degree == 0)
-        vjp_kernel<0><<<blocks, threads, 0, s>>>(a, cs);
+        GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vjp_kernel<0>, threads, 0));
     else
-        vjp_kernel<3><<<blocks, threads, 0, s>>>(a, cs);
+        GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vjp_kernel<3>, threads, 0));
+    int64_t blocks = (n + threads - 1) / threads;
+    const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    if (blocks > resident) blocks = resident;
+    if (sh_degree == 0)
+        vjp_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(a, cs);
+    else
+        vjp_kernel<3><<<(unsigned)blocks, threads, 0, s>>>(a, cs);
     GS_LAUNCH_CHECK();
     return GS_OK;
 }

@@ -7,11 +7,12 @@
 // sorted list is staged through shared memory in chunks of kChunk records
 // (gathered through the instance ids).  Each chunk is handled in two phases:
 //
-//  pairs      Gaussian-parallel: a warp takes one staged Gaussian and its lanes
-//             sweep the pixels of the Gaussian's alpha-support box inside the
-//             tile (the box comes from gs_project and provably contains every
-//             pixel whose fp32 power can reach the per-Gaussian cut tau); every
-//             pixel whose alpha passes sets bit j in its 256-bit row.
+//  pairs      Gaussian-parallel: each warp lays the (Gaussian, pixel) pairs of
+//             its 32 staged Gaussians end to end -- the pixels of each
+//             Gaussian's alpha-support box inside the tile (the box comes from
+//             gs_project and provably contains every pixel whose fp32 power can
+//             reach the per-Gaussian cut tau) -- and sweeps them 32 at a time;
+//             every pixel whose alpha passes sets bit j in its 256-bit row.
 //  composite  pixel-parallel: each pixel walks its set bits in list order and
 //             composites them, with T, the colour, the stop index and dL/dC in
 //             registers.
@@ -19,11 +20,14 @@
 // Entries that do not pass are skipped by definition, so the image, stop index
 // and evaluation counts are those of walking every list entry.  The entries a
 // pixel composited are exactly its passing bits up to its last index, so
-// backward needs no per-pixel list: each pixel walks those bits back to front
-// (T recovered by division, the colour behind accumulated), adds its 9 gradient
-// terms into per-Gaussian shared-memory accumulators, and each chunk's sums go
-// to global memory with one vector atomic per Gaussian per tile.  Chunks that
-// are no longer resident are restaged and their bits recomputed.
+// backward needs no per-pixel list.  Backward walks the chunks last to first;
+// per chunk each warp queues its pixels' composited entries grouped by pixel,
+// newest first, and handles them 32 at a time: T before an entry is a
+// segmented product of 1 / (1 - alpha) from the pixel's current T, the colour
+// behind it a segmented sum, both by warp shuffles; each entry's 9 gradient
+// terms go to the Gaussian's grad2d row with vector atomics.  The pass bits of
+// the last kRing chunks stay in shared memory (a ring), so backward re-gathers
+// only their records; older chunks also get their bits recomputed.
 //
 // All decisions use the same fp32 operations in the same order as the CPU
 // definition (see gs_common.cuh); boxes, tau and bits only avoid work whose
@@ -36,6 +40,7 @@ constexpr int kChunk = 256;      // records per shared-memory stage
 constexpr int kWords = kChunk / 32;
 constexpr int kWarps = kTileThreads / 32;
 constexpr int kQueue = 256;      // queue window (entries) per warp
+constexpr int kRing = 3;         // chunks whose pass bits stay in shared memory
 
 struct RasterArgs {
     const float4* __restrict__ rec;     // [V][n][3]
@@ -82,19 +87,17 @@ struct EntryGrad {
 };
 
 // Gradient terms of one composited entry from its transmittance before it (Ti),
-// the colour composited behind it (S0..S2) and 1 / (1 - alpha) (rc).
-__device__ __forceinline__ EntryGrad entry_grad_at(const float4 r0, const float4 r1, float cb, float dx, float dy,
-                                                   float G, float araw, float alpha, float alpha_max, float g0,
-                                                   float g1, float g2c, float Ti, float S0, float S1, float S2,
-                                                   float rc)
+// dotc = dL/dC . its colour, dots = dL/dC . the colour composited behind it, and
+// rc = 1 / (1 - alpha).
+__device__ __forceinline__ EntryGrad entry_grad_at(const float4 r0, const float4 r1, float dx, float dy, float G,
+                                                   float araw, float alpha, float alpha_max, float g0, float g1,
+                                                   float g2c, float Ti, float dotc, float dots, float rc)
 {
     EntryGrad e;
     const float wgt = alpha * Ti;
     e.gr = g0 * wgt;
     e.gg = g1 * wgt;
     e.gb = g2c * wgt;
-    const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
-    const float dots = __fmaf_rn(g0, S0, __fmaf_rn(g1, S1, g2c * S2));
     const float dalpha = __fmaf_rn(Ti, dotc, -dots * rc);
     if (araw <= alpha_max) {
         e.go = dalpha * G;
@@ -118,8 +121,9 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     __shared__ float2 s_r2[kChunk];                 // (blue, tau)
     __shared__ uint32_t s_id[kChunk];
     __shared__ uint32_t s_box[kChunk];              // tile_box of each staged Gaussian
-    __shared__ uint32_t s_bits[kWords][kTileThreads];   // bit j of pixel p: entry j passes at p
+    __shared__ uint32_t s_bits[kRing][kWords][kTileThreads];   // per ring slot: bit j of pixel p = entry j passes at p
     __shared__ uint32_t s_skip[kWarps];             // pixels that need no more pairs
+    __shared__ uint8_t s_nz[kWarps][32];            // pair phase: lane of the r-th entry with a non-empty box
     __shared__ uint16_t s_q[kWarps][kQueue];        // (owner lane << 8) | entry, grouped by pixel
     __shared__ double s_red_d[kWarps];
     __shared__ unsigned long long s_red_u[3][kWarps];
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const float4* __restrict__ recv = a.rec + (size_t)v * (size_t)a.n * 3;
     const float alpha_min = a.alpha_min, alpha_max = a.alpha_max;
 
-    // Stage chunk records, their boxes, and clear this pixel's bit row.
+    // Stage chunk records and their boxes.
     auto stage = [&](int base) {
         const int k = base + threadIdx.x;
         uint32_t box = 0u;
@@ -157,38 +161,68 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             box = tile_box(r0.x, r0.y, r2.z, r2.w, ox, oy);
         }
         s_box[threadIdx.x] = box;
-#pragma unroll
-        for (int w = 0; w < kWords; ++w) s_bits[w][threadIdx.x] = 0u;
     };
-    // Pair phase: warp-per-Gaussian sweep of each box, setting pass bits.
-    auto pairs = [&](int cnt) {
-        for (int j = warp; j < cnt; j += kWarps) {
-            const uint32_t box = s_box[j];
-            const int bx0 = box & 0xff, bw = (int)((box >> 8) & 0xff) - bx0;
-            const int by0 = (box >> 16) & 0xff, bh = (int)(box >> 24) - by0;
-            if (box == 0u) continue;
-            const int area = bw * bh;
+    // Clear this pixel's bit row in ring slot sl.
+    auto clear_bits = [&](int sl) {
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) s_bits[sl][w][threadIdx.x] = 0u;
+    };
+    // Pair phase, setting pass bits in slot sl.  Warp w owns staged entries
+    // [32 w, 32 w + 32); the (entry, box pixel) pairs of its entries are laid
+    // end to end (exclusive scan of the box areas) and swept 32 at a time, so a
+    // lane never idles on a small box.  A lane finds the entry owning its pair
+    // from the start positions inside the round and the count of entries
+    // started before it (s_nz maps that rank to the owning lane).
+    auto pairs = [&](int cnt, int sl) {
+        const int jl = warp * 32 + lane;
+        const uint32_t box = jl < cnt ? s_box[jl] : 0u;
+        const int bx0 = box & 0xff, bw = (int)((box >> 8) & 0xff) - bx0;
+        const int by0 = (box >> 16) & 0xff, bh = (int)(box >> 24) - by0;
+        const int area = box ? bw * bh : 0;
+        int incl = area;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        const int off = incl - area;
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total == 0) return;
+        const uint32_t nz = __ballot_sync(0xffffffffu, area > 0);
+        if (area > 0) s_nz[warp][__popc(nz & ((1u << lane) - 1u))] = (uint8_t)lane;
+        const float inv_w = area > 0 ? 1.0f / (float)bw : 0.0f;
+        __syncwarp();
+        int started = 0;   // entries whose pairs start before this round
+        for (int rb = 0; rb < total; rb += 32) {
+            const uint32_t mine = (area > 0 && off >= rb && off < rb + 32) ? (1u << (off - rb)) : 0u;
+            const uint32_t starts = __reduce_or_sync(0xffffffffu, mine);
+            const int rank = started + __popc(starts & ((2u << lane) - 1u)) - 1;
+            started += __popc(starts);
+            const int ol = s_nz[warp][rank];
+            const int o_off = __shfl_sync(0xffffffffu, off, ol);
+            const uint32_t o_box = __shfl_sync(0xffffffffu, box, ol);
+            const float o_inv = __shfl_sync(0xffffffffu, inv_w, ol);
+            const int pos = rb + lane;
+            if (pos >= total) continue;
+            const int q = pos - o_off;
+            const int ow = (int)((o_box >> 8) & 0xff) - (int)(o_box & 0xff);
+            const int ly = (int)(((float)q + 0.5f) * o_inv);   // exact: q < 256, box width <= 16
+            const int lx = q - ly * ow;
+            const int ix = (int)(o_box & 0xff) + lx, iy = (int)((o_box >> 16) & 0xff) + ly;
+            const int p = iy * kTile + ix;
+            if ((s_skip[p >> 5] >> (p & 31)) & 1u) continue;
+            const int j = warp * 32 + ol;
             const float4 r0 = s_r0[j];
             const float4 r1 = s_r1[j];
-            const float tau = s_r2[j].y;
-            const float inv_w = 1.0f / (float)bw;
-            const uint32_t bit = 1u << (j & 31);
-            for (int q = lane; q < area; q += 32) {
-                const int ly = (int)(((float)q + 0.5f) * inv_w);   // exact: q < 256, bw <= 16
-                const int lx = q - ly * bw;
-                const int ix = bx0 + lx, iy = by0 + ly;
-                const int p = iy * kTile + ix;
-                if ((s_skip[p >> 5] >> (p & 31)) & 1u) continue;
-                const float dx = ((float)(ox + ix) + 0.5f) - r0.x;
-                const float dy = ((float)(oy + iy) + 0.5f) - r0.y;
-                // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
-                const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                // power > 0 is skipped by definition; power < tau has alpha < alpha_min
-                if (power > 0.0f || power < tau) continue;
-                const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
-                if (alpha < alpha_min) continue;
-                atomicOr(&s_bits[j >> 5][p], bit);
-            }
+            const float dx = ((float)(ox + ix) + 0.5f) - r0.x;
+            const float dy = ((float)(oy + iy) + 0.5f) - r0.y;
+            // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
+            const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+            // power > 0 is skipped by definition; power < tau has alpha < alpha_min
+            if (power > 0.0f || power < s_r2[j].y) continue;
+            const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
+            if (alpha < alpha_min) continue;
+            atomicOr(&s_bits[sl][warp][p], 1u << ol);
         }
     };
 
@@ -214,12 +248,12 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     };
     // This lane's entry bits (passing, up to lim), their count, the warp prefix;
     // returns the warp total.
-    auto gather = [&](uint32_t (&words)[kWords], int lim, int& myoff, int& nmine) {
+    auto gather = [&](uint32_t (&words)[kWords], int lim, int sl, int& myoff, int& nmine) {
         nmine = 0;
 #pragma unroll
         for (int w = 0; w < kWords; ++w) {
             const int top = lim - (w << 5);
-            uint32_t word = top >= 0 ? s_bits[w][threadIdx.x] : 0u;
+            uint32_t word = top >= 0 ? s_bits[sl][w][threadIdx.x] : 0u;
             if (top >= 0 && top < 31) word &= (2u << top) - 1u;
             words[w] = word;
             nmine += __popc(word);
@@ -247,16 +281,18 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         const int base = c * kChunk;
         const uint32_t skip = __ballot_sync(0xffffffffu, done);
         if (lane == 0) s_skip[warp] = skip;
+        const int sl = c % kRing;
         stage(base);
+        clear_bits(sl);
         resident = c;
         __syncthreads();
         const int cnt = min(kChunk, len - base);
-        pairs(cnt);
+        pairs(cnt, sl);
         __syncthreads();
         // Composite: each pixel applies its passing entries in list order.
         if (!done) {
             for (int w = 0; w < kWords && !done; ++w) {
-                uint32_t word = s_bits[w][threadIdx.x];
+                uint32_t word = s_bits[sl][w][threadIdx.x];
                 while (word) {
                     const int j = (w << 5) | (__ffs(word) - 1);
                     word &= word - 1u;
@@ -286,6 +322,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const size_t HW = (size_t)a.W * (size_t)a.H;
     const size_t pix = (size_t)v * 3 * HW + (size_t)py * a.W + px;
     float g0 = 0.0f, g1 = 0.0f, g2c = 0.0f;
+    int gcode = 1 + 4 + 16;   // signs of dL/dC per channel, +1, two bits each
     double lsum = 0.0;
     if (inside) {
         a.image[pix] = C0;
@@ -299,6 +336,8 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             g0 = d0 > 0.0f ? a.inv3hw : (d0 < 0.0f ? -a.inv3hw : 0.0f);
             g1 = d1 > 0.0f ? a.inv3hw : (d1 < 0.0f ? -a.inv3hw : 0.0f);
             g2c = d2 > 0.0f ? a.inv3hw : (d2 < 0.0f ? -a.inv3hw : 0.0f);
+            gcode = (int)(d0 > 0.0f) - (int)(d0 < 0.0f) + 1 + 4 * ((int)(d1 > 0.0f) - (int)(d1 < 0.0f) + 1) +
+                    16 * ((int)(d2 > 0.0f) - (int)(d2 < 0.0f) + 1);
         }
     }
     // block reductions: loss, evaluation counts, last composited index
@@ -344,24 +383,32 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     }
     if (!kBackward) return;
     __syncthreads();
+    const int last_fwd = resident;   // the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
     const int max_last = s_max_last[0];
     if (max_last < 0) return;
 
     // ------------------------------------------------------------- backward
-    float S0 = T * a.bg0, S1 = T * a.bg1, S2 = T * a.bg2;
+    // dL/dC . (colour composited behind the next entry to visit), per pixel
+    float Sg = T * __fmaf_rn(g0, a.bg0, __fmaf_rn(g1, a.bg1, g2c * a.bg2));
     float Tcur = T;
     float* __restrict__ g2v = a.grad2d + (size_t)v * (size_t)a.n * GS_GRAD2D_STRIDE;
     uint8_t* __restrict__ touchv = a.touched + (size_t)v * (size_t)a.n;
     for (int c = max_last / kChunk; c >= 0; --c) {
         const int base = c * kChunk;
+        const int sl = c % kRing;
         if (c != resident) {
-            __syncthreads();   // the previous chunk's records and sums are no longer read
-            const uint32_t skip = __ballot_sync(0xffffffffu, last < base);
-            if (lane == 0) s_skip[warp] = skip;
+            __syncthreads();   // the previous chunk's records are no longer read
             stage(base);
+            if (c <= last_fwd - kRing) {
+                // pass bits no longer in the ring: recompute them for the pixels
+                // that composited an entry of this chunk
+                const uint32_t skip = __ballot_sync(0xffffffffu, last < base);
+                if (lane == 0) s_skip[warp] = skip;
+                clear_bits(sl);
+                __syncthreads();
+                pairs(min(kChunk, len - base), sl);
+            }
             resident = c;
-            __syncthreads();
-            pairs(min(kChunk, len - base));
             __syncthreads();
         }
         // This pixel's composited entries in the chunk are its passing bits up to
@@ -371,7 +418,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         // segmented exclusive sum of c * w from the pixel's current S.
         uint32_t words[kWords];
         int myoff, nmine;
-        const int nq = gather(words, last - base, myoff, nmine);
+        const int nq = gather(words, last - base, sl, myoff, nmine);
         const int myend = myoff + nmine;
         for (int wb = 0; wb < nq; wb += kQueue) {
             fill_window(words, false, myoff, nmine, wb);
@@ -385,12 +432,11 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 const int j = (int)(ent & 0xffu);
                 const int own_off = __shfl_sync(0xffffffffu, myoff, owner);
                 const float Tst = __shfl_sync(0xffffffffu, Tcur, owner);
-                const float Ss0 = __shfl_sync(0xffffffffu, S0, owner);
-                const float Ss1 = __shfl_sync(0xffffffffu, S1, owner);
-                const float Ss2 = __shfl_sync(0xffffffffu, S2, owner);
-                const float go0 = __shfl_sync(0xffffffffu, g0, owner);
-                const float go1 = __shfl_sync(0xffffffffu, g1, owner);
-                const float go2 = __shfl_sync(0xffffffffu, g2c, owner);
+                const float Sgs = __shfl_sync(0xffffffffu, Sg, owner);
+                const int gco = __shfl_sync(0xffffffffu, gcode, owner);
+                const float go0 = (float)((gco & 3) - 1) * a.inv3hw;
+                const float go1 = (float)(((gco >> 2) & 3) - 1) * a.inv3hw;
+                const float go2 = (float)(((gco >> 4) & 3) - 1) * a.inv3hw;
                 const int pidx = warp * 32 + owner;
                 const float pxo = (float)(ox + (pidx & (kTile - 1))) + 0.5f;
                 const float pyo = (float)(oy + pidx / kTile) + 0.5f;
@@ -408,43 +454,32 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                     alpha = fminf(alpha_max, araw);
                 }
                 const float rc = rcp_approx(1.0f - alpha);
-                // segmented inclusive product (T) and sums (colour behind)
-                bool hd = !valid || lane == 0 || qi == own_off;
+                // segments = pixels: a lane's segment starts at the nearest head at
+                // or below it (lane 0 always is one)
+                const uint32_t heads = __ballot_sync(0xffffffffu, !valid || lane == 0 || qi == own_off);
+                const int seg = 31 - __clz(heads & ((2u << lane) - 1u));
+                // segmented inclusive product of 1 / (1 - alpha): T before each entry
                 float P = rc;
-                float x0 = r1.z * alpha, x1 = r1.w * alpha, x2 = cb * alpha;   // c * alpha, times T below
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
                     const float Pu = __shfl_up_sync(0xffffffffu, P, d);
-                    const bool hu = __shfl_up_sync(0xffffffffu, (int)hd, d) != 0;
-                    if (lane >= d) {
-                        if (!hd) P = Pu * P;
-                        hd = hd || hu;
-                    }
+                    if (lane - d >= seg) P = Pu * P;
                 }
                 const float Tb = Tst * P;             // transmittance before this entry
-                x0 *= Tb;
-                x1 *= Tb;
-                x2 *= Tb;
-                float y0 = x0, y1 = x1, y2 = x2;
-                hd = !valid || lane == 0 || qi == own_off;
+                // dL/dC . (c * alpha * T) of this entry; the segmented sum of the
+                // entries before it in the queue (after it in the list) is dL/dC .
+                // the colour composited behind it
+                const float dotc = __fmaf_rn(go0, r1.z, __fmaf_rn(go1, r1.w, go2 * cb));
+                const float z = valid ? dotc * alpha * Tb : 0.0f;
+                float y = z;
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
-                    const float u0 = __shfl_up_sync(0xffffffffu, y0, d);
-                    const float u1 = __shfl_up_sync(0xffffffffu, y1, d);
-                    const float u2 = __shfl_up_sync(0xffffffffu, y2, d);
-                    const bool hu = __shfl_up_sync(0xffffffffu, (int)hd, d) != 0;
-                    if (lane >= d) {
-                        if (!hd) {
-                            y0 += u0;
-                            y1 += u1;
-                            y2 += u2;
-                        }
-                        hd = hd || hu;
-                    }
+                    const float u = __shfl_up_sync(0xffffffffu, y, d);
+                    if (lane - d >= seg) y += u;
                 }
                 if (valid) {
-                    const EntryGrad e = entry_grad_at(r0, r1, cb, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb,
-                                                      Ss0 + (y0 - x0), Ss1 + (y1 - x1), Ss2 + (y2 - x2), rc);
+                    const EntryGrad e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb, dotc,
+                                                      Sgs + (y - z), rc);
                     const uint32_t gid = s_id[j];
                     float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
                     atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
@@ -457,14 +492,10 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 const int k = seg_hi - 1 - r;
                 const int src = k < 0 ? 0 : (k > 31 ? 31 : k);
                 const float Tk = __shfl_sync(0xffffffffu, Tb, src);
-                const float Y0 = __shfl_sync(0xffffffffu, y0, src);
-                const float Y1 = __shfl_sync(0xffffffffu, y1, src);
-                const float Y2 = __shfl_sync(0xffffffffu, y2, src);
+                const float Yk = __shfl_sync(0xffffffffu, y, src);
                 if (seg_lo < seg_hi) {
                     Tcur = Tk;
-                    S0 += Y0;
-                    S1 += Y1;
-                    S2 += Y2;
+                    Sg += Yk;
                 }
             }
             __syncwarp();

@@ -4,7 +4,7 @@
  * One training step is five calls on one CUDA stream:
  *
  *   gs_project               EWA projection, culling, colour (per Gaussian x view)
- *   gs_bin_sort              16x16 tile binning with (tile, depth) keys + LSD radix sort
+ *   gs_bin_sort              16x16 tile binning with (tile, depth) keys + sort
  *   gs_raster_fused_fwd_bwd  forward compositing, L1 loss and backward in ONE kernel
  *   gs_grad_compact          touched-set compaction, projection VJP, scatter-add
  *   gs_adam_deferred         Adam on the touched Gaussians only, with catch-up
@@ -161,10 +161,12 @@ GS_API gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views, in
  * power > 0 or alpha < alpha_min, C += c * alpha * T, T *= 1 - alpha, stop at
  * T < t_min; C += T * bg.  The per-pixel T, colour and last index stay in
  * registers.  With a target: L1 loss per view, mean over 3*H*W values, summed in
- * fp64, and its gradient sign(C - target) / (3HW) on chip; backward walks the
- * same list back to front (transmittance recovered by division) and
- * accumulates per-Gaussian gradients with warp reductions and one atomic per
- * warp and component.
+ * fp64, and its gradient sign(C - target) / (3HW) on chip; backward walks each
+ * pixel's composited entries back to front (transmittance recovered by
+ * division): a warp queues its pixels' entries grouped by pixel and takes them
+ * 32 at a time, with T and dL/dC . (colour behind) from segmented warp scans,
+ * and adds each entry's 9 gradient terms to the Gaussian's grad2d row with
+ * vector atomics (their order varies from run to run).
  * target: [V][3][H][W] or NULL (forward only: no loss, gradients or touched).
  * image: [V][3][H][W] out.  loss: [V] fp64 out (overwritten).
  * grad2d: [V][n][GS_GRAD2D_STRIDE] accumulated (+=): d/d mean2d (x, y),
