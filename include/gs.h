@@ -231,8 +231,10 @@ GS_API gs_status gs_grad_compact_static(float* grad2d, uint8_t* touched, const f
  *   gradients (idx, n_idx, grads unused) -- call before reading or saving params.
  * params, grads, m, v: [n][stride]; last_step: [n] int32 (0 = never stepped).
  * idx: [>= *n_idx] u32, n_idx: DEVICE int64.  lr: HOST [5] per group (mean,
- * log-scale, quaternion, opacity, colour).  t >= 1.
- * Errors: INVALID_ARG for bad pointers or t < 1. */
+ * log-scale, quaternion, opacity, colour), each finite and >= 0; 0 <= beta1,
+ * beta2 < 1; eps > 0 and finite; t >= 1.  Padding entries k >= P of a block are
+ * never touched.
+ * Errors: INVALID_ARG for bad pointers, t < 1, or lr / beta / eps out of range. */
 GS_API gs_status gs_adam_deferred(float* params, float* grads, float* m, float* v, int32_t* last_step, int64_t n,
                            int32_t sh_degree, const uint32_t* idx, const int64_t* n_idx, int32_t t, const float* lr,
                            float beta1, float beta2, float eps, int32_t flush, void* stream);

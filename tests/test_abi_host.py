@@ -78,6 +78,12 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     lr = (ctypes.c_float * 5)(1, 1, 1, 1, 1)
     assert L.gs_adam_deferred(16, 16, 16, 16, 16, 10, 0, 16, 16, 0, lr, ctypes.c_float(0.9), ctypes.c_float(0.999),
                               ctypes.c_float(1e-8), 0, None) == abi.GS_ERR_INVALID_ARG
+    # Adam: learning rates >= 0 and finite, 0 <= beta < 1, eps > 0
+    for bad_lr, b1, b2, e in (((1, 1, -1e-3, 1, 1), 0.9, 0.999, 1e-8), ((1, 1, 1, float("inf"), 1), 0.9, 0.999, 1e-8),
+                              ((1, 1, 1, 1, 1), 1.0, 0.999, 1e-8), ((1, 1, 1, 1, 1), 0.9, 0.999, 0.0)):
+        lrb = (ctypes.c_float * 5)(*bad_lr)
+        assert L.gs_adam_deferred(16, 16, 16, 16, 16, 10, 0, 16, 16, 1, lrb, ctypes.c_float(b1), ctypes.c_float(b2),
+                                  ctypes.c_float(e), 0, None) == abi.GS_ERR_INVALID_ARG
     # raster with a target but no gradient buffers
     assert L.gs_raster_fused_fwd_bwd(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None, None,
                                      None, None, None) == abi.GS_ERR_INVALID_ARG
