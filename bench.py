@@ -280,16 +280,16 @@ def run_gpu(args):
     evals_per_step = e_fwd + e_bwd
     raster_ms = float(stage_ms[:, 2].mean())
 
-    # ---- end to end through the public API: pinned host target in, loss out, every step
+    # ---- end to end through the public API: every step's target copied in from pinned
+    # host memory (step k + 1's copy overlapping step k) and its loss copied out
     target_host = target.cpu().pin_memory()
-    loss_host = torch.empty(tr.V, dtype=torch.float64).pin_memory()
-    target_dev = torch.empty_like(target)
+    loss_host = torch.empty((args.steps, tr.V), dtype=torch.float64).pin_memory()
+    tr.train_steps_host([target_host] * 2, torch.empty((2, tr.V), dtype=torch.float64).pin_memory())   # buffers, stream
     tr.eval_counts.zero_()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
-    for k in range(args.steps):
-        tr.train_step_host(target_host, target_dev, loss_host)
+    tr.train_steps_host([target_host] * args.steps, loss_host)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)

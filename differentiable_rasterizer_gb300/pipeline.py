@@ -170,6 +170,46 @@ class GaussianTrainer:
         loss_host.copy_(self.loss, non_blocking=True)
         return loss_host
 
+    def train_steps_host(self, targets_host, loss_host: torch.Tensor) -> torch.Tensor:
+        """End-to-end steps from pinned host memory, pipelined: while step k runs, the
+        target of step k + 1 is copied in on a second stream (two device buffers), and
+        each step's loss is copied out right after it.
+
+        targets_host: sequence of pinned [V, 3, H, W] fp32 tensors, one per step (the
+        same tensor may repeat).  loss_host: pinned [steps, V] fp64; row k receives
+        step k's loss.  Returns loss_host (valid once the current stream is synced)."""
+        steps = len(targets_host)
+        if steps == 0:
+            return loss_host
+        main = torch.cuda.current_stream(self.device)
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream(self.device)
+        shape = tuple(targets_host[0].shape)
+        bufs = getattr(self, "_target_bufs", None)
+        if bufs is None or tuple(bufs[0].shape) != shape:
+            bufs = self._target_bufs = [torch.empty(shape, dtype=torch.float32, device=self.device) for _ in range(2)]
+        copy = self._copy_stream
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        consumed = [torch.cuda.Event(), torch.cuda.Event()]
+        copy.wait_stream(main)   # copies start after everything already queued on the main stream
+        with torch.cuda.stream(copy):
+            bufs[0].copy_(targets_host[0], non_blocking=True)
+            copied[0].record(copy)
+        for k in range(steps):
+            b = k % 2
+            main.wait_event(copied[b])
+            if k + 1 < steps:
+                nb = (k + 1) % 2
+                with torch.cuda.stream(copy):
+                    if k >= 1:
+                        copy.wait_event(consumed[nb])   # step k - 1 has finished reading that buffer
+                    bufs[nb].copy_(targets_host[k + 1], non_blocking=True)
+                    copied[nb].record(copy)
+            self.train_step(bufs[b])
+            consumed[b].record(main)
+            loss_host[k].copy_(self.loss, non_blocking=True)
+        return loss_host
+
     def render(self, params=None) -> torch.Tensor:
         """Forward only (no loss, gradients or touched flags); returns the image tensor."""
         self.project(params)

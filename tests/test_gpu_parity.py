@@ -216,3 +216,23 @@ def test_three_training_steps_track_the_oracle():
     tr.flush()
     torch.cuda.synchronize()
     assert (tr.last_step.cpu().numpy() == 3).all()
+
+
+def test_pipelined_host_steps_match_device_steps():
+    """train_steps_host (targets copied in on a second stream, one step ahead) gives
+    the same losses as device-resident steps, and leaves each step's loss in its row."""
+    sc = scenes.make_scene("tiny")
+    tgt = torch.from_numpy(np.ascontiguousarray(sc.target_uniform, np.float32))
+    a = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr)
+    b = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr)
+    dev = tgt.cuda()
+    ref = [a.train_step(dev).cpu().numpy().copy() for _ in range(4)]
+    host = tgt.pin_memory()
+    loss = torch.empty((4, 1), dtype=torch.float64).pin_memory()
+    b.train_steps_host([host] * 4, loss)
+    torch.cuda.synchronize()
+    got = loss.numpy()
+    assert abs(got[0, 0] - ref[0][0]) <= 1e-9 * abs(ref[0][0])
+    for k in range(1, 4):
+        assert abs(got[k, 0] - ref[k][0]) <= 1e-5 * abs(ref[k][0]), (k, got[k, 0], ref[k][0])
+    assert b.t == 4
