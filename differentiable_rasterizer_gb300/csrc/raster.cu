@@ -27,7 +27,10 @@
 // behind it a segmented sum, both by warp shuffles; each entry's 9 gradient
 // terms go to the Gaussian's grad2d row with vector atomics.  The pass bits of
 // the last kRing chunks stay in shared memory (a ring), so backward re-gathers
-// only their records; older chunks also get their bits recomputed.
+// only their records; older chunks also get their bits recomputed.  A chunk in
+// which the warp's pixels mostly composite the same entries (large Gaussians) is
+// walked one entry at a time for all 32 pixels instead, its gradient terms summed
+// over the warp by shuffles before one atomic per component.
 //
 // All decisions use the same fp32 operations in the same order as the CPU
 // definition (see gs_common.cuh); boxes, tau and bits only avoid work whose
@@ -41,6 +44,7 @@ constexpr int kWords = kChunk / 32;
 constexpr int kWarps = kTileThreads / 32;
 constexpr int kQueue = 256;      // queue window (entries) per warp
 constexpr int kRing = 3;         // chunks whose pass bits stay in shared memory
+constexpr int kDense = 12;       // backward: entries per distinct Gaussian from which a warp reduces per Gaussian
 
 struct RasterArgs {
     const float4* __restrict__ rec;     // [V][n][3]
@@ -420,6 +424,69 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         int myoff, nmine;
         const int nq = gather(words, last - base, sl, myoff, nmine);
         const int myend = myoff + nmine;
+        // Distinct entries composited by any of the warp's pixels in this chunk.
+        uint32_t uni[kWords];
+        int nu = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            uni[w] = __reduce_or_sync(0xffffffffu, words[w]);
+            nu += __popc(uni[w]);
+        }
+        if (nq >= kDense * nu) {
+            // Dense chunk (large Gaussians: most of the warp's pixels composite
+            // the same entries): walk the union newest first, every lane updating
+            // its own pixel's T and dL/dC . (colour behind); the 9 gradient
+            // terms are summed over the warp by a butterfly and added with one
+            // atomic per component.
+#pragma unroll
+            for (int w = kWords - 1; w >= 0; --w) {
+                uint32_t u = uni[w];
+                while (u) {
+                    const int b = 31 - __clz(u);
+                    u &= ~(1u << b);
+                    const int j = (w << 5) | b;
+                    EntryGrad e;
+                    e.gm0 = e.gm1 = e.gA = e.gB = e.gC = e.go = e.gr = e.gg = e.gb = 0.0f;
+                    if ((words[w] >> b) & 1u) {
+                        const float4 r0 = s_r0[j];
+                        const float4 r1 = s_r1[j];
+                        const float cb = s_r2[j].x;
+                        const float dx = pxf - r0.x, dy = pyf - r0.y;
+                        const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+                        const float G = pexp_neg(power);
+                        const float araw = r1.y * G;
+                        const float alpha = fminf(alpha_max, araw);
+                        const float rc = rcp_approx(1.0f - alpha);
+                        const float Tb = Tcur * rc;   // transmittance before this entry
+                        const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
+                        e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, g0, g1, g2c, Tb, dotc, Sg, rc);
+                        Sg += dotc * alpha * Tb;
+                        Tcur = Tb;
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        e.gm0 += __shfl_xor_sync(0xffffffffu, e.gm0, o);
+                        e.gm1 += __shfl_xor_sync(0xffffffffu, e.gm1, o);
+                        e.gA += __shfl_xor_sync(0xffffffffu, e.gA, o);
+                        e.gB += __shfl_xor_sync(0xffffffffu, e.gB, o);
+                        e.gC += __shfl_xor_sync(0xffffffffu, e.gC, o);
+                        e.go += __shfl_xor_sync(0xffffffffu, e.go, o);
+                        e.gr += __shfl_xor_sync(0xffffffffu, e.gr, o);
+                        e.gg += __shfl_xor_sync(0xffffffffu, e.gg, o);
+                        e.gb += __shfl_xor_sync(0xffffffffu, e.gb, o);
+                    }
+                    if (lane < 4) {
+                        const uint32_t gid = s_id[j];
+                        float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
+                        if (lane == 0) atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
+                        else if (lane == 1) atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
+                        else if (lane == 2) atomicAdd(dst + 8, e.gb);
+                        else touchv[gid] = 1;
+                    }
+                }
+            }
+            continue;
+        }
         for (int wb = 0; wb < nq; wb += kQueue) {
             fill_window(words, false, myoff, nmine, wb);
             __syncwarp();
