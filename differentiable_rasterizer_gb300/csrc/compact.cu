@@ -132,11 +132,18 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
     unsigned long long* counts = reinterpret_cast<unsigned long long*>(n_idx);
     for (int v = 0; v < n_views; ++v)
         GS_CUDA_TRY((scan_launch<uint8_t, true>(touched + (size_t)v * n, n, idx + (size_t)v * n, sums, counts + v, s)));
-    if (n > 0) {
-        union_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(touched, n, n_views, flags);
-        GS_LAUNCH_CHECK();
+    if (n_views == 1) {
+        // one view: the union is that view's list
+        if (n > 0)
+            GS_CUDA_TRY(cudaMemcpyAsync(idx + n, idx, sizeof(uint32_t) * (size_t)n, cudaMemcpyDeviceToDevice, s));
+        GS_CUDA_TRY(cudaMemcpyAsync(counts + 1, counts, sizeof(unsigned long long), cudaMemcpyDeviceToDevice, s));
+    } else {
+        if (n > 0) {
+            union_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(touched, n, n_views, flags);
+            GS_LAUNCH_CHECK();
+        }
+        GS_CUDA_TRY((scan_launch<uint8_t, true>(flags, n, idx + (size_t)n_views * n, sums, counts + n_views, s)));
     }
-    GS_CUDA_TRY((scan_launch<uint8_t, true>(flags, n, idx + (size_t)n_views * n, sums, counts + n_views, s)));
     if (n == 0) return GS_OK;
     VjpArgs a;
     a.grad2d = grad2d;

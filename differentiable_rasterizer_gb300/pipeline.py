@@ -101,7 +101,8 @@ class GaussianTrainer:
         projection 1; binning: count 1, scan 3, bucket stats 1, then (when there are
         instances) scatter 1, warp sort 1, and one more sort kernel for each of the
         size classes 257..2048, 2049..16384 and over 16384 that occurs; fused raster 1;
-        compaction: 3 per view-list scan, union 1, union scan 3, VJP 1; Adam 2.
+        compaction: 3 per view-list scan, then (several views) union 1 and union scan 3,
+        VJP 1; Adam 2.
         Memsets and copies are not kernels.  Reads the last step's ranges."""
         V, n = self.V, self.n
         r = self.ranges.view(-1, 2).to(torch.int64)
@@ -110,7 +111,7 @@ class GaussianTrainer:
         if self.n_instances:
             sort += 2 + sum(int(((c > lo) & (c <= hi)).any().item())
                             for lo, hi in ((256, 2048), (2048, 16384), (16384, 1 << 62)))
-        compact = (3 * V + 1 + 3 + 1) if n else 0
+        compact = (3 * V + (1 + 3 if V > 1 else 0) + 1) if n else 0
         return (1 if n else 0) + sort + 1 + compact + (2 if n else 0)
 
     def stream_handle(self):
