@@ -18,7 +18,8 @@
 //               every bucket through shared-memory cursors (any order);
 //   5. sort:    buckets of <= kWarpCap instances: one warp, bitonic in registers;
 //               <= kRegCap: one CTA, bitonic in registers (long strides through
-//               shared memory); <= kBigCap: one CTA, bitonic in shared memory;
+//               shared memory); <= kBigCap: one 1024-thread CTA, the same with
+//               4-16 keys per thread;
 //               larger: one CTA splits the bucket by key range into kSplit
 //               sub-buckets (counting scatter), sorts the small ones as above and
 //               splits the large ones again (depth first, at most seven levels).
@@ -36,6 +37,7 @@ constexpr int64_t kMaxCounts = 1 << 22;    // cap on (view, tile, block) count e
 constexpr int kWarpCap = 256;              // bucket sizes sorted by one warp (8 keys per lane)
 constexpr int kRegCap = 2048;              // bucket sizes sorted by one 256-thread CTA in registers
 constexpr int kRegThreads = 256;
+constexpr int kMidThreads = 1024;          // mid-class sort: kMidThreads * 16 = kBigCap keys
 constexpr int kBigCap = 16384;             // bucket sizes sorted by one CTA in shared memory
 constexpr int kSplit = 1024;               // sub-buckets per split of a larger bucket
 constexpr int kStack = 8 * kSplit;         // pending sub-buckets (<= 1023 per level, <= 7 levels)
@@ -206,30 +208,35 @@ __device__ __forceinline__ void warp_sort(const uint64_t* __restrict__ src, size
 template <int E>
 __device__ __forceinline__ int pad_slot(int i) { return i + i / E; }
 
-// A kRegThreads-thread CTA sorts src[o, o + c), c <= kRegThreads * E: thread t
+// A kT-thread CTA sorts src[o, o + c), c <= kT * E: thread t
 // holds elements [t * E, (t + 1) * E) in registers; strides below E are register
 // swaps, strides below 32 E lane exchanges, the rest go through shared memory s
-// (kRegThreads * (E + 1) keys).
-template <int E>
+// (kT * (E + 1) keys).
+template <int kT, int E, bool kUnroll>
 __device__ __forceinline__ void reg_sort(const uint64_t* __restrict__ src, size_t o, int c, uint64_t hi,
                                          uint64_t* __restrict__ keys, uint32_t* __restrict__ ids, uint64_t* s)
 {
-    constexpr int P = kRegThreads * E;
+    constexpr int P = kT * E;
     const int tid = threadIdx.x, lane = tid & 31;
-    for (int i = tid; i < P; i += kRegThreads) s[pad_slot<E>(i)] = i < c ? src[o + i] : ~0ull;
+    for (int i = tid; i < P; i += kT) s[pad_slot<E>(i)] = i < c ? src[o + i] : ~0ull;
     __syncthreads();
     uint64_t x[E];
 #pragma unroll
     for (int r = 0; r < E; ++r) x[r] = s[pad_slot<E>(tid * E + r)];
     __syncthreads();
-#pragma unroll
+    // Small networks are unrolled whole; for large ones (kUnroll = false) the
+    // stage loops run at run time and only the register-stride stages (j < E)
+    // and the per-key loops are unrolled, so every index into x stays a
+    // constant without unrolling thousands of stages.
+#pragma unroll(kUnroll ? 16 : 1)
     for (int k = 2; k <= P; k <<= 1) {
         if ((k >> 1) >= 32 * E) {
 #pragma unroll
             for (int r = 0; r < E; ++r) s[pad_slot<E>(tid * E + r)] = x[r];
             __syncthreads();
+#pragma unroll(kUnroll ? 16 : 1)
             for (int j = k >> 1; j >= 32 * E; j >>= 1) {
-                for (int i = tid; i < P; i += kRegThreads) {
+                for (int i = tid; i < P; i += kT) {
                     const int ixj = i ^ j;
                     if (ixj > i) {
                         const uint64_t a = s[pad_slot<E>(i)], b = s[pad_slot<E>(ixj)];
@@ -245,27 +252,28 @@ __device__ __forceinline__ void reg_sort(const uint64_t* __restrict__ src, size_
             for (int r = 0; r < E; ++r) x[r] = s[pad_slot<E>(tid * E + r)];
             __syncthreads();
         }
+#pragma unroll(kUnroll ? 16 : 1)
+        for (int j = (k >> 1) < 32 * E ? (k >> 1) : 16 * E; j >= E; j >>= 1) {
+            const int lj = j / E;
+            const bool lower = (lane & lj) == 0;
 #pragma unroll
-        for (int j = (k >> 1) < 32 * E ? (k >> 1) : 16 * E; j > 0; j >>= 1) {
-            if (j >= E) {
-                const int lj = j / E;
-                const bool lower = (lane & lj) == 0;
+            for (int r = 0; r < E; ++r) {
+                const bool up = (((tid * E + r) & k) == 0);
+                const uint64_t y = __shfl_xor_sync(0xffffffffu, x[r], lj);
+                x[r] = (lower == up) ? (y < x[r] ? y : x[r]) : (y > x[r] ? y : x[r]);
+            }
+        }
 #pragma unroll
-                for (int r = 0; r < E; ++r) {
+        for (int j = E / 2; j > 0; j >>= 1) {
+            if (j > (k >> 1)) continue;
+#pragma unroll
+            for (int r = 0; r < E; ++r) {
+                if ((r & j) == 0) {
                     const bool up = (((tid * E + r) & k) == 0);
-                    const uint64_t y = __shfl_xor_sync(0xffffffffu, x[r], lj);
-                    x[r] = (lower == up) ? (y < x[r] ? y : x[r]) : (y > x[r] ? y : x[r]);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < E; ++r) {
-                    if ((r & j) == 0) {
-                        const bool up = (((tid * E + r) & k) == 0);
-                        const uint64_t p = x[r], q = x[r | j];
-                        if ((p > q) == up) {
-                            x[r] = q;
-                            x[r | j] = p;
-                        }
+                    const uint64_t p = x[r], q = x[r | j];
+                    if ((p > q) == up) {
+                        x[r] = q;
+                        x[r | j] = p;
                     }
                 }
             }
@@ -274,7 +282,7 @@ __device__ __forceinline__ void reg_sort(const uint64_t* __restrict__ src, size_
 #pragma unroll
     for (int r = 0; r < E; ++r) s[pad_slot<E>(tid * E + r)] = x[r];
     __syncthreads();
-    for (int i = tid; i < c; i += kRegThreads) emit_sorted(s[pad_slot<E>(i)], hi, keys, ids, o + i);
+    for (int i = tid; i < c; i += kT) emit_sorted(s[pad_slot<E>(i)], hi, keys, ids, o + i);
 }
 
 // Bitonic sort of s[0, P) ascending (P a power of two), all threads of the block.
@@ -337,21 +345,27 @@ __global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* _
     const uint2 r = ranges[t];
     const int c = (int)(r.y - r.x);
     const uint64_t hi = (uint64_t)t << 32;
-    if (c <= 2 * kRegThreads) reg_sort<2>(tmp, r.x, c, hi, keys, ids, s);
-    else if (c <= 4 * kRegThreads) reg_sort<4>(tmp, r.x, c, hi, keys, ids, s);
-    else reg_sort<8>(tmp, r.x, c, hi, keys, ids, s);
+    if (c <= 2 * kRegThreads) reg_sort<kRegThreads, 2, true>(tmp, r.x, c, hi, keys, ids, s);
+    else if (c <= 4 * kRegThreads) reg_sort<kRegThreads, 4, true>(tmp, r.x, c, hi, keys, ids, s);
+    else reg_sort<kRegThreads, 8, true>(tmp, r.x, c, hi, keys, ids, s);
 }
 
-// One 1024-thread CTA per listed bucket of kRegCap < size <= kBigCap.
-__global__ void __launch_bounds__(1024) sort_mid_kernel(const uint32_t* __restrict__ list,
-                                                        const uint2* __restrict__ ranges,
-                                                        const uint64_t* __restrict__ tmp, uint64_t* __restrict__ keys,
-                                                        uint32_t* __restrict__ ids)
+// One kMidThreads-thread CTA per listed bucket of kRegCap < size <= kBigCap:
+// the same register / shuffle / shared-memory bitonic with 4, 8 or 16 keys per
+// thread (dynamic shared memory: kMidThreads * (E + 1) keys for the largest E).
+__global__ void __launch_bounds__(kMidThreads) sort_mid_kernel(const uint32_t* __restrict__ list,
+                                                               const uint2* __restrict__ ranges,
+                                                               const uint64_t* __restrict__ tmp,
+                                                               uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
 {
     extern __shared__ uint64_t s_mid[];
     const uint32_t t = list[blockIdx.x];
     const uint2 r = ranges[t];
-    cta_sort(s_mid, tmp, r.x, (int)(r.y - r.x), (uint64_t)t << 32, keys, ids);
+    const int c = (int)(r.y - r.x);
+    const uint64_t hi = (uint64_t)t << 32;
+    if (c <= 4 * kMidThreads) reg_sort<kMidThreads, 4, false>(tmp, r.x, c, hi, keys, ids, s_mid);
+    else if (c <= 8 * kMidThreads) reg_sort<kMidThreads, 8, false>(tmp, r.x, c, hi, keys, ids, s_mid);
+    else reg_sort<kMidThreads, 16, false>(tmp, r.x, c, hi, keys, ids, s_mid);
 }
 
 // Block-wide min / max of 64-bit values (blockDim.x == 1024).
@@ -617,11 +631,10 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
         GS_LAUNCH_CHECK();
     }
     if (host.st[2] > 0) {
-        int P = 1;
-        while (P < (int)min(host.st[0], (unsigned)kBigCap)) P <<= 1;
-        const size_t smem = sizeof(uint64_t) * (size_t)P;
+        const int e = host.st[0] <= 4u * kMidThreads ? 4 : (host.st[0] <= 8u * kMidThreads ? 8 : 16);
+        const size_t smem = sizeof(uint64_t) * (size_t)kMidThreads * (size_t)(e + 1);
         GS_CUDA_TRY(cudaFuncSetAttribute(sort_mid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        sort_mid_kernel<<<host.st[2], 1024, smem, s>>>(lists + ntile_ids, ranges, tmp, keys, ids);
+        sort_mid_kernel<<<host.st[2], kMidThreads, smem, s>>>(lists + ntile_ids, ranges, tmp, keys, ids);
         GS_LAUNCH_CHECK();
     }
     if (host.st[3] > 0) {
