@@ -31,7 +31,8 @@
 namespace gs {
 
 constexpr int kBinThreads = 1024;          // count / scatter block size
-constexpr int kBinBlocks = 304;            // count / scatter blocks over all views (2 per SM)
+constexpr int kBinBlocks = 304;            // count / scatter blocks over all views (2 per SM) ...
+constexpr int kBinBlocksOneView = 152;     // ... or for a single view (fewer count entries to scan)
 constexpr int kBandTiles = 40960;          // shared-memory tile counters per block (160 KB)
 constexpr int64_t kMaxCounts = 1 << 22;    // cap on (view, tile, block) count entries
 constexpr int kWarpCap = 256;              // bucket sizes sorted by one warp (8 keys per lane)
@@ -59,10 +60,12 @@ template <bool kScatter>
 __global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __restrict__ touched_cnt,
                                                           const ushort4* __restrict__ rect,
                                                           const float* __restrict__ depth, BinGeom G,
-                                                          uint32_t* __restrict__ cnt, uint64_t* __restrict__ tmp)
+                                                          uint32_t* __restrict__ cnt, uint64_t* __restrict__ tmp,
+                                                          unsigned int* __restrict__ stats)
 {
     extern __shared__ uint32_t s_cnt[];
     const int b = blockIdx.x, band = blockIdx.y, v = blockIdx.z;
+    if (!kScatter && b == 0 && band == 0 && v == 0 && threadIdx.x < 4) stats[threadIdx.x] = 0u;   // for bucket_stats
     const int row0 = band * G.band_rows;
     const int row1 = min(G.tiles_y, row0 + G.band_rows);
     const int nt = (row1 - row0) * G.tiles_x;
@@ -524,7 +527,7 @@ inline BinGeom bin_geom(int64_t n, int n_views, int tiles_x, int tiles_y)
     G.tiles_y = tiles_y;
     G.tiles = tiles_x * tiles_y;
     const int64_t ntile_ids = (int64_t)G.tiles * n_views;
-    int64_t B = (kBinBlocks + n_views - 1) / n_views;
+    int64_t B = n_views == 1 ? kBinBlocksOneView : (kBinBlocks + n_views - 1) / n_views;
     if (B * ntile_ids > kMaxCounts) B = kMaxCounts / ntile_ids;
     if (B > n) B = n;
     if (B < 1) B = 1;
@@ -546,8 +549,9 @@ inline WsLayout ws_layout(const BinGeom& G, int64_t ntile_ids, int64_t capacity)
     L.cnt = o;       o = align_up(o + sizeof(uint32_t) * (size_t)ncnt);
     L.off = o;       o = align_up(o + sizeof(uint32_t) * (size_t)ncnt);
     L.scan_sums = o; o = align_up(o + scan_ws_bytes(ncnt));
-    L.totals = o;    o = align_up(o + sizeof(unsigned long long));
-    L.stats = o;     o = align_up(o + 4 * sizeof(unsigned int));
+    L.totals = o;    // instance total (u64) and the bucket stats (4 x u32), read back in one copy
+    L.stats = o + sizeof(unsigned long long);
+    o = align_up(o + sizeof(unsigned long long) + 4 * sizeof(unsigned int));
     L.lists = o;     o = align_up(o + 3 * sizeof(uint32_t) * (size_t)ntile_ids);
     L.tmp = o;       o = align_up(o + sizeof(uint64_t) * (size_t)capacity);
     L.bytes = o;
@@ -595,14 +599,14 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     const dim3 bin_grid((unsigned)G.B, (unsigned)bands, (unsigned)n_views);
     const size_t bin_smem = sizeof(uint32_t) * (size_t)G.band_rows * (size_t)tiles_x;
 
-    GS_CUDA_TRY(cudaMemsetAsync(stats, 0, 4 * sizeof(unsigned int), s));
     if (n > 0) {
         GS_CUDA_TRY(cudaFuncSetAttribute(bin_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem));
         bin_kernel<false><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, cnt,
-                                                                   nullptr);
+                                                                   nullptr, stats);
         GS_LAUNCH_CHECK();
     } else {
         GS_CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * (size_t)ncnt, s));
+        GS_CUDA_TRY(cudaMemsetAsync(stats, 0, 4 * sizeof(unsigned int), s));
     }
     GS_CUDA_TRY((scan_launch<uint32_t, false>(cnt, ncnt, off, scan_sums, totals, s)));
     const int threads = 256;
@@ -613,15 +617,16 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
         unsigned long long total;
         unsigned int st[4];
     } host;
-    GS_CUDA_TRY(cudaMemcpyAsync(&host.total, totals, sizeof(host.total), cudaMemcpyDeviceToHost, s));
-    GS_CUDA_TRY(cudaMemcpyAsync(host.st, stats, sizeof(host.st), cudaMemcpyDeviceToHost, s));
+    static_assert(sizeof(host) == sizeof(unsigned long long) + 4 * sizeof(unsigned int), "host copy layout");
+    GS_CUDA_TRY(cudaMemcpyAsync(&host, totals, sizeof(host), cudaMemcpyDeviceToHost, s));
     GS_CUDA_TRY(cudaStreamSynchronize(s));
     *n_instances = (int64_t)host.total;
     if ((int64_t)host.total > capacity) return GS_ERR_CAPACITY;
     if (host.total == 0) return GS_OK;
 
     GS_CUDA_TRY(cudaFuncSetAttribute(bin_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem));
-    bin_kernel<true><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, off, tmp);
+    bin_kernel<true><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, off, tmp,
+                                                              nullptr);
     GS_LAUNCH_CHECK();
     sort_warp_kernel<<<(unsigned)((ntile_ids + kSortWarps - 1) / kSortWarps), kSortWarps * 32, 0, s>>>(
         ranges, ntile_ids, tmp, keys, ids);
