@@ -75,15 +75,16 @@ def source_sha():
     return h.hexdigest()
 
 
-def traffic_from_profile():
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it matches the source."""
+def profile_figures():
+    """Figures of the fused kernel from the committed ncu capture (DRAM bytes per launch,
+    issue slots busy), or None where the capture does not match the current source."""
     path = os.path.join(ROOT, "profiles", "raster_fused_medium_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except OSError:
-        return None
-    return d.get("dram_bytes_per_launch") if d.get("source_sha256") == source_sha() else None
+        return {}
+    return d if d.get("source_sha256") == source_sha() else {}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -303,6 +304,7 @@ def run_gpu(args):
     e2e_value = world * e2e_evals / (e2e_ms / 1e3)
 
     pk = peaks()
+    prof = profile_figures()
     t_raster = raster_ms / 1e3
     ops_b = e_fwd * (OPS_FWD + OPS_EXP) + e_bwd * (OPS_BWD + OPS_EXP)
     sfu_b = e_bwd
@@ -312,7 +314,9 @@ def run_gpu(args):
     t_a = max(ops_a / (pk["fp32_tops"] * 1e12), sfu_a / (pk["sfu_tops"] * 1e12))
     achieved = ops_b / t_raster / 1e12
     roofline = {"bound": "alu", "achieved": achieved, "peak": pk["fp32_tops"], "unit": "TFLOP/s",
-                "frac": t_b / t_raster, "traffic": traffic_from_profile(),
+                "frac": t_b / t_raster, "traffic": prof.get("dram_bytes_per_launch") if args.config == "medium" else None,
+                "issue_active_ncu": (prof.get("issue_active_pct") / 100.0 if prof.get("issue_active_pct") is not None
+                                     and args.config == "medium" else None),
                 "kernel": "raster_fused_kernel<true>",
                 "peak_basis": f"FP32 ops (an fma counts once): 152 SMs x 128 lanes x {pk['sm_max_mhz']:.0f} MHz "
                               f"(sm_max_mhz, {pk['src']}); SFU: 152 x 16 lanes",
@@ -321,7 +325,9 @@ def run_gpu(args):
                 "frac_exp_as_sfu_op": t_a / t_raster,
                 "note": "the kernel skips exp and all backward work for entries that provably cannot pass "
                         "(bit-identical results), so it does less arithmetic than this per-evaluation model "
-                        "charges; a fraction above 1 means exactly that"}
+                        "charges; a fraction above 1 means exactly that.  issue_active_ncu is the hardware's "
+                        "own figure for the same launch (issue slots busy, from the committed ncu capture of "
+                        "the medium workload)"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
