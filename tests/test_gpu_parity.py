@@ -1,7 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle, stage by
-stage, on seeded inputs (tiny, ragged, dense, multi-view, degree-3, small,
-medium), plus edge cases (no Gaussians, everything culled, instance capacity
-growth), the deferred Adam with catch-up and flush, and several training steps."""
+stage, on seeded inputs (tiny, ragged, dense lists, every bucket-sort size class
+including multi-level key-range splits, a view binned in two tile-row bands,
+multi-view with RGB and with SH 3, degree-3, small, medium), plus edge cases (no
+Gaussians, everything culled, instance capacity growth), the deferred Adam with
+catch-up and flush, several training steps, and the pipelined host-input steps."""
 import math
 
 import numpy as np
@@ -113,6 +115,21 @@ def test_multi_view_small_reduced():
         cams.append(scenes.Camera(R, np.array([0.3 * k, 0, 0.5], np.float32), 250.0, 250.0, 160.0, 90.0, 320, 180))
     sc.cameras = cams
     parity.run_stage_parity(sc)
+
+
+def test_multi_view_degree3_exclude_crossing_background():
+    """Three views of the SH-3 medium recipe at reduced size, with the crossing
+    Gaussian excluded at the stop and a non-zero background."""
+    sc = scenes.make_scene("medium", n=20000)
+    cams = []
+    for k, ang in enumerate((-0.1, 0.0, 0.12)):
+        c, s = math.cos(ang), math.sin(ang)
+        R = np.array([[c, 0, s], [0, 1, 0], [-s, 0, c]], np.float32)
+        cams.append(scenes.Camera(R, np.array([0.5 * k, 0.2, 0.0], np.float32), 300.0, 300.0, 160.0, 90.0, 320, 180))
+    sc.cameras = cams
+    sc.opts = dict(sc.opts, exclude_crossing=1, bg=(0.1, 0.4, 0.7))
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] > 0
 
 
 def test_degree3_medium_recipe_reduced():
