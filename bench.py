@@ -205,6 +205,21 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- ranks
+def job_throughput(units, ms, world, device="cpu"):
+    """Whole-job throughput of `world` replica ranks (one per GPU): the units every
+    rank processed, summed, over the slowest rank's time.  Returns (units/s, slowest
+    ms).  Every rank must call it (it is a collective when world > 1)."""
+    import torch
+    import torch.distributed as dist
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(u.item()) / (float(t.item()) / 1e3), float(t.item())
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -296,12 +311,8 @@ def run_gpu(args):
     e2e_ms = e0.elapsed_time(e1)
     e2e_evals = float(tr.eval_counts.cpu().numpy()[:2].sum())
 
-    times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = times.tolist()
-    value = world * evals_per_step * args.steps / (total_ms / 1e3)
-    e2e_value = world * e2e_evals / (e2e_ms / 1e3)
+    value, total_ms = job_throughput(evals_per_step * args.steps, total_ms, world, "cuda")
+    e2e_value, e2e_ms = job_throughput(e2e_evals, e2e_ms, world, "cuda")
 
     pk = peaks()
     prof = profile_figures()
