@@ -253,3 +253,30 @@ def test_pipelined_host_steps_match_device_steps():
     for k in range(1, 4):
         assert abs(got[k, 0] - ref[k][0]) <= 1e-5 * abs(ref[k][0]), (k, got[k, 0], ref[k][0])
     assert b.t == 4
+
+
+@pytest.mark.parametrize("seed", [101, 102, 103, 104, 105, 106])
+def test_randomised_configurations(seed):
+    """Seeded random configurations: Gaussian count, a resolution that is not a
+    multiple of 16, SH degree 0 or 3, 1-3 views, either stop variant and a random
+    background; every stage compared as in the fixed cases."""
+    rng = np.random.default_rng(seed)
+    sh = int(rng.choice([0, 3]))
+    n = int(rng.integers(500, 6000))
+    W, H = int(rng.integers(40, 200)), int(rng.integers(30, 150))
+    sc = scenes.random_small_scene(seed, n=n, width=W, height=H, sh_degree=sh, log_lo=float(rng.uniform(-4.0, -2.5)),
+                                   log_hi=float(rng.uniform(-2.3, -1.2)), logit_mu=float(rng.uniform(-1.0, 1.5)),
+                                   spread=float(rng.uniform(0.4, 1.4)))
+    views = int(rng.integers(1, 4))
+    base = sc.cameras[0]
+    cams = []
+    for k in range(views):
+        ang = 0.08 * (k - (views - 1) / 2)
+        c, s = math.cos(ang), math.sin(ang)
+        R = np.array([[c, 0, s], [0, 1, 0], [-s, 0, c]], np.float32)
+        cams.append(scenes.Camera(R, np.array([0.05 * k, 0.0, 0.0], np.float32), base.fx, base.fy, base.cx, base.cy,
+                                  W, H))
+    sc.cameras = cams
+    sc.target_uniform = rng.uniform(0, 1, (views, 3, H, W)).astype(np.float32)
+    sc.opts = dict(sc.opts, exclude_crossing=int(rng.integers(0, 2)), bg=tuple(float(x) for x in rng.uniform(0, 1, 3)))
+    parity.run_stage_parity(sc)
