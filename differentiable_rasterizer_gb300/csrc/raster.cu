@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const bool inside = px < a.W && py < a.H;
     const float pxf = (float)px + 0.5f, pyf = (float)py + 0.5f;
     const uint2 range = a.ranges[tile_lin];
-    const int lo = (int)range.x;
+    const size_t lo = range.x;                      // list start: instance counts up to 2^32 - 1
     const int len = (int)(range.y - range.x);
     const float4* __restrict__ recv = a.rec + (size_t)v * (size_t)a.n * 3;
     const float alpha_min = a.alpha_min, alpha_max = a.alpha_max;
