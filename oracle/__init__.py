@@ -64,7 +64,7 @@ def _declare(L):
         getattr(L, "oracle_project" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_project" + s).restype = _I32
         getattr(L, "oracle_render" + s).argtypes = [_P, _P, _P, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
-                                                    _P]
+                                                    _P, _P, ctypes.c_double, _P]
         getattr(L, "oracle_render" + s).restype = _I32
         getattr(L, "oracle_vjp" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_vjp" + s).restype = _I32
@@ -138,9 +138,12 @@ def project(params, sh_degree, cam, opts, prec="f32"):
 
 
 def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_last=False, want_sig=False,
-           tile_mask=None):
+           tile_mask=None, dldc_extra=None, l1_weight=1.0, want_tfinal=False):
     """O7..O10 for one view.  target: [3,H,W] or None (forward only).
-    tile_mask: None or [tiles] bool -- render only those tiles (others stay 0)."""
+    tile_mask: None or [tiles] bool -- render only those tiles (others stay 0).
+    dldc_extra: None or [3,H,W] -- another loss term's dL/dC added to the weighted L1 one.
+    l1_weight: weight of the L1 term in the loss (and its gradient).
+    want_tfinal: also return the per-pixel final transmittance ("t_final", [H, W])."""
     dt = _dt(prec)
     rec, rect, vis = proj["rec"], proj["rect"], proj["visible"]
     n = rec.shape[0]
@@ -151,12 +154,15 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
     touched = np.zeros(n, np.uint8)
     counts = np.zeros(3, np.int64)
     last = np.zeros(H * W, np.int32) if want_last else None
+    tfin = np.zeros(H * W, dt) if want_tfinal else None
     sig = np.zeros(1, np.uint64) if want_sig else None
     tgt = np.ascontiguousarray(np.asarray(target, dt)) if target is not None else None
     tm = np.ascontiguousarray(np.asarray(tile_mask, np.uint8)) if tile_mask is not None else None
+    ex = np.ascontiguousarray(np.asarray(dldc_extra, dt)) if dldc_extra is not None else None
     rc = getattr(lib(), "oracle_render_" + prec)(_ptr(rec), _ptr(rect), _ptr(vis), n, W, H, _ptr(opts9(opts)), mode,
                                                   _ptr(tgt), _ptr(img), _ptr(loss), _ptr(g2), _ptr(touched),
-                                                  _ptr(counts), _ptr(last), _ptr(sig), _ptr(tm))
+                                                  _ptr(counts), _ptr(last), _ptr(sig), _ptr(tm),
+                                                  _ptr(ex), float(l1_weight), _ptr(tfin))
     assert rc == 0
     out = dict(image=img, loss=float(loss[0]) if target is not None else None, grad2d=g2, touched=touched,
                e_fwd=int(counts[0]), e_bwd=int(counts[1]), e_comp=int(counts[2]))
@@ -164,6 +170,8 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
         out["last"] = last.reshape(H, W)
     if want_sig:
         out["sig"] = int(sig[0])
+    if want_tfinal:
+        out["t_final"] = tfin.reshape(H, W)
     return out
 
 

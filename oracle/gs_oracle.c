@@ -472,6 +472,9 @@ static uint64_t fnv(uint64_t h, uint64_t v)
  * counts: E_fwd (entries evaluated up to the stop, skipped ones included), E_bwd (sum of last+1),
  *         E_comp (entries composited).
  * last_idx: [H*W] list position of the last composited entry (-1 if none), or NULL.
+ * t_final: [H*W] transmittance after the last composited entry, or NULL.
+ * dldc_extra: [3][H][W] another loss term's dL/dC, added to the L1 one, or NULL.
+ * l1_weight: weight of the L1 term in the loss and in dL/dC (1 for plain L1).
  * sig: decision signature (hash of every discrete decision), or NULL.
  * tile_mask: NULL, or [tiles] u8: only pixels of tiles with a nonzero entry are
  *   rendered (the rest of image is left untouched and is excluded from the loss,
@@ -480,7 +483,8 @@ static uint64_t fnv(uint64_t h, uint64_t v)
 int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
                       int width, int height, const double* opts9, int mode, const REAL* target,
                       REAL* image, double* loss, double* grad2d, uint8_t* touched, int64_t* counts,
-                      int32_t* last_idx, uint64_t* sig, const uint8_t* tile_mask)
+                      int32_t* last_idx, uint64_t* sig, const uint8_t* tile_mask, const REAL* dldc_extra,
+                      double l1_weight, REAL* t_final)
 {
     opts_t op;
     load_opts(opts9, &op);
@@ -496,8 +500,9 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
     }
     comp_t* comp = (comp_t*)malloc(sizeof(comp_t) * (size_t)(n > 0 ? n : 1));
     if (!comp) { free(buf); free(tl.off); free(tl.items); return -1; }
-    /* dL/dC = sign(C - target) / (3HW) [reading: L1 = mean absolute error over pixels and channels] */
-    const REAL inv3hw = (REAL)(1.0 / (3.0 * (double)HW));
+    /* dL/dC = w sign(C - target) / (3HW) [reading: L1 = mean absolute error over pixels and channels,
+       weighted by w = l1_weight], plus dldc_extra (another loss term's dL/dC, e.g. D-SSIM) if given */
+    const REAL inv3hw = (REAL)(l1_weight * (1.0 / (3.0 * (double)HW)));
     double lsum = 0.0;
     int64_t efwd = 0, ebwd = 0, ecomp = 0;
     uint64_t h = 1469598103934665603ull;
@@ -551,6 +556,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
             ebwd += last + 1;
             ecomp += ncomp;
             if (last_idx) last_idx[(int64_t)py * width + px] = (int32_t)last;
+            if (t_final) t_final[(int64_t)py * width + px] = T;
             for (int ch = 0; ch < 3; ++ch) image[ch * HW + (int64_t)py * width + px] = C[ch];
             if (sig) {
                 h = fnv(h, (uint64_t)ncomp);
@@ -565,6 +571,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
                 const REAL diff = C[ch] - target[ch * HW + (int64_t)py * width + px];
                 lsum += (double)FABS(diff);
                 gC[ch] = diff > 0 ? inv3hw : (diff < 0 ? -inv3hw : (REAL)0);
+                if (dldc_extra) gC[ch] = gC[ch] + dldc_extra[ch * HW + (int64_t)py * width + px];
                 if (sig) h = fnv(h, (uint64_t)(diff > 0 ? 2 : (diff < 0 ? 1 : 0)));
             }
             if (!grad2d) continue;
@@ -596,7 +603,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
             }
         }
     }
-    if (loss) *loss = lsum / (3.0 * (double)HW);
+    if (loss) *loss = l1_weight * (lsum / (3.0 * (double)HW));
     if (counts) { counts[0] = efwd; counts[1] = ebwd; counts[2] = ecomp; }
     if (sig) *sig = h;
     free(comp);

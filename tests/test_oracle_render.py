@@ -77,6 +77,9 @@ def test_weights_plus_final_transmittance_is_one(name):
     total = sum_w.astype(np.float64) + t_fin.astype(np.float64)
     # each composite adds one rounding; lists are short here
     assert np.abs(total - 1.0).max() < 64 * np.finfo(np.float32).eps
+    # the stored final transmittance is the one the background was weighted with
+    out = oracle.render(oracle.project(p_zero, 0, cam, opts_t), cam, opts_t, want_tfinal=True)
+    assert np.array_equal(out["t_final"], t_fin[0]) and np.array_equal(out["t_final"], t_fin[2])
 
 
 @pytest.mark.parametrize("excl", [0, 1])
