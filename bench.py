@@ -31,6 +31,10 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "fused raster fwd+bwd Gaussian-pixel evals/s and ms/iter at 1 GB300; % of roofline"
+# D-SSIM loss kernel: FP32 operations per pixel and channel of the separable form
+# (5 windowed moments at 2 x 11 fma each plus 3 products, 32 for S and its three
+# derivatives, 3 derivative maps at 2 x 11 fma, 11 for dL/dC and the loss terms).
+OPS_DSSIM = 222
 UNIT = "Gaussian-pixel evals/s"
 
 WORKLOADS = {
@@ -235,7 +239,8 @@ def run_gpu(args):
     gs_build.build()
 
     sc = scenes.make_scene(args.config)
-    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda")
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda",
+                                  dssim_lambda=args.dssim)
     if sc.target_kind == "uniform":
         target = torch.from_numpy(sc.target_uniform).cuda()
     else:
@@ -256,7 +261,10 @@ def run_gpu(args):
         tr.bin_sort()
         if ev is not None:
             ev[2].record(stream)
-        tr.raster(target)
+        if args.dssim is None:
+            tr.raster(target)
+        else:
+            tr.raster_dssim(target, events=None if ev is None else (ev[6], ev[7]))
         if ev is not None:
             ev[3].record(stream)
         tr.compact()
@@ -271,7 +279,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     # ---- device-resident timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv") if os.path.isdir(
         os.path.join(ROOT, "gpurun_out")) else f"/tmp/bench_clocks_r{rank}.csv"
@@ -295,6 +303,9 @@ def run_gpu(args):
     e_fwd, e_bwd, e_comp = counts / args.steps
     evals_per_step = e_fwd + e_bwd
     raster_ms = float(stage_ms[:, 2].mean())
+    if args.dssim is not None:
+        split = np.array([[e[2].elapsed_time(e[6]), e[6].elapsed_time(e[7]), e[7].elapsed_time(e[3])] for e in evs])
+        fwd_ms, dssim_ms, bwd_ms = (float(x) for x in split.mean(0))
 
     # ---- end to end through the public API: every step's target copied in from pinned
     # host memory (step k + 1's copy overlapping step k) and its loss copied out
@@ -315,8 +326,8 @@ def run_gpu(args):
     e2e_value, e2e_ms = job_throughput(e2e_evals, e2e_ms, world, "cuda")
 
     pk = peaks()
-    prof = profile_figures()
-    t_raster = raster_ms / 1e3
+    prof = profile_figures() if args.dssim is None else {}
+    t_raster = (raster_ms if args.dssim is None else fwd_ms + bwd_ms) / 1e3
     ops_b = e_fwd * (OPS_FWD + OPS_EXP) + e_bwd * (OPS_BWD + OPS_EXP)
     sfu_b = e_bwd
     ops_a = e_fwd * OPS_FWD + e_bwd * OPS_BWD
@@ -328,7 +339,8 @@ def run_gpu(args):
                 "frac": t_b / t_raster, "traffic": prof.get("dram_bytes_per_launch") if args.config == "medium" else None,
                 "issue_active_ncu": (prof.get("issue_active_pct") / 100.0 if prof.get("issue_active_pct") is not None
                                      and args.config == "medium" else None),
-                "kernel": "raster_fused_kernel<true>",
+                "kernel": "raster_fused_kernel<kFused>" if args.dssim is None else
+                          "raster_fused_kernel<kFwd> + raster_fused_kernel<kBwdState> (D-SSIM kernel excluded)",
                 "peak_basis": f"FP32 ops (an fma counts once): 152 SMs x 128 lanes x {pk['sm_max_mhz']:.0f} MHz "
                               f"(sm_max_mhz, {pk['src']}); SFU: 152 x 16 lanes",
                 "work": "per forward evaluation 14 FP32 ops + exp, per backward evaluation 47 FP32 ops + exp + "
@@ -359,6 +371,19 @@ def run_gpu(args):
                     "d2h_bytes_per_step": int(tr.V * 8)},
             "gpu_launches": int(tr.kernel_launches_per_step() * args.steps),
             "clocks": clocks}
+    if args.dssim is not None:
+        pixels = sc.n_views * sc.cameras[0].width * sc.cameras[0].height
+        ops_d = pixels * 3 * OPS_DSSIM
+        t_d = ops_d / (pk["fp32_tops"] * 1e12)
+        line["config"]["loss"] = f"(1 - {args.dssim}) L1 + {args.dssim} (1 - SSIM), 11x11 Gaussian window"
+        line["raster_split_ms"] = {"forward_state": fwd_ms, "dssim_loss_grad": dssim_ms, "backward_state": bwd_ms}
+        line["dssim"] = {"ms": dssim_ms, "bound": "alu", "achieved": ops_d / (dssim_ms / 1e3) / 1e12,
+                         "peak": pk["fp32_tops"], "unit": "TFLOP/s", "frac": t_d / (dssim_ms / 1e3),
+                         "hbm_bytes": pixels * 3 * 12, "hbm_frac": pixels * 3 * 12 / (dssim_ms / 1e3) /
+                         (pk["hbm_gbs"] * 1e9),
+                         "work": f"{OPS_DSSIM} FP32 ops per pixel and channel (separable window: 5 moments x 22 "
+                                 "fma + 3 products, 32 for S and its derivatives, 3 derivative maps x 22 fma, 11 "
+                                 "for dL/dC and the loss); 12 bytes (image, target in, dL/dC out)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, args)
     if world > 1:
@@ -388,6 +413,8 @@ def main():
     ap.add_argument("--config", default="medium", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dssim", type=float, default=None, metavar="LAMBDA",
+                    help="train with (1 - LAMBDA) L1 + LAMBDA D-SSIM (three raster launches instead of the fused one)")
     ap.add_argument("--cpu-rows", type=int, default=270)
     ap.add_argument("--ref-rows", type=int, default=68)
     args = ap.parse_args()

@@ -23,6 +23,7 @@ GS_REC_FLOAT4 = 3
 GS_GRAD2D_STRIDE = 12
 
 EXPORTS = ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
+           "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_grad_compact_static",
            "gs_error_string", "gs_param_rows", "gs_param_stride", "gs_num_tiles", "gs_version")
 
 
@@ -73,7 +74,12 @@ def lib():
         L.gs_grad_compact.argtypes = [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P,
                                       ctypes.POINTER(ctypes.c_size_t), _P]
         L.gs_adam_deferred.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _P, _P, _I32, _P, _F, _F, _F, _I32, _P]
-        for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred"):
+        L.gs_raster_forward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P]
+        L.gs_dssim_loss_grad.argtypes = [_P, _P, _I32, _I32, _I32, _F, _P, _P, _P]
+        L.gs_raster_backward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
+                                               _P, _P]
+        for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
+                     "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state"):
             getattr(L, name).restype = ctypes.c_int
         L.gs_error_string.argtypes = [ctypes.c_int]
         L.gs_error_string.restype = ctypes.c_char_p
@@ -149,6 +155,25 @@ def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, targ
     _check("gs_raster_fused_fwd_bwd",
            lib().gs_raster_fused_fwd_bwd(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
                                          target, image, loss, grad2d, touched, eval_counts, stream))
+
+
+def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, eval_counts,
+                            stream):
+    _check("gs_raster_forward_state",
+           lib().gs_raster_forward_state(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
+                                         image, t_final, last_idx, eval_counts, stream))
+
+
+def gs_dssim_loss_grad(image, target, n_views, width, height, lam, loss, dldc, stream):
+    _check("gs_dssim_loss_grad", lib().gs_dssim_loss_grad(image, target, n_views, width, height, lam, loss, dldc,
+                                                          stream))
+
+
+def gs_raster_backward_state(proj, n, tile_ranges, ids, cams, n_views, opts, t_final, last_idx, dldc, grad2d, touched,
+                             stream):
+    _check("gs_raster_backward_state",
+           lib().gs_raster_backward_state(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
+                                          t_final, last_idx, dldc, grad2d, touched, stream))
 
 
 def gs_grad_compact_ws_bytes(n) -> int:

@@ -1,0 +1,321 @@
+// dssim.cu -- gs_dssim_loss_grad: the L1 + D-SSIM training loss of the standard
+// 3DGS recipe (On Scaling Up 3D Gaussian Splatting Training, summary of the
+// loss) and its gradient with respect to the rendered colour.
+//
+// SSIM per channel with an 11 x 11 Gaussian window (sigma 1.5), the image
+// zero-padded outside its borders, C1 = 0.01^2, C2 = 0.03^2:
+//   S = (2 mu_x mu_y + C1)(2 s_xy + C2) / ((mu_x^2 + mu_y^2 + C1)(s_xx + s_yy + C2))
+// loss = (1 - lambda) mean|x - y| + lambda (1 - mean S).
+// The gradient goes through the three windowed moments that depend on x:
+//   dSSIM/dx_q = (1/N) [w * dS/dmu_x + 2 x_q (w * dS/dE[x^2]) + y_q (w * dS/dE[xy])](q)
+// (w symmetric, so the adjoint of a window sum is a window sum; the maps are
+// zero outside the image).  With A, B, C, D the four factors of S:
+//   dS/dmu_x = (2 mu_y (B - A) - 2 mu_x S (D - C)) / (C D),
+//   dS/dE[x^2] = -S / D,  dS/dE[xy] = 2 A / (C D).
+//
+// One CTA per (32 x 32 output tile, channel, view).  The output needs the
+// derivative maps on the tile plus a 5-pixel ring (42 x 42), which need the
+// moments there, which need the two images on the tile plus a 10-pixel ring
+// (52 x 52).  Four separable window passes in shared memory, each thread
+// sliding the 11 taps over a short run of outputs held in registers:
+//   P1 rows of the 52 x 52 images  -> 5 horizontally summed products (52 x 42)
+//   P2 columns                     -> moments, S and its 3 derivatives (42 x 42)
+//   P3 rows of the derivative maps -> 3 x (42 x 32)
+//   P4 columns                     -> dL/dC on the 32 x 32 tile
+// The moments are taken of the images minus a per-CTA constant (the mean of the
+// loaded 52 x 52 region, padding included): variances and the covariance are
+// invariant to the shift, so s_xx = E[x'^2] - mu_x'^2 etc. with x' = x - c_x, and
+// in smooth or flat regions the cancellation that fp32 E[x^2] - mu_x^2 suffers
+// is gone.  With mu_x = mu_x' + c_x the derivatives by the shifted moments are
+//   dS/dmu_x' = (2 (mu_y B - A mu_y') - 2 S (mu_x D - C mu_x')) / (C D)
+// (the same two others), and the gradient uses x' and y' in place of x and y.
+// fp32 throughout; the loss partial sums are fp64 (one atomic per CTA).
+#include "gs_common.cuh"
+
+namespace gs {
+
+namespace ssim {
+constexpr int kR = 5;                 // window radius
+constexpr int kWin = 2 * kR + 1;
+constexpr int kTO = 32;               // output tile
+constexpr int kTM = kTO + 2 * kR;     // derivative-map region (42)
+constexpr int kTI = kTO + 4 * kR;     // input region (52)
+constexpr int kThreads = 256;
+constexpr int kK1 = 3;                // outputs per thread in P1 (kTM / kK1 runs per row)
+constexpr int kK2 = 3;                // P2
+constexpr int kK3 = 4;                // P3
+constexpr int kK4 = 4;                // P4
+static_assert(kTM % kK1 == 0 && kTM % kK2 == 0 && kTO % kK3 == 0 && kTO % kK4 == 0, "runs must tile the regions");
+constexpr int kSmemA = 2 * kTI * kTI;     // images, later the 3 derivative maps
+constexpr int kSmemB = 5 * kTI * kTM;     // P1 sums, later the P3 sums
+static_assert(3 * kTM * kTM <= kSmemA && 3 * kTM * kTO <= kSmemB, "aliased buffers must fit");
+constexpr size_t kSmemBytes = sizeof(float) * (kSmemA + kSmemB);
+}  // namespace ssim
+
+struct SsimArgs {
+    const float* __restrict__ image;    // [V][3][H][W]
+    const float* __restrict__ target;
+    float* dldc;
+    double* loss;                       // [V]
+    int W, H, tiles_x;
+    float w[ssim::kWin];                // normalised 1-D window
+    float c1, c2;
+    float l1_coef;                      // (1 - lambda) / N
+    float ssim_coef;                    // -lambda / N (gradient of the SSIM term)
+    double l1_coef_d, ssim_loss_coef_d; // (1 - lambda) / N, lambda / N
+};
+
+__global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
+{
+    using namespace ssim;
+    extern __shared__ float smem[];
+    float* const sx = smem;                       // [kTI][kTI]
+    float* const sy = smem + kTI * kTI;           // [kTI][kTI]
+    float* const dm = smem;                       // [3][kTM][kTM] (after P1)
+    float* const h1 = smem + kSmemA;              // [5][kTI][kTM]
+    float* const h3 = smem + kSmemA;              // [3][kTM][kTO] (after P2)
+    __shared__ double s_red[kThreads / 32];
+    __shared__ float s_c[2][kThreads / 32];
+
+    const int tx = blockIdx.x % a.tiles_x, ty = blockIdx.x / a.tiles_x;
+    const int ch = blockIdx.y, v = blockIdx.z;
+    const int ox = tx * kTO, oy = ty * kTO;       // output tile origin
+    const size_t HW = (size_t)a.W * (size_t)a.H;
+    const size_t plane = ((size_t)v * 3 + ch) * HW;
+    const float* __restrict__ X = a.image + plane;
+    const float* __restrict__ Y = a.target + plane;
+
+    // images on the tile + 10-pixel ring, zero outside; their means over the region
+    float sumx = 0.0f, sumy = 0.0f;
+    for (int i = threadIdx.x; i < kTI * kTI; i += kThreads) {
+        const int r = i / kTI, c = i - r * kTI;
+        const int gy = oy - 2 * kR + r, gx = ox - 2 * kR + c;
+        float x = 0.0f, y = 0.0f;
+        if (gy >= 0 && gy < a.H && gx >= 0 && gx < a.W) {
+            const size_t o = (size_t)gy * a.W + gx;
+            x = __ldg(X + o);
+            y = __ldg(Y + o);
+        }
+        sx[i] = x;
+        sy[i] = y;
+        sumx += x;
+        sumy += y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sumx += __shfl_xor_sync(0xffffffffu, sumx, o);
+        sumy += __shfl_xor_sync(0xffffffffu, sumy, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_c[0][threadIdx.x >> 5] = sumx;
+        s_c[1][threadIdx.x >> 5] = sumy;
+    }
+    __syncthreads();
+    float cx = 0.0f, cy = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        cx += s_c[0][w];
+        cy += s_c[1][w];
+    }
+    cx = cx * (1.0f / (float)(kTI * kTI));
+    cy = cy * (1.0f / (float)(kTI * kTI));
+
+    // P1: horizontal window sums of x', y', x'^2, y'^2, x'y'
+    constexpr int kRuns1 = kTM / kK1;
+    for (int it = threadIdx.x; it < kTI * kRuns1; it += kThreads) {
+        const int r = it / kRuns1, c0 = (it - r * kRuns1) * kK1;
+        float acc[5][kK1];
+#pragma unroll
+        for (int q = 0; q < 5; ++q)
+#pragma unroll
+            for (int j = 0; j < kK1; ++j) acc[q][j] = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kK1 + 2 * kR; ++t) {
+            const float x = sx[r * kTI + c0 + t] - cx, y = sy[r * kTI + c0 + t] - cy;
+            const float xx = x * x, yy = y * y, xy = x * y;
+#pragma unroll
+            for (int j = 0; j < kK1; ++j) {
+                const int k = t - j;
+                if (k >= 0 && k < kWin) {
+                    acc[0][j] = __fmaf_rn(a.w[k], x, acc[0][j]);
+                    acc[1][j] = __fmaf_rn(a.w[k], y, acc[1][j]);
+                    acc[2][j] = __fmaf_rn(a.w[k], xx, acc[2][j]);
+                    acc[3][j] = __fmaf_rn(a.w[k], yy, acc[3][j]);
+                    acc[4][j] = __fmaf_rn(a.w[k], xy, acc[4][j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 5; ++q)
+#pragma unroll
+            for (int j = 0; j < kK1; ++j) h1[(q * kTI + r) * kTM + c0 + j] = acc[q][j];
+    }
+    __syncthreads();
+
+    // P2: vertical sums -> moments; S and its derivatives on the 42 x 42 region
+    // (zero outside the image); S summed over the output tile for the loss
+    double ssum = 0.0;
+    constexpr int kRuns2 = kTM / kK2;
+    for (int it = threadIdx.x; it < kTM * kRuns2; it += kThreads) {
+        const int c = it % kTM, r0 = (it / kTM) * kK2;
+        float m[5][kK2];
+#pragma unroll
+        for (int q = 0; q < 5; ++q) {
+#pragma unroll
+            for (int j = 0; j < kK2; ++j) m[q][j] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < kK2 + 2 * kR; ++t) {
+                const float h = h1[(q * kTI + r0 + t) * kTM + c];
+#pragma unroll
+                for (int j = 0; j < kK2; ++j) {
+                    const int k = t - j;
+                    if (k >= 0 && k < kWin) m[q][j] = __fmaf_rn(a.w[k], h, m[q][j]);
+                }
+            }
+        }
+        const int gx = ox - kR + c;
+#pragma unroll
+        for (int j = 0; j < kK2; ++j) {
+            const int r = r0 + j;
+            const int gy = oy - kR + r;
+            float dmu = 0.0f, dxx = 0.0f, dxy = 0.0f;
+            if (gy >= 0 && gy < a.H && gx >= 0 && gx < a.W) {
+                const float mxs = m[0][j], mys = m[1][j];          // shifted means
+                const float mx = mxs + cx, my = mys + cy;
+                const float A = 2.0f * (mx * my) + a.c1;
+                const float B = 2.0f * (m[4][j] - mxs * mys) + a.c2;
+                const float C = (mx * mx + my * my) + a.c1;
+                const float D = ((m[2][j] - mxs * mxs) + (m[3][j] - mys * mys)) + a.c2;
+                const float rC = 1.0f / C, rD = 1.0f / D;
+                const float inv = rC * rD;
+                const float S = (A * B) * inv;
+                dmu = (2.0f * (my * B - A * mys) - 2.0f * S * (mx * D - C * mxs)) * inv;
+                dxx = -S * rD;
+                dxy = 2.0f * A * inv;
+                if (r >= kR && r < kR + kTO && c >= kR && c < kR + kTO) ssum += (double)(1.0f - S);
+            }
+            dm[(0 * kTM + r) * kTM + c] = dmu;
+            dm[(1 * kTM + r) * kTM + c] = dxx;
+            dm[(2 * kTM + r) * kTM + c] = dxy;
+        }
+    }
+    __syncthreads();
+
+    // P3: horizontal sums of the derivative maps (42 rows x 32 columns)
+    constexpr int kRuns3 = kTO / kK3;
+    for (int it = threadIdx.x; it < kTM * kRuns3; it += kThreads) {
+        const int r = it / kRuns3, c0 = (it - r * kRuns3) * kK3;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            float acc[kK3];
+#pragma unroll
+            for (int j = 0; j < kK3; ++j) acc[j] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < kK3 + 2 * kR; ++t) {
+                const float d = dm[(q * kTM + r) * kTM + c0 + t];
+#pragma unroll
+                for (int j = 0; j < kK3; ++j) {
+                    const int k = t - j;
+                    if (k >= 0 && k < kWin) acc[j] = __fmaf_rn(a.w[k], d, acc[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kK3; ++j) h3[(q * kTM + r) * kTO + c0 + j] = acc[j];
+        }
+    }
+    __syncthreads();
+
+    // P4: vertical sums -> dL/dC on the output tile
+    double l1sum = 0.0;
+    constexpr int kRuns4 = kTO / kK4;
+    for (int it = threadIdx.x; it < kTO * kRuns4; it += kThreads) {
+        const int c = it % kTO, r0 = (it / kTO) * kK4;
+        float b[3][kK4];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+#pragma unroll
+            for (int j = 0; j < kK4; ++j) b[q][j] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < kK4 + 2 * kR; ++t) {
+                const float h = h3[(q * kTM + r0 + t) * kTO + c];
+#pragma unroll
+                for (int j = 0; j < kK4; ++j) {
+                    const int k = t - j;
+                    if (k >= 0 && k < kWin) b[q][j] = __fmaf_rn(a.w[k], h, b[q][j]);
+                }
+            }
+        }
+        const int gx = ox + c;
+#pragma unroll
+        for (int j = 0; j < kK4; ++j) {
+            const int gy = oy + r0 + j;
+            if (gy < a.H && gx < a.W) {
+                // x and y again from global memory (L2): their shared copies now hold the maps
+                const size_t o = (size_t)gy * a.W + gx;
+                const float x = __ldg(X + o), y = __ldg(Y + o);
+                const float d = x - y;
+                const float sgn = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
+                const float gs = b[0][j] + 2.0f * (x - cx) * b[1][j] + (y - cy) * b[2][j];
+                a.dldc[plane + o] = __fmaf_rn(a.ssim_coef, gs, sgn * a.l1_coef);
+                l1sum += (double)fabsf(d);
+            }
+        }
+    }
+
+    // loss partial: (1 - lambda)/N sum|x - y| + lambda/N sum(1 - S)
+    double part = l1sum * a.l1_coef_d + ssum * a.ssim_loss_coef_d;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = part;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) t += s_red[w];
+        if (t != 0.0) atomicAdd(a.loss + v, t);
+    }
+}
+
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" gs_status gs_dssim_loss_grad(const float* image, const float* target, int32_t n_views, int32_t width,
+                                        int32_t height, float lambda, double* loss, float* dldc, void* stream)
+{
+    using namespace ssim;
+    if (!image || !target || !loss || !dldc) return GS_ERR_INVALID_ARG;
+    if (n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 || height < 1) return GS_ERR_INVALID_ARG;
+    if (!(lambda >= 0.0f && lambda <= 1.0f)) return GS_ERR_INVALID_ARG;
+    SsimArgs a;
+    a.image = image;
+    a.target = target;
+    a.dldc = dldc;
+    a.loss = loss;
+    a.W = width;
+    a.H = height;
+    a.tiles_x = (width + kTO - 1) / kTO;
+    const long long tiles_y = (height + kTO - 1) / kTO;
+    const long long tiles = (long long)a.tiles_x * tiles_y;
+    if (tiles > INT32_MAX) return GS_ERR_INVALID_ARG;
+    double g[kWin], gsum = 0.0;
+    for (int i = 0; i < kWin; ++i) {
+        const double t = (double)(i - kR);
+        g[i] = exp(-t * t / (2.0 * 1.5 * 1.5));
+        gsum += g[i];
+    }
+    for (int i = 0; i < kWin; ++i) a.w[i] = (float)(g[i] / gsum);
+    a.c1 = (float)(0.01 * 0.01);
+    a.c2 = (float)(0.03 * 0.03);
+    const double N = 3.0 * (double)width * (double)height;
+    a.l1_coef_d = (1.0 - (double)lambda) / N;
+    a.ssim_loss_coef_d = (double)lambda / N;
+    a.l1_coef = (float)a.l1_coef_d;
+    a.ssim_coef = (float)(-(double)lambda / N);
+    cudaStream_t s = (cudaStream_t)stream;
+    // more than the 48 KB default of dynamic shared memory (set on the current device)
+    GS_CUDA_TRY(cudaFuncSetAttribute(dssim_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
+    GS_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(double) * (size_t)n_views, s));
+    dssim_kernel<<<dim3((unsigned)tiles, 3, (unsigned)n_views), kThreads, kSmemBytes, s>>>(a);
+    GS_LAUNCH_CHECK();
+    return GS_OK;
+}

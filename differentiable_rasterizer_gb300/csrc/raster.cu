@@ -46,11 +46,19 @@ constexpr int kQueue = 256;      // queue window (entries) per warp
 constexpr int kRing = 3;         // chunks whose pass bits stay in shared memory
 constexpr int kDense = 12;       // backward: entries per distinct Gaussian from which a warp reduces per Gaussian
 
+// Kernel modes.
+constexpr int kFwd = 0;          // forward only (image; optionally final T and last index per pixel)
+constexpr int kFused = 1;        // forward, L1 loss and backward in one pass
+constexpr int kBwdState = 2;     // backward only, from a stored final T / last index and a given dL/dC
+
 struct RasterArgs {
     const float4* __restrict__ rec;     // [V][n][3]
     const uint2* __restrict__ ranges;   // [V * tiles]
     const uint32_t* __restrict__ ids;
     const float* __restrict__ target;   // [V][3][H][W] or null
+    const float* __restrict__ dldc;     // [V][3][H][W]: dL/dC (backward from stored state)
+    float* t_final;                     // [V][H][W]: final transmittance per pixel, or null
+    int32_t* last_idx;                  // [V][H][W]: last composited list index per pixel (-1: none)
     float* image;                       // [V][3][H][W]
     double* loss;                       // [V]
     float* grad2d;                      // [V][n][12]
@@ -118,9 +126,10 @@ __device__ __forceinline__ EntryGrad entry_grad_at(const float4 r0, const float4
     return e;
 }
 
-template <bool kBackward>
+template <int kMode>
 __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a)
 {
+    constexpr bool kBackward = kMode != kFwd;
     __shared__ float4 s_r0[kChunk], s_r1[kChunk];
     __shared__ float2 s_r2[kChunk];                 // (blue, tau)
     __shared__ uint32_t s_id[kChunk];
@@ -133,9 +142,12 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     __shared__ unsigned long long s_red_u[3][kWarps];
     __shared__ int s_max_last[kWarps];
 
-    const int tile_lin = blockIdx.x;                 // v * tiles + tile
-    const int v = tile_lin / a.tiles;
-    const int tile = tile_lin - v * a.tiles;
+    // Views interleaved (CTA i: view i mod V, tile i / V) so the heavy central
+    // tiles of all views are spread over the launch instead of queued view by
+    // view (batched: 45.5 -> 43.2 ms).
+    const int v = (int)(blockIdx.x % (unsigned)a.n_views);
+    const int tile = (int)(blockIdx.x / (unsigned)a.n_views);
+    const int tile_lin = v * a.tiles + tile;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ox = tx * kTile, oy = ty * kTile;
@@ -279,7 +291,13 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     int stop = -1;                      // list index where this pixel stopped, -1 if it never did
     bool done = !inside;
     int resident = -1;                  // chunk currently in shared memory
-    const int nchunks = (len + kChunk - 1) / kChunk;
+    const size_t HW = (size_t)a.W * (size_t)a.H;
+    const size_t spix = (size_t)v * HW + (size_t)py * a.W + px;   // per-pixel state index
+    if (kMode == kBwdState && inside) {
+        T = a.t_final[spix];
+        last = a.last_idx[spix];
+    }
+    const int nchunks = kMode == kBwdState ? 0 : (len + kChunk - 1) / kChunk;
     for (int c = 0; c < nchunks; ++c) {
         if (__syncthreads_and(done)) break;
         const int base = c * kChunk;
@@ -323,15 +341,24 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     C0 = C0 + T * a.bg0;
     C1 = C1 + T * a.bg1;
     C2 = C2 + T * a.bg2;
-    const size_t HW = (size_t)a.W * (size_t)a.H;
     const size_t pix = (size_t)v * 3 * HW + (size_t)py * a.W + px;
     float g0 = 0.0f, g1 = 0.0f, g2c = 0.0f;
     int gcode = 1 + 4 + 16;   // signs of dL/dC per channel, +1, two bits each
     double lsum = 0.0;
-    if (inside) {
+    if (kMode == kBwdState) {
+        if (inside) {
+            g0 = __ldg(a.dldc + pix);
+            g1 = __ldg(a.dldc + pix + HW);
+            g2c = __ldg(a.dldc + pix + 2 * HW);
+        }
+    } else if (inside) {
         a.image[pix] = C0;
         a.image[pix + HW] = C1;
         a.image[pix + 2 * HW] = C2;
+        if (kMode == kFwd && a.t_final) {
+            a.t_final[spix] = T;
+            a.last_idx[spix] = last;
+        }
         if (kBackward) {
             const float d0 = C0 - __ldg(a.target + pix);
             const float d1 = C1 - __ldg(a.target + pix + HW);
@@ -377,7 +404,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             ec += s_red_u[2][w];
             ml = max(ml, s_max_last[w]);
         }
-        if (kBackward && ls != 0.0) atomicAdd(a.loss + v, ls * a.inv3hw_d);
+        if (kMode == kFused && ls != 0.0) atomicAdd(a.loss + v, ls * a.inv3hw_d);
         if (a.counts) {
             atomicAdd(a.counts, ef);
             atomicAdd(a.counts + 1, eb);
@@ -387,7 +414,9 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     }
     if (!kBackward) return;
     __syncthreads();
-    const int last_fwd = resident;   // the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
+    // the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
+    // (none when the forward ran in an earlier launch)
+    const int last_fwd = kMode == kBwdState ? INT32_MAX / 2 : resident;
     const int max_last = s_max_last[0];
     if (max_last < 0) return;
 
@@ -500,10 +529,17 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 const int own_off = __shfl_sync(0xffffffffu, myoff, owner);
                 const float Tst = __shfl_sync(0xffffffffu, Tcur, owner);
                 const float Sgs = __shfl_sync(0xffffffffu, Sg, owner);
-                const int gco = __shfl_sync(0xffffffffu, gcode, owner);
-                const float go0 = (float)((gco & 3) - 1) * a.inv3hw;
-                const float go1 = (float)(((gco >> 2) & 3) - 1) * a.inv3hw;
-                const float go2 = (float)(((gco >> 4) & 3) - 1) * a.inv3hw;
+                float go0, go1, go2;
+                if (kMode == kBwdState) {
+                    go0 = __shfl_sync(0xffffffffu, g0, owner);
+                    go1 = __shfl_sync(0xffffffffu, g1, owner);
+                    go2 = __shfl_sync(0xffffffffu, g2c, owner);
+                } else {
+                    const int gco = __shfl_sync(0xffffffffu, gcode, owner);
+                    go0 = (float)((gco & 3) - 1) * a.inv3hw;
+                    go1 = (float)(((gco >> 2) & 3) - 1) * a.inv3hw;
+                    go2 = (float)(((gco >> 4) & 3) - 1) * a.inv3hw;
+                }
                 const int pidx = warp * 32 + owner;
                 const float pxo = (float)(ox + (pidx & (kTile - 1))) + 0.5f;
                 const float pyo = (float)(oy + pidx / kTile) + 0.5f;
@@ -574,29 +610,21 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
 
 using namespace gs;
 
-extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
-                                             const uint32_t* ids, const gs_camera* cams, int32_t n_views,
-                                             const gs_render_opts* opts, const float* target, float* image,
-                                             double* loss, float* grad2d, uint8_t* touched, uint64_t* eval_counts,
-                                             void* stream)
+// Arguments shared by the three launches.
+static gs_status raster_args(RasterArgs& a, const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                             const uint32_t* ids, const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
+                             long long& grid)
 {
-    if (!proj || !tile_ranges || !opts_ok(opts) || !image || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
+    if (!proj || !tile_ranges || !opts_ok(opts) || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
     gs_status st = check_views(cams, n_views);
     if (st != GS_OK) return st;
-    if (target && (!loss || (n > 0 && (!grad2d || !touched)))) return GS_ERR_INVALID_ARG;
     if (n > 0 && (!proj->rec || !ids)) return GS_ERR_INVALID_ARG;
-    if (!aligned16(proj->rec) || (grad2d && !aligned16(grad2d))) return GS_ERR_INVALID_ARG;
+    if (!aligned16(proj->rec)) return GS_ERR_INVALID_ARG;
     const int W = cams[0].width, H = cams[0].height;
-    RasterArgs a;
+    a = RasterArgs{};
     a.rec = reinterpret_cast<const float4*>(proj->rec);
     a.ranges = reinterpret_cast<const uint2*>(tile_ranges);
     a.ids = ids;
-    a.target = target;
-    a.image = image;
-    a.loss = loss;
-    a.grad2d = grad2d;
-    a.touched = touched;
-    a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
     a.n = n;
     a.W = W;
     a.H = H;
@@ -612,15 +640,78 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
     a.inv3hw_d = 1.0 / (3.0 * (double)W * (double)H);
     a.inv3hw = (float)a.inv3hw_d;
     a.exclude_crossing = opts->exclude_crossing ? 1 : 0;
-    cudaStream_t s = (cudaStream_t)stream;
-    const long long grid = (long long)a.tiles * n_views;
+    grid = (long long)a.tiles * n_views;
     if (grid > INT32_MAX) return GS_ERR_INVALID_ARG;
+    return GS_OK;
+}
+
+extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                             const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                             const gs_render_opts* opts, const float* target, float* image,
+                                             double* loss, float* grad2d, uint8_t* touched, uint64_t* eval_counts,
+                                             void* stream)
+{
+    RasterArgs a;
+    long long grid = 0;
+    gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
+    if (st != GS_OK) return st;
+    if (!image) return GS_ERR_INVALID_ARG;
+    if (target && (!loss || (n > 0 && (!grad2d || !touched)))) return GS_ERR_INVALID_ARG;
+    if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    a.target = target;
+    a.image = image;
+    a.loss = loss;
+    a.grad2d = grad2d;
+    a.touched = touched;
+    a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
+    cudaStream_t s = (cudaStream_t)stream;
     if (target) {
         GS_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(double) * (size_t)n_views, s));
-        raster_fused_kernel<true><<<(unsigned)grid, kTileThreads, 0, s>>>(a);
+        raster_fused_kernel<kFused><<<(unsigned)grid, kTileThreads, 0, s>>>(a);
     } else {
-        raster_fused_kernel<false><<<(unsigned)grid, kTileThreads, 0, s>>>(a);
+        raster_fused_kernel<kFwd><<<(unsigned)grid, kTileThreads, 0, s>>>(a);
     }
+    GS_LAUNCH_CHECK();
+    return GS_OK;
+}
+
+extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                             const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                             const gs_render_opts* opts, float* image, float* t_final,
+                                             int32_t* last_idx, uint64_t* eval_counts, void* stream)
+{
+    RasterArgs a;
+    long long grid = 0;
+    gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
+    if (st != GS_OK) return st;
+    if (!image || !t_final || !last_idx) return GS_ERR_INVALID_ARG;
+    a.image = image;
+    a.t_final = t_final;
+    a.last_idx = last_idx;
+    a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
+    raster_fused_kernel<kFwd><<<(unsigned)grid, kTileThreads, 0, (cudaStream_t)stream>>>(a);
+    GS_LAUNCH_CHECK();
+    return GS_OK;
+}
+
+extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                              const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                              const gs_render_opts* opts, const float* t_final,
+                                              const int32_t* last_idx, const float* dldc, float* grad2d,
+                                              uint8_t* touched, void* stream)
+{
+    RasterArgs a;
+    long long grid = 0;
+    gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
+    if (st != GS_OK) return st;
+    if (!t_final || !last_idx || !dldc || (n > 0 && (!grad2d || !touched))) return GS_ERR_INVALID_ARG;
+    if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    a.t_final = const_cast<float*>(t_final);
+    a.last_idx = const_cast<int32_t*>(last_idx);
+    a.dldc = dldc;
+    a.grad2d = grad2d;
+    a.touched = touched;
+    raster_fused_kernel<kBwdState><<<(unsigned)grid, kTileThreads, 0, (cudaStream_t)stream>>>(a);
     GS_LAUNCH_CHECK();
     return GS_OK;
 }

@@ -5,6 +5,10 @@ memory) and calls the five C-ABI entry points in order on one stream:
 
     gs_project -> gs_bin_sort -> gs_raster_fused_fwd_bwd -> gs_grad_compact -> gs_adam_deferred
 
+With ``dssim_lambda`` set, the loss is (1 - lambda) L1 + lambda (1 - SSIM) and the
+fused call is replaced by three: gs_raster_forward_state -> gs_dssim_loss_grad ->
+gs_raster_backward_state (the SSIM window reaches into neighbouring tiles).
+
 Buffer layout in HBM (fp32 unless stated):
     params, grads, adam_m, adam_v   [n, stride]      stride = 16 (RGB, P = 14) or 64 (SH 3, P = 59);
                                                      one aligned block per Gaussian
@@ -17,6 +21,7 @@ Buffer layout in HBM (fp32 unless stated):
     grad2d                          [V, n, 12]  (kept all-zero between steps)
     touched                         [V, n] u8   (kept all-zero between steps)
     idx, n_idx                      [V + 1, n] u32, [V + 1] int64 (per-view lists + union)
+    t_final, last_idx, dldc         [V, H, W], [V, H, W] int32, [V, 3, H, W]  (D-SSIM loss only)
 The sizes follow the workload: nothing is allocated per step once the instance
 capacity has been reached (it grows by 25 % headroom when a step needs more).
 """
@@ -32,8 +37,10 @@ from . import abi
 
 class GaussianTrainer:
     def __init__(self, params: np.ndarray | torch.Tensor, sh_degree: int, cameras, opts: dict, lr,
-                 betas=(0.9, 0.999), eps=1e-8, device="cuda", capacity: int | None = None):
+                 betas=(0.9, 0.999), eps=1e-8, device="cuda", capacity: int | None = None,
+                 dssim_lambda: float | None = None):
         self.device = torch.device(device)
+        self.dssim_lambda = None if dssim_lambda is None else float(dssim_lambda)
         self.sh_degree = sh_degree
         self.P = abi.gs_param_rows(sh_degree)
         self.stride = abi.gs_param_stride(sh_degree)
@@ -69,6 +76,10 @@ class GaussianTrainer:
         self.n_idx = torch.zeros(V + 1, dtype=torch.int64, device=dev)
         self.eval_counts = torch.zeros(3, dtype=torch.int64, device=dev)
         self.compact_ws = torch.empty(abi.gs_grad_compact_ws_bytes(n), dtype=torch.uint8, device=dev)
+        if self.dssim_lambda is not None:
+            self.t_final = torch.empty((V, self.H, self.W), dtype=torch.float32, device=dev)
+            self.last_idx = torch.empty((V, self.H, self.W), dtype=torch.int32, device=dev)
+            self.dldc = torch.empty((V, 3, self.H, self.W), dtype=torch.float32, device=dev)
         self.proj = abi.proj_struct(self.rec.data_ptr(), self.depth.data_ptr(), self.rect.data_ptr(),
                                     self.tiles_touched.data_ptr())
         self.capacity = 0
@@ -100,9 +111,9 @@ class GaussianTrainer:
         """Kernels the library launches for one train_step, from its launch structure:
         projection 1; binning: count 1, scan 3, bucket stats 1, then (when there are
         instances) scatter 1, warp sort 1, and one more sort kernel for each of the
-        size classes 257..2048, 2049..16384 and over 16384 that occurs; fused raster 1;
-        compaction: 3 per view-list scan, then (several views) union 1 and union scan 3,
-        VJP 1; Adam 2.
+        size classes 257..2048, 2049..16384 and over 16384 that occurs; fused raster 1
+        (with the D-SSIM loss: forward, D-SSIM and backward, 3); compaction: 3 per
+        view-list scan, then (several views) union 1 and union scan 3, VJP 1; Adam 2.
         Memsets and copies are not kernels.  Reads the last step's ranges."""
         V, n = self.V, self.n
         r = self.ranges.view(-1, 2).to(torch.int64)
@@ -112,7 +123,8 @@ class GaussianTrainer:
             sort += 2 + sum(int(((c > lo) & (c <= hi)).any().item())
                             for lo, hi in ((256, 2048), (2048, 16384), (16384, 1 << 62)))
         compact = (3 * V + (1 + 3 if V > 1 else 0) + 1) if n else 0
-        return (1 if n else 0) + sort + 1 + compact + (2 if n else 0)
+        raster = 1 if self.dssim_lambda is None else 3
+        return (1 if n else 0) + sort + raster + compact + (2 if n else 0)
 
     def stream_handle(self):
         return torch.cuda.current_stream(self.device).cuda_stream
@@ -134,11 +146,30 @@ class GaussianTrainer:
             self._alloc_instances(int(math.ceil(cnt * 1.25)) + 1024)
 
     def raster(self, target=None, count_evals=True):
+        if target is not None and self.dssim_lambda is not None:
+            return self.raster_dssim(target, count_evals)
         abi.gs_raster_fused_fwd_bwd(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,
                                     self.opts, target.data_ptr() if target is not None else None,
                                     self.image.data_ptr(), self.loss.data_ptr(), self.grad2d.data_ptr(),
                                     self.touched.data_ptr(), self.eval_counts.data_ptr() if count_evals else None,
                                     self.stream_handle())
+
+    def raster_dssim(self, target, count_evals=True, events=None):
+        """L1 + D-SSIM: forward with stored per-pixel state, loss and dL/dC, backward.
+        events: None or two CUDA events recorded after the forward and after the loss."""
+        sh = self.stream_handle()
+        abi.gs_raster_forward_state(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,
+                                    self.opts, self.image.data_ptr(), self.t_final.data_ptr(),
+                                    self.last_idx.data_ptr(), self.eval_counts.data_ptr() if count_evals else None, sh)
+        if events is not None:
+            events[0].record(torch.cuda.current_stream(self.device))
+        abi.gs_dssim_loss_grad(self.image.data_ptr(), target.data_ptr(), self.V, self.W, self.H, self.dssim_lambda,
+                               self.loss.data_ptr(), self.dldc.data_ptr(), sh)
+        if events is not None:
+            events[1].record(torch.cuda.current_stream(self.device))
+        abi.gs_raster_backward_state(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams,
+                                     self.V, self.opts, self.t_final.data_ptr(), self.last_idx.data_ptr(),
+                                     self.dldc.data_ptr(), self.grad2d.data_ptr(), self.touched.data_ptr(), sh)
 
     def compact(self):
         abi.gs_grad_compact(self.grad2d.data_ptr(), self.touched.data_ptr(), self.params.data_ptr(), self.n,

@@ -183,6 +183,52 @@ GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const u
                                   const float* target, float* image, double* loss, float* grad2d, uint8_t* touched,
                                   uint64_t* eval_counts, void* stream);
 
+/* ---- L1 + D-SSIM loss (the standard 3DGS loss: On Scaling Up 3D Gaussian
+ * Splatting Training, summary of the loss) ----
+ * The SSIM window reaches 10 pixels beyond a tile, into tiles other CTAs
+ * render, so this loss cannot live inside the fused kernel.  A step with it is
+ * three launches instead of one:
+ *   gs_raster_forward_state   image + per-pixel final T and last index
+ *   gs_dssim_loss_grad        loss and dL/dC from image and target
+ *   gs_raster_backward_state  backward from the stored state and dL/dC
+ * The backward recomputes the pass bits of every chunk (the fused kernel keeps
+ * the last three on chip), otherwise it is the fused kernel's backward. */
+
+/* Forward rasterization as in gs_raster_fused_fwd_bwd without a target, that
+ * also stores per pixel the final transmittance and the last composited list
+ * index (-1 if none).
+ * image: [V][3][H][W] out.  t_final: [V][H][W] fp32 out.  last_idx: [V][H][W]
+ * int32 out.  eval_counts: NULL or [3] u64 accumulated (+=), as for the fused call.
+ * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
+GS_API gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                         const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                         const gs_render_opts* opts, float* image, float* t_final, int32_t* last_idx,
+                                         uint64_t* eval_counts, void* stream);
+
+/* Loss (1 - lambda) L1 + lambda (1 - SSIM) per view and its gradient
+ * dL/dC.  L1 = mean |image - target| over 3*H*W values; SSIM = mean over
+ * channels and pixels of the SSIM map, per channel with an 11 x 11 Gaussian
+ * window (sigma 1.5, weights normalised to sum 1), the images zero outside
+ * their borders, C1 = 0.01^2, C2 = 0.03^2.  dL/dC = (1 - lambda) sign(image -
+ * target) / (3HW) - lambda dSSIM/dimage.  fp32 arithmetic, loss summed in fp64.
+ * image, target: [V][3][H][W].  loss: [V] fp64 out (overwritten).
+ * dldc: [V][3][H][W] fp32 out.  0 <= lambda <= 1 (3DGS uses 0.2).
+ * Errors: INVALID_ARG for bad pointers, sizes or lambda; CUDA on launch failure. */
+GS_API gs_status gs_dssim_loss_grad(const float* image, const float* target, int32_t n_views, int32_t width,
+                                    int32_t height, float lambda, double* loss, float* dldc, void* stream);
+
+/* Backward rasterization from a stored forward state: the pixels' composited
+ * entries are walked back to front exactly as in gs_raster_fused_fwd_bwd, with
+ * dL/dC taken from dldc instead of the L1 sign.  proj, tile lists, cams and
+ * opts must be those of the gs_raster_forward_state call that wrote t_final
+ * and last_idx.  dldc: [V][3][H][W].  grad2d, touched: as for the fused call
+ * (accumulated; zero on entry).
+ * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
+GS_API gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                          const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                          const gs_render_opts* opts, const float* t_final, const int32_t* last_idx,
+                                          const float* dldc, float* grad2d, uint8_t* touched, void* stream);
+
 /* Sparse-gradient compaction ("encoder") and aggregation ("decoder"):
  * per view, idx[v] = ascending list of touched Gaussians, n_idx[v] its length;
  * idx[n_views] / n_idx[n_views] = the union over views.  For every Gaussian of

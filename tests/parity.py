@@ -293,3 +293,115 @@ def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, de
     del tr
     torch.cuda.empty_cache()
     return stats
+
+
+# ----------------------------------------------------------------------------- L1 + D-SSIM
+# Bars of the D-SSIM stage, carried over from the step's own:
+# - the SSIM map is an image-like per-pixel quantity: the loss, lambda times the
+#   mean of 1 - S plus the L1 term, must agree within lambda * IMG_ATOL (which bounds
+#   the mean of per-pixel errors of IMG_ATOL), plus half an ulp of each fp32
+#   difference x - y in the L1 term;
+# - dL/dC is a gradient, but the SSIM part is a sum of three terms
+#   (w * dS/dmu_x + 2 x (w * dS/dE[x^2]) + y (w * dS/dE[xy])) / N that cancel
+#   where x is close to y, so its relative error is taken against the sum of the
+#   terms' magnitudes M (w * |dS/dmu_x| + 2|x| (w * |dS/dE[x^2]|) + |y| (w * |dS/dE[xy]|)):
+#   |gpu - oracle| <= GRAD_RTOL * lambda / N * M + 4 u |oracle|; the L1 part is a
+#   signed constant that must be exact.
+_U = 2.0 ** -24
+
+
+def dssim_reference(x, y, lam):
+    """Oracle loss and dL/dC of (1 - lam) L1 + lam (1 - SSIM) for images [3, H, W],
+    with the elementwise and total tolerances above."""
+    from oracle import dssim
+    lam = float(np.float32(lam))   # the kernel is given lambda in fp32
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    N = float(x.size)
+    t = dssim.ssim_terms(x, y)
+    l1 = float(np.abs(x - y).mean())
+    loss = (1.0 - lam) * l1 + lam * (1.0 - float(t["S"].mean()))
+    l1_part = np.sign(x - y) * float(np.float32((1.0 - lam) / N))
+    g_ssim = (dssim.wsum(t["d_mu"]) + 2.0 * x * dssim.wsum(t["d_exx"]) + y * dssim.wsum(t["d_exy"])) / N
+    dldc = l1_part - lam * g_ssim
+    M = dssim.wsum(np.abs(t["d_mu"])) + 2 * np.abs(x) * dssim.wsum(np.abs(t["d_exx"])) \
+        + np.abs(y) * dssim.wsum(np.abs(t["d_exy"]))
+    tol = GRAD_RTOL * lam / N * M + 4 * _U * np.abs(dldc)
+    tol_loss = lam * IMG_ATOL + (1.0 - lam) * _U * l1 + 1e-12 * abs(loss)
+    return dict(loss=loss, dldc=dldc, tol=tol, tol_loss=tol_loss, M=lam / N * M)
+
+
+def check_dssim_stage(img, tgt, lam, loss_gpu, dldc_gpu, stats=None, tag=""):
+    """GPU loss and dL/dC of the D-SSIM stage against the oracle on the same images."""
+    ref = dssim_reference(img, tgt, lam)
+    err = np.abs(np.asarray(dldc_gpu, np.float64) - ref["dldc"])
+    bad = err > ref["tol"]
+    assert not bad.any(), f"{tag} dL/dC out of tolerance at {np.argwhere(bad)[:5].tolist()}: " \
+                          f"gpu {np.asarray(dldc_gpu)[bad][:3]} oracle {ref['dldc'][bad][:3]} tol {ref['tol'][bad][:3]}"
+    assert abs(loss_gpu - ref["loss"]) <= ref["tol_loss"], (tag, loss_gpu, ref["loss"], ref["tol_loss"])
+    if stats is not None:
+        scale = np.maximum(ref["M"], 1e-300)
+        stats.setdefault("dldc_err_over_M", []).append(float((err / scale).max()) if lam > 0 else 0.0)
+        stats.setdefault("dldc_err_over_tol", []).append(float((err / ref["tol"]).max()))
+        stats.setdefault("loss_err", []).append(float(abs(loss_gpu - ref["loss"])))
+        stats.setdefault("loss_tol", []).append(float(ref["tol_loss"]))
+
+
+def run_dssim_parity(sc, lam=0.2, targets=None, device="cuda", log=print):
+    """One L1 + D-SSIM step stage by stage: forward with stored state (image, final
+    T, last index, counts), the loss and dL/dC, the backward from the stored state
+    (fed the GPU's dL/dC on both sides), compaction + VJP."""
+    stats = {}
+    if targets is None:
+        targets = oracle_targets(sc)
+    V, n = sc.n_views, sc.n
+    P = sc.params.shape[0]
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device=device,
+                                  dssim_lambda=lam)
+    tgt_dev = torch.from_numpy(targets).to(device)
+    tr.project()
+    tr.bin_sort()
+    tr.eval_counts.zero_()
+    tr.raster(tgt_dev)
+    torch.cuda.synchronize()
+    img = tr.image.cpu().numpy()
+    tfin = tr.t_final.cpu().numpy()
+    last = tr.last_idx.cpu().numpy()
+    loss = tr.loss.cpu().numpy()
+    dldc = tr.dldc.cpu().numpy()
+    g2d = tr.grad2d.cpu().numpy()[..., :9].copy()
+    touched = tr.touched.cpu().numpy().copy()
+    counts = tr.eval_counts.cpu().numpy()
+    ref_grads = np.zeros((P, n), np.float64)
+    ef = eb = ec = 0
+    touched_o = []
+    for v, cam in enumerate(sc.cameras):
+        pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
+        fw = oracle.render(pr, cam, sc.opts, want_last=True, want_tfinal=True)
+        d = np.abs(img[v].astype(np.float64) - fw["image"])
+        assert d.max() <= IMG_ATOL, f"view {v}: image max abs err {d.max()}"
+        assert np.array_equal(last[v], fw["last"]), f"view {v}: last index differs"
+        assert np.abs(tfin[v].astype(np.float64) - fw["t_final"]).max() <= 1e-6, f"view {v}: final T"
+        stats.setdefault("t_final_exact_frac", []).append(float((bits(tfin[v]) == bits(fw["t_final"])).mean()))
+        ef += fw["e_fwd"]
+        eb += fw["e_bwd"]
+        ec += fw["e_comp"]
+        check_dssim_stage(img[v], targets[v], lam, loss[v], dldc[v], stats, tag=f"view {v}")
+        bw = oracle.render(pr, cam, sc.opts, target=targets[v], dldc_extra=dldc[v], l1_weight=0.0)
+        assert np.array_equal(touched[v], bw["touched"]), f"view {v}: touched sets differ"
+        ok, st = grad_report(g2d[v][bw["touched"] > 0], bw["grad2d"][bw["touched"] > 0])
+        stats.setdefault("grad2d", []).append(st)
+        assert ok, f"view {v}: grad2d out of tolerance {st}"
+        oracle.vjp(sc.params, sc.sh_degree, cam, sc.opts, bw["grad2d"], bw["touched"], pr["clamp"], ref_grads)
+        touched_o.append(bw["touched"])
+    assert (int(counts[0]), int(counts[1]), int(counts[2])) == (ef, eb, ec), (counts, ef, eb, ec)
+    tr.compact()
+    torch.cuda.synchronize()
+    union = oracle.compact(np.any(np.stack(touched_o), 0).astype(np.uint8))
+    n_idx = tr.n_idx.cpu().numpy()
+    assert n_idx[V] == union.size and np.array_equal(tr.idx.cpu().numpy().view(np.uint32)[V][:n_idx[V]], union)
+    ok, st = grad_report(tr.rows(tr.grads).cpu().numpy(), ref_grads)
+    stats["grads"] = st
+    assert ok, f"dense gradients out of tolerance {st}"
+    log(f"[dssim parity] {sc.name} lambda={lam}: {stats}")
+    return stats

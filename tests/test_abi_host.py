@@ -87,6 +87,18 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     # raster with a target but no gradient buffers
     assert L.gs_raster_fused_fwd_bwd(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None, None,
                                      None, None, None) == abi.GS_ERR_INVALID_ARG
+    # forward with state: state buffers required; backward from state: dL/dC and gradient buffers required
+    assert L.gs_raster_forward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, None, 16, None,
+                                     None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_raster_backward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None, 16,
+                                      16, None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_raster_backward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, 16, None,
+                                      16, None) == abi.GS_ERR_INVALID_ARG
+    # D-SSIM: 0 <= lambda <= 1, at least one pixel and one view
+    for lam, V, W, H in ((-0.1, 1, 8, 8), (1.5, 1, 8, 8), (float("nan"), 1, 8, 8), (0.2, 0, 8, 8), (0.2, 1, 0, 8),
+                         (0.2, 33, 8, 8)):
+        assert L.gs_dssim_loss_grad(16, 16, V, W, H, ctypes.c_float(lam), 16, 16, None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_dssim_loss_grad(16, None, 1, 8, 8, ctypes.c_float(0.2), 16, 16, None) == abi.GS_ERR_INVALID_ARG
 
 
 def test_binding_raises_without_the_library(tmp_path, monkeypatch):
