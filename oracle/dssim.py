@@ -71,21 +71,16 @@ def wsum(img: np.ndarray) -> np.ndarray:
     return out
 
 
-def _moments(x, y):
+def ssim_map(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """Per-channel, per-pixel SSIM of images [3, H, W]."""
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
     mx, my = wsum(x), wsum(y)
     exx, eyy, exy = wsum(x * x), wsum(y * y), wsum(x * y)
     A = 2.0 * mx * my + C1
     B = 2.0 * (exy - mx * my) + C2
     C = mx * mx + my * my + C1
     D = (exx - mx * mx) + (eyy - my * my) + C2
-    return mx, my, A, B, C, D
-
-
-def ssim_map(x: np.ndarray, y: np.ndarray) -> np.ndarray:
-    """Per-channel, per-pixel SSIM of images [3, H, W]."""
-    x = np.asarray(x, np.float64)
-    y = np.asarray(y, np.float64)
-    _, _, A, B, C, D = _moments(x, y)
     return (A * B) / (C * D)
 
 
@@ -93,17 +88,31 @@ def ssim(x, y) -> float:
     return float(ssim_map(x, y).mean())
 
 
+def ssim_terms(x, y) -> dict:
+    """Every intermediate of the SSIM map and of its derivatives, per channel and pixel:
+    the moments, A, B, C, D, S and the three derivative maps dS/dmu_x, dS/dE[x^2],
+    dS/dE[xy]."""
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    mx, my = wsum(x), wsum(y)
+    exx, eyy, exy = wsum(x * x), wsum(y * y), wsum(x * y)
+    A = 2.0 * mx * my + C1
+    B = 2.0 * (exy - mx * my) + C2
+    C = mx * mx + my * my + C1
+    D = (exx - mx * mx) + (eyy - my * my) + C2
+    CD = C * D
+    S = (A * B) / CD
+    return dict(mx=mx, my=my, exx=exx, eyy=eyy, exy=exy, A=A, B=B, C=C, D=D, S=S,
+                d_mu=2.0 * my * (B - A) / CD - 2.0 * mx * S * (D - C) / CD,
+                d_exx=-S / D, d_exy=2.0 * A / CD)
+
+
 def ssim_grad(x, y) -> np.ndarray:
     """d SSIM / d x for images [3, H, W] (SSIM = mean of the map)."""
     x = np.asarray(x, np.float64)
     y = np.asarray(y, np.float64)
-    mx, my, A, B, C, D = _moments(x, y)
-    CD = C * D
-    S = (A * B) / CD
-    d_mu = 2.0 * my * (B - A) / CD - 2.0 * mx * S * (D - C) / CD
-    d_exx = -S / D
-    d_exy = 2.0 * A / CD
-    return (wsum(d_mu) + 2.0 * x * wsum(d_exx) + y * wsum(d_exy)) / float(x.size)
+    t = ssim_terms(x, y)
+    return (wsum(t["d_mu"]) + 2.0 * x * wsum(t["d_exx"]) + y * wsum(t["d_exy"])) / float(x.size)
 
 
 def loss(x, y, lam: float = LAMBDA) -> float:
