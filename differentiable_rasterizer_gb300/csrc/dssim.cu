@@ -34,6 +34,13 @@
 
 namespace gs {
 
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 namespace ssim {
 constexpr int kR = 5;                 // window radius
 constexpr int kWin = 2 * kR + 1;
@@ -42,11 +49,13 @@ constexpr int kTM = kTO + 2 * kR;     // derivative-map region (42)
 constexpr int kTI = kTO + 4 * kR;     // input region (52)
 constexpr int kThreads = 256;
 constexpr int kK1 = 3;                // outputs per thread in P1 (kTM / kK1 runs per row)
-constexpr int kK2 = 3;                // P2
+constexpr int kK2 = 7;                // P2: 42 columns x 6 runs = 252 items, one round
 constexpr int kK3 = 4;                // P3
 constexpr int kK4 = 4;                // P4
 static_assert(kTM % kK1 == 0 && kTM % kK2 == 0 && kTO % kK3 == 0 && kTO % kK4 == 0, "runs must tile the regions");
-constexpr int kSmemA = 2 * kTI * kTI;     // images, later the 3 derivative maps
+constexpr int kLoadIters = (kTI * kTI + kThreads - 1) / kThreads;
+static_assert(kTO * (kTO / kK4) == kThreads, "P4: one run per thread");
+constexpr int kSmemA = 2 * kTI * kTI;     // images (x, y interleaved), later the 3 derivative maps
 constexpr int kSmemB = 5 * kTI * kTM;     // P1 sums, later the P3 sums
 static_assert(3 * kTM * kTM <= kSmemA && 3 * kTM * kTO <= kSmemB, "aliased buffers must fit");
 constexpr size_t kSmemBytes = sizeof(float) * (kSmemA + kSmemB);
@@ -69,8 +78,7 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
 {
     using namespace ssim;
     extern __shared__ float smem[];
-    float* const sx = smem;                       // [kTI][kTI]
-    float* const sy = smem + kTI * kTI;           // [kTI][kTI]
+    float2* const sxy = reinterpret_cast<float2*>(smem);   // [kTI][kTI] (x, y)
     float* const dm = smem;                       // [3][kTM][kTM] (after P1)
     float* const h1 = smem + kSmemA;              // [5][kTI][kTM]
     float* const h3 = smem + kSmemA;              // [3][kTM][kTO] (after P2)
@@ -85,21 +93,31 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     const float* __restrict__ X = a.image + plane;
     const float* __restrict__ Y = a.target + plane;
 
-    // images on the tile + 10-pixel ring, zero outside; their means over the region
+    // images on the tile + 10-pixel ring, zero outside (all loads issued before
+    // the first store); their means over the region
     float sumx = 0.0f, sumy = 0.0f;
-    for (int i = threadIdx.x; i < kTI * kTI; i += kThreads) {
-        const int r = i / kTI, c = i - r * kTI;
-        const int gy = oy - 2 * kR + r, gx = ox - 2 * kR + c;
-        float x = 0.0f, y = 0.0f;
-        if (gy >= 0 && gy < a.H && gx >= 0 && gx < a.W) {
-            const size_t o = (size_t)gy * a.W + gx;
-            x = __ldg(X + o);
-            y = __ldg(Y + o);
+    {
+        float lx[kLoadIters], ly[kLoadIters];
+#pragma unroll
+        for (int k = 0; k < kLoadIters; ++k) {
+            const int i = k * kThreads + threadIdx.x;
+            const int r = i / kTI, c = i - r * kTI;
+            const int gy = oy - 2 * kR + r, gx = ox - 2 * kR + c;
+            lx[k] = 0.0f;
+            ly[k] = 0.0f;
+            if (i < kTI * kTI && gy >= 0 && gy < a.H && gx >= 0 && gx < a.W) {
+                const size_t o = (size_t)gy * a.W + gx;
+                lx[k] = __ldg(X + o);
+                ly[k] = __ldg(Y + o);
+            }
         }
-        sx[i] = x;
-        sy[i] = y;
-        sumx += x;
-        sumy += y;
+#pragma unroll
+        for (int k = 0; k < kLoadIters; ++k) {
+            const int i = k * kThreads + threadIdx.x;
+            if (i < kTI * kTI) sxy[i] = make_float2(lx[k], ly[k]);
+            sumx += lx[k];
+            sumy += ly[k];
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -119,6 +137,15 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     }
     cx = cx * (1.0f / (float)(kTI * kTI));
     cy = cy * (1.0f / (float)(kTI * kTI));
+    // this thread's P4 outputs: column tid % 32, rows 4 (tid / 32) .. + 3
+    const int c4 = threadIdx.x % kTO, r4 = (threadIdx.x / kTO) * kK4;
+    float ox4[kK4], oy4[kK4];
+#pragma unroll
+    for (int j = 0; j < kK4; ++j) {
+        const float2 v2 = sxy[(r4 + j + 2 * kR) * kTI + c4 + 2 * kR];
+        ox4[j] = v2.x;
+        oy4[j] = v2.y;
+    }
 
     // P1: horizontal window sums of x', y', x'^2, y'^2, x'y'
     constexpr int kRuns1 = kTM / kK1;
@@ -131,7 +158,8 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
             for (int j = 0; j < kK1; ++j) acc[q][j] = 0.0f;
 #pragma unroll
         for (int t = 0; t < kK1 + 2 * kR; ++t) {
-            const float x = sx[r * kTI + c0 + t] - cx, y = sy[r * kTI + c0 + t] - cy;
+            const float2 v2 = sxy[r * kTI + c0 + t];
+            const float x = v2.x - cx, y = v2.y - cy;
             const float xx = x * x, yy = y * y, xy = x * y;
 #pragma unroll
             for (int j = 0; j < kK1; ++j) {
@@ -186,7 +214,8 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
                 const float B = 2.0f * (m[4][j] - mxs * mys) + a.c2;
                 const float C = (mx * mx + my * my) + a.c1;
                 const float D = ((m[2][j] - mxs * mxs) + (m[3][j] - mys * mys)) + a.c2;
-                const float rC = 1.0f / C, rD = 1.0f / D;
+                // C >= C1 and D >= C2: far from the approximate reciprocal's limits
+                const float rC = rcp_approx(C), rD = rcp_approx(D);
                 const float inv = rC * rD;
                 const float S = (A * B) * inv;
                 dmu = (2.0f * (my * B - A * mys) - 2.0f * S * (mx * D - C * mxs)) * inv;
@@ -225,11 +254,9 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     }
     __syncthreads();
 
-    // P4: vertical sums -> dL/dC on the output tile
+    // P4: vertical sums -> dL/dC on the output tile (one 4-row run per thread)
     double l1sum = 0.0;
-    constexpr int kRuns4 = kTO / kK4;
-    for (int it = threadIdx.x; it < kTO * kRuns4; it += kThreads) {
-        const int c = it % kTO, r0 = (it / kTO) * kK4;
+    {
         float b[3][kK4];
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
@@ -237,7 +264,7 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
             for (int j = 0; j < kK4; ++j) b[q][j] = 0.0f;
 #pragma unroll
             for (int t = 0; t < kK4 + 2 * kR; ++t) {
-                const float h = h3[(q * kTM + r0 + t) * kTO + c];
+                const float h = h3[(q * kTM + r4 + t) * kTO + c4];
 #pragma unroll
                 for (int j = 0; j < kK4; ++j) {
                     const int k = t - j;
@@ -245,18 +272,16 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
                 }
             }
         }
-        const int gx = ox + c;
+        const int gx = ox + c4;
 #pragma unroll
         for (int j = 0; j < kK4; ++j) {
-            const int gy = oy + r0 + j;
+            const int gy = oy + r4 + j;
             if (gy < a.H && gx < a.W) {
-                // x and y again from global memory (L2): their shared copies now hold the maps
-                const size_t o = (size_t)gy * a.W + gx;
-                const float x = __ldg(X + o), y = __ldg(Y + o);
+                const float x = ox4[j], y = oy4[j];
                 const float d = x - y;
                 const float sgn = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
                 const float gs = b[0][j] + 2.0f * (x - cx) * b[1][j] + (y - cy) * b[2][j];
-                a.dldc[plane + o] = __fmaf_rn(a.ssim_coef, gs, sgn * a.l1_coef);
+                a.dldc[plane + (size_t)gy * a.W + gx] = __fmaf_rn(a.ssim_coef, gs, sgn * a.l1_coef);
                 l1sum += (double)fabsf(d);
             }
         }
