@@ -68,7 +68,7 @@ def _declare(L):
         getattr(L, "oracle_render" + s).restype = _I32
         getattr(L, "oracle_vjp" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_vjp" + s).restype = _I32
-        getattr(L, "oracle_tile_lists" + s).argtypes = [_P, _P, _P, _I64, _I32, _I32, _P, _P]
+        getattr(L, "oracle_tile_lists" + s).argtypes = [_P, _P, _P, _I64, _I32, _I32, _I64, _P, _P]
         getattr(L, "oracle_tile_lists" + s).restype = _I64
         getattr(L, "oracle_compact" + s).argtypes = [_P, _I64, _P]
         getattr(L, "oracle_compact" + s).restype = _I64
@@ -98,11 +98,13 @@ def cam16(cam) -> np.ndarray:
     return np.ascontiguousarray(v)
 
 
-def opts9(opts: dict) -> np.ndarray:
+def optsv(opts: dict) -> np.ndarray:
+    """Options as 10 doubles: near_z, lowpass, alpha_min, alpha_max, t_min, bg (3),
+    exclude_crossing, tile_budget (0: no pruning; values taken from float32 where fp)."""
     f = lambda x: float(np.float32(x))
     return np.array([f(opts["near_z"]), f(opts["lowpass"]), f(opts["alpha_min"]), f(opts["alpha_max"]),
                      f(opts["t_min"]), f(opts["bg"][0]), f(opts["bg"][1]), f(opts["bg"][2]),
-                     float(opts.get("exclude_crossing", 0))], np.float64)
+                     float(opts.get("exclude_crossing", 0)), float(int(opts.get("tile_budget", 0)))], np.float64)
 
 
 def pexp_f32(x) -> np.ndarray:
@@ -130,7 +132,7 @@ def project(params, sh_degree, cam, opts, prec="f32"):
     vis = np.zeros(n, np.uint8)
     clamp = np.zeros(n, np.uint8)
     c = cam16(cam)
-    o = opts9(opts)
+    o = optsv(opts)
     rc = getattr(lib(), "oracle_project_" + prec)(_ptr(p), n, sh_degree, _ptr(c), cam.width, cam.height, _ptr(o),
                                                    _ptr(rec), _ptr(rect), _ptr(vis), _ptr(clamp))
     assert rc == 0
@@ -159,7 +161,7 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
     tgt = np.ascontiguousarray(np.asarray(target, dt)) if target is not None else None
     tm = np.ascontiguousarray(np.asarray(tile_mask, np.uint8)) if tile_mask is not None else None
     ex = np.ascontiguousarray(np.asarray(dldc_extra, dt)) if dldc_extra is not None else None
-    rc = getattr(lib(), "oracle_render_" + prec)(_ptr(rec), _ptr(rect), _ptr(vis), n, W, H, _ptr(opts9(opts)), mode,
+    rc = getattr(lib(), "oracle_render_" + prec)(_ptr(rec), _ptr(rect), _ptr(vis), n, W, H, _ptr(optsv(opts)), mode,
                                                   _ptr(tgt), _ptr(img), _ptr(loss), _ptr(g2), _ptr(touched),
                                                   _ptr(counts), _ptr(last), _ptr(sig), _ptr(tm),
                                                   _ptr(ex), float(l1_weight), _ptr(tfin))
@@ -183,23 +185,24 @@ def vjp(params, sh_degree, cam, opts, grad2d, touched, clamp, grads=None, prec="
     if grads is None:
         grads = np.zeros((P, n), np.float64)
     rc = getattr(lib(), "oracle_vjp_" + prec)(_ptr(p), n, sh_degree, _ptr(cam16(cam)), cam.width, cam.height,
-                                               _ptr(opts9(opts)), _ptr(np.ascontiguousarray(grad2d, np.float64)),
+                                               _ptr(optsv(opts)), _ptr(np.ascontiguousarray(grad2d, np.float64)),
                                                _ptr(np.ascontiguousarray(touched, np.uint8)),
                                                _ptr(np.ascontiguousarray(clamp, np.uint8)), _ptr(grads))
     assert rc == 0
     return grads
 
 
-def tile_lists(proj, cam, prec="f32"):
-    """Sorted per-tile candidate lists: (offsets[tiles+1], ids[I])."""
+def tile_lists(proj, cam, prec="f32", budget=0):
+    """Sorted per-tile candidate lists: (offsets[tiles+1], ids[I]); budget > 0: pruned lists."""
     rec, rect, vis = proj["rec"], proj["rect"], proj["visible"]
     n = rec.shape[0]
     tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
     off = np.zeros(tiles + 1, np.int64)
     L = getattr(lib(), "oracle_tile_lists_" + prec)
-    total = L(_ptr(rec), _ptr(rect), _ptr(vis), n, cam.width, cam.height, _ptr(off), None)
+    total = L(_ptr(rec), _ptr(rect), _ptr(vis), n, cam.width, cam.height, int(budget), _ptr(off), None)
     ids = np.zeros(max(total, 1), np.int64)
-    total = L(_ptr(rec), _ptr(rect), _ptr(vis), n, cam.width, cam.height, _ptr(off), _ptr(ids))
+    total = L(_ptr(rec), _ptr(rect), _ptr(vis), n, cam.width, cam.height, int(budget), _ptr(off), _ptr(ids))
+    assert total >= 0
     return off, ids[:total]
 
 

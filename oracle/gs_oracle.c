@@ -130,6 +130,7 @@ typedef struct {
 typedef struct {
     REAL near_z, lowpass, alpha_min, alpha_max, t_min, bg[3];
     int exclude_crossing;
+    int64_t tile_budget;   /* 0: no pruning */
 } opts_t;
 
 /* cam16 = R(9, row-major world->camera), t(3), fx, fy, cx, cy */
@@ -141,13 +142,14 @@ static void load_cam(const double* c16, int W, int H, cam_t* c)
     c->W = W; c->H = H;
 }
 
-/* opts9 = near_z, lowpass, alpha_min, alpha_max, t_min, bg r, g, b, exclude_crossing */
-static void load_opts(const double* o9, opts_t* o)
+/* optsv = near_z, lowpass, alpha_min, alpha_max, t_min, bg r, g, b, exclude_crossing, tile_budget */
+static void load_opts(const double* ov, opts_t* o)
 {
-    o->near_z = (REAL)o9[0]; o->lowpass = (REAL)o9[1]; o->alpha_min = (REAL)o9[2];
-    o->alpha_max = (REAL)o9[3]; o->t_min = (REAL)o9[4];
-    o->bg[0] = (REAL)o9[5]; o->bg[1] = (REAL)o9[6]; o->bg[2] = (REAL)o9[7];
-    o->exclude_crossing = (int)o9[8];
+    o->near_z = (REAL)ov[0]; o->lowpass = (REAL)ov[1]; o->alpha_min = (REAL)ov[2];
+    o->alpha_max = (REAL)ov[3]; o->t_min = (REAL)ov[4];
+    o->bg[0] = (REAL)ov[5]; o->bg[1] = (REAL)ov[6]; o->bg[2] = (REAL)ov[7];
+    o->exclude_crossing = (int)ov[8];
+    o->tile_budget = (int64_t)ov[9];
 }
 
 /* ------------------------------------------------------------------------- */
@@ -345,11 +347,11 @@ static int project_one(const REAL* P, int64_t n, int64_t g, int deg, const cam_t
 }
 
 int FN(oracle_project)(const REAL* params, int64_t n, int sh_degree, const double* cam16, int width, int height,
-                       const double* opts9, REAL* rec, int32_t* rect, uint8_t* visible, uint8_t* clampmask)
+                       const double* optsv, REAL* rec, int32_t* rect, uint8_t* visible, uint8_t* clampmask)
 {
     cam_t cam; opts_t op;
     load_cam(cam16, width, height, &cam);
-    load_opts(opts9, &op);
+    load_opts(optsv, &op);
     for (int64_t g = 0; g < n; ++g) {
         memset(rec + 10 * g, 0, sizeof(REAL) * 10);
         rect[4 * g + 0] = rect[4 * g + 1] = rect[4 * g + 2] = rect[4 * g + 3] = 0;
@@ -384,23 +386,62 @@ static int in_rect(const int32_t* rc, int tx, int ty)
     return tx >= rc[0] && tx < rc[2] && ty >= rc[1] && ty < rc[3];
 }
 
+/* ------------------------------------------------------------------------- */
+/* Hardware-aware pruning (ByteSplat, English abstract: pruning that weighs   */
+/* rendering quality against the per-tile shared-memory budget).  [reading]   */
+/* A tile list longer than the budget K keeps its K most opaque entries        */
+/* (opacity = the projected o; equal opacities: the nearer entry, i.e. the     */
+/* earlier list position, is kept) and stays in depth order.                   */
+/* ------------------------------------------------------------------------- */
+typedef struct { REAL o; int64_t pos; } prune_t;
+
+static int prune_cmp(const void* pa, const void* pb)
+{
+    const prune_t* a = (const prune_t*)pa;
+    const prune_t* b = (const prune_t*)pb;
+    if (a->o > b->o) return -1;
+    if (a->o < b->o) return 1;
+    return (a->pos < b->pos) ? -1 : (a->pos > b->pos) ? 1 : 0;
+}
+
+static int pos_cmp(const void* pa, const void* pb)
+{
+    const prune_t* a = (const prune_t*)pa;
+    const prune_t* b = (const prune_t*)pb;
+    return (a->pos < b->pos) ? -1 : (a->pos > b->pos) ? 1 : 0;
+}
+
+/* Prunes list[0..len) in place; returns the new length (-1 on allocation failure). */
+static int64_t prune_list(const REAL* rec, cand_t* list, int64_t len, int64_t budget)
+{
+    if (budget <= 0 || len <= budget) return len;
+    prune_t* p = (prune_t*)malloc(sizeof(prune_t) * (size_t)len);
+    if (!p) return -1;
+    for (int64_t i = 0; i < len; ++i) { p[i].o = rec[10 * list[i].g + 5]; p[i].pos = i; }
+    qsort(p, (size_t)len, sizeof(prune_t), prune_cmp);     /* most opaque first */
+    qsort(p, (size_t)budget, sizeof(prune_t), pos_cmp);    /* the kept ones back in list order */
+    for (int64_t i = 0; i < budget; ++i) list[i] = list[p[i].pos];   /* p[i].pos >= i: forward copy is safe */
+    free(p);
+    return budget;
+}
+
 /* Literal mode: scan all n Gaussians for this pixel's tile. */
 static int64_t list_literal(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
-                            int tx, int ty, cand_t* buf)
+                            int tx, int ty, int64_t budget, cand_t* buf)
 {
     int64_t m = 0;
     for (int64_t g = 0; g < n; ++g)
         if (visible[g] && in_rect(rect + 4 * g, tx, ty)) { buf[m].depth = rec[10 * g + 9]; buf[m].g = g; ++m; }
     qsort(buf, (size_t)m, sizeof(cand_t), cand_cmp);
-    return m;
+    return prune_list(rec, buf, m, budget);
 }
 
 /* Tile-list mode: the same list, computed once per tile (every pixel of a tile */
 /* has the same candidate list under the support rule), by bucketing then qsort. */
-typedef struct { int64_t* off; cand_t* items; } tile_lists_t;
+typedef struct { int64_t* off; int64_t* len; cand_t* items; } tile_lists_t;   /* tile t: items[off[t] .. + len[t]) */
 
 static int build_tile_lists(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
-                            int tiles_x, int tiles_y, const uint8_t* tile_mask, tile_lists_t* tl)
+                            int tiles_x, int tiles_y, const uint8_t* tile_mask, int64_t budget, tile_lists_t* tl)
 {
     int64_t nt = (int64_t)tiles_x * tiles_y;
     int64_t* cnt = (int64_t*)calloc((size_t)nt + 1, sizeof(int64_t));
@@ -428,27 +469,37 @@ static int build_tile_lists(const REAL* rec, const int32_t* rect, const uint8_t*
                 items[k].g = g;
             }
     }
-    for (int64_t i = 0; i < nt; ++i)
+    /* fill is reused for the (pruned) lengths */
+    for (int64_t i = 0; i < nt; ++i) {
         qsort(items + cnt[i], (size_t)(cnt[i + 1] - cnt[i]), sizeof(cand_t), cand_cmp);
-    free(fill);
+        fill[i] = prune_list(rec, items + cnt[i], cnt[i + 1] - cnt[i], budget);
+        if (fill[i] < 0) { free(cnt); free(items); free(fill); return -1; }
+    }
     tl->off = cnt;
+    tl->len = fill;
     tl->items = items;
     return 0;
 }
 
 /* Sorted per-tile lists as flat arrays (for the bit-exact sort-order check). */
+/* With budget > 0 the lists are the pruned ones, concatenated. */
 int64_t FN(oracle_tile_lists)(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
-                              int width, int height, int64_t* offsets /* [tiles+1] */, int64_t* ids /* [I] or NULL */)
+                              int width, int height, int64_t budget, int64_t* offsets /* [tiles+1] */,
+                              int64_t* ids /* [I] or NULL */)
 {
     int tiles_x = (width + TILE - 1) / TILE, tiles_y = (height + TILE - 1) / TILE;
     int64_t nt = (int64_t)tiles_x * tiles_y;
     tile_lists_t tl;
-    if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, 0, &tl)) return -1;
-    int64_t total = tl.off[nt];
-    memcpy(offsets, tl.off, sizeof(int64_t) * (size_t)(nt + 1));
-    if (ids)
-        for (int64_t i = 0; i < total; ++i) ids[i] = tl.items[i].g;
+    if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, 0, budget, &tl)) return -1;
+    offsets[0] = 0;
+    for (int64_t t = 0; t < nt; ++t) {
+        if (ids)
+            for (int64_t i = 0; i < tl.len[t]; ++i) ids[offsets[t] + i] = tl.items[tl.off[t] + i].g;
+        offsets[t + 1] = offsets[t] + tl.len[t];
+    }
+    int64_t total = offsets[nt];
     free(tl.off);
+    free(tl.len);
     free(tl.items);
     return total;
 }
@@ -481,19 +532,19 @@ static uint64_t fnv(uint64_t h, uint64_t v)
  *   the gradients and the counts); used to check large images tile by tile.
  */
 int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
-                      int width, int height, const double* opts9, int mode, const REAL* target,
+                      int width, int height, const double* optsv, int mode, const REAL* target,
                       REAL* image, double* loss, double* grad2d, uint8_t* touched, int64_t* counts,
                       int32_t* last_idx, uint64_t* sig, const uint8_t* tile_mask, const REAL* dldc_extra,
                       double l1_weight, REAL* t_final)
 {
     opts_t op;
-    load_opts(opts9, &op);
+    load_opts(optsv, &op);
     const int tiles_x = (width + TILE - 1) / TILE, tiles_y = (height + TILE - 1) / TILE;
     const int64_t HW = (int64_t)width * height;
-    tile_lists_t tl = {0, 0};
+    tile_lists_t tl = {0, 0, 0};
     cand_t* buf = 0;
     if (mode == 1) {
-        if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, tile_mask, &tl)) return -1;
+        if (build_tile_lists(rec, rect, visible, n, tiles_x, tiles_y, tile_mask, op.tile_budget, &tl)) return -1;
     } else {
         buf = (cand_t*)malloc(sizeof(cand_t) * (size_t)(n > 0 ? n : 1));
         if (!buf) return -1;
@@ -520,9 +571,10 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
             if (mode == 1) {
                 int64_t t = (int64_t)ty * tiles_x + tx;
                 list = tl.items + tl.off[t];
-                len = tl.off[t + 1] - tl.off[t];
+                len = tl.len[t];
             } else {
-                len = list_literal(rec, rect, visible, n, tx, ty, buf);
+                len = list_literal(rec, rect, visible, n, tx, ty, op.tile_budget, buf);
+                if (len < 0) { free(comp); free(buf); return -1; }
                 list = buf;
             }
             const REAL pxc = (REAL)px + (REAL)0.5, pyc = (REAL)py + (REAL)0.5;
@@ -609,6 +661,7 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
     free(comp);
     free(buf);
     free(tl.off);
+    free(tl.len);
     free(tl.items);
     return 0;
 }
@@ -618,12 +671,12 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
 /* grads [P][n] += d loss / d params for every touched g.                     */
 /* ------------------------------------------------------------------------- */
 int FN(oracle_vjp)(const REAL* params, int64_t n, int sh_degree, const double* cam16, int width, int height,
-                   const double* opts9, const double* grad2d, const uint8_t* touched, const uint8_t* clampmask,
+                   const double* optsv, const double* grad2d, const uint8_t* touched, const uint8_t* clampmask,
                    double* grads)
 {
     (void)width; (void)height;
     opts_t op;
-    load_opts(opts9, &op);
+    load_opts(optsv, &op);
     const double* W = cam16;  /* row-major world->camera rotation */
     const double* tc = cam16 + 9;
     const double fx = cam16[12], fy = cam16[13];
