@@ -240,13 +240,26 @@ def run_gpu(args):
 
     sc = scenes.make_scene(args.config)
     tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda",
-                                  dssim_lambda=args.dssim)
+                                  dssim_lambda=args.dssim, tile_budget=args.tile_budget)
     if sc.target_kind == "uniform":
         target = torch.from_numpy(sc.target_uniform).cuda()
     else:
         pert = tr.to_device_layout(sc.perturbed_params)
         target = tr.render(pert).clone()     # training target: render of the perturbed scene
         del pert
+    torch.cuda.synchronize()
+    prune_quality = None
+    if args.tile_budget:
+        # quality of the pruned render against the unpruned one (which matches the oracle)
+        pruned = tr.render().clone()
+        tr.tile_budget = None
+        full = tr.render().clone()
+        tr.tile_budget = args.tile_budget
+        mse = float(((pruned.double() - full.double()) ** 2).mean())
+        prune_quality = {"psnr_vs_unpruned_db": (10 * math.log10(1.0 / mse)) if mse > 0 else None,
+                         "max_abs_diff": float((pruned - full).abs().max()),
+                         "pixels_changed": float((pruned != full).any(1).double().mean())}
+        del pruned, full
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
@@ -371,6 +384,9 @@ def run_gpu(args):
                     "d2h_bytes_per_step": int(tr.V * 8)},
             "gpu_launches": int(tr.kernel_launches_per_step() * args.steps),
             "clocks": clocks}
+    if args.tile_budget:
+        line["config"]["tile_budget"] = args.tile_budget
+        line["prune_quality"] = prune_quality
     if args.dssim is not None:
         pixels = sc.n_views * sc.cameras[0].width * sc.cameras[0].height
         ops_d = pixels * 3 * OPS_DSSIM
@@ -413,6 +429,8 @@ def main():
     ap.add_argument("--config", default="medium", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-budget", type=int, default=None, metavar="K",
+                    help="prune every tile list to its K most opaque entries before rasterizing")
     ap.add_argument("--dssim", type=float, default=None, metavar="LAMBDA",
                     help="train with (1 - LAMBDA) L1 + LAMBDA D-SSIM (three raster launches instead of the fused one)")
     ap.add_argument("--cpu-rows", type=int, default=270)

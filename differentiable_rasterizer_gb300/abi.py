@@ -24,6 +24,7 @@ GS_GRAD2D_STRIDE = 12
 
 EXPORTS = ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
            "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_grad_compact_static",
+           "gs_prune_tiles",
            "gs_error_string", "gs_param_rows", "gs_param_stride", "gs_num_tiles", "gs_version")
 
 
@@ -78,8 +79,9 @@ def lib():
         L.gs_dssim_loss_grad.argtypes = [_P, _P, _I32, _I32, _I32, _F, _P, _P, _P]
         L.gs_raster_backward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
                                                _P, _P]
+        L.gs_prune_tiles.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I32, _P, _P, _P]
         for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
-                     "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state"):
+                     "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_prune_tiles"):
             getattr(L, name).restype = ctypes.c_int
         L.gs_error_string.argtypes = [ctypes.c_int]
         L.gs_error_string.restype = ctypes.c_char_p
@@ -155,6 +157,11 @@ def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, targ
     _check("gs_raster_fused_fwd_bwd",
            lib().gs_raster_fused_fwd_bwd(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
                                          target, image, loss, grad2d, touched, eval_counts, stream))
+
+
+def gs_prune_tiles(proj, n, n_views, width, height, budget, ids, tile_ranges, stream):
+    _check("gs_prune_tiles", lib().gs_prune_tiles(ctypes.byref(proj), n, n_views, width, height, budget, ids,
+                                                  tile_ranges, stream))
 
 
 def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, eval_counts,

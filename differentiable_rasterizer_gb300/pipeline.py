@@ -38,8 +38,11 @@ from . import abi
 class GaussianTrainer:
     def __init__(self, params: np.ndarray | torch.Tensor, sh_degree: int, cameras, opts: dict, lr,
                  betas=(0.9, 0.999), eps=1e-8, device="cuda", capacity: int | None = None,
-                 dssim_lambda: float | None = None):
+                 dssim_lambda: float | None = None, tile_budget: int | None = None):
         self.device = torch.device(device)
+        if tile_budget is None:
+            tile_budget = opts.get("tile_budget", 0)
+        self.tile_budget = int(tile_budget) if tile_budget else None
         self.dssim_lambda = None if dssim_lambda is None else float(dssim_lambda)
         self.sh_degree = sh_degree
         self.P = abi.gs_param_rows(sh_degree)
@@ -111,7 +114,8 @@ class GaussianTrainer:
         """Kernels the library launches for one train_step, from its launch structure:
         projection 1; binning: count 1, scan 3, bucket stats 1, then (when there are
         instances) scatter 1, warp sort 1, and one more sort kernel for each of the
-        size classes 257..2048, 2049..16384 and over 16384 that occurs; fused raster 1
+        size classes 257..2048, 2049..16384 and over 16384 that occurs; pruning (with a
+        tile budget) 1; fused raster 1
         (with the D-SSIM loss: forward, D-SSIM and backward, 3); compaction: 3 per
         view-list scan, then (several views) union 1 and union scan 3, VJP 1; Adam 2.
         Memsets and copies are not kernels.  Reads the last step's ranges."""
@@ -124,7 +128,8 @@ class GaussianTrainer:
                             for lo, hi in ((256, 2048), (2048, 16384), (16384, 1 << 62)))
         compact = (3 * V + (1 + 3 if V > 1 else 0) + 1) if n else 0
         raster = 1 if self.dssim_lambda is None else 3
-        return (1 if n else 0) + sort + raster + compact + (2 if n else 0)
+        prune = 1 if self.tile_budget else 0
+        return (1 if n else 0) + sort + prune + raster + compact + (2 if n else 0)
 
     def stream_handle(self):
         return torch.cuda.current_stream(self.device).cuda_stream
@@ -142,6 +147,9 @@ class GaussianTrainer:
                                       self.sort_ws.numel(), self.stream_handle())
             self.n_instances = cnt
             if st == abi.GS_OK:
+                if self.tile_budget:
+                    abi.gs_prune_tiles(self.proj, self.n, self.V, self.W, self.H, self.tile_budget,
+                                       self.ids.data_ptr(), self.ranges.data_ptr(), self.stream_handle())
                 return cnt
             self._alloc_instances(int(math.ceil(cnt * 1.25)) + 1024)
 

@@ -156,6 +156,21 @@ GS_API gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views, in
                       int64_t capacity, uint64_t* keys, uint32_t* ids, uint32_t* tile_ranges,
                       int64_t* n_instances, void* ws, size_t* ws_bytes, void* stream);
 
+/* Hardware-aware pruning of the sorted tile lists (ByteSplat, English abstract:
+ * pruning that weighs rendering quality against the per-tile shared-memory
+ * budget).  A tile list longer than `budget` keeps its `budget` most opaque
+ * entries (equal opacities: the earlier, nearer entry) in depth order; its
+ * ids are compacted in place at the start of its range and the range end
+ * becomes start + budget.  Other lists are untouched.  The fused raster kernel
+ * keeps the pass bits of 3 x 256 entries per tile on chip, so budget = 768
+ * bounds every list to what its backward can take without recomputing them.
+ * proj: as given to gs_bin_sort (opacity = record float 5).  ids, tile_ranges:
+ * gs_bin_sort's outputs, updated in place (keys are left as sorted).
+ * budget >= 1.
+ * Errors: INVALID_ARG for bad pointers, sizes or budget; CUDA on launch failure. */
+GS_API gs_status gs_prune_tiles(const gs_proj* proj, int64_t n, int32_t n_views, int32_t width, int32_t height,
+                                int32_t budget, uint32_t* ids, uint32_t* tile_ranges, void* stream);
+
 /* Fused forward + backward rasterization: one CTA per 16x16 tile (256 threads,
  * one pixel each).  Forward: front-to-back over the tile's sorted list, skip
  * power > 0 or alpha < alpha_min, C += c * alpha * T, T *= 1 - alpha, stop at

@@ -99,19 +99,31 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
     ids = tr.ids[:N].cpu().numpy().view(np.uint32)
     ranges = tr.ranges.cpu().numpy().view(np.uint32).reshape(V, -1, 2)
     tiles = tr.tiles
+    budget = int(sc.opts.get("tile_budget", 0))
     base = 0
     for v, cam in enumerate(sc.cameras):
         off, oids = oracle.tile_lists(oprojs[v], cam)
         m = oids.size
-        assert np.array_equal(ids[base:base + m], oids.astype(np.uint32)), f"view {v}: sorted ids differ"
         tile_of = np.repeat(np.arange(tiles, dtype=np.uint64), np.diff(off).astype(np.int64))
         dbits = bits(oprojs[v]["rec"][oids, 9]).astype(np.uint64)
         exp_keys = ((np.uint64(v * tiles) + tile_of) << np.uint64(32)) | dbits
         assert np.array_equal(keys[base:base + m], exp_keys), f"view {v}: sorted keys differ"
         full = np.diff(off) > 0      # an empty tile only has to have start == end
         assert np.array_equal(ranges[v][full, 0], (off[:-1][full] + base).astype(np.uint32)), f"view {v}: range starts"
-        assert np.array_equal(ranges[v][full, 1], (off[1:][full] + base).astype(np.uint32)), f"view {v}: range ends"
         assert np.array_equal(ranges[v][~full, 0], ranges[v][~full, 1]), f"view {v}: empty tiles"
+        if not budget:
+            assert np.array_equal(ids[base:base + m], oids.astype(np.uint32)), f"view {v}: sorted ids differ"
+            assert np.array_equal(ranges[v][full, 1], (off[1:][full] + base).astype(np.uint32)), f"view {v}: ends"
+        else:
+            # pruned: each tile's kept ids at the start of its range, in list order
+            offp, oidsp = oracle.tile_lists(oprojs[v], cam, budget=budget)
+            lenp = np.diff(offp)
+            assert np.array_equal(ranges[v][full, 1] - ranges[v][full, 0], lenp[full].astype(np.uint32)), \
+                f"view {v}: pruned lengths"
+            pos = np.repeat(off[:-1] + base - offp[:-1], lenp) + np.arange(offp[-1])
+            assert np.array_equal(ids[pos], oidsp.astype(np.uint32)), f"view {v}: pruned ids differ"
+            stats.setdefault("pruned_tiles", []).append(int((np.diff(off) > budget).sum()))
+            stats.setdefault("pruned_entries", []).append(int(m - offp[-1]))
         base += m
     assert base == N
     stats["instances"] = int(N)

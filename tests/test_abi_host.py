@@ -94,6 +94,9 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
                                       16, None) == abi.GS_ERR_INVALID_ARG
     assert L.gs_raster_backward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, 16, None,
                                       16, None) == abi.GS_ERR_INVALID_ARG
+    # pruning: budget >= 1
+    assert L.gs_prune_tiles(ctypes.byref(proj), 10, 1, 64, 64, 0, 16, 16, None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_prune_tiles(ctypes.byref(proj), 10, 1, 64, 64, 8, 16, None, None) == abi.GS_ERR_INVALID_ARG
     # D-SSIM: 0 <= lambda <= 1, at least one pixel and one view
     for lam, V, W, H in ((-0.1, 1, 8, 8), (1.5, 1, 8, 8), (float("nan"), 1, 8, 8), (0.2, 0, 8, 8), (0.2, 1, 0, 8),
                          (0.2, 33, 8, 8)):
