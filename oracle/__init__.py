@@ -252,3 +252,33 @@ def train_step(scene, targets, state, t, lr_rows, betas, eps, mode=1, prec="f32"
     adam_deferred(state["params"], state["m"], state["v"], g, state["last_step"], lr, union, t,
                   betas[0], betas[1], eps, prec=prec)
     return dict(views=views, grads=grads, union=union)
+
+
+def render_subsets(proj, cam, opts, splits, prec="f32"):
+    """Partial renders of disjoint depth slabs (Splaxel, English abstract: each part
+    renders its local subset of Gaussians; the partial pixel values are composed).
+
+    splits: ascending depths z_1 < ... < z_{S-1}; slab s holds the visible Gaussians
+    with z_s <= depth < z_{s+1} (z_0 = -inf, z_S = +inf).  Each slab is rendered on
+    its own with a zero background.  Returns a list of (C [3,H,W], T [H,W])."""
+    z = np.concatenate([[-np.inf], np.asarray(splits, np.float64), [np.inf]])
+    depth = proj["rec"][:, 9].astype(np.float64)
+    parts = []
+    for s in range(z.size - 1):
+        sub = dict(proj)
+        sub["visible"] = (proj["visible"].astype(bool) & (depth >= z[s]) & (depth < z[s + 1])).astype(np.uint8)
+        out = render(sub, cam, dict(opts, bg=(0.0, 0.0, 0.0)), prec=prec, want_tfinal=True)
+        parts.append((out["image"], out["t_final"]))
+    return parts
+
+
+def compose(parts, bg):
+    """Front-to-back composition of partial renders, in fp64:
+    C = sum_s (prod_{j<s} T_j) C_s + (prod_s T_s) bg, T = prod_s T_s."""
+    C = np.zeros(parts[0][0].shape, np.float64)
+    T = np.ones(parts[0][1].shape, np.float64)
+    for Cs, Ts in parts:
+        C += T[None] * Cs.astype(np.float64)
+        T *= Ts.astype(np.float64)
+    C += T[None] * np.asarray([float(np.float32(b)) for b in bg], np.float64)[:, None, None]
+    return C, T
