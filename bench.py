@@ -408,6 +408,48 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
+def run_partial(args):
+    """Forward render as S depth slabs rendered on their own and composed, against the
+    one-pass forward render of the same scene (both: projection, binning, raster)."""
+    import torch
+    from differentiable_rasterizer_gb300 import build as gs_build, pipeline, scenes
+    torch.cuda.set_device(0)
+    gs_build.build()
+    sc = scenes.make_scene(args.config)
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda")
+    S = args.partial
+    tr.project()
+    splits = []
+    for v in range(tr.V):
+        d = tr.depth[v][tr.tiles_touched[v] > 0].double().sort().values
+        splits.append([float(np.float32(d[int(len(d) * s / S)].item())) for s in range(1, S)])
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    one_ms = timed(lambda: tr.render())
+    one = tr.image.clone()
+    part_ms = timed(lambda: tr.render_partial(splits))
+    diff = float((tr.image - one).abs().max())
+    line = {"metric": "partial render + compose: ms per forward render (projection, binning, raster)",
+            "value": part_ms, "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "dtype": "f32", "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOADS[args.config], "subsets": S, "split": "per-view depth quantiles"},
+            "one_pass_ms": one_ms, "max_abs_diff_vs_one_pass": diff,
+            "gpu_launches_note": "slab sub-ranges 1 + S forward rasters + compose 1 on top of the one-pass launches"}
+    print(json.dumps(line), flush=True)
+
+
 def cpu_baseline(sc, args):
     """The oracle timed on a bounded sample (a band of rows) of the same workload, one core."""
     rows = args.cpu_rows
@@ -429,6 +471,8 @@ def main():
     ap.add_argument("--config", default="medium", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partial", type=int, default=None, metavar="S",
+                    help="time the forward render as S depth slabs rendered separately and composed")
     ap.add_argument("--tile-budget", type=int, default=None, metavar="K",
                     help="prune every tile list to its K most opaque entries before rasterizing")
     ap.add_argument("--dssim", type=float, default=None, metavar="LAMBDA",
@@ -441,6 +485,9 @@ def main():
         if int(os.environ.get("RANK", "0")) != 0:
             return
         run_reference(args)
+        return
+    if args.partial:
+        run_partial(args)
         return
     run_gpu(args)
 

@@ -24,7 +24,7 @@ GS_GRAD2D_STRIDE = 12
 
 EXPORTS = ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
            "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_grad_compact_static",
-           "gs_prune_tiles",
+           "gs_prune_tiles", "gs_split_ranges", "gs_compose",
            "gs_error_string", "gs_param_rows", "gs_param_stride", "gs_num_tiles", "gs_version")
 
 
@@ -80,8 +80,11 @@ def lib():
         L.gs_raster_backward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
                                                _P, _P]
         L.gs_prune_tiles.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I32, _P, _P, _P]
+        L.gs_split_ranges.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
+        L.gs_compose.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
         for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
-                     "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_prune_tiles"):
+                     "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_prune_tiles",
+                     "gs_split_ranges", "gs_compose"):
             getattr(L, name).restype = ctypes.c_int
         L.gs_error_string.argtypes = [ctypes.c_int]
         L.gs_error_string.restype = ctypes.c_char_p
@@ -162,6 +165,20 @@ def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, targ
 def gs_prune_tiles(proj, n, n_views, width, height, budget, ids, tile_ranges, stream):
     _check("gs_prune_tiles", lib().gs_prune_tiles(ctypes.byref(proj), n, n_views, width, height, budget, ids,
                                                   tile_ranges, stream))
+
+
+def gs_split_ranges(keys, tile_ranges, n_views, width, height, n_subsets, depth_splits, sub_ranges, stream):
+    """depth_splits: host sequence [V][S-1] (converted to fp32)."""
+    flat = [float(z) for row in depth_splits for z in row] if n_subsets > 1 else []
+    arr = (ctypes.c_float * max(1, len(flat)))(*flat)
+    _check("gs_split_ranges", lib().gs_split_ranges(keys, tile_ranges, n_views, width, height, n_subsets,
+                                                    arr if flat else None, sub_ranges, stream))
+
+
+def gs_compose(c_parts, t_parts, n_subsets, n_views, width, height, bg, image, t_final, stream):
+    bga = (ctypes.c_float * 3)(*[float(b) for b in bg])
+    _check("gs_compose", lib().gs_compose(c_parts, t_parts, n_subsets, n_views, width, height, bga, image, t_final,
+                                          stream))
 
 
 def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, eval_counts,

@@ -20,7 +20,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgs_gb300.so")
-SOURCES = ["abi.cu", "project.cu", "binsort.cu", "prune.cu", "raster.cu", "dssim.cu", "compact.cu", "adam.cu"]
+SOURCES = ["abi.cu", "project.cu", "binsort.cu", "prune.cu", "raster.cu", "dssim.cu", "compose.cu", "compact.cu", "adam.cu"]
 HEADERS = ["gs_common.cuh", "project_math.cuh", "scan.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -55,6 +55,7 @@ class GaussianTrainer:
         self.tiles = abi.gs_num_tiles(self.W, self.H)
         self.cams = abi.cameras(cameras)
         self.opts = abi.render_opts(opts)
+        self._opts_dict = dict(opts)
         self.lr = tuple(float(x) for x in lr)
         self.betas = betas
         self.eps = eps
@@ -255,6 +256,38 @@ class GaussianTrainer:
         self.project(params)
         self.bin_sort()
         self.raster(None, count_evals=False)
+        return self.image
+
+    def render_partial(self, depth_splits, params=None):
+        """Forward only, as S = len(depth_splits[0]) + 1 depth slabs rendered on their own
+        (zero background) and composed front to back; returns the composed image.
+        depth_splits: [V][S-1] ascending positive depths.  The slabs' (C, T) stay in
+        self.c_parts [S, V, 3, H, W] and self.t_parts [S, V, H, W]."""
+        S = len(depth_splits[0]) + 1
+        V, H, W = self.V, self.H, self.W
+        dev = self.device
+        if getattr(self, "c_parts", None) is None or self.c_parts.shape[0] != S:
+            self.c_parts = torch.empty((S, V, 3, H, W), dtype=torch.float32, device=dev)
+            self.t_parts = torch.empty((S, V, H, W), dtype=torch.float32, device=dev)
+            self.l_parts = torch.empty((S, V, H, W), dtype=torch.int32, device=dev)
+            self.sub_ranges = torch.empty((S, V * self.tiles, 2), dtype=torch.int32, device=dev)
+            self.t_composed = torch.empty((V, H, W), dtype=torch.float32, device=dev)
+        budget, self.tile_budget = self.tile_budget, None   # slabs split the unpruned lists
+        try:
+            self.project(params)
+            self.bin_sort()
+        finally:
+            self.tile_budget = budget
+        sh = self.stream_handle()
+        abi.gs_split_ranges(self.keys.data_ptr(), self.ranges.data_ptr(), V, W, H, S, depth_splits,
+                            self.sub_ranges.data_ptr(), sh)
+        zero_bg = abi.render_opts(dict(self._opts_dict, bg=(0.0, 0.0, 0.0)))
+        for s in range(S):
+            abi.gs_raster_forward_state(self.proj, self.n, self.sub_ranges[s].data_ptr(), self.ids.data_ptr(),
+                                        self.cams, V, zero_bg, self.c_parts[s].data_ptr(),
+                                        self.t_parts[s].data_ptr(), self.l_parts[s].data_ptr(), None, sh)
+        abi.gs_compose(self.c_parts.data_ptr(), self.t_parts.data_ptr(), S, V, W, H, self._opts_dict["bg"],
+                       self.image.data_ptr(), self.t_composed.data_ptr(), sh)
         return self.image
 
     def flush(self):

@@ -244,6 +244,39 @@ GS_API gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const 
                                           const gs_render_opts* opts, const float* t_final, const int32_t* last_idx,
                                           const float* dldc, float* grad2d, uint8_t* touched, void* stream);
 
+/* ---- Partial render + compose (Splaxel, English abstract: each part renders
+ * its local subset of Gaussians; only partial pixel values -- colour and
+ * transmittance -- are exchanged and composed) ----
+ * Subsets are per-view depth slabs: slab s = the Gaussians with
+ * z_s <= depth < z_{s+1} (z_0 = 0, z_S = +inf).  A slab's entries in a tile are a
+ * contiguous part of the tile's sorted list, so a partial render is
+ * gs_raster_forward_state over the slab's sub-ranges with a zero background.
+ * Composing the slabs front to back regroups the one-pass compositing; it
+ * differs from the one-pass render only where a pixel stops before its last
+ * slab, by at most the transmittance at the stop (below t_min, or below
+ * t_min / (1 - alpha_max) with the crossing entry excluded) times the largest
+ * colour value. */
+
+/* Sub-ranges of every tile list per slab.
+ * keys, tile_ranges: gs_bin_sort's outputs (unpruned lists).  depth_splits: HOST
+ * [V][S-1] fp32, positive, finite and ascending per view.  sub_ranges:
+ * [S][V * tiles][2] u32 out (slab s of view v, tile t at (s * V + v) * tiles + t).
+ * 1 <= n_subsets <= 8.
+ * Errors: INVALID_ARG for bad pointers, sizes or splits; CUDA on launch failure. */
+GS_API gs_status gs_split_ranges(const uint64_t* keys, const uint32_t* tile_ranges, int32_t n_views, int32_t width,
+                                 int32_t height, int32_t n_subsets, const float* depth_splits, uint32_t* sub_ranges,
+                                 void* stream);
+
+/* Front-to-back composition of partial renders, per pixel in fp32 with fused
+ * multiply-adds: C = sum_s (prod_{j<s} T_j) C_s + (prod_s T_s) bg,
+ * T = prod_s T_s.
+ * c_parts: [S][V][3][H][W]; t_parts: [S][V][H][W]; bg: HOST [3].
+ * image: [V][3][H][W] out; t_final: [V][H][W] out or NULL.  1 <= n_subsets <= 8.
+ * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
+GS_API gs_status gs_compose(const float* c_parts, const float* t_parts, int32_t n_subsets, int32_t n_views,
+                            int32_t width, int32_t height, const float* bg, float* image, float* t_final,
+                            void* stream);
+
 /* Sparse-gradient compaction ("encoder") and aggregation ("decoder"):
  * per view, idx[v] = ascending list of touched Gaussians, n_idx[v] its length;
  * idx[n_views] / n_idx[n_views] = the union over views.  For every Gaussian of

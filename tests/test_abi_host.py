@@ -97,6 +97,15 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     # pruning: budget >= 1
     assert L.gs_prune_tiles(ctypes.byref(proj), 10, 1, 64, 64, 0, 16, 16, None) == abi.GS_ERR_INVALID_ARG
     assert L.gs_prune_tiles(ctypes.byref(proj), 10, 1, 64, 64, 8, 16, None, None) == abi.GS_ERR_INVALID_ARG
+    # partial render + compose: 1..8 slabs, positive ascending splits
+    two = (ctypes.c_float * 2)(2.0, 1.0)
+    assert L.gs_split_ranges(16, 16, 1, 64, 64, 3, two, 16, None) == abi.GS_ERR_INVALID_ARG
+    neg = (ctypes.c_float * 1)(-1.0)
+    assert L.gs_split_ranges(16, 16, 1, 64, 64, 2, neg, 16, None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_split_ranges(16, 16, 1, 64, 64, 9, None, 16, None) == abi.GS_ERR_INVALID_ARG
+    bg = (ctypes.c_float * 3)(0, 0, 0)
+    assert L.gs_compose(16, 16, 0, 1, 64, 64, bg, 16, None, None) == abi.GS_ERR_INVALID_ARG
+    assert L.gs_compose(16, 16, 2, 1, 64, 64, None, 16, None, None) == abi.GS_ERR_INVALID_ARG
     # D-SSIM: 0 <= lambda <= 1, at least one pixel and one view
     for lam, V, W, H in ((-0.1, 1, 8, 8), (1.5, 1, 8, 8), (float("nan"), 1, 8, 8), (0.2, 0, 8, 8), (0.2, 1, 0, 8),
                          (0.2, 33, 8, 8)):
