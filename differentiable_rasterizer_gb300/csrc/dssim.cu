@@ -22,13 +22,14 @@
 //   P2 columns                     -> moments, S and its 3 derivatives (42 x 42)
 //   P3 rows of the derivative maps -> 3 x (42 x 32)
 //   P4 columns                     -> dL/dC on the 32 x 32 tile
-// The moments are taken of the images minus a per-CTA constant (the mean of the
-// loaded 52 x 52 region, padding included): variances and the covariance are
-// invariant to the shift, so s_xx = E[x'^2] - mu_x'^2 etc. with x' = x - c_x, and
-// in smooth or flat regions the cancellation that fp32 E[x^2] - mu_x^2 suffers
-// is gone.  With mu_x = mu_x' + c_x the derivatives by the shifted moments are
-//   dS/dmu_x' = (2 (mu_y B - A mu_y') - 2 S (mu_x D - C mu_x')) / (C D)
-// (the same two others), and the gradient uses x' and y' in place of x and y.
+// The second moments are taken of the images minus a per-CTA constant (the mean
+// of the in-image pixels of the loaded 52 x 52 region): variances and the covariance
+// are invariant to the shift, so s_xx = E[x'^2] - mu_x'^2 with x' = x - c_x and
+// mu_x' = mu_x - c_x sum(w), and in smooth or flat regions the cancellation that
+// fp32 E[x^2] - mu_x^2 suffers is gone.  The means themselves are plain window
+// sums of the (non-negative) images, accurate even where they are tiny next to a
+// dark region, and the derivative maps and their combination are the unshifted
+// formulas above, as in the definition.
 // fp32 throughout; the loss partial sums are fp64 (one atomic per CTA).
 #include "gs_common.cuh"
 
@@ -69,6 +70,7 @@ struct SsimArgs {
     int W, H, tiles_x;
     float w[ssim::kWin];                // normalised 1-D window
     float c1, c2;
+    float wsum;                         // sum of the 2-D window's fp32 weights (1 up to rounding)
     float l1_coef;                      // (1 - lambda) / N
     float ssim_coef;                    // -lambda / N (gradient of the SSIM term)
     double l1_coef_d, ssim_loss_coef_d; // (1 - lambda) / N, lambda / N
@@ -135,8 +137,14 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
         cx += s_c[0][w];
         cy += s_c[1][w];
     }
-    cx = cx * (1.0f / (float)(kTI * kTI));
-    cy = cy * (1.0f / (float)(kTI * kTI));
+    {
+        // in-image pixels of the region (at least the tile's first pixel)
+        const int rows = min(oy + kTO + 2 * kR, a.H) - max(oy - 2 * kR, 0);
+        const int cols = min(ox + kTO + 2 * kR, a.W) - max(ox - 2 * kR, 0);
+        const float inv = 1.0f / (float)(rows * cols);
+        cx = cx * inv;
+        cy = cy * inv;
+    }
     // this thread's P4 outputs: column tid % 32, rows 4 (tid / 32) .. + 3
     const int c4 = threadIdx.x % kTO, r4 = (threadIdx.x / kTO) * kK4;
     float ox4[kK4], oy4[kK4];
@@ -147,7 +155,7 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
         oy4[j] = v2.y;
     }
 
-    // P1: horizontal window sums of x', y', x'^2, y'^2, x'y'
+    // P1: horizontal window sums of x, y, x'^2, y'^2, x'y'
     constexpr int kRuns1 = kTM / kK1;
     for (int it = threadIdx.x; it < kTI * kRuns1; it += kThreads) {
         const int r = it / kRuns1, c0 = (it - r * kRuns1) * kK1;
@@ -159,8 +167,9 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
 #pragma unroll
         for (int t = 0; t < kK1 + 2 * kR; ++t) {
             const float2 v2 = sxy[r * kTI + c0 + t];
-            const float x = v2.x - cx, y = v2.y - cy;
-            const float xx = x * x, yy = y * y, xy = x * y;
+            const float x = v2.x, y = v2.y;
+            const float xs = x - cx, ys = y - cy;
+            const float xx = xs * xs, yy = ys * ys, xy = xs * ys;
 #pragma unroll
             for (int j = 0; j < kK1; ++j) {
                 const int k = t - j;
@@ -208,8 +217,8 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
             const int gy = oy - kR + r;
             float dmu = 0.0f, dxx = 0.0f, dxy = 0.0f;
             if (gy >= 0 && gy < a.H && gx >= 0 && gx < a.W) {
-                const float mxs = m[0][j], mys = m[1][j];          // shifted means
-                const float mx = mxs + cx, my = mys + cy;
+                const float mx = m[0][j], my = m[1][j];
+                const float mxs = mx - cx * a.wsum, mys = my - cy * a.wsum;   // means of x', y'
                 const float A = 2.0f * (mx * my) + a.c1;
                 const float B = 2.0f * (m[4][j] - mxs * mys) + a.c2;
                 const float C = (mx * mx + my * my) + a.c1;
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
                 const float rC = rcp_approx(C), rD = rcp_approx(D);
                 const float inv = rC * rD;
                 const float S = (A * B) * inv;
-                dmu = (2.0f * (my * B - A * mys) - 2.0f * S * (mx * D - C * mxs)) * inv;
+                dmu = (2.0f * my * (B - A) - 2.0f * mx * S * (D - C)) * inv;
                 dxx = -S * rD;
                 dxy = 2.0f * A * inv;
                 if (r >= kR && r < kR + kTO && c >= kR && c < kR + kTO) ssum += (double)(1.0f - S);
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
                 const float x = ox4[j], y = oy4[j];
                 const float d = x - y;
                 const float sgn = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
-                const float gs = b[0][j] + 2.0f * (x - cx) * b[1][j] + (y - cy) * b[2][j];
+                const float gs = b[0][j] + 2.0f * x * b[1][j] + y * b[2][j];
                 a.dldc[plane + (size_t)gy * a.W + gx] = __fmaf_rn(a.ssim_coef, gs, sgn * a.l1_coef);
                 l1sum += (double)fabsf(d);
             }
@@ -328,7 +337,12 @@ extern "C" gs_status gs_dssim_loss_grad(const float* image, const float* target,
         g[i] = exp(-t * t / (2.0 * 1.5 * 1.5));
         gsum += g[i];
     }
-    for (int i = 0; i < kWin; ++i) a.w[i] = (float)(g[i] / gsum);
+    double ws = 0.0;
+    for (int i = 0; i < kWin; ++i) {
+        a.w[i] = (float)(g[i] / gsum);
+        ws += (double)a.w[i];
+    }
+    a.wsum = (float)(ws * ws);
     a.c1 = (float)(0.01 * 0.01);
     a.c2 = (float)(0.03 * 0.03);
     const double N = 3.0 * (double)width * (double)height;

@@ -317,8 +317,11 @@ def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, de
 #   (w * dS/dmu_x + 2 x (w * dS/dE[x^2]) + y (w * dS/dE[xy])) / N that cancel
 #   where x is close to y, so its relative error is taken against the sum of the
 #   terms' magnitudes M (w * |dS/dmu_x| + 2|x| (w * |dS/dE[x^2]|) + |y| (w * |dS/dE[xy]|)):
-#   |gpu - oracle| <= GRAD_RTOL * lambda / N * M + 4 u |oracle|; the L1 part is a
-#   signed constant that must be exact.
+#   |gpu - oracle| <= GRAD_RTOL * lambda / N * M + 4 u |oracle| + 1e-6 max|oracle|;
+#   the L1 part is a signed constant that must be exact.  The last term is the
+#   gradient bar's absolute floor relative to the map's scale: where the image and
+#   the target are equal over a whole window M is 0, but the kernel's mean-centred
+#   form leaves a residual of rounding size.
 _U = 2.0 ** -24
 
 
@@ -338,7 +341,7 @@ def dssim_reference(x, y, lam):
     dldc = l1_part - lam * g_ssim
     M = dssim.wsum(np.abs(t["d_mu"])) + 2 * np.abs(x) * dssim.wsum(np.abs(t["d_exx"])) \
         + np.abs(y) * dssim.wsum(np.abs(t["d_exy"]))
-    tol = GRAD_RTOL * lam / N * M + 4 * _U * np.abs(dldc)
+    tol = GRAD_RTOL * lam / N * M + 4 * _U * np.abs(dldc) + 1e-6 * float(np.abs(dldc).max())
     tol_loss = lam * IMG_ATOL + (1.0 - lam) * _U * l1 + 1e-12 * abs(loss)
     return dict(loss=loss, dldc=dldc, tol=tol, tol_loss=tol_loss, M=lam / N * M)
 
@@ -416,4 +419,66 @@ def run_dssim_parity(sc, lam=0.2, targets=None, device="cuda", log=print):
     stats["grads"] = st
     assert ok, f"dense gradients out of tolerance {st}"
     log(f"[dssim parity] {sc.name} lambda={lam}: {stats}")
+    return stats
+
+
+# ----------------------------------------------------------------------------- partial render + compose
+def depth_splits(sc, S):
+    """Per view: S - 1 fp32 depth quantiles of the visible Gaussians."""
+    out = []
+    for cam in sc.cameras:
+        pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
+        d = pr["rec"][pr["visible"] > 0, 9].astype(np.float64)
+        z = np.unique(np.quantile(d, np.arange(1, S) / S).astype(np.float32)) if S > 1 else np.zeros(0, np.float32)
+        assert z.size == S - 1
+        out.append([float(x) for x in z])
+    return out
+
+
+def run_compose_parity(sc, S):
+    """Partial render + compose of S depth slabs against the oracle: slab sub-ranges,
+    each slab's (C, T), the composition, and the one-pass render within the stop bound."""
+    splits = depth_splits(sc, S)
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr)
+    img = tr.render_partial(splits).clone()
+    torch.cuda.synchronize()
+    cparts = tr.c_parts.cpu().numpy()
+    tparts = tr.t_parts.cpu().numpy()
+    sub = tr.sub_ranges.cpu().numpy().view(np.uint32).reshape(S, sc.n_views, -1, 2)
+    ids = tr.ids.cpu().numpy().view(np.uint32)
+    tcomp = tr.t_composed.cpu().numpy()
+    img = img.cpu().numpy()
+    stats = {}
+    for v, cam in enumerate(sc.cameras):
+        pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
+        parts = oracle.render_subsets(pr, cam, sc.opts, splits[v])
+        z = np.concatenate([[-np.inf], np.asarray(splits[v], np.float64), [np.inf]])
+        depth = pr["rec"][:, 9].astype(np.float64)
+        for s in range(S):
+            # the slab's tile lists
+            slab = dict(pr, visible=(pr["visible"].astype(bool) & (depth >= z[s]) & (depth < z[s + 1])).astype(np.uint8))
+            off, oids = oracle.tile_lists(slab, cam)
+            r = sub[s, v].astype(np.int64)
+            assert np.array_equal(r[:, 1] - r[:, 0], np.diff(off)), f"view {v} slab {s}: sub-range lengths"
+            pos = np.repeat(r[:, 0] - off[:-1], np.diff(off)) + np.arange(off[-1])
+            assert np.array_equal(ids[pos], oids.astype(np.uint32)), f"view {v} slab {s}: sub-range ids"
+            if s + 1 < S:
+                assert np.array_equal(r[:, 1], sub[s + 1, v][:, 0]), "slabs must tile the list"
+            # the slab's partial render
+            Cs, Ts = parts[s]
+            assert np.abs(cparts[s, v].astype(np.float64) - Cs).max() <= IMG_ATOL, f"view {v} slab {s}: C"
+            assert np.abs(tparts[s, v].astype(np.float64) - Ts).max() <= 1e-6, f"view {v} slab {s}: T"
+        C, T = oracle.compose(parts, sc.opts["bg"])
+        d = np.abs(img[v].astype(np.float64) - C)
+        assert d.max() <= IMG_ATOL, f"view {v}: composed image {d.max()}"
+        assert np.abs(tcomp[v] - T).max() <= 1e-6
+        one = oracle.render(pr, cam, sc.opts)["image"].astype(np.float64)
+        cmax = max(float(pr["rec"][pr["visible"] > 0, 6:9].max(initial=0.0)), max(sc.opts["bg"]))
+        # T where a pixel stops: below t_min, or (crossing entry excluded) below t_min / (1 - alpha_max)
+        t_stop = sc.opts["t_min"] / ((1.0 - sc.opts["alpha_max"]) if sc.opts.get("exclude_crossing") else 1.0)
+        d1 = np.abs(img[v].astype(np.float64) - one)
+        assert d1.max() <= t_stop * cmax + IMG_ATOL, f"view {v}: vs one pass {d1.max()}"
+        stats.setdefault("vs_one_pass_max", []).append(float(d1.max()))
+        stats.setdefault("vs_compose_max", []).append(float(d.max()))
+    print(f"[compose parity] {sc.name} S={S}: {stats}")
     return stats
