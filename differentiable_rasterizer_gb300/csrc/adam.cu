@@ -4,7 +4,8 @@
 // equal to dense Adam by replaying the skipped zero-gradient steps first.
 //
 // Work unit: a (listed Gaussian, float4 chunk of its [stride] parameter block)
-// pair, 16 contiguous bytes of params, m, v and grads; a grid of resident
+// pair, 16 contiguous bytes of params, m, v and grads (grads only read: the
+// decoder overwrites a Gaussian's block in the step it lists it); a grid of resident
 // blocks strides over the units.  Elements with a zero gradient on a zero state
 // are exact no-ops and skip the arithmetic.  The bias
 // corrections of the current step come from the host (the same fp64 binary
@@ -125,7 +126,6 @@ __global__ void __launch_bounds__(256, 5) adam_deferred_kernel(AdamArgs a)
         *reinterpret_cast<float4*>(a.params + off) = p;
         *reinterpret_cast<float4*>(a.m + off) = m;
         *reinterpret_cast<float4*>(a.v + off) = v;
-        if (!kFlush) *reinterpret_cast<float4*>(a.grads + off) = zero;
     }
 }
 

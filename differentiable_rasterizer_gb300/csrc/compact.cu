@@ -6,9 +6,9 @@
 //   per view v: idx[v] = ascending list of Gaussians with touched[v][g] != 0
 //   union:      idx[V] = ascending list of Gaussians touched in any view
 //   decode:     for each Gaussian of the union, the projection VJP of every
-//               touching view is summed in view order in registers and added to
-//               the dense gradient with one read-modify-write of the Gaussian's
-//               block ([n][stride] layout, float4 accesses); the consumed
+//               touching view is summed in view order in registers and written
+//               as the Gaussian's dense gradient block ([n][stride] layout,
+//               float4 stores; other blocks are not touched); the consumed
 //               grad2d / touched entries are cleared.
 // With one owner (this GPU) no record leaves the device, so the "send" of the
 // encoded list is the list itself.
@@ -39,26 +39,19 @@ struct VjpArgs {
     float* __restrict__ grads;
 };
 
-// Projection VJP of Gaussian g summed over its touching views, added to its
-// dense gradient block; the consumed grad2d / touched entries are cleared.
+// Projection VJP of Gaussian g summed over its touching views, written as its
+// dense gradient block (write only: the block's previous contents are not
+// read); the consumed grad2d / touched entries are cleared.
 template <int DEG>
 __device__ __forceinline__ void vjp_gaussian(const VjpArgs& a, const CamSet& cs, int64_t g)
 {
     GaussParams<DEG> gp;
     gp.load(a.params, g);
-    // Current gradient values are loaded up front with the parameters, so the
-    // write-back is a run of independent stores.
     constexpr int kVec = GaussParams<DEG>::kVec;
     float4* gdst = reinterpret_cast<float4*>(a.grads + (size_t)g * GaussParams<DEG>::kStride);
     float grad[kVec * 4];
 #pragma unroll
-    for (int i = 0; i < kVec; ++i) {
-        const float4 t = gdst[i];
-        grad[4 * i] = t.x;
-        grad[4 * i + 1] = t.y;
-        grad[4 * i + 2] = t.z;
-        grad[4 * i + 3] = t.w;
-    }
+    for (int i = 0; i < kVec * 4; ++i) grad[i] = 0.0f;
     for (int v = 0; v < cs.n_views; ++v) {
         const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
         if (!a.touched[o]) continue;

@@ -11,7 +11,8 @@ gs_raster_backward_state (the SSIM window reaches into neighbouring tiles).
 
 Buffer layout in HBM (fp32 unless stated):
     params, grads, adam_m, adam_v   [n, stride]      stride = 16 (RGB, P = 14) or 64 (SH 3, P = 59);
-                                                     one aligned block per Gaussian
+                                                     one aligned block per Gaussian (grads: valid for
+                                                     the Gaussians of the current step's union only)
     last_step                       [n] int32
     rec                             [V, n, 12]       3 float4 per (view, Gaussian)
     depth, tiles_touched, rect      [V, n], [V, n], [V, n, 4] uint16

@@ -281,10 +281,11 @@ GS_API gs_status gs_compose(const float* c_parts, const float* t_parts, int32_t 
  * per view, idx[v] = ascending list of touched Gaussians, n_idx[v] its length;
  * idx[n_views] / n_idx[n_views] = the union over views.  For every Gaussian of
  * the union the projection VJP of each touching view is summed in view order
- * and added to grads (one read-modify-write per Gaussian).  grad2d and touched
- * are cleared for the entries consumed.
+ * and written as its gradient block (write only; the blocks of Gaussians
+ * outside the union are not touched, so they keep whatever an earlier step
+ * left there).  grad2d and touched are cleared for the entries consumed.
  * idx: [(n_views + 1) * n] u32 out; n_idx: [n_views + 1] int64 DEVICE out.
- * grads: [n][stride] fp32 accumulated (+=).  cams/opts: HOST, as given to gs_project.
+ * grads: [n][stride] fp32 out (union blocks only).  cams/opts: HOST, as given to gs_project.
  * Errors: INVALID_ARG for bad pointers, sizes or a too small workspace. */
 GS_API gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const float* params, int64_t n, int32_t sh_degree,
                           const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
@@ -317,7 +318,8 @@ GS_API gs_status gs_grad_compact_static(float* grad2d, uint8_t* touched, const f
 
 /* Deferred Adam (dense-equivalent).  For every listed Gaussian g with
  * s = last_step[g] < t: the skipped zero-gradient steps j = s+1 .. t-1 are
- * replayed, then step t uses grads; last_step[g] = t and grads[:, g] = 0.
+ * replayed, then step t uses grads; last_step[g] = t.  grads is only read (the
+ * listed Gaussians' blocks, as gs_grad_compact wrote them this step).
  * One step: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
  *           p -= lr * ((m / bc1) / (sqrt(v / bc2) + eps)),
  * bc = 1 - beta^j with beta^j by binary exponentiation in fp64, rounded to fp32.

@@ -191,7 +191,6 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
         assert np.array_equal(bits(tr.rows(tr.adam_m).cpu().numpy()), bits(m_o)), "Adam m"
         assert np.array_equal(bits(tr.rows(tr.adam_v).cpu().numpy()), bits(v_o)), "Adam v"
         assert np.array_equal(tr.last_step.cpu().numpy(), last_o), "last_step"
-        assert not tr.grads.any().item(), "grads not cleared"
     log(f"[parity] {sc.name}: {stats}")
     return stats
 
