@@ -75,10 +75,11 @@ def lib():
         L.gs_grad_compact.argtypes = [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P,
                                       ctypes.POINTER(ctypes.c_size_t), _P]
         L.gs_adam_deferred.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _P, _P, _I32, _P, _F, _F, _F, _I32, _P]
-        L.gs_raster_forward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P]
+        L.gs_raster_forward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P,
+                                              _P, _P]
         L.gs_dssim_loss_grad.argtypes = [_P, _P, _I32, _I32, _I32, _F, _P, _P, _P]
         L.gs_raster_backward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
-                                               _P, _P]
+                                               _P, _P, _P, _P]
         L.gs_prune_tiles.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.gs_split_ranges.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.gs_compose.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
@@ -181,11 +182,11 @@ def gs_compose(c_parts, t_parts, n_subsets, n_views, width, height, bg, image, t
                                           stream))
 
 
-def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, eval_counts,
-                            stream):
+def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, pass_bits,
+                            bits_chunk, eval_counts, stream):
     _check("gs_raster_forward_state",
            lib().gs_raster_forward_state(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
-                                         image, t_final, last_idx, eval_counts, stream))
+                                         image, t_final, last_idx, pass_bits, bits_chunk, eval_counts, stream))
 
 
 def gs_dssim_loss_grad(image, target, n_views, width, height, lam, loss, dldc, stream):
@@ -193,11 +194,11 @@ def gs_dssim_loss_grad(image, target, n_views, width, height, lam, loss, dldc, s
                                                           stream))
 
 
-def gs_raster_backward_state(proj, n, tile_ranges, ids, cams, n_views, opts, t_final, last_idx, dldc, grad2d, touched,
-                             stream):
+def gs_raster_backward_state(proj, n, tile_ranges, ids, cams, n_views, opts, t_final, last_idx, pass_bits, bits_chunk,
+                             dldc, grad2d, touched, stream):
     _check("gs_raster_backward_state",
            lib().gs_raster_backward_state(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
-                                          t_final, last_idx, dldc, grad2d, touched, stream))
+                                          t_final, last_idx, pass_bits, bits_chunk, dldc, grad2d, touched, stream))
 
 
 def gs_grad_compact_ws_bytes(n) -> int:

@@ -59,6 +59,8 @@ struct RasterArgs {
     const float* __restrict__ dldc;     // [V][3][H][W]: dL/dC (backward from stored state)
     float* t_final;                     // [V][H][W]: final transmittance per pixel, or null
     int32_t* last_idx;                  // [V][H][W]: last composited list index per pixel (-1: none)
+    uint32_t* bits;                     // [V * tiles][kWords][256]: pass bits of one chunk per tile, or null
+    int32_t* bits_chunk;                // [V * tiles]: the chunk those bits belong to (-1: none)
     float* image;                       // [V][3][H][W]
     double* loss;                       // [V]
     float* grad2d;                      // [V][n][12]
@@ -412,6 +414,19 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         }
         s_max_last[0] = ml;
     }
+    if (kMode == kFwd && a.bits) {
+        // Keep the pass bits of the chunk holding the tile's last composited entry
+        // (where a backward from this state starts), if the ring still has them.
+        __syncthreads();
+        const int cl = s_max_last[0] >= 0 ? s_max_last[0] / kChunk : -1;
+        const bool keep = cl >= 0 && cl >= resident - kRing + 1;
+        uint32_t* dst = a.bits + (size_t)tile_lin * kWords * kTileThreads;
+        if (keep) {
+#pragma unroll
+            for (int w = 0; w < kWords; ++w) dst[w * kTileThreads + threadIdx.x] = s_bits[cl % kRing][w][threadIdx.x];
+        }
+        if (threadIdx.x == 0) a.bits_chunk[tile_lin] = keep ? cl : -1;
+    }
     if (!kBackward) return;
     __syncthreads();
     // the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
@@ -419,6 +434,16 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const int last_fwd = kMode == kBwdState ? INT32_MAX / 2 : resident;
     const int max_last = s_max_last[0];
     if (max_last < 0) return;
+    // backward from a stored state: the chunk whose pass bits the forward kept
+    int c_kept = -1;
+    if (kMode == kBwdState && a.bits) {
+        c_kept = a.bits_chunk[tile_lin];
+        if (c_kept >= 0) {
+            const uint32_t* src = a.bits + (size_t)tile_lin * kWords * kTileThreads;
+#pragma unroll
+            for (int w = 0; w < kWords; ++w) s_bits[c_kept % kRing][w][threadIdx.x] = src[w * kTileThreads + threadIdx.x];
+        }
+    }
 
     // ------------------------------------------------------------- backward
     // dL/dC . (colour composited behind the next entry to visit), per pixel
@@ -432,7 +457,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         if (c != resident) {
             __syncthreads();   // the previous chunk's records are no longer read
             stage(base);
-            if (c <= last_fwd - kRing) {
+            if (kMode == kBwdState ? c != c_kept : c <= last_fwd - kRing) {
                 // pass bits no longer in the ring: recompute them for the pixels
                 // that composited an entry of this chunk
                 const uint32_t skip = __ballot_sync(0xffffffffu, last < base);
@@ -678,16 +703,19 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
 extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                              const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                              const gs_render_opts* opts, float* image, float* t_final,
-                                             int32_t* last_idx, uint64_t* eval_counts, void* stream)
+                                             int32_t* last_idx, uint32_t* pass_bits, int32_t* bits_chunk,
+                                             uint64_t* eval_counts, void* stream)
 {
     RasterArgs a;
     long long grid = 0;
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
     if (st != GS_OK) return st;
-    if (!image || !t_final || !last_idx) return GS_ERR_INVALID_ARG;
+    if (!image || !t_final || !last_idx || (pass_bits && !bits_chunk)) return GS_ERR_INVALID_ARG;
     a.image = image;
     a.t_final = t_final;
     a.last_idx = last_idx;
+    a.bits = pass_bits;
+    a.bits_chunk = bits_chunk;
     a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
     raster_fused_kernel<kFwd><<<(unsigned)grid, kTileThreads, 0, (cudaStream_t)stream>>>(a);
     GS_LAUNCH_CHECK();
@@ -697,7 +725,8 @@ extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, con
 extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                               const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                               const gs_render_opts* opts, const float* t_final,
-                                              const int32_t* last_idx, const float* dldc, float* grad2d,
+                                              const int32_t* last_idx, const uint32_t* pass_bits,
+                                              const int32_t* bits_chunk, const float* dldc, float* grad2d,
                                               uint8_t* touched, void* stream)
 {
     RasterArgs a;
@@ -705,6 +734,9 @@ extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, co
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
     if (st != GS_OK) return st;
     if (!t_final || !last_idx || !dldc || (n > 0 && (!grad2d || !touched))) return GS_ERR_INVALID_ARG;
+    if (pass_bits && !bits_chunk) return GS_ERR_INVALID_ARG;
+    a.bits = const_cast<uint32_t*>(pass_bits);
+    a.bits_chunk = const_cast<int32_t*>(bits_chunk);
     if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
     a.t_final = const_cast<float*>(t_final);
     a.last_idx = const_cast<int32_t*>(last_idx);

@@ -206,19 +206,26 @@ GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const u
  *   gs_raster_forward_state   image + per-pixel final T and last index
  *   gs_dssim_loss_grad        loss and dL/dC from image and target
  *   gs_raster_backward_state  backward from the stored state and dL/dC
- * The backward recomputes the pass bits of every chunk (the fused kernel keeps
- * the last three on chip), otherwise it is the fused kernel's backward. */
+ * The backward reuses the pass bits of the chunk it starts in (stored by the
+ * forward) and recomputes older chunks' (the fused kernel keeps the last three
+ * on chip); otherwise it is the fused kernel's backward. */
 
 /* Forward rasterization as in gs_raster_fused_fwd_bwd without a target, that
  * also stores per pixel the final transmittance and the last composited list
- * index (-1 if none).
+ * index (-1 if none), and optionally, per tile, the pass bits of the chunk of
+ * 256 list entries that holds the tile's last composited entry (the backward
+ * starts there and reuses them instead of recomputing them).
  * image: [V][3][H][W] out.  t_final: [V][H][W] fp32 out.  last_idx: [V][H][W]
- * int32 out.  eval_counts: NULL or [3] u64 accumulated (+=), as for the fused call.
+ * int32 out.  pass_bits: NULL or [V * tiles][8][256] u32 out (bit j of word w of
+ * pixel p: entry 32 w + j of that chunk passes at p); bits_chunk: [V * tiles]
+ * int32 out, the chunk they belong to, -1 if none (required with pass_bits).
+ * eval_counts: NULL or [3] u64 accumulated (+=), as for the fused call.
  * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
 GS_API gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                          const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                          const gs_render_opts* opts, float* image, float* t_final, int32_t* last_idx,
-                                         uint64_t* eval_counts, void* stream);
+                                         uint32_t* pass_bits, int32_t* bits_chunk, uint64_t* eval_counts,
+                                         void* stream);
 
 /* Loss (1 - lambda) L1 + lambda (1 - SSIM) per view and its gradient
  * dL/dC.  L1 = mean |image - target| over 3*H*W values; SSIM = mean over
@@ -235,14 +242,16 @@ GS_API gs_status gs_dssim_loss_grad(const float* image, const float* target, int
 /* Backward rasterization from a stored forward state: the pixels' composited
  * entries are walked back to front exactly as in gs_raster_fused_fwd_bwd, with
  * dL/dC taken from dldc instead of the L1 sign.  proj, tile lists, cams and
- * opts must be those of the gs_raster_forward_state call that wrote t_final
- * and last_idx.  dldc: [V][3][H][W].  grad2d, touched: as for the fused call
- * (accumulated; zero on entry).
+ * opts must be those of the gs_raster_forward_state call that wrote t_final,
+ * last_idx and (if given) pass_bits / bits_chunk; without them every chunk's
+ * pass bits are recomputed.  dldc: [V][3][H][W].  grad2d, touched: as for the
+ * fused call (accumulated; zero on entry).
  * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
 GS_API gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                           const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                           const gs_render_opts* opts, const float* t_final, const int32_t* last_idx,
-                                          const float* dldc, float* grad2d, uint8_t* touched, void* stream);
+                                          const uint32_t* pass_bits, const int32_t* bits_chunk, const float* dldc,
+                                          float* grad2d, uint8_t* touched, void* stream);
 
 /* ---- Partial render + compose (Splaxel, English abstract: each part renders
  * its local subset of Gaussians; only partial pixel values -- colour and
