@@ -76,14 +76,56 @@ struct SsimArgs {
     double l1_coef_d, ssim_loss_coef_d; // (1 - lambda) / N, lambda / N
 };
 
+// Two fp32 lanes in one 64-bit register, for Blackwell's packed fp32
+// instructions: each lane is an ordinary IEEE-rounded fp32 operation, so the
+// results are those of the scalar operations, at one issue slot per pair.
+typedef unsigned long long f2x;
+
+__device__ __forceinline__ f2x pack2(float a, float b)
+{
+    f2x r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(f2x v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ f2x fma2(f2x a, f2x b, f2x c)
+{
+    f2x d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2x mul2(f2x a, f2x b)
+{
+    f2x d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2x sub2(f2x a, f2x b)
+{
+    f2x d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
 {
     using namespace ssim;
+    // Shared-memory layout: pairs of quantities sit in one 8-byte slot so a
+    // pass loads them with one 64-bit access and updates them with one packed
+    // multiply-add.
     extern __shared__ float smem[];
-    float2* const sxy = reinterpret_cast<float2*>(smem);   // [kTI][kTI] (x, y)
-    float* const dm = smem;                       // [3][kTM][kTM] (after P1)
-    float* const h1 = smem + kSmemA;              // [5][kTI][kTM]
-    float* const h3 = smem + kSmemA;              // [3][kTM][kTO] (after P2)
+    f2x* const sxy = reinterpret_cast<f2x*>(smem);                 // [kTI][kTI] (x, y)
+    f2x* const dmp = reinterpret_cast<f2x*>(smem);                 // [kTM][kTM] (dS/dmu, dS/dE[x^2]) (after P1)
+    float* const dms = smem + 2 * kTM * kTM;                       // [kTM][kTM] dS/dE[xy]
+    f2x* const h1p = reinterpret_cast<f2x*>(smem + kSmemA);        // [2][kTI][kTM] (x, y), (x'^2, y'^2) sums
+    float* const h1s = smem + kSmemA + 4 * kTI * kTM;              // [kTI][kTM] x'y' sums
+    f2x* const h3p = reinterpret_cast<f2x*>(smem + kSmemA);        // [kTM][kTO] (after P2)
+    float* const h3s = smem + kSmemA + 2 * kTM * kTO;              // [kTM][kTO]
     __shared__ double s_red[kThreads / 32];
     __shared__ float s_c[2][kThreads / 32];
 
@@ -94,9 +136,12 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     const size_t plane = ((size_t)v * 3 + ch) * HW;
     const float* __restrict__ X = a.image + plane;
     const float* __restrict__ Y = a.target + plane;
+    f2x w2[kWin];                                 // the window weights, one per lane
+#pragma unroll
+    for (int k = 0; k < kWin; ++k) w2[k] = pack2(a.w[k], a.w[k]);
 
     // images on the tile + 10-pixel ring, zero outside (all loads issued before
-    // the first store); their means over the region
+    // the first store); their means over the region's in-image pixels
     float sumx = 0.0f, sumy = 0.0f;
     {
         float lx[kLoadIters], ly[kLoadIters];
@@ -116,7 +161,7 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
 #pragma unroll
         for (int k = 0; k < kLoadIters; ++k) {
             const int i = k * kThreads + threadIdx.x;
-            if (i < kTI * kTI) sxy[i] = make_float2(lx[k], ly[k]);
+            if (i < kTI * kTI) sxy[i] = pack2(lx[k], ly[k]);
             sumx += lx[k];
             sumy += ly[k];
         }
@@ -145,47 +190,53 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
         cx = cx * inv;
         cy = cy * inv;
     }
+    const f2x cxy = pack2(cx, cy);
     // this thread's P4 outputs: column tid % 32, rows 4 (tid / 32) .. + 3
     const int c4 = threadIdx.x % kTO, r4 = (threadIdx.x / kTO) * kK4;
     float ox4[kK4], oy4[kK4];
 #pragma unroll
     for (int j = 0; j < kK4; ++j) {
-        const float2 v2 = sxy[(r4 + j + 2 * kR) * kTI + c4 + 2 * kR];
+        const float2 v2 = unpack2(sxy[(r4 + j + 2 * kR) * kTI + c4 + 2 * kR]);
         ox4[j] = v2.x;
         oy4[j] = v2.y;
     }
 
-    // P1: horizontal window sums of x, y, x'^2, y'^2, x'y'
+    // P1: horizontal window sums of (x, y), (x'^2, y'^2) and x'y'
     constexpr int kRuns1 = kTM / kK1;
     for (int it = threadIdx.x; it < kTI * kRuns1; it += kThreads) {
         const int r = it / kRuns1, c0 = (it - r * kRuns1) * kK1;
-        float acc[5][kK1];
+        f2x am[kK1], aq[kK1];
+        float ac[kK1];
 #pragma unroll
-        for (int q = 0; q < 5; ++q)
-#pragma unroll
-            for (int j = 0; j < kK1; ++j) acc[q][j] = 0.0f;
+        for (int j = 0; j < kK1; ++j) {
+            am[j] = 0ull;
+            aq[j] = 0ull;
+            ac[j] = 0.0f;
+        }
 #pragma unroll
         for (int t = 0; t < kK1 + 2 * kR; ++t) {
-            const float2 v2 = sxy[r * kTI + c0 + t];
-            const float x = v2.x, y = v2.y;
-            const float xs = x - cx, ys = y - cy;
-            const float xx = xs * xs, yy = ys * ys, xy = xs * ys;
+            const f2x xy = sxy[r * kTI + c0 + t];
+            const f2x d = sub2(xy, cxy);
+            const f2x sq = mul2(d, d);
+            const float2 dd = unpack2(d);
+            const float cr = dd.x * dd.y;
 #pragma unroll
             for (int j = 0; j < kK1; ++j) {
                 const int k = t - j;
                 if (k >= 0 && k < kWin) {
-                    acc[0][j] = __fmaf_rn(a.w[k], x, acc[0][j]);
-                    acc[1][j] = __fmaf_rn(a.w[k], y, acc[1][j]);
-                    acc[2][j] = __fmaf_rn(a.w[k], xx, acc[2][j]);
-                    acc[3][j] = __fmaf_rn(a.w[k], yy, acc[3][j]);
-                    acc[4][j] = __fmaf_rn(a.w[k], xy, acc[4][j]);
+                    am[j] = fma2(w2[k], xy, am[j]);
+                    aq[j] = fma2(w2[k], sq, aq[j]);
+                    ac[j] = __fmaf_rn(a.w[k], cr, ac[j]);
                 }
             }
         }
 #pragma unroll
-        for (int q = 0; q < 5; ++q)
-#pragma unroll
-            for (int j = 0; j < kK1; ++j) h1[(q * kTI + r) * kTM + c0 + j] = acc[q][j];
+        for (int j = 0; j < kK1; ++j) {
+            const int o = r * kTM + c0 + j;
+            h1p[o] = am[j];
+            h1p[kTI * kTM + o] = aq[j];
+            h1s[o] = ac[j];
+        }
     }
     __syncthreads();
 
@@ -195,18 +246,26 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     constexpr int kRuns2 = kTM / kK2;
     for (int it = threadIdx.x; it < kTM * kRuns2; it += kThreads) {
         const int c = it % kTM, r0 = (it / kTM) * kK2;
-        float m[5][kK2];
+        f2x mm[kK2], mq[kK2];
+        float mc[kK2];
 #pragma unroll
-        for (int q = 0; q < 5; ++q) {
+        for (int j = 0; j < kK2; ++j) {
+            mm[j] = 0ull;
+            mq[j] = 0ull;
+            mc[j] = 0.0f;
+        }
 #pragma unroll
-            for (int j = 0; j < kK2; ++j) m[q][j] = 0.0f;
+        for (int t = 0; t < kK2 + 2 * kR; ++t) {
+            const int o = (r0 + t) * kTM + c;
+            const f2x hm = h1p[o], hq = h1p[kTI * kTM + o];
+            const float hc = h1s[o];
 #pragma unroll
-            for (int t = 0; t < kK2 + 2 * kR; ++t) {
-                const float h = h1[(q * kTI + r0 + t) * kTM + c];
-#pragma unroll
-                for (int j = 0; j < kK2; ++j) {
-                    const int k = t - j;
-                    if (k >= 0 && k < kWin) m[q][j] = __fmaf_rn(a.w[k], h, m[q][j]);
+            for (int j = 0; j < kK2; ++j) {
+                const int k = t - j;
+                if (k >= 0 && k < kWin) {
+                    mm[j] = fma2(w2[k], hm, mm[j]);
+                    mq[j] = fma2(w2[k], hq, mq[j]);
+                    mc[j] = __fmaf_rn(a.w[k], hc, mc[j]);
                 }
             }
         }
@@ -217,12 +276,13 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
             const int gy = oy - kR + r;
             float dmu = 0.0f, dxx = 0.0f, dxy = 0.0f;
             if (gy >= 0 && gy < a.H && gx >= 0 && gx < a.W) {
-                const float mx = m[0][j], my = m[1][j];
+                const float2 m01 = unpack2(mm[j]), m23 = unpack2(mq[j]);
+                const float mx = m01.x, my = m01.y;
                 const float mxs = mx - cx * a.wsum, mys = my - cy * a.wsum;   // means of x', y'
                 const float A = 2.0f * (mx * my) + a.c1;
-                const float B = 2.0f * (m[4][j] - mxs * mys) + a.c2;
+                const float B = 2.0f * (mc[j] - mxs * mys) + a.c2;
                 const float C = (mx * mx + my * my) + a.c1;
-                const float D = ((m[2][j] - mxs * mxs) + (m[3][j] - mys * mys)) + a.c2;
+                const float D = ((m23.x - mxs * mxs) + (m23.y - mys * mys)) + a.c2;
                 // C >= C1 and D >= C2: far from the approximate reciprocal's limits
                 const float rC = rcp_approx(C), rD = rcp_approx(D);
                 const float inv = rC * rD;
@@ -232,9 +292,8 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
                 dxy = 2.0f * A * inv;
                 if (r >= kR && r < kR + kTO && c >= kR && c < kR + kTO) ssum += (double)(1.0f - S);
             }
-            dm[(0 * kTM + r) * kTM + c] = dmu;
-            dm[(1 * kTM + r) * kTM + c] = dxx;
-            dm[(2 * kTM + r) * kTM + c] = dxy;
+            dmp[r * kTM + c] = pack2(dmu, dxx);
+            dms[r * kTM + c] = dxy;
         }
     }
     __syncthreads();
@@ -243,22 +302,30 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     constexpr int kRuns3 = kTO / kK3;
     for (int it = threadIdx.x; it < kTM * kRuns3; it += kThreads) {
         const int r = it / kRuns3, c0 = (it - r * kRuns3) * kK3;
+        f2x ap[kK3];
+        float as[kK3];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-            float acc[kK3];
+        for (int j = 0; j < kK3; ++j) {
+            ap[j] = 0ull;
+            as[j] = 0.0f;
+        }
 #pragma unroll
-            for (int j = 0; j < kK3; ++j) acc[j] = 0.0f;
+        for (int t = 0; t < kK3 + 2 * kR; ++t) {
+            const f2x dp = dmp[r * kTM + c0 + t];
+            const float ds = dms[r * kTM + c0 + t];
 #pragma unroll
-            for (int t = 0; t < kK3 + 2 * kR; ++t) {
-                const float d = dm[(q * kTM + r) * kTM + c0 + t];
-#pragma unroll
-                for (int j = 0; j < kK3; ++j) {
-                    const int k = t - j;
-                    if (k >= 0 && k < kWin) acc[j] = __fmaf_rn(a.w[k], d, acc[j]);
+            for (int j = 0; j < kK3; ++j) {
+                const int k = t - j;
+                if (k >= 0 && k < kWin) {
+                    ap[j] = fma2(w2[k], dp, ap[j]);
+                    as[j] = __fmaf_rn(a.w[k], ds, as[j]);
                 }
             }
+        }
 #pragma unroll
-            for (int j = 0; j < kK3; ++j) h3[(q * kTM + r) * kTO + c0 + j] = acc[j];
+        for (int j = 0; j < kK3; ++j) {
+            h3p[r * kTO + c0 + j] = ap[j];
+            h3s[r * kTO + c0 + j] = as[j];
         }
     }
     __syncthreads();
@@ -266,18 +333,23 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
     // P4: vertical sums -> dL/dC on the output tile (one 4-row run per thread)
     double l1sum = 0.0;
     {
-        float b[3][kK4];
+        f2x bp[kK4];
+        float bs[kK4];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
+        for (int j = 0; j < kK4; ++j) {
+            bp[j] = 0ull;
+            bs[j] = 0.0f;
+        }
 #pragma unroll
-            for (int j = 0; j < kK4; ++j) b[q][j] = 0.0f;
+        for (int t = 0; t < kK4 + 2 * kR; ++t) {
+            const f2x hp = h3p[(r4 + t) * kTO + c4];
+            const float hs = h3s[(r4 + t) * kTO + c4];
 #pragma unroll
-            for (int t = 0; t < kK4 + 2 * kR; ++t) {
-                const float h = h3[(q * kTM + r4 + t) * kTO + c4];
-#pragma unroll
-                for (int j = 0; j < kK4; ++j) {
-                    const int k = t - j;
-                    if (k >= 0 && k < kWin) b[q][j] = __fmaf_rn(a.w[k], h, b[q][j]);
+            for (int j = 0; j < kK4; ++j) {
+                const int k = t - j;
+                if (k >= 0 && k < kWin) {
+                    bp[j] = fma2(w2[k], hp, bp[j]);
+                    bs[j] = __fmaf_rn(a.w[k], hs, bs[j]);
                 }
             }
         }
@@ -289,7 +361,8 @@ __global__ void __launch_bounds__(ssim::kThreads, 3) dssim_kernel(SsimArgs a)
                 const float x = ox4[j], y = oy4[j];
                 const float d = x - y;
                 const float sgn = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
-                const float gs = b[0][j] + 2.0f * x * b[1][j] + y * b[2][j];
+                const float2 b01 = unpack2(bp[j]);
+                const float gs = b01.x + 2.0f * x * b01.y + y * bs[j];
                 a.dldc[plane + (size_t)gy * a.W + gx] = __fmaf_rn(a.ssim_coef, gs, sgn * a.l1_coef);
                 l1sum += (double)fabsf(d);
             }
