@@ -52,12 +52,14 @@ __device__ __forceinline__ void vjp_gaussian(const VjpArgs& a, const CamSet& cs,
     float grad[kVec * 4];
 #pragma unroll
     for (int i = 0; i < kVec * 4; ++i) grad[i] = 0.0f;
+    GaussAct ac;
+    activate<DEG>(gp, ac);   // view-independent: once for all views
     for (int v = 0; v < cs.n_views; ++v) {
         const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
         if (!a.touched[o]) continue;
         ProjOut po;
         ProjInter it;
-        if (project_one<DEG>(gp, cs.cam[v], a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, &it)) {
+        if (project_view<DEG>(gp, ac, cs.cam[v], a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, &it)) {
             float4* src = reinterpret_cast<float4*>(a.grad2d + o * GS_GRAD2D_STRIDE);
             const float4 x0 = src[0], x1 = src[1], x2 = src[2];
             const float g2[9] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x};

@@ -71,10 +71,12 @@ __global__ void __launch_bounds__(128) project_kernel(ProjectArgs a, CamSet cs)
     if (g >= a.n) return;
     GaussParams<DEG> gp;
     gp.load(a.params, g);
+    GaussAct ac;
+    activate<DEG>(gp, ac);   // view-independent: once for all views
     for (int v = 0; v < cs.n_views; ++v) {
         const size_t o = (size_t)v * (size_t)a.n + (size_t)g;
         ProjOut po;
-        const bool vis = project_one<DEG>(gp, cs.cam[v], a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, nullptr);
+        const bool vis = project_view<DEG>(gp, ac, cs.cam[v], a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, nullptr);
         if (!vis) {
             a.tiles_touched[o] = 0u;
             continue;

@@ -1,6 +1,7 @@
 // project_math.cuh -- per-Gaussian projection and its vector-Jacobian product.
 //
-// project_one() evaluates, in a fixed IEEE operation order:
+// project_one() (= activate() once per Gaussian + project_view() per view)
+// evaluates, in a fixed IEEE operation order:
 //   activation   s = exp(log_scale), q^ = q / |q|, R(q^), M = R diag(s), Sigma = M M^T,
 //                o = 1 / (1 + exp(-logit))
 //   view         t = R_cam mu + t_cam, culled unless t_z > near_z
@@ -64,9 +65,47 @@ struct ProjInter {
     float o;
 };
 
+// The view-independent part of the projection of one Gaussian: scale, rotation,
+// 3D covariance and opacity (computed once for all views).
+struct GaussAct {
+    float s[3], qn, qh[4], R[9], M[9], S[9], o;
+};
+
 template <int DEG>
-__device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs_camera& cam, float near_z,
-                                            float lowpass, int tiles_x, int tiles_y, ProjOut& out, ProjInter* it)
+__device__ __forceinline__ void activate(const GaussParams<DEG>& gp, GaussAct& ac)
+{
+#pragma unroll
+    for (int j = 0; j < 3; ++j) ac.s[j] = pexp(gp.ls[j]);
+    const float q0 = gp.q[0], q1 = gp.q[1], q2 = gp.q[2], q3 = gp.q[3];
+    const float qn = sqrtf(((q0 * q0 + q1 * q1) + q2 * q2) + q3 * q3);
+    ac.qn = qn;
+    const float w = q0 / qn, x = q1 / qn, y = q2 / qn, z = q3 / qn;
+    ac.qh[0] = w; ac.qh[1] = x; ac.qh[2] = y; ac.qh[3] = z;
+    const float xx = x * x, yy = y * y, zz = z * z, xy = x * y, xz = x * z, yz = y * z;
+    const float wx = w * x, wy = w * y, wz = w * z;
+    float* R = ac.R;
+    R[0] = 1.0f - 2.0f * (yy + zz); R[1] = 2.0f * (xy - wz);        R[2] = 2.0f * (xz + wy);
+    R[3] = 2.0f * (xy + wz);        R[4] = 1.0f - 2.0f * (xx + zz); R[5] = 2.0f * (yz - wx);
+    R[6] = 2.0f * (xz - wy);        R[7] = 2.0f * (yz + wx);        R[8] = 1.0f - 2.0f * (xx + yy);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) ac.M[3 * i + j] = R[3 * i + j] * ac.s[j];
+    const float* M = ac.M;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            ac.S[3 * i + j] = (M[3 * i + 0] * M[3 * j + 0] + M[3 * i + 1] * M[3 * j + 1]) + M[3 * i + 2] * M[3 * j + 2];
+    ac.o = 1.0f / (1.0f + pexp(-gp.logit));
+}
+
+// The per-view part, given the Gaussian's activation (same operations and
+// order as evaluating everything per view).
+template <int DEG>
+__device__ __forceinline__ bool project_view(const GaussParams<DEG>& gp, const GaussAct& ac, const gs_camera& cam,
+                                             float near_z, float lowpass, int tiles_x, int tiles_y, ProjOut& out,
+                                             ProjInter* it)
 {
     const float* W = cam.R;
     float t[3];
@@ -74,30 +113,8 @@ __device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs
     for (int i = 0; i < 3; ++i)
         t[i] = ((W[3 * i + 0] * gp.mu[0] + W[3 * i + 1] * gp.mu[1]) + W[3 * i + 2] * gp.mu[2]) + cam.t[i];
     if (!(t[2] > near_z)) return false;
-    float s[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) s[j] = pexp(gp.ls[j]);
-    const float q0 = gp.q[0], q1 = gp.q[1], q2 = gp.q[2], q3 = gp.q[3];
-    const float qn = sqrtf(((q0 * q0 + q1 * q1) + q2 * q2) + q3 * q3);
-    if (!(qn > 0.0f)) return false;
-    const float w = q0 / qn, x = q1 / qn, y = q2 / qn, z = q3 / qn;
-    const float xx = x * x, yy = y * y, zz = z * z, xy = x * y, xz = x * z, yz = y * z;
-    const float wx = w * x, wy = w * y, wz = w * z;
-    float R[9];
-    R[0] = 1.0f - 2.0f * (yy + zz); R[1] = 2.0f * (xy - wz);        R[2] = 2.0f * (xz + wy);
-    R[3] = 2.0f * (xy + wz);        R[4] = 1.0f - 2.0f * (xx + zz); R[5] = 2.0f * (yz - wx);
-    R[6] = 2.0f * (xz - wy);        R[7] = 2.0f * (yz + wx);        R[8] = 1.0f - 2.0f * (xx + yy);
-    float M[9];
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) M[3 * i + j] = R[3 * i + j] * s[j];
-    float S[9];
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-            S[3 * i + j] = (M[3 * i + 0] * M[3 * j + 0] + M[3 * i + 1] * M[3 * j + 1]) + M[3 * i + 2] * M[3 * j + 2];
+    if (!(ac.qn > 0.0f)) return false;
+    const float* S = ac.S;
     const float fx = cam.fx, fy = cam.fy;
     const float tz2 = t[2] * t[2];
     const float j00 = fx / t[2], j11 = fy / t[2];
@@ -135,7 +152,7 @@ __device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs
     if (fx1 > (float)tiles_x) fx1 = (float)tiles_x;
     if (fy1 > (float)tiles_y) fy1 = (float)tiles_y;
     if (!(fx0 < fx1 && fy0 < fy1)) return false;
-    const float o = 1.0f / (1.0f + pexp(-gp.logit));
+    const float o = ac.o;
     float col[3];
     uint32_t cm = 0;
     float dir[3] = {0.0f, 0.0f, 0.0f}, nv = 0.0f;
@@ -168,13 +185,24 @@ __device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs
     out.clamp = cm;
     if (it) {
 #pragma unroll
-        for (int i = 0; i < 3; ++i) { it->t[i] = t[i]; it->s[i] = s[i]; it->dir[i] = dir[i]; it->T0[i] = T0[i]; it->T1[i] = T1[i]; }
-        it->qn = qn; it->qh[0] = w; it->qh[1] = x; it->qh[2] = y; it->qh[3] = z;
+        for (int i = 0; i < 3; ++i) { it->t[i] = t[i]; it->s[i] = ac.s[i]; it->dir[i] = dir[i]; it->T0[i] = T0[i]; it->T1[i] = T1[i]; }
+        it->qn = ac.qn;
 #pragma unroll
-        for (int i = 0; i < 9; ++i) { it->R[i] = R[i]; it->M[i] = M[i]; it->S[i] = S[i]; }
+        for (int i = 0; i < 4; ++i) it->qh[i] = ac.qh[i];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) { it->R[i] = ac.R[i]; it->M[i] = ac.M[i]; it->S[i] = S[i]; }
         it->a = a; it->b = b; it->c = c; it->det = det; it->nv = nv; it->o = o;
     }
     return true;
+}
+
+template <int DEG>
+__device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs_camera& cam, float near_z,
+                                            float lowpass, int tiles_x, int tiles_y, ProjOut& out, ProjInter* it)
+{
+    GaussAct ac;
+    activate<DEG>(gp, ac);
+    return project_view<DEG>(gp, ac, cam, near_z, lowpass, tiles_x, tiles_y, out, it);
 }
 
 // d loss / d params of one (Gaussian, view) given d loss / d (mean2d, conic, opacity, colour).
