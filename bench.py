@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -294,8 +295,8 @@ def run_gpu(args):
     # ---- device-resident timed region
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else f"/tmp/bench_clocks_r{rank}.csv"
+    clock_path = os.path.join(os.environ.get("GS_BENCH_CLOCKS_DIR", tempfile.gettempdir()),
+                              f"bench_clocks_r{rank}.csv")
     sampler = start_clock_sampler(clock_path, local)
     time.sleep(0.5)
     tr.eval_counts.zero_()
