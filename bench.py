@@ -3,6 +3,10 @@
 forward/backward rasterization, compaction + VJP, deferred Adam) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config medium] [--impl gpu|reference]
+                    [--dssim LAMBDA] [--tile-budget K] [--partial S]
+
+The options time the variants: the L1 + D-SSIM loss, per-tile pruned lists,
+and (a separate line) the forward render as S composed depth slabs.
 
 Prints ONE JSON line (rank 0).  The metric is Gaussian-pixel evaluations per
 second (forward evaluations up to each pixel's stop, plus backward evaluations
