@@ -35,6 +35,14 @@
 // All decisions use the same fp32 operations in the same order as the CPU
 // definition (see gs_common.cuh); boxes, tau and bits only avoid work whose
 // outcome is already known.
+//
+// Modes (template argument): kFused -- forward, L1 loss and backward in one
+// pass; kFwd -- forward only, optionally storing per pixel the final T and last
+// index and per tile the pass bits of the chunk holding the last composited
+// entry; kBwdState -- the backward alone, started from that stored state with
+// dL/dC given per pixel (for losses whose gradient needs other tiles' colours).
+// Views are interleaved over the grid (CTA i: view i mod V, tile i / V) so the
+// heavy central tiles of all views spread over the launch.
 #include "gs_common.cuh"
 
 namespace gs {
