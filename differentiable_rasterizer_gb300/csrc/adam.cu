@@ -1,6 +1,6 @@
 // adam.cu -- gs_adam_deferred: Adam applied only to the Gaussians with a
-// gradient this step (GS-Scale, abstract: "deferred optimizer update to minimize
-// unnecessary memory accesses for Gaussians with zero gradients"), made exactly
+// gradient this step (GS-Scale, abstract: the optimizer update of Gaussians
+// whose gradient is zero is deferred, saving their memory traffic), made exactly
 // equal to dense Adam by replaying the skipped zero-gradient steps first.
 //
 // Work unit: a (listed Gaussian, float4 chunk of its [stride] parameter block)

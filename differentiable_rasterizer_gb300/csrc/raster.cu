@@ -1,7 +1,7 @@
 // raster.cu -- gs_raster_fused_fwd_bwd: forward compositing, L1 loss and
-// backward rasterization in ONE kernel (ByteSplat, English abstract: "fuses
-// forward rasterization and backward rasterization into a single GPU kernel,
-// retaining intermediate results on-chip").
+// backward rasterization in ONE kernel (ByteSplat, English abstract: the two
+// rasterization passes are one kernel whose intermediate results stay on chip
+// instead of going through off-chip memory).
 //
 // One CTA per 16x16 tile; thread t owns pixel (t % 16, t / 16).  The tile's
 // sorted list is staged through shared memory in chunks of kChunk records

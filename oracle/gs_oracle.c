@@ -824,8 +824,8 @@ int64_t FN(oracle_compact)(const uint8_t* touched, int64_t n, uint32_t* idx)
 }
 
 /* ------------------------------------------------------------------------- */
-/* O12: Adam (Kingma & Ba) and its deferred form (GS-Scale, abstract:          */
-/* "deferred optimizer update" for Gaussians with zero gradients).            */
+/* O12: Adam (Kingma & Ba) and its deferred form (GS-Scale, abstract: the     */
+/* update of Gaussians with zero gradients is deferred).                      */
 /* beta^j is computed in fp64 by right-to-left binary exponentiation; the bias */
 /* corrections are rounded to REAL once.  One step j on one scalar:            */
 /*   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g);                           */
