@@ -167,3 +167,17 @@ def test_backward_with_stored_pass_bits_equals_recomputing_them():
     m = t_bits[0].cpu().numpy() > 0
     ok, st = parity.grad_report(g_bits.cpu().numpy()[0][m][:, :9], tr.grad2d.cpu().numpy()[0][m][:, :9])
     assert ok, st
+
+
+def test_dssim_maximum_view_count():
+    """The D-SSIM step over GS_MAX_VIEWS (32) views."""
+    sc = scenes.random_small_scene(53, n=300, width=36, height=20, sh_degree=0, log_lo=-3.0, log_hi=-2.0)
+    cams = []
+    for k in range(32):
+        ang = -0.3 + 0.6 * k / 31
+        c, s = math.cos(ang), math.sin(ang)
+        R = np.array([[c, 0, s], [0, 1, 0], [-s, 0, c]], np.float32)
+        cams.append(scenes.Camera(R, np.zeros(3, np.float32), 36.0, 36.0, 18.0, 10.0, 36, 20))
+    sc.cameras = cams
+    sc.target_uniform = np.random.default_rng(54).uniform(0, 1, (32, 3, 20, 36)).astype(np.float32)
+    parity.run_dssim_parity(sc, 0.2)

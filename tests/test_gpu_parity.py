@@ -235,6 +235,23 @@ def test_three_training_steps_track_the_oracle():
     assert (tr.last_step.cpu().numpy() == 3).all()
 
 
+def test_maximum_view_count():
+    """GS_MAX_VIEWS (32) views of a small scene in one step: every per-view
+    stage and the union over all of them."""
+    sc = scenes.random_small_scene(51, n=400, width=40, height=24, sh_degree=0, log_lo=-3.0, log_hi=-2.0)
+    cams = []
+    for k in range(32):
+        ang = -0.3 + 0.6 * k / 31
+        c, s = math.cos(ang), math.sin(ang)
+        R = np.array([[c, 0, s], [0, 1, 0], [-s, 0, c]], np.float32)
+        cams.append(scenes.Camera(R, np.array([0.05 * (k % 4), 0.0, 0.1 * (k // 16)], np.float32), 40.0, 40.0,
+                                  20.0, 12.0, 40, 24))
+    sc.cameras = cams
+    sc.target_uniform = np.random.default_rng(52).uniform(0, 1, (32, 3, 24, 40)).astype(np.float32)
+    st = parity.run_stage_parity(sc)
+    assert len(st["visible"]) == 32 and min(st["visible"]) > 0
+
+
 def test_pipelined_host_steps_match_device_steps():
     """train_steps_host (targets copied in on a second stream, one step ahead) gives
     the same losses as device-resident steps, and leaves each step's loss in its row."""
