@@ -61,9 +61,14 @@ __global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __rest
                                                           const ushort4* __restrict__ rect,
                                                           const float* __restrict__ depth, BinGeom G,
                                                           uint32_t* __restrict__ cnt, uint64_t* __restrict__ tmp,
-                                                          unsigned int* __restrict__ stats)
+                                                          unsigned int* __restrict__ stats,
+                                                          const unsigned long long* __restrict__ total,
+                                                          unsigned long long capacity)
 {
     extern __shared__ uint32_t s_cnt[];
+    // the scatter runs before the host has seen the instance count: it writes
+    // nothing when the count exceeds the caller's capacity
+    if (kScatter && *total > capacity) return;
     const int b = blockIdx.x, band = blockIdx.y, v = blockIdx.z;
     if (!kScatter && b == 0 && band == 0 && v == 0 && threadIdx.x < 4) stats[threadIdx.x] = 0u;   // for bucket_stats
     const int row0 = band * G.band_rows;
@@ -327,8 +332,11 @@ __device__ __forceinline__ void cta_sort(uint64_t* s, const uint64_t* src, size_
 __global__ void __launch_bounds__(kSortWarps * 32) sort_warp_kernel(const uint2* __restrict__ ranges, int64_t nb,
                                                                     const uint64_t* __restrict__ tmp,
                                                                     uint64_t* __restrict__ keys,
-                                                                    uint32_t* __restrict__ ids)
+                                                                    uint32_t* __restrict__ ids,
+                                                                    const unsigned long long* __restrict__ total,
+                                                                    unsigned long long capacity)
 {
+    if (*total > capacity) return;   // launched before the host's capacity check, like the scatter
     const int64_t t = (int64_t)blockIdx.x * kSortWarps + (threadIdx.x >> 5);
     if (t >= nb) return;
     const uint2 r = ranges[t];
@@ -602,7 +610,7 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (n > 0) {
         GS_CUDA_TRY(cudaFuncSetAttribute(bin_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem));
         bin_kernel<false><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, cnt,
-                                                                   nullptr, stats);
+                                                                   nullptr, stats, nullptr, 0ull);
         GS_LAUNCH_CHECK();
     } else {
         GS_CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * (size_t)ncnt, s));
@@ -613,24 +621,49 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     bucket_stats_kernel<<<(unsigned)((ntile_ids + threads - 1) / threads), threads, 0, s>>>(off, G.B, ntile_ids, totals,
                                                                                            ranges, stats, lists);
     GS_LAUNCH_CHECK();
-    struct {
+    struct HostCounts {
         unsigned long long total;
         unsigned int st[4];
-    } host;
-    static_assert(sizeof(host) == sizeof(unsigned long long) + 4 * sizeof(unsigned int), "host copy layout");
-    GS_CUDA_TRY(cudaMemcpyAsync(&host, totals, sizeof(host), cudaMemcpyDeviceToHost, s));
-    GS_CUDA_TRY(cudaStreamSynchronize(s));
+    };
+    static_assert(sizeof(HostCounts) == sizeof(unsigned long long) + 4 * sizeof(unsigned int), "host copy layout");
+    // Read back through one pinned host buffer per calling thread (allocated on the
+    // first call, kept for the thread's life): a copy to pageable memory would
+    // block this call until the GPU had drained the stream.
+    static thread_local HostCounts* t_counts = nullptr;
+    if (!t_counts) {
+        void* p = nullptr;
+        GS_CUDA_TRY(cudaHostAlloc(&p, sizeof(HostCounts), cudaHostAllocPortable));
+        t_counts = static_cast<HostCounts*>(p);
+    }
+    HostCounts& host = *t_counts;
+    GS_CUDA_TRY(cudaMemcpyAsync(&host, totals, sizeof(HostCounts), cudaMemcpyDeviceToHost, s));
+    // The host waits for this copy only (an event), not for the stream: the
+    // scatter and the warp-size bucket sort, which need no host-side count, are
+    // queued behind it and keep the GPU busy during the round trip.  Both check
+    // the device-held count against the capacity and do nothing if it is short.
+    cudaEvent_t copied;
+    GS_CUDA_TRY(cudaEventCreateWithFlags(&copied, cudaEventDisableTiming));
+    cudaError_t ce = cudaEventRecord(copied, s);
+    if (ce == cudaSuccess && n > 0) {
+        ce = cudaFuncSetAttribute(bin_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem);
+        if (ce == cudaSuccess) {
+            bin_kernel<true><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, off,
+                                                                      tmp, nullptr, totals,
+                                                                      (unsigned long long)capacity);
+            ce = cudaGetLastError();
+        }
+        if (ce == cudaSuccess) {
+            sort_warp_kernel<<<(unsigned)((ntile_ids + kSortWarps - 1) / kSortWarps), kSortWarps * 32, 0, s>>>(
+                ranges, ntile_ids, tmp, keys, ids, totals, (unsigned long long)capacity);
+            ce = cudaGetLastError();
+        }
+    }
+    if (ce == cudaSuccess) ce = cudaEventSynchronize(copied);
+    cudaEventDestroy(copied);
+    if (ce != cudaSuccess) return GS_ERR_CUDA;
     *n_instances = (int64_t)host.total;
     if ((int64_t)host.total > capacity) return GS_ERR_CAPACITY;
     if (host.total == 0) return GS_OK;
-
-    GS_CUDA_TRY(cudaFuncSetAttribute(bin_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bin_smem));
-    bin_kernel<true><<<bin_grid, kBinThreads, bin_smem, s>>>(proj->tiles_touched, rect4, proj->depth, G, off, tmp,
-                                                              nullptr);
-    GS_LAUNCH_CHECK();
-    sort_warp_kernel<<<(unsigned)((ntile_ids + kSortWarps - 1) / kSortWarps), kSortWarps * 32, 0, s>>>(
-        ranges, ntile_ids, tmp, keys, ids);
-    GS_LAUNCH_CHECK();
     if (host.st[1] > 0) {
         sort_reg_kernel<<<host.st[1], kRegThreads, 0, s>>>(lists, ranges, tmp, keys, ids);
         GS_LAUNCH_CHECK();

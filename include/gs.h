@@ -29,8 +29,10 @@
  *   - Returns gs_status; nothing is thrown across the ABI.
  *   - All array pointers are DEVICE pointers owned by the caller unless the
  *     argument says "host".  The library allocates no device memory and keeps no
- *     state between calls; calls that need scratch take (ws, ws_bytes): pass
- *     ws == NULL to query the size into *ws_bytes.
+ *     state between calls (two exceptions, both stated with their calls:
+ *     gs_bin_sort's 24-byte pinned host buffer per calling thread and
+ *     gs_grad_compact_static's device scratch); calls that need scratch take
+ *     (ws, ws_bytes): pass ws == NULL to query the size into *ws_bytes.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  gs_bin_sort is the only call that synchronises the host
  *     (it reads the instance count back to size the sort).
@@ -148,8 +150,13 @@ GS_API gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, c
  * keys, ids: [capacity] outputs (sorted); tile_ranges: [n_views * tiles][2]
  * uint32 [start, end) into the sorted arrays (start == end: empty tile).
  * n_instances: HOST out, set even when the capacity is too small.
- * ws / ws_bytes: scratch (ws == NULL: query).  Synchronises the host once.
- * Errors: CAPACITY if n_instances > capacity (outputs untouched);
+ * ws / ws_bytes: scratch (ws == NULL: query).  Synchronises the host once, on
+ * the read-back of the instance count (an event after the copy, so the scatter
+ * and the sort of the smallest buckets, already queued, run meanwhile).  The
+ * count is read into a 24-byte pinned host buffer that each calling thread
+ * allocates on its first call and keeps for its lifetime.
+ * Errors: CAPACITY if n_instances > capacity (outputs untouched: the queued
+ * kernels check the count on the device and write nothing);
  * INVALID_ARG for bad sizes (width above 655360, i.e. more than 40960 tiles in a
  * row) or a too small workspace. */
 GS_API gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views, int32_t width, int32_t height,
