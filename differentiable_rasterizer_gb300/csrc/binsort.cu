@@ -346,12 +346,18 @@ __global__ void __launch_bounds__(kSortWarps * 32) sort_warp_kernel(const uint2*
 }
 
 // One kRegThreads-thread CTA per listed bucket of kWarpCap < size <= kRegCap.
+// Launched before the host knows the class size: one block per possible bucket,
+// the ones past the device-held count (or all, if the capacity is short) exit.
 __global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* __restrict__ list,
                                                                const uint2* __restrict__ ranges,
                                                                const uint64_t* __restrict__ tmp,
-                                                               uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
+                                                               uint64_t* __restrict__ keys, uint32_t* __restrict__ ids,
+                                                               const unsigned int* __restrict__ count,
+                                                               const unsigned long long* __restrict__ total,
+                                                               unsigned long long capacity)
 {
     __shared__ uint64_t s[kRegThreads * 9];
+    if (*total > capacity || blockIdx.x >= *count) return;
     const uint32_t t = list[blockIdx.x];
     const uint2 r = ranges[t];
     const int c = (int)(r.y - r.x);
@@ -657,6 +663,12 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
                 ranges, ntile_ids, tmp, keys, ids, totals, (unsigned long long)capacity);
             ce = cudaGetLastError();
         }
+        if (ce == cudaSuccess) {
+            // buckets of 257..2048 instances: at most one per (view, tile)
+            sort_reg_kernel<<<(unsigned)ntile_ids, kRegThreads, 0, s>>>(lists, ranges, tmp, keys, ids, stats + 1,
+                                                                        totals, (unsigned long long)capacity);
+            ce = cudaGetLastError();
+        }
     }
     if (ce == cudaSuccess) ce = cudaEventSynchronize(copied);
     cudaEventDestroy(copied);
@@ -664,10 +676,6 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     *n_instances = (int64_t)host.total;
     if ((int64_t)host.total > capacity) return GS_ERR_CAPACITY;
     if (host.total == 0) return GS_OK;
-    if (host.st[1] > 0) {
-        sort_reg_kernel<<<host.st[1], kRegThreads, 0, s>>>(lists, ranges, tmp, keys, ids);
-        GS_LAUNCH_CHECK();
-    }
     if (host.st[2] > 0) {
         const int e = host.st[0] <= 4u * kMidThreads ? 4 : (host.st[0] <= 8u * kMidThreads ? 8 : 16);
         const size_t smem = sizeof(uint64_t) * (size_t)kMidThreads * (size_t)(e + 1);

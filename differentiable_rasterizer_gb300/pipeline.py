@@ -117,9 +117,10 @@ class GaussianTrainer:
 
     def kernel_launches_per_step(self) -> int:
         """Kernels the library launches for one train_step, from its launch structure:
-        projection 1; binning: count 1, scan 3, bucket stats 1, then (when there are
-        instances) scatter 1, warp sort 1, and one more sort kernel for each of the
-        size classes 257..2048, 2049..16384 and over 16384 that occurs; pruning (with a
+        projection 1; binning: count 1, scan 3, bucket stats 1, scatter 1, warp sort 1,
+        sort of 257..2048 1 (these three queued before the count is known), and one
+        more sort kernel for each of the size classes 2049..16384 and over 16384 that
+        occurs; pruning (with a
         tile budget) 1; fused raster 1
         (with the D-SSIM loss: forward, D-SSIM and backward, 3); compaction: 3 per
         view-list scan, then (several views) union 1 and union scan 3, VJP 1; Adam 2.
@@ -127,10 +128,9 @@ class GaussianTrainer:
         V, n = self.V, self.n
         r = self.ranges.view(-1, 2).to(torch.int64)
         c = r[:, 1] - r[:, 0]
-        sort = (1 if n * V else 0) + 3 + 1
+        sort = (1 if n * V else 0) + 3 + 1 + (3 if n else 0)
         if self.n_instances:
-            sort += 2 + sum(int(((c > lo) & (c <= hi)).any().item())
-                            for lo, hi in ((256, 2048), (2048, 16384), (16384, 1 << 62)))
+            sort += sum(int(((c > lo) & (c <= hi)).any().item()) for lo, hi in ((2048, 16384), (16384, 1 << 62)))
         compact = (3 * V + (1 + 3 if V > 1 else 0) + 1) if n else 0
         raster = 1 if self.dssim_lambda is None else 3
         prune = 1 if self.tile_budget else 0
