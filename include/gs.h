@@ -152,7 +152,8 @@ GS_API gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, c
  * n_instances: HOST out, set even when the capacity is too small.
  * ws / ws_bytes: scratch (ws == NULL: query).  Synchronises the host once, on
  * the read-back of the instance count (an event after the copy, so the scatter
- * and the sort of the smallest buckets, already queued, run meanwhile).  The
+ * and the sorts of buckets up to 2048 instances, already queued, run
+ * meanwhile).  The
  * count is read into a 24-byte pinned host buffer that each calling thread
  * allocates on its first call and keeps for its lifetime.
  * Errors: CAPACITY if n_instances > capacity (outputs untouched: the queued
