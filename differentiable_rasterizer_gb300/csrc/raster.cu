@@ -594,28 +594,30 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 // or below it (lane 0 always is one)
                 const uint32_t heads = __ballot_sync(0xffffffffu, !valid || lane == 0 || qi == own_off);
                 const int seg = 31 - __clz(heads & ((2u << lane) - 1u));
-                // segmented inclusive product of 1 / (1 - alpha): T before each entry
-                float P = rc;
+                // One segmented scan gives both running quantities relative to the
+                // pixel's current T:  P = product of 1 / (1 - alpha) up to this
+                // entry (T before it = T * P) and Y = sum of dL/dC . c * alpha * P
+                // up to it (dL/dC . the colour composited behind an entry = T * the
+                // sum over the entries before it in the queue, after it in the
+                // list).  Pairs combine as (P1, Y1) then (P2, Y2) ->
+                // (P1 P2, Y1 + P1 Y2): five dependent steps instead of ten.
+                const float dotc = __fmaf_rn(go0, r1.z, __fmaf_rn(go1, r1.w, go2 * cb));
+                const float da = valid ? dotc * alpha : 0.0f;
+                float P = rc, Y = da * rc;
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
                     const float Pu = __shfl_up_sync(0xffffffffu, P, d);
-                    if (lane - d >= seg) P = Pu * P;
+                    const float Yu = __shfl_up_sync(0xffffffffu, Y, d);
+                    if (lane - d >= seg) {
+                        Y = __fmaf_rn(Pu, Y, Yu);
+                        P = Pu * P;
+                    }
                 }
                 const float Tb = Tst * P;             // transmittance before this entry
-                // dL/dC . (c * alpha * T) of this entry; the segmented sum of the
-                // entries before it in the queue (after it in the list) is dL/dC .
-                // the colour composited behind it
-                const float dotc = __fmaf_rn(go0, r1.z, __fmaf_rn(go1, r1.w, go2 * cb));
-                const float z = valid ? dotc * alpha * Tb : 0.0f;
-                float y = z;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, y, d);
-                    if (lane - d >= seg) y += u;
-                }
+                const float y = Tst * Y;
                 if (valid) {
                     const EntryGrad e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb, dotc,
-                                                      Sgs + (y - z), rc);
+                                                      Sgs + Tst * (Y - da * P), rc);
                     const uint32_t gid = s_id[j];
                     float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
                     atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
