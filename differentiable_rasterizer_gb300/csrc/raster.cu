@@ -108,6 +108,51 @@ struct EntryGrad {
     float gm0, gm1, gA, gB, gC, go, gr, gg, gb;
 };
 
+// One step of the halving sum below: of the 2H partial sums v (the lower half
+// kept by lanes with `upper` clear), a lane keeps its half and adds the
+// partner's (lane ^ o) copy of that half.
+template <int H>
+__device__ __forceinline__ void halve(const float (&v)[2 * H], float (&k)[H], bool upper, int o)
+{
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+        const float send = upper ? v[i] : v[H + i];
+        const float keep = upper ? v[H + i] : v[i];
+        k[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+}
+
+// Warp sum of the nine gradient terms by recursive halving: at xor distances
+// 16, 8, 4, 2, 1 each lane keeps the half of its partial sums that its lane bit
+// selects (12 shuffles instead of a full butterfly's 45).  Every partial sum is
+// own + partner at the same distances as the butterfly, so the totals are the
+// butterfly's bit for bit.  Returns the total of term reduce_term(lane).
+__device__ __forceinline__ float warp_sum_terms(const EntryGrad& e, int lane)
+{
+    const float v10[10] = {e.gm0, e.gm1, e.gA, e.gB, e.gC, e.go, e.gr, e.gg, e.gb, 0.0f};
+    float k5[5];
+    halve<5>(v10, k5, (lane & 16) != 0, 16);            // terms 0..4 | 5..9
+    const float v6[6] = {k5[0], k5[1], k5[2], k5[3], k5[4], 0.0f};
+    float k3[3];
+    halve<3>(v6, k3, (lane & 8) != 0, 8);               // 0..2 | 3, 4, pad
+    const float v4[4] = {k3[0], k3[1], k3[2], 0.0f};
+    float k2[2];
+    halve<2>(v4, k2, (lane & 4) != 0, 4);               // 0, 1 | 2, pad
+    float k1[1];
+    halve<1>(k2, k1, (lane & 2) != 0, 2);
+    return k1[0] + __shfl_xor_sync(0xffffffffu, k1[0], 1);
+}
+
+// The term whose warp total warp_sum_terms leaves in this lane (even lanes
+// only; -1: a padding slot or an odd lane).
+__device__ __forceinline__ int reduce_term(int lane)
+{
+    const int m = ((lane & 4) ? 2 : 0) + ((lane & 2) ? 1 : 0);   // of the 3 kept after distance 8
+    const int i = ((lane & 8) ? 3 : 0) + m;                        // of the 5 kept after distance 16
+    const int t = ((lane & 16) ? 5 : 0) + i;
+    return ((lane & 1) || m > 2 || i > 4 || t > 8) ? -1 : t;
+}
+
 // Gradient terms of one composited entry from its transmittance before it (Ti),
 // dotc = dL/dC . its colour, dots = dL/dC . the colour composited behind it, and
 // rc = 1 / (1 - alpha).
@@ -160,6 +205,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const int tile_lin = v * a.tiles + tile;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int red_term = reduce_term(lane);   // dense backward: the gradient term this lane adds
     const int ox = tx * kTile, oy = ty * kTile;
     const int px = ox + (threadIdx.x & (kTile - 1));
     const int py = oy + (threadIdx.x / kTile);
@@ -498,7 +544,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             // Dense chunk (large Gaussians: most of the warp's pixels composite
             // the same entries): walk the union newest first, every lane updating
             // its own pixel's T and dL/dC . (colour behind); the 9 gradient
-            // terms are summed over the warp by a butterfly and added with one
+            // terms are summed over the warp (warp_sum_terms) and added with one
             // atomic per component.
 #pragma unroll
             for (int w = kWords - 1; w >= 0; --w) {
@@ -525,26 +571,10 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                         Sg += dotc * alpha * Tb;
                         Tcur = Tb;
                     }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        e.gm0 += __shfl_xor_sync(0xffffffffu, e.gm0, o);
-                        e.gm1 += __shfl_xor_sync(0xffffffffu, e.gm1, o);
-                        e.gA += __shfl_xor_sync(0xffffffffu, e.gA, o);
-                        e.gB += __shfl_xor_sync(0xffffffffu, e.gB, o);
-                        e.gC += __shfl_xor_sync(0xffffffffu, e.gC, o);
-                        e.go += __shfl_xor_sync(0xffffffffu, e.go, o);
-                        e.gr += __shfl_xor_sync(0xffffffffu, e.gr, o);
-                        e.gg += __shfl_xor_sync(0xffffffffu, e.gg, o);
-                        e.gb += __shfl_xor_sync(0xffffffffu, e.gb, o);
-                    }
-                    if (lane < 4) {
-                        const uint32_t gid = s_id[j];
-                        float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
-                        if (lane == 0) atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
-                        else if (lane == 1) atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
-                        else if (lane == 2) atomicAdd(dst + 8, e.gb);
-                        else touchv[gid] = 1;
-                    }
+                    const float sum = warp_sum_terms(e, lane);
+                    const uint32_t gid = s_id[j];
+                    if (red_term >= 0) atomicAdd(g2v + (size_t)gid * GS_GRAD2D_STRIDE + red_term, sum);
+                    if (lane == 1) touchv[gid] = 1;
                 }
             }
             continue;
