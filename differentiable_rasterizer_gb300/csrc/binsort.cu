@@ -644,9 +644,10 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     HostCounts& host = *t_counts;
     GS_CUDA_TRY(cudaMemcpyAsync(&host, totals, sizeof(HostCounts), cudaMemcpyDeviceToHost, s));
     // The host waits for this copy only (an event), not for the stream: the
-    // scatter and the warp-size bucket sort, which need no host-side count, are
-    // queued behind it and keep the GPU busy during the round trip.  Both check
-    // the device-held count against the capacity and do nothing if it is short.
+    // scatter and the sorts of buckets up to kRegCap instances, which need no
+    // host-side count, are queued behind it and keep the GPU busy during the
+    // round trip.  They check the device-held count against the capacity and do
+    // nothing if it is short.
     cudaEvent_t copied;
     GS_CUDA_TRY(cudaEventCreateWithFlags(&copied, cudaEventDisableTiming));
     cudaError_t ce = cudaEventRecord(copied, s);
