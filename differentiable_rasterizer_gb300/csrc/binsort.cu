@@ -5,9 +5,9 @@
 // Gaussian index, is done as a counting sort on the high part followed by a
 // sort of every (view, tile) bucket on (bits(depth), index):
 //
-//   1. count:   block b of view v owns a contiguous range of that view's
-//               Gaussians and counts their instances per tile in shared memory
-//               (native integer atomics); the counts go out tile-major,
+//   1. count:   block b owns a contiguous range of Gaussians and, view after
+//               view, counts their instances per tile in shared memory (native
+//               integer atomics); the counts go out tile-major,
 //               cnt[(v * tiles + tile) * B + b];
 //   2. scan:    one exclusive scan of cnt gives, for every (tile, block), where
 //               that block's instances of that tile start in the output;
@@ -31,10 +31,10 @@
 namespace gs {
 
 constexpr int kBinThreads = 1024;          // count / scatter block size
-constexpr int kBinBlocks = 304;            // count / scatter blocks over all views (2 per SM) ...
+constexpr int kBinBlocks = 304;            // count / scatter blocks for several views (2 per SM) ...
 constexpr int kBinBlocksOneView = 152;     // ... or for a single view (fewer count entries to scan)
 constexpr int kBandTiles = 40960;          // shared-memory tile counters per block (160 KB)
-constexpr int64_t kMaxCounts = 1 << 22;    // cap on (view, tile, block) count entries
+constexpr int64_t kMaxCounts = 1 << 26;    // cap on (view, tile, block) count entries
 constexpr int kWarpCap = 256;              // bucket sizes sorted by one warp (8 keys per lane)
 constexpr int kRegCap = 2048;              // bucket sizes sorted by one 256-thread CTA in registers
 constexpr int kRegThreads = 256;
@@ -48,14 +48,17 @@ constexpr int kSortWarps = 8;              // warps per block of the warp-sort k
 struct BinGeom {
     int64_t n;           // Gaussians per view
     int64_t per_block;   // Gaussians per block
-    int32_t B;           // blocks per view
+    int32_t B;           // blocks (each takes its Gaussian range in every view)
+    int32_t views;
     int32_t tiles_x, tiles_y, tiles;
     int32_t band_rows;   // tile rows per block band
 };
 
 // -------------------------------------------------------------------- count / scatter
-// Block (b, band, v): Gaussians [b * per_block, (b + 1) * per_block) of view v,
-// tile rows [band * band_rows, ...) of that view.
+// Block (b, band): Gaussians [b * per_block, (b + 1) * per_block) in tile rows
+// [band * band_rows, ...), view after view.  All blocks work on about the same
+// view at a time, so the scatter's writes stay within one view's part of the
+// output (a few L2-sized regions instead of all views' at once).
 template <bool kScatter>
 __global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __restrict__ touched_cnt,
                                                           const ushort4* __restrict__ rect,
@@ -69,51 +72,56 @@ __global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __rest
     // the scatter runs before the host has seen the instance count: it writes
     // nothing when the count exceeds the caller's capacity
     if (kScatter && *total > capacity) return;
-    const int b = blockIdx.x, band = blockIdx.y, v = blockIdx.z;
-    if (!kScatter && b == 0 && band == 0 && v == 0 && threadIdx.x < 4) stats[threadIdx.x] = 0u;   // for bucket_stats
+    const int b = blockIdx.x, band = blockIdx.y;
+    if (!kScatter && b == 0 && band == 0 && threadIdx.x < 4) stats[threadIdx.x] = 0u;   // for bucket_stats
     const int row0 = band * G.band_rows;
     const int row1 = min(G.tiles_y, row0 + G.band_rows);
     const int nt = (row1 - row0) * G.tiles_x;
-    const size_t cbase = ((size_t)v * (size_t)G.tiles + (size_t)row0 * (size_t)G.tiles_x) * (size_t)G.B + (size_t)b;
-    // counters (count) or cursors = this block's start in every bucket (scatter)
-    for (int i = threadIdx.x; i < nt; i += blockDim.x) s_cnt[i] = kScatter ? cnt[cbase + (size_t)i * G.B] : 0u;
-    __syncthreads();
     const int64_t g0 = (int64_t)b * G.per_block;
     const int64_t g1 = min(G.n, g0 + G.per_block);
-    const size_t vb = (size_t)v * (size_t)G.n;
-    constexpr int U = 4;   // Gaussians in flight per thread
-    for (int64_t gb = g0 + threadIdx.x; gb < g1; gb += (int64_t)U * blockDim.x) {
-        uint32_t tc[U];
+    for (int v = 0; v < G.views; ++v) {
+        const size_t cbase =
+            ((size_t)v * (size_t)G.tiles + (size_t)row0 * (size_t)G.tiles_x) * (size_t)G.B + (size_t)b;
+        if (v > 0) __syncthreads();   // the previous view's counters are out of use
+        // counters (count) or cursors = this block's start in every bucket (scatter)
+        for (int i = threadIdx.x; i < nt; i += blockDim.x) s_cnt[i] = kScatter ? cnt[cbase + (size_t)i * G.B] : 0u;
+        __syncthreads();
+        const size_t vb = (size_t)v * (size_t)G.n;
+        constexpr int U = 4;   // Gaussians in flight per thread
+        for (int64_t gb = g0 + threadIdx.x; gb < g1; gb += (int64_t)U * blockDim.x) {
+            uint32_t tc[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t g = gb + (int64_t)u * blockDim.x;
-            tc[u] = g < g1 ? __ldg(touched_cnt + vb + g) : 0u;
-        }
-        ushort4 r[U];
-        uint64_t key[U];
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = gb + (int64_t)u * blockDim.x;
+                tc[u] = g < g1 ? __ldg(touched_cnt + vb + g) : 0u;
+            }
+            ushort4 r[U];
+            uint64_t key[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t g = gb + (int64_t)u * blockDim.x;
-            r[u] = tc[u] ? __ldg(rect + vb + g) : make_ushort4(0, 0, 0, 0);
-            if (kScatter)
-                key[u] = tc[u] ? (((uint64_t)__float_as_uint(__ldg(depth + vb + g)) << 32) | (uint64_t)g) : 0ull;
-        }
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = gb + (int64_t)u * blockDim.x;
+                r[u] = tc[u] ? __ldg(rect + vb + g) : make_ushort4(0, 0, 0, 0);
+                if (kScatter)
+                    key[u] = tc[u] ? (((uint64_t)__float_as_uint(__ldg(depth + vb + g)) << 32) | (uint64_t)g) : 0ull;
+            }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (!tc[u]) continue;
-            const int y0 = max((int)r[u].y, row0), y1 = min((int)r[u].w, row1);
-            for (int ty = y0; ty < y1; ++ty) {
-                uint32_t* row = s_cnt + (ty - row0) * G.tiles_x;
-                for (int tx = r[u].x; tx < r[u].z; ++tx) {
-                    const uint32_t pos = atomicAdd(row + tx, 1u);
-                    if (kScatter) tmp[pos] = key[u];
+            for (int u = 0; u < U; ++u) {
+                if (!tc[u]) continue;
+                const int y0 = max((int)r[u].y, row0), y1 = min((int)r[u].w, row1);
+                for (int ty = y0; ty < y1; ++ty) {
+                    uint32_t* row = s_cnt + (ty - row0) * G.tiles_x;
+                    for (int tx = r[u].x; tx < r[u].z; ++tx) {
+                        const uint32_t pos = atomicAdd(row + tx, 1u);
+                        if (kScatter) tmp[pos] = key[u];
+                    }
                 }
             }
         }
+        if (!kScatter) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < nt; i += blockDim.x) cnt[cbase + (size_t)i * G.B] = s_cnt[i];
+        }
     }
-    if (kScatter) return;
-    __syncthreads();
-    for (int i = threadIdx.x; i < nt; i += blockDim.x) cnt[cbase + (size_t)i * G.B] = s_cnt[i];
 }
 
 // Per (view, tile): range [start, end) from the scanned counts; stats[0] =
@@ -541,7 +549,8 @@ inline BinGeom bin_geom(int64_t n, int n_views, int tiles_x, int tiles_y)
     G.tiles_y = tiles_y;
     G.tiles = tiles_x * tiles_y;
     const int64_t ntile_ids = (int64_t)G.tiles * n_views;
-    int64_t B = n_views == 1 ? kBinBlocksOneView : (kBinBlocks + n_views - 1) / n_views;
+    G.views = n_views;
+    int64_t B = n_views == 1 ? kBinBlocksOneView : kBinBlocks;
     if (B * ntile_ids > kMaxCounts) B = kMaxCounts / ntile_ids;
     if (B > n) B = n;
     if (B < 1) B = 1;
@@ -610,7 +619,7 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     const ushort4* rect4 = reinterpret_cast<const ushort4*>(proj->rect);
     const int64_t ncnt = ntile_ids * G.B;
     const int bands = (tiles_y + G.band_rows - 1) / G.band_rows;
-    const dim3 bin_grid((unsigned)G.B, (unsigned)bands, (unsigned)n_views);
+    const dim3 bin_grid((unsigned)G.B, (unsigned)bands, 1u);
     const size_t bin_smem = sizeof(uint32_t) * (size_t)G.band_rows * (size_t)tiles_x;
 
     if (n > 0) {
