@@ -64,7 +64,7 @@ def _declare(L):
         getattr(L, "oracle_project" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_project" + s).restype = _I32
         getattr(L, "oracle_render" + s).argtypes = [_P, _P, _P, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
-                                                    _P, _P, ctypes.c_double, _P]
+                                                    _P, _P, ctypes.c_double, _P, _P]
         getattr(L, "oracle_render" + s).restype = _I32
         getattr(L, "oracle_vjp" + s).argtypes = [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P]
         getattr(L, "oracle_vjp" + s).restype = _I32
@@ -140,12 +140,15 @@ def project(params, sh_degree, cam, opts, prec="f32"):
 
 
 def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_last=False, want_sig=False,
-           tile_mask=None, dldc_extra=None, l1_weight=1.0, want_tfinal=False):
+           tile_mask=None, dldc_extra=None, l1_weight=1.0, want_tfinal=False, want_mag=False):
     """O7..O10 for one view.  target: [3,H,W] or None (forward only).
     tile_mask: None or [tiles] bool -- render only those tiles (others stay 0).
     dldc_extra: None or [3,H,W] -- another loss term's dL/dC added to the weighted L1 one.
     l1_weight: weight of the L1 term in the loss (and its gradient).
-    want_tfinal: also return the per-pixel final transmittance ("t_final", [H, W])."""
+    want_tfinal: also return the per-pixel final transmittance ("t_final", [H, W]).
+    want_mag: also return "grad2d_mag" [n, 9]: per entry the sum of the magnitudes of
+    the terms grad2d sums (each term with its inner sums taken by absolute value),
+    the scale of the comparison tolerance."""
     dt = _dt(prec)
     rec, rect, vis = proj["rec"], proj["rect"], proj["visible"]
     n = rec.shape[0]
@@ -153,6 +156,7 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
     img = np.zeros((3, H, W), dt)
     loss = np.zeros(1, np.float64)
     g2 = np.zeros((n, 9), np.float64) if (grads and target is not None) else None
+    g2m = np.zeros((n, 9), np.float64) if (want_mag and g2 is not None) else None
     touched = np.zeros(n, np.uint8)
     counts = np.zeros(3, np.int64)
     last = np.zeros(H * W, np.int32) if want_last else None
@@ -164,7 +168,7 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
     rc = getattr(lib(), "oracle_render_" + prec)(_ptr(rec), _ptr(rect), _ptr(vis), n, W, H, _ptr(optsv(opts)), mode,
                                                   _ptr(tgt), _ptr(img), _ptr(loss), _ptr(g2), _ptr(touched),
                                                   _ptr(counts), _ptr(last), _ptr(sig), _ptr(tm),
-                                                  _ptr(ex), float(l1_weight), _ptr(tfin))
+                                                  _ptr(ex), float(l1_weight), _ptr(tfin), _ptr(g2m))
     assert rc == 0
     out = dict(image=img, loss=float(loss[0]) if target is not None else None, grad2d=g2, touched=touched,
                e_fwd=int(counts[0]), e_bwd=int(counts[1]), e_comp=int(counts[2]))
@@ -174,6 +178,8 @@ def render(proj, cam, opts, target=None, mode=1, grads=True, prec="f32", want_la
         out["sig"] = int(sig[0])
     if want_tfinal:
         out["t_final"] = tfin.reshape(H, W)
+    if g2m is not None:
+        out["grad2d_mag"] = g2m
     return out
 
 
@@ -190,6 +196,28 @@ def vjp(params, sh_degree, cam, opts, grad2d, touched, clamp, grads=None, prec="
                                                _ptr(np.ascontiguousarray(clamp, np.uint8)), _ptr(grads))
     assert rc == 0
     return grads
+
+
+def vjp_mag(params, sh_degree, cam, opts, grad2d_mag, touched, clamp, out=None):
+    """Scale of the dense gradient's comparison tolerance, accumulated (+=) into
+    ``out`` [P, n]: sum over the nine 2D gradient components k of
+    |d param / d grad2d_k| * grad2d_mag[:, k].  The VJP is linear in grad2d, so
+    each column's Jacobian row comes from one VJP call with only that column set."""
+    P, n = np.shape(params)
+    if out is None:
+        out = np.zeros((P, n), np.float64)
+    sel = np.flatnonzero(np.asarray(touched))
+    p = np.ascontiguousarray(np.asarray(params, np.float32)[:, sel])
+    m = np.asarray(grad2d_mag, np.float64)[sel]
+    one = np.ones(sel.size, np.uint8)
+    cl = np.ascontiguousarray(np.asarray(clamp, np.uint8)[sel])
+    acc = np.zeros((P, sel.size), np.float64)
+    for k in range(9):
+        col = np.zeros((sel.size, 9), np.float64)
+        col[:, k] = m[:, k]
+        acc += np.abs(vjp(p, sh_degree, cam, opts, col, one, cl))
+    out[:, sel] += acc
+    return out
 
 
 def tile_lists(proj, cam, prec="f32", budget=0):

@@ -530,12 +530,19 @@ static uint64_t fnv(uint64_t h, uint64_t v)
  * tile_mask: NULL, or [tiles] u8: only pixels of tiles with a nonzero entry are
  *   rendered (the rest of image is left untouched and is excluded from the loss,
  *   the gradients and the counts); used to check large images tile by tile.
+ * grad2d_mag: NULL, or [n][9] fp64 accumulated (+=) beside grad2d: for every term
+ *   added to a grad2d entry, the same term with every factor and every sum inside
+ *   it taken by absolute value (dL/dalpha as T |dL/dC|.c + |dL/dC|.S / (1 - alpha),
+ *   d power / d mean2d as |A dx| + |B dy|, ...).  It bounds |grad2d| and is the
+ *   scale at which a sum of these terms in another order, or each term formed
+ *   in fp32, may differ from grad2d: the tolerance of a GPU comparison.  It
+ *   changes nothing else.
  */
 int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visible, int64_t n,
                       int width, int height, const double* optsv, int mode, const REAL* target,
                       REAL* image, double* loss, double* grad2d, uint8_t* touched, int64_t* counts,
                       int32_t* last_idx, uint64_t* sig, const uint8_t* tile_mask, const REAL* dldc_extra,
-                      double l1_weight, REAL* t_final)
+                      double l1_weight, REAL* t_final, double* grad2d_mag)
 {
     opts_t op;
     load_opts(optsv, &op);
@@ -635,14 +642,20 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
                 const REAL* r = rec + 10 * e->g;
                 double* gg = grad2d + 9 * e->g;
                 const double al = e->alpha, Ti = e->T, wgt = al * Ti;
-                double dotc = 0, dots = 0;
+                double dotc = 0, dots = 0, dotc_m = 0, dots_m = 0;
                 for (int ch = 0; ch < 3; ++ch) {
                     gg[6 + ch] += (double)gC[ch] * wgt;
                     dotc += (double)gC[ch] * (double)r[6 + ch];
                     dots += (double)gC[ch] * S[ch];
+                    dotc_m += fabs((double)gC[ch] * (double)r[6 + ch]);
+                    dots_m += fabs((double)gC[ch] * S[ch]);
                 }
                 const double dalpha = Ti * dotc - dots / (1.0 - al);
+                const double dalpha_m = Ti * dotc_m + dots_m / (1.0 - al);
                 for (int ch = 0; ch < 3; ++ch) S[ch] += (double)r[6 + ch] * wgt;
+                double* mm = grad2d_mag ? grad2d_mag + 9 * e->g : 0;
+                if (mm)
+                    for (int ch = 0; ch < 3; ++ch) mm[6 + ch] += fabs((double)gC[ch]) * wgt;
                 if (e->clamped) continue;  /* alpha = 0.99 constant: no gradient to o or power */
                 const double dx = e->dx, dy = e->dy;
                 const double dpow = dalpha * al;
@@ -652,6 +665,15 @@ int FN(oracle_render)(const REAL* rec, const int32_t* rect, const uint8_t* visib
                 gg[4] += dpow * (-0.5 * dy * dy);
                 gg[0] += dpow * ((double)r[2] * dx + (double)r[3] * dy);
                 gg[1] += dpow * ((double)r[3] * dx + (double)r[4] * dy);
+                if (mm) {
+                    const double dpow_m = dalpha_m * al;
+                    mm[5] += dalpha_m * (double)e->G;
+                    mm[2] += dpow_m * (0.5 * dx * dx);
+                    mm[3] += dpow_m * fabs(dx * dy);
+                    mm[4] += dpow_m * (0.5 * dy * dy);
+                    mm[0] += dpow_m * (fabs((double)r[2] * dx) + fabs((double)r[3] * dy));
+                    mm[1] += dpow_m * (fabs((double)r[3] * dx) + fabs((double)r[4] * dy));
+                }
             }
         }
     }

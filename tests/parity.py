@@ -10,6 +10,17 @@ absolute floor of 1e-6.  Projection records, evaluation counts and the touched
 set are compared bit for bit as well, since the forward decisions are
 specified to be reproducible (IEEE operations in a fixed order and one
 portable exp on both sides).
+
+Gradients pass two bars, both asserted.  The literal one, |gpu - ref| <=
+1e-6 + 2e-3 |ref|, says little at full size: the L1 loss is a mean over 3HW
+values, so at 1080p a pixel's dL/dC is 1.6e-7 and most gradient entries are
+below the 1e-6 floor.  The scaled one reads "relative 2e-3, a margin for the
+order of atomic accumulation" against what a sum in another order can change:
+|gpu - ref| <= 2e-3 M + 1e-6 max(M), with M the oracle's sum of the magnitudes
+of the terms each entry is made of (grad2d: ``grad2d_mag``; dense gradients:
+sum_k |d param / d grad2d_k| M_k over views, ``oracle.vjp_mag``) and max(M)
+taken per gradient component (grad2d column, parameter row).  M >= |ref|, and
+M = |ref| where the terms do not cancel, so there the bar is 2e-3 |ref|.
 """
 from __future__ import annotations
 
@@ -40,8 +51,11 @@ def bits(a):
     return a.view(np.uint32) if a.dtype == np.float32 else a.view(np.uint64)
 
 
-def grad_report(gpu, ref, rtol=GRAD_RTOL, atol=GRAD_ATOL):
-    """(ok, stats) for |gpu - ref| <= atol + rtol |ref| elementwise."""
+def grad_report(gpu, ref, mag=None, axis=0, rtol=GRAD_RTOL, atol=GRAD_ATOL):
+    """(ok, stats) for the literal bar |gpu - ref| <= atol + rtol |ref| and, with
+    ``mag`` (same shape as ref: the oracle's sum of term magnitudes), the scaled
+    bar |gpu - ref| <= rtol mag + atol max(mag), max taken along ``axis`` (the axis
+    over Gaussians: 0 for [m, 9] grad2d rows, 1 for [P, n] dense gradients)."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     err = np.abs(gpu - ref)
@@ -49,9 +63,19 @@ def grad_report(gpu, ref, rtol=GRAD_RTOL, atol=GRAD_ATOL):
     scale = np.abs(ref).max() if ref.size else 0.0
     big = np.abs(ref) > 1e-3 * scale
     rel_big = (err[big] / np.abs(ref[big])).max() if big.any() else 0.0
-    return bool(ok.all()), dict(n=int(ref.size), bad=int((~ok).sum()), max_abs_err=float(err.max(initial=0.0)),
-                                max_abs_ref=float(scale), max_rel_err_significant=float(rel_big),
-                                n_significant=int(big.sum()))
+    st = dict(n=int(ref.size), bad=int((~ok).sum()), max_abs_err=float(err.max(initial=0.0)),
+              max_abs_ref=float(scale), max_rel_err_significant=float(rel_big), n_significant=int(big.sum()))
+    if mag is not None:
+        mag = np.asarray(mag, np.float64)
+        assert mag.shape == ref.shape
+        floor = mag.max(axis=axis, keepdims=True, initial=0.0) if mag.size else mag
+        tol = rtol * mag + atol * floor
+        ok_s = err <= tol
+        st.update(bad_scaled=int((~ok_s).sum()),
+                  max_err_over_scaled_tol=float((err / np.maximum(tol, 1e-300)).max(initial=0.0)),
+                  max_err_over_mag=float((err / np.maximum(mag, 1e-300)).max(initial=0.0)))
+        ok = ok & ok_s
+    return bool(ok.all()), st
 
 
 def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print):
@@ -140,7 +164,7 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
     efwd = ebwd = ecomp = 0
     orend = []
     for v, cam in enumerate(sc.cameras):
-        out = oracle.render(oprojs[v], cam, sc.opts, target=targets[v])
+        out = oracle.render(oprojs[v], cam, sc.opts, target=targets[v], want_mag=True)
         orend.append(out)
         d = np.abs(img[v].astype(np.float64) - out["image"])
         stats.setdefault("img_max_abs_err", []).append(float(d.max()))
@@ -148,7 +172,8 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
         assert d.max() <= IMG_ATOL, f"view {v}: image max abs err {d.max()}"
         assert abs(loss[v] - out["loss"]) <= 1e-9 * max(1.0, abs(out["loss"])), (loss[v], out["loss"])
         assert np.array_equal(touched[v], out["touched"]), f"view {v}: touched sets differ"
-        ok, st = grad_report(g2d[v][out["touched"] > 0], out["grad2d"][out["touched"] > 0])
+        tv = out["touched"] > 0
+        ok, st = grad_report(g2d[v][tv], out["grad2d"][tv], out["grad2d_mag"][tv])
         stats.setdefault("grad2d", []).append(st)
         assert ok, f"view {v}: grad2d out of tolerance {st}"
         efwd += out["e_fwd"]
@@ -163,15 +188,18 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
     idx = tr.idx.cpu().numpy().view(np.uint32)
     n_idx = tr.n_idx.cpu().numpy()
     ref_grads = np.zeros((P, n), np.float64)
+    ref_mag = np.zeros((P, n), np.float64)
     for v, cam in enumerate(sc.cameras):
         exp_idx = oracle.compact(orend[v]["touched"])
         assert n_idx[v] == exp_idx.size and np.array_equal(idx[v][:n_idx[v]], exp_idx), f"view {v}: compacted list"
         oracle.vjp(sc.params, sc.sh_degree, cam, sc.opts, orend[v]["grad2d"], orend[v]["touched"],
                    oprojs[v]["clamp"], ref_grads)
+        oracle.vjp_mag(sc.params, sc.sh_degree, cam, sc.opts, orend[v]["grad2d_mag"], orend[v]["touched"],
+                       oprojs[v]["clamp"], ref_mag)
     union = oracle.compact(np.any(np.stack([o["touched"] for o in orend]), 0).astype(np.uint8))
     assert n_idx[V] == union.size and np.array_equal(idx[V][:n_idx[V]], union), "union list"
     grads = tr.rows(tr.grads).cpu().numpy()
-    ok, st = grad_report(grads, ref_grads)
+    ok, st = grad_report(grads, ref_grads, ref_mag, axis=1)
     stats["grads"] = st
     assert ok, f"dense gradients out of tolerance {st}"
     assert not tr.grad2d.any().item() and not tr.touched.any().item(), "grad2d / touched not cleared"
@@ -195,18 +223,35 @@ def run_stage_parity(sc, targets=None, device="cuda", check_adam=True, log=print
     return stats
 
 
+def _parallel(fn, items, threads=None):
+    """fn over items on threads: each oracle call is one single-threaded C call made
+    through ctypes, which releases the GIL, so independent views run side by side.
+    The oracle's lazily built constants are built first, on this thread."""
+    import concurrent.futures
+    import os
+    oracle.pexp_f32([0.0])
+    oracle.sh_basis(np.array([[0.0, 0.0, 1.0]]))
+    threads = threads or max(1, min(len(items), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(fn, items))
+
+
 def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, device="cuda", log=print):
     """Parity at full size where the oracle cannot render whole images quickly.
 
     Per checked view the oracle projects every Gaussian (visibility and records
     compared for all), builds every tile list (sorted keys/ids/ranges compared for
     all), and renders a sample of tiles: random ones plus every tile of a sample
-    of Gaussians, so those Gaussians' 2D gradients are complete.  Images are
-    compared on the sampled tiles; the training target of the GPU (its render of
-    the perturbed scene) must equal the oracle's render of the perturbed scene
-    there bit for bit, and the oracle's loss terms use the oracle's own target.
-    Single-view scenes also compare the sampled Gaussians' dense gradients and
-    their Adam update."""
+    of Gaussians, so those Gaussians' 2D gradients are complete.  The sampled
+    Gaussians are drawn among those whose tile rect is at most 4 tiles in every
+    checked view, and their tiles are rendered in every checked view, so that with
+    all views checked their gradients summed over the views are complete too.
+    Images are compared on the sampled tiles; the training target of the GPU (its
+    render of the perturbed scene) must equal the oracle's render of the perturbed
+    scene there bit for bit, and the oracle's loss terms use the oracle's own
+    target.  With every view checked, the sampled Gaussians' membership of each
+    view's compacted list and of the union, their dense gradients (summed over
+    the views) and their Adam update are compared as well."""
     rng = np.random.default_rng(seed)
     V, n = sc.n_views, sc.n
     views = list(range(V)) if check_views is None else list(check_views)
@@ -230,76 +275,124 @@ def run_sampled_parity(sc, check_views=None, n_tiles=48, n_gauss=300, seed=0, de
     stats = dict(instances=int(N), views=views)
     tiles = tr.tiles
     tiles_x = (sc.cameras[0].width + 15) // 16
-    sampled_g = {}
-    for v in views:
+
+    # phase 1, per view: every record, every tile list; which Gaussians have small rects
+    def lists(v):
         cam = sc.cameras[v]
         pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
         vis = pr["visible"].astype(bool)
         assert np.array_equal(tt[v] > 0, vis), f"view {v}: visibility"
-        rec = tr.rec[v][torch.from_numpy(np.flatnonzero(vis)).to(device)].cpu().numpy()
         o = pr["rec"][vis]
         exp = np.stack([o[:, 0], o[:, 1], np.float32(-0.5) * o[:, 2], o[:, 3], np.float32(-0.5) * o[:, 4], o[:, 5],
                         o[:, 6], o[:, 7], o[:, 8]], 1).astype(np.float32)
+        rec = tr.rec[v][torch.from_numpy(np.flatnonzero(vis)).to(device)].cpu().numpy()
         assert np.array_equal(bits(rec[:, :9]), bits(exp)), f"view {v}: projection records"
+        del rec
         off, oids = oracle.tile_lists(pr, cam)
         base = int(ranges[v][:, 0][np.diff(off) > 0].min()) if off[-1] else 0
         m = oids.size
         assert np.array_equal(ids[base:base + m], oids.astype(np.uint32)), f"view {v}: sorted ids"
         tile_of = np.repeat(np.arange(tiles, dtype=np.uint64), np.diff(off).astype(np.int64))
         dbits = bits(pr["rec"][oids, 9]).astype(np.uint64)
-        assert np.array_equal(keys[base:base + m], ((np.uint64(v * tiles) + tile_of) << np.uint64(32)) | dbits)
+        assert np.array_equal(keys[base:base + m], ((np.uint64(v * tiles) + tile_of) << np.uint64(32)) | dbits), \
+            f"view {v}: sorted keys"
         full = np.diff(off) > 0
         assert np.array_equal(ranges[v][full, 0], (off[:-1][full] + base).astype(np.uint32)), f"view {v}: ranges"
-        # sampled tiles: random ones + all tiles of sampled Gaussians with small rects
+        assert np.array_equal(ranges[v][full, 1], (off[1:][full] + base).astype(np.uint32)), f"view {v}: range ends"
         rect = pr["rect"]
         area = (rect[:, 2] - rect[:, 0]) * (rect[:, 3] - rect[:, 1])
-        cand = np.flatnonzero(vis & (area <= 4))
-        gs = rng.choice(cand, min(n_gauss, cand.size), replace=False)
+        return vis, vis & (area <= 4), int(m)
+
+    p1 = _parallel(lists, views)
+    stats["checked_instances"] = int(sum(x[2] for x in p1))
+    any_vis = np.zeros(n, bool)
+    small_everywhere = np.ones(n, bool)
+    for vis, small, _ in p1:
+        any_vis |= vis
+        small_everywhere &= (~vis) | small
+    del p1
+    cand = np.flatnonzero(any_vis & small_everywhere)
+    gs = np.sort(rng.choice(cand, min(n_gauss, cand.size), replace=False))
+    sub = np.ascontiguousarray(sc.params[:, gs])
+    sub_pert = np.ascontiguousarray(sc.perturbed_params[:, gs])
+    g2d_gpu = tr.grad2d[:, torch.from_numpy(gs).to(device)].cpu().numpy()[..., :9]
+    tch_gpu = tr.touched[:, torch.from_numpy(gs).to(device)].cpu().numpy()
+
+    # phase 2, per view: the sampled tiles rendered (target and training render)
+    def tiles_of(v):
+        cam = sc.cameras[v]
+        prs = oracle.project(sub, sc.sh_degree, cam, sc.opts)
+        rect = prs["rect"]
         mask = np.zeros(tiles, bool)
-        mask[rng.choice(tiles, n_tiles, replace=False)] = True
-        for g in gs:
-            for ty in range(rect[g, 1], rect[g, 3]):
-                mask[ty * tiles_x + rect[g, 0]:ty * tiles_x + rect[g, 2]] = True
+        mask[np.random.default_rng([seed, v]).choice(tiles, n_tiles, replace=False)] = True
+        for k in np.flatnonzero(prs["visible"]):
+            for ty in range(rect[k, 1], rect[k, 3]):
+                mask[ty * tiles_x + rect[k, 0]:ty * tiles_x + rect[k, 2]] = True
         prp = oracle.project(sc.perturbed_params, sc.sh_degree, cam, sc.opts)
         otgt = oracle.render(prp, cam, sc.opts, tile_mask=mask)["image"]
+        del prp
         H, W = cam.height, cam.width
         pix = np.repeat(np.repeat(mask.reshape(-1, tiles_x), 16, 0), 16, 1)[:H, :W]
         assert np.array_equal(bits(tgt_gpu[v][:, pix]), bits(otgt[:, pix])), f"view {v}: target render"
-        out = oracle.render(pr, cam, sc.opts, target=otgt, tile_mask=mask)
+        pr = oracle.project(sc.params, sc.sh_degree, cam, sc.opts)
+        out = oracle.render(pr, cam, sc.opts, target=otgt, tile_mask=mask, want_mag=True)
         d = np.abs(img[v][:, pix].astype(np.float64) - out["image"][:, pix])
         assert d.max() <= IMG_ATOL, f"view {v}: image max abs err {d.max()}"
-        g2d = tr.grad2d[v][torch.from_numpy(gs).to(device)].cpu().numpy()[:, :9]
-        tch = tr.touched[v][torch.from_numpy(gs).to(device)].cpu().numpy()
-        assert np.array_equal(tch, out["touched"][gs]), f"view {v}: touched (sampled)"
-        ok, st = grad_report(g2d, out["grad2d"][gs])
+        assert np.array_equal(tch_gpu[v], out["touched"][gs]), f"view {v}: touched (sampled)"
+        ok, st = grad_report(g2d_gpu[v], out["grad2d"][gs], out["grad2d_mag"][gs])
         assert ok, f"view {v}: grad2d (sampled) {st}"
-        stats.setdefault("grad2d", []).append(st)
-        stats.setdefault("sampled_pixels", []).append(int(pix.sum()))
-        sampled_g[v] = (gs, out["grad2d"][gs], out["touched"][gs], pr["clamp"][gs])
-    if V == 1:
-        gs, g2, tch, clamp = sampled_g[0]
+        return dict(st=st, pix=int(pix.sum()), g2=out["grad2d"][gs], mag=out["grad2d_mag"][gs],
+                    tch=out["touched"][gs], clamp=pr["clamp"][gs])
+
+    p2 = _parallel(tiles_of, views)
+    stats["grad2d"] = [x["st"] for x in p2]
+    stats["sampled_pixels"] = [x["pix"] for x in p2]
+    stats["sampled_gaussians"] = int(gs.size)
+    if len(views) == V:
         tr.compact()
         torch.cuda.synchronize()
-        sub = np.ascontiguousarray(sc.params[:, gs])
-        ref = oracle.vjp(sub, sc.sh_degree, sc.cameras[0], sc.opts, g2, tch, clamp)
-        got = tr.rows(tr.grads)[:, torch.from_numpy(gs).to(device)].cpu().numpy()
-        ok, st = grad_report(got, ref)
+        n_idx = tr.n_idx.cpu().numpy()
+        idx = tr.idx.cpu().numpy().view(np.uint32)
+        tch_any = np.zeros(gs.size, bool)
+        for v in range(V):
+            lst = idx[v][:n_idx[v]]
+            assert np.all(np.diff(lst.astype(np.int64)) > 0), f"view {v}: compacted list not ascending"
+            assert np.array_equal(np.isin(gs, lst), p2[v]["tch"] > 0), f"view {v}: compacted list (sampled)"
+            tch_any |= p2[v]["tch"] > 0
+        union = idx[V][:n_idx[V]]
+        assert np.all(np.diff(union.astype(np.int64)) > 0), "union list not ascending"
+        assert np.array_equal(np.isin(gs, union), tch_any), "union list (sampled)"
+        if V > 1:
+            allv = np.unique(np.concatenate([idx[v][:n_idx[v]] for v in range(V)]))
+            assert np.array_equal(union, allv), "union = the per-view lists merged"
+        stats["union"] = int(n_idx[V])
+        ref = np.zeros(sub.shape, np.float64)
+        mag = np.zeros(sub.shape, np.float64)
+        for v in range(V):
+            cam = sc.cameras[v]
+            oracle.vjp(sub, sc.sh_degree, cam, sc.opts, p2[v]["g2"], p2[v]["tch"], p2[v]["clamp"], ref)
+            oracle.vjp_mag(sub, sc.sh_degree, cam, sc.opts, p2[v]["mag"], p2[v]["tch"], p2[v]["clamp"], mag)
+        gidx = torch.from_numpy(gs).to(device)
+        got = tr.rows(tr.grads)[:, gidx].cpu().numpy()
+        m = tch_any
+        ok, st = grad_report(got[:, m], ref[:, m], mag[:, m], axis=1)
         assert ok, f"dense gradients (sampled) {st}"
         stats["grads"] = st
-        # Adam for the sampled Gaussians, fed the GPU's gradients
+        # Adam for the sampled Gaussians, fed the GPU's gradients, at the scene's learning rates
         p_o = sub.copy()
         m_o = np.zeros_like(p_o)
         v_o = np.zeros_like(p_o)
         last_o = np.zeros(gs.size, np.int32)
-        sel = np.flatnonzero(tch).astype(np.uint32)
+        sel = np.flatnonzero(tch_any).astype(np.uint32)
         g_o = got.astype(np.float32).copy()
         oracle.adam_deferred(p_o, m_o, v_o, g_o, last_o, scenes.lr_rows(sc.lr, sc.sh_degree), sel, 1,
                              tr.betas[0], tr.betas[1], tr.eps)
         tr.adam(1)
         torch.cuda.synchronize()
-        idx = torch.from_numpy(gs).to(device)
-        assert np.array_equal(bits(tr.rows(tr.params)[:, idx].cpu().numpy()), bits(p_o)), "Adam params (sampled)"
-        assert np.array_equal(bits(tr.rows(tr.adam_m)[:, idx].cpu().numpy()), bits(m_o)), "Adam m (sampled)"
+        assert np.array_equal(bits(tr.rows(tr.params)[:, gidx].cpu().numpy()), bits(p_o)), "Adam params (sampled)"
+        assert np.array_equal(bits(tr.rows(tr.adam_m)[:, gidx].cpu().numpy()), bits(m_o)), "Adam m (sampled)"
+        assert np.array_equal(bits(tr.rows(tr.adam_v)[:, gidx].cpu().numpy()), bits(v_o)), "Adam v (sampled)"
+        assert np.array_equal(tr.last_step[gidx].cpu().numpy(), last_o), "last_step (sampled)"
     log(f"[sampled parity] {sc.name}: {stats}")
     del tr
     torch.cuda.empty_cache()
@@ -387,6 +480,7 @@ def run_dssim_parity(sc, lam=0.2, targets=None, device="cuda", log=print):
     touched = tr.touched.cpu().numpy().copy()
     counts = tr.eval_counts.cpu().numpy()
     ref_grads = np.zeros((P, n), np.float64)
+    ref_mag = np.zeros((P, n), np.float64)
     ef = eb = ec = 0
     touched_o = []
     for v, cam in enumerate(sc.cameras):
@@ -401,12 +495,14 @@ def run_dssim_parity(sc, lam=0.2, targets=None, device="cuda", log=print):
         eb += fw["e_bwd"]
         ec += fw["e_comp"]
         check_dssim_stage(img[v], targets[v], lam, loss[v], dldc[v], stats, tag=f"view {v}")
-        bw = oracle.render(pr, cam, sc.opts, target=targets[v], dldc_extra=dldc[v], l1_weight=0.0)
+        bw = oracle.render(pr, cam, sc.opts, target=targets[v], dldc_extra=dldc[v], l1_weight=0.0, want_mag=True)
         assert np.array_equal(touched[v], bw["touched"]), f"view {v}: touched sets differ"
-        ok, st = grad_report(g2d[v][bw["touched"] > 0], bw["grad2d"][bw["touched"] > 0])
+        tv = bw["touched"] > 0
+        ok, st = grad_report(g2d[v][tv], bw["grad2d"][tv], bw["grad2d_mag"][tv])
         stats.setdefault("grad2d", []).append(st)
         assert ok, f"view {v}: grad2d out of tolerance {st}"
         oracle.vjp(sc.params, sc.sh_degree, cam, sc.opts, bw["grad2d"], bw["touched"], pr["clamp"], ref_grads)
+        oracle.vjp_mag(sc.params, sc.sh_degree, cam, sc.opts, bw["grad2d_mag"], bw["touched"], pr["clamp"], ref_mag)
         touched_o.append(bw["touched"])
     assert (int(counts[0]), int(counts[1]), int(counts[2])) == (ef, eb, ec), (counts, ef, eb, ec)
     tr.compact()
@@ -414,7 +510,7 @@ def run_dssim_parity(sc, lam=0.2, targets=None, device="cuda", log=print):
     union = oracle.compact(np.any(np.stack(touched_o), 0).astype(np.uint8))
     n_idx = tr.n_idx.cpu().numpy()
     assert n_idx[V] == union.size and np.array_equal(tr.idx.cpu().numpy().view(np.uint32)[V][:n_idx[V]], union)
-    ok, st = grad_report(tr.rows(tr.grads).cpu().numpy(), ref_grads)
+    ok, st = grad_report(tr.rows(tr.grads).cpu().numpy(), ref_grads, ref_mag, axis=1)
     stats["grads"] = st
     assert ok, f"dense gradients out of tolerance {st}"
     log(f"[dssim parity] {sc.name} lambda={lam}: {stats}")

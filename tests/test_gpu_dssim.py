@@ -138,7 +138,9 @@ def test_lambda_zero_reproduces_the_fused_l1_kernel():
     assert np.array_equal(a["t"], b["t"]) and np.array_equal(a["c"], b["c"])
     assert abs(a["loss"][0] - b["loss"][0]) <= 1e-12 * a["loss"][0]
     m = a["t"][0] > 0
-    ok, st = parity.grad_report(b["g"][0][m], a["g"][0][m])
+    pr = oracle.project(sc.params, sc.sh_degree, sc.cameras[0], sc.opts)
+    mag = oracle.render(pr, sc.cameras[0], sc.opts, target=targets[0], want_mag=True)["grad2d_mag"]
+    ok, st = parity.grad_report(b["g"][0][m], a["g"][0][m], mag[m])
     assert ok, st
 
 
@@ -165,7 +167,10 @@ def test_backward_with_stored_pass_bits_equals_recomputing_them():
     torch.cuda.synchronize()
     assert torch.equal(t_bits, tr.touched)
     m = t_bits[0].cpu().numpy() > 0
-    ok, st = parity.grad_report(g_bits.cpu().numpy()[0][m][:, :9], tr.grad2d.cpu().numpy()[0][m][:, :9])
+    pr = oracle.project(sc.params, 0, sc.cameras[0], sc.opts)
+    mag = oracle.render(pr, sc.cameras[0], sc.opts, target=parity.oracle_targets(sc)[0],
+                        dldc_extra=tr.dldc[0].cpu().numpy(), l1_weight=0.0, want_mag=True)["grad2d_mag"]
+    ok, st = parity.grad_report(g_bits.cpu().numpy()[0][m][:, :9], tr.grad2d.cpu().numpy()[0][m][:, :9], mag[m])
     assert ok, st
 
 
