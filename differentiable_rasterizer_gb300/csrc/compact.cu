@@ -195,10 +195,32 @@ __device__ __align__(256) unsigned char g_compact_scratch[kStaticScratchBytes];
 
 // Device address of g_compact_scratch per device ordinal.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and cached.
+// per device, with that device current, and cached together with the id of the
+// context it belongs to: a device reset (cudaDeviceReset) destroys that context
+// and the array with it, and the next call, seeing another context, looks the
+// address up again instead of handing a stale pointer to the kernels.
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
+
+// Id of the current context (cuCtxGetId, through the runtime's driver entry
+// point: no link dependency on the driver library); false if there is none yet.
+bool current_context_id(unsigned long long* id)
+{
+    using CtxGetId = int (*)(void*, unsigned long long*);
+    static CtxGetId fn = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetId>(p);
+        looked_up = true;
+    }
+    return fn && fn(nullptr, id) == 0;
+}
 
 gs_status static_scratch(void** out)
 {
@@ -206,10 +228,14 @@ gs_status static_scratch(void** out)
     if (cudaGetDevice(&dev) != cudaSuccess) return GS_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return GS_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    unsigned long long ctx = 0;
+    const bool known = current_context_id(&ctx);
+    if (!g_scratch_addr[dev] || !known || ctx != g_scratch_ctx[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_compact_scratch) != cudaSuccess || !p) return GS_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        // the lookup makes the device's context current if it was not yet
+        g_scratch_ctx[dev] = current_context_id(&ctx) ? ctx : 0;
     }
     *out = g_scratch_addr[dev];
     return GS_OK;

@@ -297,3 +297,166 @@ def test_randomised_configurations(seed):
     sc.target_uniform = rng.uniform(0, 1, (views, 3, H, W)).astype(np.float32)
     sc.opts = dict(sc.opts, exclude_crossing=int(rng.integers(0, 2)), bg=tuple(float(x) for x in rng.uniform(0, 1, 3)))
     parity.run_stage_parity(sc)
+
+
+def _corrupt_rows(sc, seed):
+    """Rows of the scene's parameters made non-finite or degenerate, one kind per row:
+    NaN / +inf means, NaN / +inf log-scales, zero, NaN and +inf quaternions, NaN
+    logits, NaN / +inf colours (degree 3: DC coefficients); degree 3 also gets -inf
+    higher-band coefficients (a colour clamped at 0: visible on both sides)."""
+    rng = np.random.default_rng(seed)
+    p = sc.params.copy()
+    kinds = [(0, np.nan), (1, np.inf), (2, np.nan), (3, np.nan), (4, np.inf), ("q", 0.0), ("q", np.nan),
+             ("q", np.inf), (10, np.nan), (11, np.nan), (12, np.inf)]
+    rows = rng.choice(p.shape[1], 4 * len(kinds), replace=False)
+    culled = []
+    for i, g in enumerate(rows):
+        what, val = kinds[i % len(kinds)]
+        if what == "q":
+            p[6:10, g] = val
+        else:
+            p[what, g] = val
+        culled.append(g)
+    clamped = []
+    if sc.sh_degree == 3:
+        extra = rng.choice(np.setdiff1d(np.arange(p.shape[1]), rows), 40, replace=False)
+        p[11 + 3 * 5, extra] = -np.inf
+        clamped = list(extra)
+    sc.params = p
+    return np.asarray(culled), np.asarray(clamped, np.int64)
+
+
+@pytest.mark.parametrize("sh", [0, 3])
+def test_non_finite_and_degenerate_rows_are_culled_as_the_oracle_culls_them(sh):
+    """NaN / inf parameters and zero quaternions go through projection, binning,
+    raster, compaction and Adam on the GPU exactly as through the oracle: the rows
+    culled there (and only those) are culled here, every other output compared as
+    usual, and the culled rows' parameters come out of Adam untouched."""
+    if sh == 0:
+        sc = scenes.make_scene("tiny")
+    else:
+        sc = scenes.make_scene("medium", n=20000)
+        c = sc.cameras[0]
+        sc.cameras = [scenes.Camera(c.R, c.t, 350.0, 350.0, 240.0, 135.0, 480, 270)]
+        sc.target_kind = "uniform"
+        sc.target_uniform = np.random.default_rng(9).uniform(0, 1, (1, 3, 270, 480)).astype(np.float32)
+    culled, clamped = _corrupt_rows(sc, 30 + sh)
+    pr = oracle.project(sc.params, sc.sh_degree, sc.cameras[0], sc.opts)
+    assert not pr["visible"][culled].any()
+    if clamped.size:
+        assert pr["visible"][clamped].sum() > 10 and (pr["clamp"][clamped][pr["visible"][clamped] > 0] > 0).all()
+    st = parity.run_stage_parity(sc)
+    assert st["visible"][0] > 0
+
+
+def test_checkpoint_resume_reproduces_the_next_step(tmp_path):
+    """Three steps, a checkpoint (state_dict flushes the deferred Adam states, then
+    copies; saved to disk), then step 4 two ways: in the same trainer, and in a
+    fresh trainer loaded from the file.  The loaded state is the saved one bit for
+    bit, and so is everything step 4 decides (records, lists, image, counts,
+    touched and union lists).  The loss and the gradients are sums of atomic
+    additions whose order varies from run to run -- even two runs of one trainer
+    from one state differ in their last bits -- so they are held to the parity
+    bars (loss 1e-9 relative; gradients the scaled gradient bar, its scale taken
+    from the oracle at the checkpointed parameters), and Adam, fed one trainer's
+    gradients, to bit equality."""
+    sc = scenes.make_scene("medium", n=20000)
+    c = sc.cameras[0]
+    sc.cameras = [scenes.Camera(c.R, c.t, 350.0, 350.0, 240.0, 135.0, 480, 270)]
+    targets = parity.oracle_targets(sc)
+    tgt = torch.from_numpy(targets).cuda()
+
+    def trainer():
+        return pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr)
+
+    a = trainer()
+    for _ in range(3):
+        a.train_step(tgt)
+    path = tmp_path / "ckpt.pt"
+    saved = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in a.state_dict().items()}
+    torch.save(saved, path)
+    assert (a.last_step.cpu().numpy() == 3).all()
+    b = trainer()
+    b.load_state_dict(torch.load(path))
+    assert b.t == 3
+    for name, key in (("params", "params"), ("adam_m", "m"), ("adam_v", "v"), ("last_step", "last_step")):
+        assert torch.equal(getattr(b, name).cpu(), saved[key]) and torch.equal(getattr(a, name), getattr(b, name))
+    p3 = a.rows(a.params).cpu().numpy()
+    out = []
+    for tr in (a, b):
+        tr.t += 1
+        tr.project()
+        tr.bin_sort()
+        tr.raster(tgt)
+        tr.compact()
+        torch.cuda.synchronize()
+        n_idx = tr.n_idx.cpu().numpy().copy()
+        vis = tr.tiles_touched[0].cpu().numpy() > 0          # culled Gaussians' records are not written
+        out.append(dict(vis=vis, rec=tr.rec[0].cpu().numpy()[vis], ids=tr.ids[:tr.n_instances].cpu().numpy().copy(),
+                        keys=tr.keys[:tr.n_instances].cpu().numpy().copy(), img=tr.image.cpu().numpy().copy(),
+                        loss=float(tr.loss[0]), n_idx=n_idx, idx=tr.idx[1, :n_idx[1]].cpu().numpy().copy(),
+                        grads=tr.rows(tr.grads).cpu().numpy().copy()))
+    x, y = out
+    for k in ("vis", "rec", "ids", "keys", "img", "n_idx", "idx"):
+        assert np.array_equal(x[k], y[k]), k
+    assert abs(x["loss"] - y["loss"]) <= 1e-9 * abs(x["loss"])
+    pr = oracle.project(p3, sc.sh_degree, sc.cameras[0], sc.opts)
+    ro = oracle.render(pr, sc.cameras[0], sc.opts, target=targets[0], want_mag=True)
+    mag = oracle.vjp_mag(p3, sc.sh_degree, sc.cameras[0], sc.opts, ro["grad2d_mag"], ro["touched"], pr["clamp"])
+    u = x["idx"].astype(np.int64)
+    ok, st = parity.grad_report(y["grads"][:, u], x["grads"][:, u], mag[:, u], axis=1)
+    assert ok, st
+    b.grads.copy_(a.grads)
+    for tr in (a, b):
+        tr.adam(tr.t)
+    torch.cuda.synchronize()
+    for name in ("params", "adam_m", "adam_v", "last_step"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert int(a.last_step.max()) == 4 and int(a.last_step.min()) == 3   # still deferred where untouched
+
+
+@pytest.mark.parametrize("exclude", [0, 1])
+def test_work_counting_variant_matches_the_fused_kernel(exclude):
+    """gs_raster_work_counts renders and differentiates exactly like the fused call
+    (image, loss, touched set bit for bit; 2D gradients at the bar), and its counts
+    obey what the method fixes: every composited (pixel, entry) is processed once
+    in the backward (queued + per-Gaussian = E_comp); every entry the composite
+    walks is composited, except, with the crossing entry excluded, the one each
+    stopping pixel stops at; every chunk of every list is staged unless its tile
+    stopped early."""
+    from differentiable_rasterizer_gb300 import abi
+    sc = scenes.random_small_scene(71, n=5000, width=96, height=80, sh_degree=0, log_lo=-3.2, log_hi=-1.6,
+                                   logit_mu=1.0, spread=1.2)
+    sc.opts = dict(sc.opts, exclude_crossing=exclude)
+    tgt = torch.from_numpy(parity.oracle_targets(sc)).cuda()
+    tr = pipeline.GaussianTrainer(sc.params, 0, sc.cameras, sc.opts, sc.lr)
+    tr.project()
+    tr.bin_sort()
+    tr.eval_counts.zero_()
+    tr.raster(tgt)
+    torch.cuda.synchronize()
+    ref = dict(img=tr.image.clone(), loss=tr.loss.clone(), g=tr.grad2d.clone(), t=tr.touched.clone(),
+               c=tr.eval_counts.cpu().numpy().copy())
+    tr.grad2d.zero_()
+    tr.touched.zero_()
+    w = tr.work_counts(tgt)
+    torch.cuda.synchronize()
+    assert torch.equal(tr.image, ref["img"]) and torch.equal(tr.touched, ref["t"])
+    assert abs(float(tr.loss[0]) - float(ref["loss"][0])) <= 1e-12 * abs(float(ref["loss"][0]))
+    m = ref["t"][0].cpu().numpy() > 0
+    ok, st = parity.grad_report(tr.grad2d[0].cpu().numpy()[m][:, :9], ref["g"][0].cpu().numpy()[m][:, :9])
+    assert ok, st
+    e_comp = int(ref["c"][2])
+    assert w["sparse_entries"] + w["dense_entries"] == e_comp, (w, e_comp)
+    pixels = sc.cameras[0].width * sc.cameras[0].height
+    if exclude:
+        assert e_comp <= w["composite_walks"] <= e_comp + pixels
+    else:
+        assert w["composite_walks"] == e_comp, (w, e_comp)
+    assert w["pairs"] >= w["pair_exps"] >= w["composite_walks"] - (pixels if exclude else 0)
+    ranges = tr.ranges.cpu().numpy().view(np.uint32).reshape(-1, 2)
+    lens = (ranges[:, 1] - ranges[:, 0]).astype(np.int64)
+    assert (lens > 256).any()
+    assert 0 < w["chunks"] <= int(((lens + 255) // 256).sum())
+    assert 0 < w["restaged_chunks"] and w["recomputed_chunks"] <= w["restaged_chunks"]
+    assert w["sparse_rounds"] * 32 >= w["sparse_entries"]

@@ -1,8 +1,13 @@
-"""GPU parity on the full-size large and batched workloads (sampled tiles and
-Gaussians, every record and every tile list), on the batched recipe at a
-reduced size where every output is compared, and on the medium workload (the
-one the bench times) for the next-ranked rows: the L1 + D-SSIM step, the step
-on pruned lists, and the partial render + compose -- every output compared."""
+"""GPU parity at full size: the large workload with every output compared (the
+whole 4096x2160 image, loss, counts, touched set, every 2D and dense gradient,
+Adam); the batched workload (20 M Gaussians x 16 views) with every record and
+every tile list of all 16 views compared, images and 2D gradients on sampled
+tiles and Gaussians in every view, and the sampled Gaussians' compacted-list and
+union membership, dense gradients summed over the 16 views and Adam update at
+the batch-scaled learning rates; the batched recipe at a reduced size where every
+output is compared; and the medium workload (the one the bench times) for the
+next-ranked rows: the L1 + D-SSIM step, the step on pruned lists, and the
+partial render + compose -- every output compared."""
 import math
 
 import numpy as np
@@ -25,15 +30,19 @@ def _built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def test_large_full_size_sampled():
-    st = parity.run_sampled_parity(scenes.make_scene("large"), n_tiles=64, n_gauss=400, seed=1)
+def test_large_full_size_every_output():
+    st = parity.run_stage_parity(scenes.make_scene("large"))
     assert st["instances"] > 5_000_000
+    assert st["grads"]["bad"] == 0 and st["grads"]["bad_scaled"] == 0
 
 
-def test_batched_full_size_sampled_views():
-    st = parity.run_sampled_parity(scenes.make_scene("batched"), check_views=(0, 9), n_tiles=32, n_gauss=200,
-                                   seed=2)
-    assert st["instances"] > 100_000_000
+def test_batched_full_size_all_views():
+    sc = scenes.make_scene("batched")
+    # Grendel, abstract: the learning rate scales with the square root of the batch size
+    assert np.allclose(sc.lr, np.asarray(scenes.DEFAULT_LR) * math.sqrt(16.0))
+    st = parity.run_sampled_parity(sc, n_tiles=32, n_gauss=240, seed=2)
+    assert st["instances"] > 100_000_000 and st["checked_instances"] == st["instances"]
+    assert len(st["grad2d"]) == 16 and st["grads"]["bad_scaled"] == 0
 
 
 def test_batched_recipe_reduced_all_views_elementwise():
