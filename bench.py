@@ -50,14 +50,29 @@ WORKLOADS = {
     "batched": "batched: 20,000,000 Gaussians, SH degree 3, 16 views 1920x1080, gradients summed",
 }
 
-# Algorithmic work of the fused raster kernel per unit, as the hot-path survey
-# states it (one FP32 op = one FP32-pipe lane instruction; an fma counts once):
-#   every forward evaluation:  14 FP32 ops + 1 exp
-#   every backward evaluation: 47 FP32 ops + 1 exp + 1 reciprocal
-# (a) exp and the reciprocal as one special-function (SFU) op each;
-# (b) exp as the portable polynomial's FP32 ops (14: scale, round, 2-fma reduction,
-#     7-fma Horner, exponent add), the reciprocal on the SFU.
-# The roofline time is the slower of the FP32 pipe and the SFU pipe.
+# Work of the fused raster kernel.  The metric's units are the method's
+# evaluations (E_fwd: list entries up to each pixel's stop; E_bwd: entries up to
+# its last composited one), but the kernel executes far fewer: the per-Gaussian
+# support box and alpha cut skip, with results unchanged, every pair that cannot
+# pass.  The roofline therefore charges what the kernel executes, counted by its
+# counting variant (gs_raster_work_counts) in one untimed launch, at the FP32
+# operations each item performs in the source (an fma counts once; compares,
+# integer and shared-memory work not counted):
+#   pair swept:          14  (pixel centre, dx, dy, power, the row/column split)
+#   pair exponential:    14  (portable exp 12: scale, round, 2-fma reduction,
+#                             7-fma Horner; alpha = min(0.99, o G) 2)
+#   composite walk:      33  (dx, dy, power, exp, alpha, T update, C += c w T)
+#   backward, queued:    74  + 1 SFU reciprocal (power, exp, alpha, 1 / (1 - alpha),
+#                             dL/dC . c, 5-step (product, sum) scan, 9 gradient terms)
+#   backward, per Gaussian: 56 + 1 SFU reciprocal per (entry, pixel), and 12 adds
+#                             per lane per warp step (recursive-halving warp sum)
+#   per pixel:           15  (background, L1 difference, signs, S init)
+W_OPS = {"pairs": 14, "pair_exps": 14, "composite_walks": 33, "sparse_entries": 74, "dense_entries": 56,
+         "dense_steps": 12 * 32}
+W_OPS_PIXEL = 15
+# The per-evaluation model the metric's units suggest (kept beside it for
+# comparison): every forward evaluation 14 FP32 ops + exp, every backward
+# evaluation 47 + exp + reciprocal, exp as the polynomial's 14 FP32 ops.
 OPS_FWD, OPS_BWD, OPS_EXP = 14, 47, 14
 SMS, FP32_LANES, SFU_LANES = 152, 128, 16
 
@@ -346,29 +361,7 @@ def run_gpu(args):
     pk = peaks()
     prof = profile_figures() if args.dssim is None else {}
     t_raster = (raster_ms if args.dssim is None else fwd_ms + bwd_ms) / 1e3
-    ops_b = e_fwd * (OPS_FWD + OPS_EXP) + e_bwd * (OPS_BWD + OPS_EXP)
-    sfu_b = e_bwd
-    ops_a = e_fwd * OPS_FWD + e_bwd * OPS_BWD
-    sfu_a = e_fwd + 2 * e_bwd
-    t_b = max(ops_b / (pk["fp32_tops"] * 1e12), sfu_b / (pk["sfu_tops"] * 1e12))
-    t_a = max(ops_a / (pk["fp32_tops"] * 1e12), sfu_a / (pk["sfu_tops"] * 1e12))
-    achieved = ops_b / t_raster / 1e12
-    roofline = {"bound": "alu", "achieved": achieved, "peak": pk["fp32_tops"], "unit": "TFLOP/s",
-                "frac": t_b / t_raster, "traffic": prof.get("dram_bytes_per_launch") if args.config == "medium" else None,
-                "issue_active_ncu": (prof.get("issue_active_pct") / 100.0 if prof.get("issue_active_pct") is not None
-                                     and args.config == "medium" else None),
-                "kernel": "raster_fused_kernel<kFused>" if args.dssim is None else
-                          "raster_fused_kernel<kFwd> + raster_fused_kernel<kBwdState> (D-SSIM kernel excluded)",
-                "peak_basis": f"FP32 ops (an fma counts once): 152 SMs x 128 lanes x {pk['sm_max_mhz']:.0f} MHz "
-                              f"(sm_max_mhz, {pk['src']}); SFU: 152 x 16 lanes",
-                "work": "per forward evaluation 14 FP32 ops + exp, per backward evaluation 47 FP32 ops + exp + "
-                        "reciprocal; exp = the portable polynomial's 14 FP32 ops",
-                "frac_exp_as_sfu_op": t_a / t_raster,
-                "note": "the kernel skips exp and all backward work for entries that provably cannot pass "
-                        "(bit-identical results), so it does less arithmetic than this per-evaluation model "
-                        "charges; a fraction above 1 means exactly that.  issue_active_ncu is the hardware's "
-                        "own figure for the same launch (issue slots busy, from the committed ncu capture of "
-                        "the medium workload)"}
+    roofline = raster_roofline(tr, target, args, pk, prof, t_raster, e_fwd, e_bwd)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -411,6 +404,51 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def raster_roofline(tr, target, args, pk, prof, t_raster, e_fwd, e_bwd):
+    """Roofline of the fused raster kernel against its executed work (see W_OPS),
+    counted in one untimed launch of the counting variant on a fresh step's lists."""
+    work, ops, sfu = None, None, None
+    if args.dssim is None:
+        tr.project()
+        tr.bin_sort()
+        work = tr.work_counts(target)
+        tr.compact()                      # consumes grad2d / touched as a step would
+        import torch
+        torch.cuda.synchronize()
+        pixels = tr.V * tr.W * tr.H
+        ops = sum(W_OPS[k] * work[k] for k in W_OPS) + W_OPS_PIXEL * pixels
+        sfu = work["sparse_entries"] + work["dense_entries"]
+    t_model = e_fwd * (OPS_FWD + OPS_EXP) + e_bwd * (OPS_BWD + OPS_EXP)
+    fp32 = pk["fp32_tops"] * 1e12
+    r = {"bound": "alu", "peak": pk["fp32_tops"], "unit": "TFLOP/s",
+         "traffic": prof.get("dram_bytes_per_launch") if args.config == "medium" else None,
+         "kernel": "raster_fused_kernel<kFused>" if args.dssim is None else
+                   "raster_fused_kernel<kFwd> + raster_fused_kernel<kBwdState> (D-SSIM kernel excluded)",
+         "peak_basis": f"FP32 pipe: 152 SMs x 128 lanes x {pk['sm_max_mhz']:.0f} MHz (sm_max_mhz, {pk['src']}; "
+                       f"an fma counts once); SFU: 152 x 16 lanes",
+         "frac_per_evaluation_model": (t_model / fp32) / t_raster}
+    if work is not None:
+        t_work = max(ops / fp32, sfu / (pk["sfu_tops"] * 1e12))
+        r.update(achieved=ops / t_raster / 1e12, frac=t_work / t_raster, executed=work,
+                 ops_per_launch=ops, sfu_per_launch=sfu,
+                 work="executed FP32 ops: " + ", ".join(f"{v} per {k}" for k, v in W_OPS.items()) +
+                      f", {W_OPS_PIXEL} per pixel (counting variant, one untimed launch); SFU: one reciprocal "
+                      "per backward entry")
+    else:
+        r.update(achieved=t_model / t_raster / 1e12, frac=(t_model / fp32) / t_raster,
+                 work="per-evaluation model (no counting variant for the split D-SSIM launches)")
+    for key, src in (("issue_active_ncu", "issue_active_pct"), ("pipe_fma_ncu", "pipe_fma_pct"),
+                     ("pipe_alu_ncu", "pipe_alu_pct"), ("pipe_xu_ncu", "pipe_xu_pct"),
+                     ("pipe_lsu_ncu", "pipe_lsu_pct")):
+        if prof.get(src) is not None and args.config == "medium" and args.dssim is None:
+            r[key] = prof[src] / 100.0
+    r["note"] = ("frac = the time the executed FP32 work needs at the FP32-pipe peak over the kernel's mean "
+                 "CUDA-event time; frac_per_evaluation_model charges every E_fwd / E_bwd evaluation instead "
+                 "(above 1: the kernel skips provably failing pairs).  The *_ncu fields are the hardware's own "
+                 "shares for the same kernel from the committed ncu capture of the medium workload.")
+    return r
 
 
 def run_partial(args):

@@ -24,7 +24,7 @@ GS_GRAD2D_STRIDE = 12
 
 EXPORTS = ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
            "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_grad_compact_static",
-           "gs_prune_tiles", "gs_split_ranges", "gs_compose",
+           "gs_prune_tiles", "gs_split_ranges", "gs_compose", "gs_raster_work_counts",
            "gs_error_string", "gs_param_rows", "gs_param_stride", "gs_num_tiles", "gs_version")
 
 
@@ -83,9 +83,11 @@ def lib():
         L.gs_prune_tiles.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.gs_split_ranges.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.gs_compose.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
+        L.gs_raster_work_counts.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P,
+                                            _P, _P]
         for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
                      "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_prune_tiles",
-                     "gs_split_ranges", "gs_compose"):
+                     "gs_split_ranges", "gs_compose", "gs_raster_work_counts"):
             getattr(L, name).restype = ctypes.c_int
         L.gs_error_string.argtypes = [ctypes.c_int]
         L.gs_error_string.restype = ctypes.c_char_p
@@ -161,6 +163,18 @@ def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, targ
     _check("gs_raster_fused_fwd_bwd",
            lib().gs_raster_fused_fwd_bwd(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
                                          target, image, loss, grad2d, touched, eval_counts, stream))
+
+
+GS_RASTER_WORK_COUNTERS = 10
+RASTER_WORK_NAMES = ("pairs", "pair_exps", "composite_walks", "sparse_entries", "sparse_rounds", "dense_entries",
+                     "dense_steps", "chunks", "restaged_chunks", "recomputed_chunks")
+
+
+def gs_raster_work_counts(proj, n, tile_ranges, ids, cams, n_views, opts, target, image, loss, grad2d, touched, work,
+                          stream):
+    _check("gs_raster_work_counts",
+           lib().gs_raster_work_counts(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
+                                       target, image, loss, grad2d, touched, work, stream))
 
 
 def gs_prune_tiles(proj, n, n_views, width, height, budget, ids, tile_ranges, stream):

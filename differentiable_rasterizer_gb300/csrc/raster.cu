@@ -74,6 +74,7 @@ struct RasterArgs {
     float* grad2d;                      // [V][n][12]
     uint8_t* touched;                   // [V][n]
     unsigned long long* counts;         // [3] or null
+    unsigned long long* work;           // [kWCount] executed-work counters (counting variant) or null
     int64_t n;
     int32_t W, H, tiles_x, tiles, n_views;
     float alpha_min, alpha_max, t_min, bg0, bg1, bg2, inv3hw;
@@ -181,21 +182,60 @@ __device__ __forceinline__ EntryGrad entry_grad_at(const float4 r0, const float4
     return e;
 }
 
-template <int kMode>
-__global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a)
+// 16-byte asynchronous global -> shared copy (cp.async, L2 only) and its group
+// commit / wait.  The wait is the hardware's: it ends when the copies land.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Executed-work counters of the counting variant (kCount): what the kernel
+// actually does, as opposed to the E_fwd / E_bwd evaluations the method defines.
+enum WorkCounter {
+    kWPairs = 0,        // (Gaussian, pixel) pairs swept: power evaluated
+    kWPairExp,          // ... of which reached the exponential (tau <= power <= 0)
+    kWCompWalk,         // composite: passing entries walked (power, exp, alpha, T)
+    kWSparseEntries,    // backward, queued path: entries processed (valid lanes)
+    kWSparseRounds,     // ... warp rounds of 32 lanes
+    kWDenseEntries,     // backward, per-Gaussian path: (entry, pixel) evaluations
+    kWDenseSteps,       // ... warp steps (one union entry for 32 lanes, one warp sum)
+    kWChunks,           // chunks staged in the forward
+    kWRestaged,         // chunks staged again in the backward
+    kWRecomputed,       // ... of which had their pass bits recomputed
+    kWCount
+};
+
+// Shared memory of one block (dynamic: about 54 KB, four blocks per SM).
+struct RasterSmem {
+    float4 r0[2][kChunk], r1[2][kChunk], r2[2][kChunk];   // records of two chunks; r2: (blue, tau, hx, hy)
+    uint32_t id[2][kChunk];                                // their instance ids
+    uint32_t bits[kRing][kWords][kTileThreads];            // per ring slot: bit j of pixel p = entry j passes at p
+    uint32_t skip[kWarps];                                 // pixels that need no more pairs
+    int max_last[kWarps];
+    double red_loss[kWarps];                               // per warp: loss sum ...
+    unsigned long long red_counts[3][kWarps];              // ... and evaluation counts
+    uint16_t q[kWarps][kQueue];                            // (owner lane << 8) | entry, grouped by pixel
+    uint8_t nz[kWarps][32];                                // pair phase: lane of the r-th entry with a non-empty box
+};
+
+template <int kMode, bool kCount>
+__global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_kernel(RasterArgs a)
 {
     constexpr bool kBackward = kMode != kFwd;
-    __shared__ float4 s_r0[kChunk], s_r1[kChunk];
-    __shared__ float2 s_r2[kChunk];                 // (blue, tau)
-    __shared__ uint32_t s_id[kChunk];
-    __shared__ uint32_t s_box[kChunk];              // tile_box of each staged Gaussian
-    __shared__ uint32_t s_bits[kRing][kWords][kTileThreads];   // per ring slot: bit j of pixel p = entry j passes at p
-    __shared__ uint32_t s_skip[kWarps];             // pixels that need no more pairs
-    __shared__ uint8_t s_nz[kWarps][32];            // pair phase: lane of the r-th entry with a non-empty box
-    __shared__ uint16_t s_q[kWarps][kQueue];        // (owner lane << 8) | entry, grouped by pixel
-    __shared__ double s_red_d[kWarps];
-    __shared__ unsigned long long s_red_u[3][kWarps];
-    __shared__ int s_max_last[kWarps];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RasterSmem& sm = *reinterpret_cast<RasterSmem*>(smem_raw);
+    auto& s_r0 = sm.r0;
+    auto& s_r1 = sm.r1;
+    auto& s_r2 = sm.r2;
+    auto& s_id = sm.id;
+    auto& s_bits = sm.bits;
+    auto& s_skip = sm.skip;
+    auto& s_nz = sm.nz;
+    auto& s_q = sm.q;
+    auto& s_max_last = sm.max_last;
 
     // Views interleaved (CTA i: view i mod V, tile i / V) so the heavy central
     // tiles of all views are spread over the launch instead of queued view by
@@ -216,38 +256,53 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     const int len = (int)(range.y - range.x);
     const float4* __restrict__ recv = a.rec + (size_t)v * (size_t)a.n * 3;
     const float alpha_min = a.alpha_min, alpha_max = a.alpha_max;
+    unsigned long long work[kCount ? kWCount : 1];
+    if (kCount)
+#pragma unroll
+        for (int k = 0; k < kWCount; ++k) work[k] = 0ull;
 
-    // Stage chunk records and their boxes.
-    auto stage = [&](int base) {
-        const int k = base + threadIdx.x;
-        uint32_t box = 0u;
-        if (k < len) {
-            const uint32_t g = __ldg(a.ids + lo + k);
+    // Staging of a chunk, asynchronous: the instance id is loaded first (early,
+    // into a register), then the three record float4s are copied into buffer b
+    // with cp.async while the block works on the chunk before.  Waiting for them
+    // (cp_async_wait_all) and a block barrier make them visible.
+    constexpr uint32_t kNone = 0xffffffffu;        // no entry (ids are < 2^31)
+    auto stage_id = [&](int base) -> uint32_t {
+        const int k = base + (int)threadIdx.x;
+        return k < len ? __ldg(a.ids + lo + k) : kNone;
+    };
+    auto stage_copy = [&](uint32_t g, int b) {
+        if (g != kNone) {
             const float4* r = recv + (size_t)g * 3;
-            const float4 r0 = __ldg(r);
-            s_r0[threadIdx.x] = r0;
-            s_r1[threadIdx.x] = __ldg(r + 1);
-            const float4 r2 = __ldg(r + 2);
-            s_r2[threadIdx.x] = make_float2(r2.x, r2.y);
-            s_id[threadIdx.x] = g;
-            box = tile_box(r0.x, r0.y, r2.z, r2.w, ox, oy);
+            cp_async16(&s_r0[b][threadIdx.x], r);
+            cp_async16(&s_r1[b][threadIdx.x], r + 1);
+            cp_async16(&s_r2[b][threadIdx.x], r + 2);
         }
-        s_box[threadIdx.x] = box;
+        s_id[b][threadIdx.x] = g;
+        cp_async_commit();
     };
     // Clear this pixel's bit row in ring slot sl.
     auto clear_bits = [&](int sl) {
 #pragma unroll
         for (int w = 0; w < kWords; ++w) s_bits[sl][w][threadIdx.x] = 0u;
     };
-    // Pair phase, setting pass bits in slot sl.  Warp w owns staged entries
-    // [32 w, 32 w + 32); the (entry, box pixel) pairs of its entries are laid
-    // end to end (exclusive scan of the box areas) and swept 32 at a time, so a
-    // lane never idles on a small box.  A lane finds the entry owning its pair
-    // from the start positions inside the round and the count of entries
-    // started before it (s_nz maps that rank to the owning lane).
-    auto pairs = [&](int cnt, int sl) {
-        const int jl = warp * 32 + lane;
-        const uint32_t box = jl < cnt ? s_box[jl] : 0u;
+    // Pair phase on the chunk in buffer b, setting pass bits in slot sl.  The cnt
+    // staged entries are dealt out evenly, warp w owning [w E, w E + E) with
+    // E = ceil(cnt / 8) <= 32 (a partial chunk keeps every warp equally busy);
+    // the (entry, box pixel) pairs of a warp's entries are laid end to end
+    // (exclusive scan of the box areas) and swept 32 at a time, so a lane never
+    // idles on a small box.  A lane finds the entry owning its pair from the
+    // start positions inside the round and the count of entries started before
+    // it (s_nz maps that rank to the owning lane).  Entry j sets bit j & 31 of
+    // word j >> 5 of each pixel where it passes.
+    auto pairs = [&](int cnt, int sl, int b) {
+        const int per = (cnt + kWarps - 1) / kWarps;
+        const int j0 = warp * per;
+        const int jl = j0 + lane;
+        uint32_t box = 0u;
+        if (lane < per && jl < cnt) {
+            const float4 q0 = s_r0[b][jl], q2 = s_r2[b][jl];
+            box = tile_box(q0.x, q0.y, q2.z, q2.w, ox, oy);
+        }
         const int bx0 = box & 0xff, bw = (int)((box >> 8) & 0xff) - bx0;
         const int by0 = (box >> 16) & 0xff, bh = (int)(box >> 24) - by0;
         const int area = box ? bw * bh : 0;
@@ -283,18 +338,20 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             const int ix = (int)(o_box & 0xff) + lx, iy = (int)((o_box >> 16) & 0xff) + ly;
             const int p = iy * kTile + ix;
             if ((s_skip[p >> 5] >> (p & 31)) & 1u) continue;
-            const int j = warp * 32 + ol;
-            const float4 r0 = s_r0[j];
-            const float4 r1 = s_r1[j];
+            const int j = j0 + ol;
+            const float4 r0 = s_r0[b][j];
+            const float4 r1 = s_r1[b][j];
             const float dx = ((float)(ox + ix) + 0.5f) - r0.x;
             const float dy = ((float)(oy + iy) + 0.5f) - r0.y;
             // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
             const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+            if (kCount) ++work[kWPairs];
             // power > 0 is skipped by definition; power < tau has alpha < alpha_min
-            if (power > 0.0f || power < s_r2[j].y) continue;
+            if (power > 0.0f || power < s_r2[b][j].y) continue;
+            if (kCount) ++work[kWPairExp];
             const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
             if (alpha < alpha_min) continue;
-            atomicOr(&s_bits[sl][warp][p], 1u << ol);
+            atomicOr(&s_bits[sl][j >> 5][p], 1u << (j & 31));
         }
     };
 
@@ -346,7 +403,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
     int last = -1, ncomp = 0;
     int stop = -1;                      // list index where this pixel stopped, -1 if it never did
     bool done = !inside;
-    int resident = -1;                  // chunk currently in shared memory
+    int resident = -1;                  // chunk whose records the block last worked on (buffer resident & 1)
     const size_t HW = (size_t)a.W * (size_t)a.H;
     const size_t spix = (size_t)v * HW + (size_t)py * a.W + px;   // per-pixel state index
     if (kMode == kBwdState && inside) {
@@ -354,18 +411,23 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         last = a.last_idx[spix];
     }
     const int nchunks = kMode == kBwdState ? 0 : (len + kChunk - 1) / kChunk;
+    if (nchunks > 0) stage_copy(stage_id(0), 0);
     for (int c = 0; c < nchunks; ++c) {
+        cp_async_wait_all();
+        // one barrier: chunk c's records visible, chunk c - 1 no longer read
         if (__syncthreads_and(done)) break;
-        const int base = c * kChunk;
+        const int base = c * kChunk, b = c & 1;
         const uint32_t skip = __ballot_sync(0xffffffffu, done);
         if (lane == 0) s_skip[warp] = skip;
         const int sl = c % kRing;
-        stage(base);
         clear_bits(sl);
         resident = c;
+        if (kCount && threadIdx.x == 0) ++work[kWChunks];
         __syncthreads();
+        const uint32_t g_next = c + 1 < nchunks ? stage_id(base + kChunk) : kNone;
         const int cnt = min(kChunk, len - base);
-        pairs(cnt, sl);
+        pairs(cnt, sl, b);
+        if (c + 1 < nchunks) stage_copy(g_next, b ^ 1);
         __syncthreads();
         // Composite: each pixel applies its passing entries in list order.
         if (!done) {
@@ -374,17 +436,18 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 while (word) {
                     const int j = (w << 5) | (__ffs(word) - 1);
                     word &= word - 1u;
-                    const float4 r0 = s_r0[j];
+                    const float4 r0 = s_r0[b][j];
                     const float dx = pxf - r0.x, dy = pyf - r0.y;
-                    const float4 r1 = s_r1[j];
+                    const float4 r1 = s_r1[b][j];
                     const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
                     const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
                     const float Tn = T * (1.0f - alpha);
+                    if (kCount) ++work[kWCompWalk];
                     if (a.exclude_crossing && Tn < a.t_min) { done = true; stop = base + j; break; }
                     const float wgt = alpha * T;
                     C0 = C0 + r1.z * wgt;
                     C1 = C1 + r1.w * wgt;
-                    C2 = C2 + s_r2[j].x * wgt;
+                    C2 = C2 + s_r2[b][j].x * wgt;
                     T = Tn;
                     last = base + j;
                     ++ncomp;
@@ -393,6 +456,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             }
         }
     }
+    cp_async_wait_all();   // a break above can leave the next chunk's copies in flight
     const int nev = inside ? (stop >= 0 ? stop + 1 : len) : 0;
     C0 = C0 + T * a.bg0;
     C1 = C1 + T * a.bg1;
@@ -427,11 +491,14 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                     16 * ((int)(d2 > 0.0f) - (int)(d2 < 0.0f) + 1);
         }
     }
-    // block reductions: loss, evaluation counts, last composited index
-    {
+    // Warp sums of the loss and the evaluation counts go to shared memory; the
+    // block's are added to global memory once, at the end of the kernel (a block
+    // retires with its slowest warp anyway), so the warps go on to the backward
+    // without waiting for one another.
+    int ml = last;
+    if (kMode != kBwdState) {
         unsigned long long ef = (unsigned long long)nev, eb = (unsigned long long)(last + 1);
         unsigned long long ec = (unsigned long long)ncomp;
-        int ml = last;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
@@ -441,38 +508,43 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             ml = max(ml, __shfl_xor_sync(0xffffffffu, ml, o));
         }
         if (lane == 0) {
-            s_red_d[warp] = lsum;
-            s_red_u[0][warp] = ef;
-            s_red_u[1][warp] = eb;
-            s_red_u[2][warp] = ec;
-            s_max_last[warp] = ml;
+            sm.red_loss[warp] = lsum;
+            sm.red_counts[0][warp] = ef;
+            sm.red_counts[1][warp] = eb;
+            sm.red_counts[2][warp] = ec;
         }
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double ls = 0.0;
-        unsigned long long ef = 0, eb = 0, ec = 0;
-        int ml = -1;
-        for (int w = 0; w < kWarps; ++w) {
-            ls += s_red_d[w];
-            ef += s_red_u[0][w];
-            eb += s_red_u[1][w];
-            ec += s_red_u[2][w];
-            ml = max(ml, s_max_last[w]);
+    // Adds the block's loss and counts (after a barrier that every thread reaches).
+    auto flush_sums = [&]() {
+        if (threadIdx.x == 0) {
+            double ls = 0.0;
+            unsigned long long x0 = 0ull, x1 = 0ull, x2 = 0ull;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                ls += sm.red_loss[w];
+                x0 += sm.red_counts[0][w];
+                x1 += sm.red_counts[1][w];
+                x2 += sm.red_counts[2][w];
+            }
+            if (kMode == kFused && ls != 0.0) atomicAdd(a.loss + v, ls * a.inv3hw_d);
+            if (a.counts) {
+                atomicAdd(a.counts, x0);
+                atomicAdd(a.counts + 1, x1);
+                atomicAdd(a.counts + 2, x2);
+            }
         }
-        if (kMode == kFused && ls != 0.0) atomicAdd(a.loss + v, ls * a.inv3hw_d);
-        if (a.counts) {
-            atomicAdd(a.counts, ef);
-            atomicAdd(a.counts + 1, eb);
-            atomicAdd(a.counts + 2, ec);
-        }
-        s_max_last[0] = ml;
-    }
-    if (kMode == kFwd && a.bits) {
+    };
+    if (kMode == kFwd) {
+        if (lane == 0) s_max_last[warp] = ml;
+        __syncthreads();
+        flush_sums();
+        if (!a.bits) return;
         // Keep the pass bits of the chunk holding the tile's last composited entry
         // (where a backward from this state starts), if the ring still has them.
-        __syncthreads();
-        const int cl = s_max_last[0] >= 0 ? s_max_last[0] / kChunk : -1;
+        int tl = -1;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tl = max(tl, s_max_last[w]);
+        const int cl = tl >= 0 ? tl / kChunk : -1;
         const bool keep = cl >= 0 && cl >= resident - kRing + 1;
         uint32_t* dst = a.bits + (size_t)tile_lin * kWords * kTileThreads;
         if (keep) {
@@ -480,14 +552,18 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             for (int w = 0; w < kWords; ++w) dst[w * kTileThreads + threadIdx.x] = s_bits[cl % kRing][w][threadIdx.x];
         }
         if (threadIdx.x == 0) a.bits_chunk[tile_lin] = keep ? cl : -1;
+        return;
     }
-    if (!kBackward) return;
-    __syncthreads();
-    // the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
-    // (none when the forward ran in an earlier launch)
+
+    // ------------------------------------------------------------- backward
+    // The chunks are visited from the forward's last (still in shared memory) down
+    // to 0; the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
+    // (none when the forward ran in an earlier launch).  A chunk other than the
+    // resident one is staged again only if some pixel of the tile composited an
+    // entry at or after its start (one vote at the barrier that precedes it); the
+    // chunk below it is copied in while the warps work on it.
     const int last_fwd = kMode == kBwdState ? INT32_MAX / 2 : resident;
-    const int max_last = s_max_last[0];
-    if (max_last < 0) return;
+    const int c_top = kMode == kBwdState ? (len > 0 ? (len - 1) / kChunk : -1) : resident;
     // backward from a stored state: the chunk whose pass bits the forward kept
     int c_kept = -1;
     if (kMode == kBwdState && a.bits) {
@@ -498,19 +574,37 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             for (int w = 0; w < kWords; ++w) s_bits[c_kept % kRing][w][threadIdx.x] = src[w * kTileThreads + threadIdx.x];
         }
     }
-
-    // ------------------------------------------------------------- backward
+    int fetched = -1;    // chunk whose records were last copied into buffer fetched & 1
+    if (resident >= 1) {
+        // the chunk below the resident one, copied in speculatively; its buffer
+        // held chunk resident + 1 (never read) or resident - 1 (finished)
+        stage_copy(stage_id((resident - 1) * kChunk), (resident - 1) & 1);
+        fetched = resident - 1;
+    }
     // dL/dC . (colour composited behind the next entry to visit), per pixel
     float Sg = T * __fmaf_rn(g0, a.bg0, __fmaf_rn(g1, a.bg1, g2c * a.bg2));
     float Tcur = T;
     float* __restrict__ g2v = a.grad2d + (size_t)v * (size_t)a.n * GS_GRAD2D_STRIDE;
     uint8_t* __restrict__ touchv = a.touched + (size_t)v * (size_t)a.n;
-    for (int c = max_last / kChunk; c >= 0; --c) {
+    for (int c = c_top; c >= 0; --c) {
         const int base = c * kChunk;
         const int sl = c % kRing;
+        const int b = c & 1;
         if (c != resident) {
-            __syncthreads();   // the previous chunk's records are no longer read
-            stage(base);
+            if (fetched != c) {
+                // not copied in ahead (the chunk above was skipped): copy it now;
+                // its buffer's previous chunk was finished before the last barrier
+                stage_copy(stage_id(base), b);
+                fetched = c;
+            }
+            cp_async_wait_all();
+            // barrier: the chunk above is finished by every warp, this one's records visible
+            if (!__syncthreads_or(last >= base)) continue;   // no pixel composited anything here or after
+            if (c >= 1) {
+                stage_copy(stage_id(base - kChunk), b ^ 1);
+                fetched = c - 1;
+            }
+            if (kCount && threadIdx.x == 0) ++work[kWRestaged];
             if (kMode == kBwdState ? c != c_kept : c <= last_fwd - kRing) {
                 // pass bits no longer in the ring: recompute them for the pixels
                 // that composited an entry of this chunk
@@ -518,7 +612,8 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 if (lane == 0) s_skip[warp] = skip;
                 clear_bits(sl);
                 __syncthreads();
-                pairs(min(kChunk, len - base), sl);
+                pairs(min(kChunk, len - base), sl, b);
+                if (kCount && threadIdx.x == 0) ++work[kWRecomputed];
             }
             resident = c;
             __syncthreads();
@@ -531,6 +626,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
         uint32_t words[kWords];
         int myoff, nmine;
         const int nq = gather(words, last - base, sl, myoff, nmine);
+        if (nq == 0) continue;
         const int myend = myoff + nmine;
         // Distinct entries composited by any of the warp's pixels in this chunk.
         uint32_t uni[kWords];
@@ -550,15 +646,15 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             for (int w = kWords - 1; w >= 0; --w) {
                 uint32_t u = uni[w];
                 while (u) {
-                    const int b = 31 - __clz(u);
-                    u &= ~(1u << b);
-                    const int j = (w << 5) | b;
+                    const int bt = 31 - __clz(u);
+                    u &= ~(1u << bt);
+                    const int j = (w << 5) | bt;
                     EntryGrad e;
                     e.gm0 = e.gm1 = e.gA = e.gB = e.gC = e.go = e.gr = e.gg = e.gb = 0.0f;
-                    if ((words[w] >> b) & 1u) {
-                        const float4 r0 = s_r0[j];
-                        const float4 r1 = s_r1[j];
-                        const float cb = s_r2[j].x;
+                    if ((words[w] >> bt) & 1u) {
+                        const float4 r0 = s_r0[b][j];
+                        const float4 r1 = s_r1[b][j];
+                        const float cb = s_r2[b][j].x;
                         const float dx = pxf - r0.x, dy = pyf - r0.y;
                         const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
                         const float G = pexp_neg(power);
@@ -570,9 +666,11 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                         e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, g0, g1, g2c, Tb, dotc, Sg, rc);
                         Sg += dotc * alpha * Tb;
                         Tcur = Tb;
+                        if (kCount) ++work[kWDenseEntries];
                     }
+                    if (kCount && lane == 0) ++work[kWDenseSteps];
                     const float sum = warp_sum_terms(e, lane);
-                    const uint32_t gid = s_id[j];
+                    const uint32_t gid = s_id[b][j];
                     if (red_term >= 0) atomicAdd(g2v + (size_t)gid * GS_GRAD2D_STRIDE + red_term, sum);
                     if (lane == 1) touchv[gid] = 1;
                 }
@@ -609,16 +707,18 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 float4 r0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), r1 = r0;
                 float cb = 0.0f, dx = 0.0f, dy = 0.0f, G = 0.0f, araw = 0.0f, alpha = 0.0f;
                 if (valid) {
-                    r0 = s_r0[j];
-                    r1 = s_r1[j];
-                    cb = s_r2[j].x;
+                    r0 = s_r0[b][j];
+                    r1 = s_r1[b][j];
+                    cb = s_r2[b][j].x;
                     dx = pxo - r0.x;
                     dy = pyo - r0.y;
                     const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
                     G = pexp_neg(power);
                     araw = r1.y * G;
                     alpha = fminf(alpha_max, araw);
+                    if (kCount) ++work[kWSparseEntries];
                 }
+                if (kCount && lane == 0) ++work[kWSparseRounds];
                 const float rc = rcp_approx(1.0f - alpha);
                 // segments = pixels: a lane's segment starts at the nearest head at
                 // or below it (lane 0 always is one)
@@ -648,7 +748,7 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
                 if (valid) {
                     const EntryGrad e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb, dotc,
                                                       Sgs + Tst * (Y - da * P), rc);
-                    const uint32_t gid = s_id[j];
+                    const uint32_t gid = s_id[b][j];
                     float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
                     atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
                     atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
@@ -669,11 +769,43 @@ __global__ void __launch_bounds__(kTileThreads) raster_fused_kernel(RasterArgs a
             __syncwarp();
         }
     }
+    cp_async_wait_all();   // no copy outlives the block
+    if (kMode == kFused) {
+        __syncthreads();
+        flush_sums();
+    }
+    if (kCount) {
+#pragma unroll
+        for (int k = 0; k < kWCount; ++k) {
+            unsigned long long x = work[k];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0 && x) atomicAdd(a.work + k, x);
+        }
+    }
 }
 
 }  // namespace gs
 
 using namespace gs;
+
+// Launch with the block's dynamic shared memory (opted in once per variant; the
+// maximum shared-memory carveout lets four blocks share an SM).
+template <int kMode, bool kCount>
+static gs_status launch_raster(const RasterArgs& a, long long grid, cudaStream_t s)
+{
+    static bool configured = false;
+    if (!configured) {
+        GS_CUDA_TRY(cudaFuncSetAttribute(raster_fused_kernel<kMode, kCount>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RasterSmem)));
+        GS_CUDA_TRY(cudaFuncSetAttribute(raster_fused_kernel<kMode, kCount>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout, 100));
+        configured = true;
+    }
+    raster_fused_kernel<kMode, kCount><<<(unsigned)grid, kTileThreads, sizeof(RasterSmem), s>>>(a);
+    GS_LAUNCH_CHECK();
+    return GS_OK;
+}
 
 // Arguments shared by the three launches.
 static gs_status raster_args(RasterArgs& a, const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
@@ -732,12 +864,33 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
     cudaStream_t s = (cudaStream_t)stream;
     if (target) {
         GS_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(double) * (size_t)n_views, s));
-        raster_fused_kernel<kFused><<<(unsigned)grid, kTileThreads, 0, s>>>(a);
-    } else {
-        raster_fused_kernel<kFwd><<<(unsigned)grid, kTileThreads, 0, s>>>(a);
+        return launch_raster<kFused, false>(a, grid, s);
     }
-    GS_LAUNCH_CHECK();
-    return GS_OK;
+    return launch_raster<kFwd, false>(a, grid, s);
+}
+
+extern "C" gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                           const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                           const gs_render_opts* opts, const float* target, float* image,
+                                           double* loss, float* grad2d, uint8_t* touched, uint64_t* work,
+                                           void* stream)
+{
+    RasterArgs a;
+    long long grid = 0;
+    gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
+    if (st != GS_OK) return st;
+    if (!image || !target || !loss || !work || (n > 0 && (!grad2d || !touched))) return GS_ERR_INVALID_ARG;
+    if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    static_assert(kWCount == GS_RASTER_WORK_COUNTERS, "counter layout");
+    a.target = target;
+    a.image = image;
+    a.loss = loss;
+    a.grad2d = grad2d;
+    a.touched = touched;
+    a.work = reinterpret_cast<unsigned long long*>(work);
+    cudaStream_t s = (cudaStream_t)stream;
+    GS_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(double) * (size_t)n_views, s));
+    return launch_raster<kFused, true>(a, grid, s);
 }
 
 extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
@@ -757,9 +910,7 @@ extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, con
     a.bits = pass_bits;
     a.bits_chunk = bits_chunk;
     a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
-    raster_fused_kernel<kFwd><<<(unsigned)grid, kTileThreads, 0, (cudaStream_t)stream>>>(a);
-    GS_LAUNCH_CHECK();
-    return GS_OK;
+    return launch_raster<kFwd, false>(a, grid, (cudaStream_t)stream);
 }
 
 extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
@@ -783,7 +934,5 @@ extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, co
     a.dldc = dldc;
     a.grad2d = grad2d;
     a.touched = touched;
-    raster_fused_kernel<kBwdState><<<(unsigned)grid, kTileThreads, 0, (cudaStream_t)stream>>>(a);
-    GS_LAUNCH_CHECK();
-    return GS_OK;
+    return launch_raster<kBwdState, false>(a, grid, (cudaStream_t)stream);
 }

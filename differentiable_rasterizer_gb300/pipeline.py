@@ -167,6 +167,19 @@ class GaussianTrainer:
                                     self.touched.data_ptr(), self.eval_counts.data_ptr() if count_evals else None,
                                     self.stream_handle())
 
+    def work_counts(self, target) -> dict:
+        """One fused raster launch in its counting variant (gs_raster_work_counts) on
+        the current projection and lists: the same outputs as raster(target), plus
+        what the kernel executed (pairs swept, exponentials, composite walks,
+        backward entries and rounds, chunks staged).  grad2d and touched are left
+        filled as after raster(); compact() consumes them."""
+        work = torch.zeros(abi.GS_RASTER_WORK_COUNTERS, dtype=torch.int64, device=self.device)
+        abi.gs_raster_work_counts(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,
+                                  self.opts, target.data_ptr(), self.image.data_ptr(), self.loss.data_ptr(),
+                                  self.grad2d.data_ptr(), self.touched.data_ptr(), work.data_ptr(),
+                                  self.stream_handle())
+        return dict(zip(abi.RASTER_WORK_NAMES, (int(x) for x in work.cpu().tolist())))
+
     def raster_dssim(self, target, count_evals=True, events=None):
         """L1 + D-SSIM: forward with stored per-pixel state, loss and dL/dC, backward.
         events: None or two CUDA events recorded after the forward and after the loss."""

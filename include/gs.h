@@ -182,7 +182,9 @@ GS_API gs_status gs_prune_tiles(const gs_proj* proj, int64_t n, int32_t n_views,
 /* Fused forward + backward rasterization: one CTA per 16x16 tile (256 threads,
  * one pixel each).  Forward: front-to-back over the tile's sorted list, skip
  * power > 0 or alpha < alpha_min, C += c * alpha * T, T *= 1 - alpha, stop at
- * T < t_min; C += T * bg.  The per-pixel T, colour and last index stay in
+ * T < t_min; C += T * bg.  The list's records pass through shared memory in
+ * chunks of 256, the next chunk copied in (cp.async) while the block works on
+ * the current one.  The per-pixel T, colour and last index stay in
  * registers.  With a target: L1 loss per view, mean over 3*H*W values, summed in
  * fp64, and its gradient sign(C - target) / (3HW) on chip; backward walks each
  * pixel's composited entries back to front (transmittance recovered by
@@ -205,6 +207,26 @@ GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const u
                                   const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
                                   const float* target, float* image, double* loss, float* grad2d, uint8_t* touched,
                                   uint64_t* eval_counts, void* stream);
+
+/* Executed-work counters of the fused kernel -- a measurement aid with no
+ * counterpart on the pages: the kernel skips, with results unchanged, the
+ * (entry, pixel) pairs its per-Gaussian support box and alpha cut prove
+ * cannot pass, so the work it executes is far below E_fwd + E_bwd.  Runs the
+ * same step as gs_raster_fused_fwd_bwd (target required; same outputs, eval
+ * counts not taken) in a variant that also counts, into work[] (DEVICE u64,
+ * accumulated +=), in this order:
+ *   0 pairs swept (power evaluated)      1 of which reached the exponential
+ *   2 composite entries walked            3 backward queued entries
+ *   4 backward queued rounds (per warp)   5 backward per-Gaussian evaluations
+ *   6 backward per-Gaussian steps (warp)  7 chunks staged in the forward
+ *   8 chunks staged again in the backward 9 of which had pass bits recomputed
+ * The counting makes it slower; time gs_raster_fused_fwd_bwd, count here.
+ * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
+#define GS_RASTER_WORK_COUNTERS 10
+GS_API gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
+                                       const uint32_t* ids, const gs_camera* cams, int32_t n_views,
+                                       const gs_render_opts* opts, const float* target, float* image, double* loss,
+                                       float* grad2d, uint8_t* touched, uint64_t* work, void* stream);
 
 /* ---- L1 + D-SSIM loss (the standard 3DGS loss: On Scaling Up 3D Gaussian
  * Splatting Training, summary of the loss) ----
@@ -324,7 +346,10 @@ GS_API gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const float* p
  * n > GS_COMPACT_STATIC_MAX_N returns GS_ERR_INVALID_ARG.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array: calls
+ * first call before any stream capture.  A device reset (cudaDeviceReset)
+ * destroys the array's context: the next call on that device sees a new
+ * context, looks the address up again (make it, too, before any capture) and
+ * finds the array's contents undefined, which the call does not rely on.  All calls share the one array: calls
  * whose work overlaps on the GPU (other streams, other threads) race on it and
  * must be serialised by the caller.  Nothing in it needs to start at zero; it
  * keeps whatever the last call left there. */
