@@ -356,6 +356,46 @@ __global__ void __launch_bounds__(kSortWarps * 32) sort_warp_kernel(const uint2*
 // One kRegThreads-thread CTA per listed bucket of kWarpCap < size <= kRegCap.
 // Launched before the host knows the class size: one block per possible bucket,
 // the ones past the device-held count (or all, if the capacity is short) exit.
+// The bucket is split by uniform slices of its [min, max] key interval into
+// kSlices sub-buckets (the monotone digit of the huge-bucket splitter below), a
+// counting scatter through shared memory puts the sub-buckets in digit order,
+// and each sub-bucket is sorted on its own: up to kThreadCap keys by one thread
+// (insertion), larger ones by a warp (register bitonic, as for small buckets).
+// That is O(c) work plus small sorts where the bitonic network over the whole
+// bucket needs O(c log^2 c).  Keys are unique within a bucket, so the result
+// does not depend on the scatter's order.  A bucket with a sub-bucket of more
+// than kWarpCap keys (a tight cluster of depths) is sorted by the block's
+// register bitonic network instead.
+constexpr int kSlices = kRegThreads;
+constexpr int kThreadCap = 8;
+
+// One warp sorts s[0, c), c <= 32 E, in place (shared memory).
+template <int E>
+__device__ __forceinline__ void warp_sort_smem_e(uint64_t* s, int c)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t x[E];
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = lane * E + r;
+        x[r] = i < c ? s[i] : ~0ull;
+    }
+    warp_bitonic<E>(x);
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int i = lane * E + r;
+        if (i < c) s[i] = x[r];
+    }
+}
+
+__device__ __forceinline__ void warp_sort_smem(uint64_t* s, int c)
+{
+    if (c <= 32) warp_sort_smem_e<1>(s, c);
+    else if (c <= 64) warp_sort_smem_e<2>(s, c);
+    else if (c <= 128) warp_sort_smem_e<4>(s, c);
+    else warp_sort_smem_e<8>(s, c);
+}
+
 __global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* __restrict__ list,
                                                                const uint2* __restrict__ ranges,
                                                                const uint64_t* __restrict__ tmp,
@@ -364,15 +404,112 @@ __global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* _
                                                                const unsigned long long* __restrict__ total,
                                                                unsigned long long capacity)
 {
-    __shared__ uint64_t s[kRegThreads * 9];
+    __shared__ uint64_t s[kRegThreads * 9];          // the bucket's keys (the bitonic path's workspace)
+    __shared__ uint64_t s_out[kRegCap];              // ... scattered into sub-bucket order
+    __shared__ uint32_t s_start[kSlices], s_cur[kSlices], s_big[kSlices];
+    __shared__ uint32_t s_nbig;
+    __shared__ uint64_t s_red[2][kRegThreads / 32];
+    __shared__ uint32_t s_wsum[kRegThreads / 32], s_wmax[kRegThreads / 32];
     if (*total > capacity || blockIdx.x >= *count) return;
     const uint32_t t = list[blockIdx.x];
     const uint2 r = ranges[t];
     const int c = (int)(r.y - r.x);
     const uint64_t hi = (uint64_t)t << 32;
-    if (c <= 2 * kRegThreads) reg_sort<kRegThreads, 2, true>(tmp, r.x, c, hi, keys, ids, s);
-    else if (c <= 4 * kRegThreads) reg_sort<kRegThreads, 4, true>(tmp, r.x, c, hi, keys, ids, s);
-    else reg_sort<kRegThreads, 8, true>(tmp, r.x, c, hi, keys, ids, s);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kW = kRegThreads / 32;
+    // keys and their interval
+    uint64_t kmin = ~0ull, kmax = 0ull;
+    for (int i = tid; i < c; i += kRegThreads) {
+        const uint64_t k = tmp[(size_t)r.x + i];
+        s[i] = k;
+        kmin = k < kmin ? k : kmin;
+        kmax = k > kmax ? k : kmax;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t a = __shfl_xor_sync(0xffffffffu, kmin, o);
+        const uint64_t b = __shfl_xor_sync(0xffffffffu, kmax, o);
+        kmin = a < kmin ? a : kmin;
+        kmax = b > kmax ? b : kmax;
+    }
+    if (lane == 0) {
+        s_red[0][warp] = kmin;
+        s_red[1][warp] = kmax;
+    }
+    s_start[tid] = 0u;
+    if (tid == 0) s_nbig = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+        kmin = s_red[0][w] < kmin ? s_red[0][w] : kmin;
+        kmax = s_red[1][w] > kmax ? s_red[1][w] : kmax;
+    }
+    // digit(k) = floor((k - kmin) * scale / 2^64): non-decreasing in k, below kSlices
+    const uint64_t range = kmax - kmin;
+    const bool direct = range < (uint64_t)kSlices;
+    const uint64_t scale = direct ? 0ull : (~0ull / (range + 1ull)) * (uint64_t)kSlices;
+    auto digit = [&](uint64_t k) -> uint32_t {
+        const uint64_t d = k - kmin;
+        return direct ? (uint32_t)d : (uint32_t)__umul64hi(d, scale);
+    };
+    for (int i = tid; i < c; i += kRegThreads) atomicAdd(&s_start[digit(s[i])], 1u);
+    __syncthreads();
+    // exclusive scan of the sub-bucket sizes, and the largest
+    const uint32_t mine = s_start[tid];
+    uint32_t incl = mine, mx = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    if (lane == 0) s_wmax[warp] = mx;
+    __syncthreads();
+    uint32_t wpre = 0, bmax = 0;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+        wpre += w < warp ? s_wsum[w] : 0u;
+        bmax = max(bmax, s_wmax[w]);
+    }
+    const uint32_t start = wpre + incl - mine;
+    if (bmax > (uint32_t)kWarpCap) {
+        // a tight cluster of keys: the bitonic network (it reloads the keys into s)
+        __syncthreads();
+        if (c <= 2 * kRegThreads) reg_sort<kRegThreads, 2, true>(tmp, r.x, c, hi, keys, ids, s);
+        else if (c <= 4 * kRegThreads) reg_sort<kRegThreads, 4, true>(tmp, r.x, c, hi, keys, ids, s);
+        else reg_sort<kRegThreads, 8, true>(tmp, r.x, c, hi, keys, ids, s);
+        return;
+    }
+    s_cur[tid] = start;
+    __syncthreads();
+    for (int i = tid; i < c; i += kRegThreads) {
+        const uint64_t k = s[i];
+        s_out[atomicAdd(&s_cur[digit(k)], 1u)] = k;
+    }
+    __syncthreads();
+    if (mine > (uint32_t)kThreadCap) {
+        s_big[atomicAdd(&s_nbig, 1u)] = tid;     // sub-bucket for a warp
+        s_cur[tid] = start;                      // its start (s_cur held its end)
+    } else {
+        // thread tid: insertion sort of its sub-bucket [start, start + mine)
+        for (uint32_t a = start + 1; a < start + mine; ++a) {
+            const uint64_t k = s_out[a];
+            uint32_t b = a;
+            while (b > start && s_out[b - 1] > k) {
+                s_out[b] = s_out[b - 1];
+                --b;
+            }
+            s_out[b] = k;
+        }
+    }
+    __syncthreads();
+    for (uint32_t b = warp; b < s_nbig; b += kW) {
+        const uint32_t d = s_big[b];
+        warp_sort_smem(s_out + s_cur[d], (int)s_start[d]);   // s_start[d]: the size of sub-bucket d
+    }
+    __syncthreads();
+    for (int i = tid; i < c; i += kRegThreads) emit_sorted(s_out[i], hi, keys, ids, (size_t)r.x + i);
 }
 
 // One kMidThreads-thread CTA per listed bucket of kRegCap < size <= kBigCap:

@@ -63,7 +63,7 @@ __device__ __forceinline__ void vjp_gaussian(const VjpArgs& a, const CamSet& cs,
             float4* src = reinterpret_cast<float4*>(a.grad2d + o * GS_GRAD2D_STRIDE);
             const float4 x0 = src[0], x1 = src[1], x2 = src[2];
             const float g2[9] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x};
-            vjp_one<DEG>(gp, cs.cam[v], it, po.clamp, g2, grad);
+            vjp_one<DEG>(gp, cs.cam[v], ac, it, po.clamp, g2, grad, grad + 11);
             const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             src[0] = z; src[1] = z; src[2] = z;
         }

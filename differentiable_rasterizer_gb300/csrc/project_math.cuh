@@ -51,18 +51,27 @@ struct GaussParams {
     }
 };
 
+// The same parameters with the colour coefficients left in a shared-memory row
+// (col[3 k + c]) instead of registers.
+template <int DEG>
+struct GaussParamsShared {
+    static constexpr int kCol = GaussParams<DEG>::kCol;
+    float mu[3], ls[3], q[4], logit;
+    const float* col;
+};
+
 struct ProjOut {
     float mx, my, cA, cB, cC, opacity, col[3], depth;
     int x0, y0, x1, y1;
     uint32_t clamp;   // bit c: colour channel c clamped at 0
 };
 
-// Forward intermediates kept for the VJP.
+// Per-view forward intermediates kept for the VJP (the view-independent ones
+// are the Gaussian's GaussAct).
 struct ProjInter {
-    float t[3], s[3], qn, qh[4], R[9], M[9], S[9], T0[3], T1[3];
+    float t[3], T0[3], T1[3];
     float a, b, c, det;
     float dir[3], nv;
-    float o;
 };
 
 // The view-independent part of the projection of one Gaussian: scale, rotation,
@@ -71,8 +80,8 @@ struct GaussAct {
     float s[3], qn, qh[4], R[9], M[9], S[9], o;
 };
 
-template <int DEG>
-__device__ __forceinline__ void activate(const GaussParams<DEG>& gp, GaussAct& ac)
+template <int DEG, class GP>
+__device__ __forceinline__ void activate(const GP& gp, GaussAct& ac)
 {
 #pragma unroll
     for (int j = 0; j < 3; ++j) ac.s[j] = pexp(gp.ls[j]);
@@ -102,8 +111,8 @@ __device__ __forceinline__ void activate(const GaussParams<DEG>& gp, GaussAct& a
 
 // The per-view part, given the Gaussian's activation (same operations and
 // order as evaluating everything per view).
-template <int DEG>
-__device__ __forceinline__ bool project_view(const GaussParams<DEG>& gp, const GaussAct& ac, const gs_camera& cam,
+template <int DEG, class GP>
+__device__ __forceinline__ bool project_view(const GP& gp, const GaussAct& ac, const gs_camera& cam,
                                              float near_z, float lowpass, int tiles_x, int tiles_y, ProjOut& out,
                                              ProjInter* it)
 {
@@ -185,13 +194,8 @@ __device__ __forceinline__ bool project_view(const GaussParams<DEG>& gp, const G
     out.clamp = cm;
     if (it) {
 #pragma unroll
-        for (int i = 0; i < 3; ++i) { it->t[i] = t[i]; it->s[i] = ac.s[i]; it->dir[i] = dir[i]; it->T0[i] = T0[i]; it->T1[i] = T1[i]; }
-        it->qn = ac.qn;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) it->qh[i] = ac.qh[i];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) { it->R[i] = ac.R[i]; it->M[i] = ac.M[i]; it->S[i] = S[i]; }
-        it->a = a; it->b = b; it->c = c; it->det = det; it->nv = nv; it->o = o;
+        for (int i = 0; i < 3; ++i) { it->t[i] = t[i]; it->dir[i] = dir[i]; it->T0[i] = T0[i]; it->T1[i] = T1[i]; }
+        it->a = a; it->b = b; it->c = c; it->det = det; it->nv = nv;
     }
     return true;
 }
@@ -206,10 +210,12 @@ __device__ __forceinline__ bool project_one(const GaussParams<DEG>& gp, const gs
 }
 
 // d loss / d params of one (Gaussian, view) given d loss / d (mean2d, conic, opacity, colour).
-// g2: mx, my, A, B, C, o, r, g, b.  grad[] is accumulated (+=), rows as in the parameter buffer.
-template <int DEG>
-__device__ __forceinline__ void vjp_one(const GaussParams<DEG>& gp, const gs_camera& cam, const ProjInter& it,
-                                        uint32_t clamp, const float g2[9], float* grad)
+// g2: mx, my, A, B, C, o, r, g, b.  Accumulated (+=): grad[0..10] the geometry rows,
+// gcol[0..kCol) the colour rows (row 11 + i), as in the parameter buffer; the
+// derivative of each SH basis polynomial is formed where it is used.
+template <int DEG, class GP>
+__device__ __forceinline__ void vjp_one(const GP& gp, const gs_camera& cam, const GaussAct& ac, const ProjInter& it,
+                                        uint32_t clamp, const float g2[9], float* grad, float* gcol_out)
 {
     const float* W = cam.R;
     const float fx = cam.fx, fy = cam.fy;
@@ -226,8 +232,8 @@ __device__ __forceinline__ void vjp_one(const GaussParams<DEG>& gp, const gs_cam
     float ST0[3], ST1[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-        ST0[k] = __fmaf_rn(it.S[3 * k], it.T0[0], __fmaf_rn(it.S[3 * k + 1], it.T0[1], it.S[3 * k + 2] * it.T0[2]));
-        ST1[k] = __fmaf_rn(it.S[3 * k], it.T1[0], __fmaf_rn(it.S[3 * k + 1], it.T1[1], it.S[3 * k + 2] * it.T1[2]));
+        ST0[k] = __fmaf_rn(ac.S[3 * k], it.T0[0], __fmaf_rn(ac.S[3 * k + 1], it.T0[1], ac.S[3 * k + 2] * it.T0[2]));
+        ST1[k] = __fmaf_rn(ac.S[3 * k], it.T1[0], __fmaf_rn(ac.S[3 * k + 1], it.T1[1], ac.S[3 * k + 2] * it.T1[2]));
     }
     float gT0[3], gT1[3];
 #pragma unroll
@@ -249,17 +255,17 @@ __device__ __forceinline__ void vjp_one(const GaussParams<DEG>& gp, const gs_cam
     for (int i = 0; i < 3; ++i)
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
-            const float gM = 2.0f * __fmaf_rn(Gs[3 * i], it.M[j], __fmaf_rn(Gs[3 * i + 1], it.M[3 + j], Gs[3 * i + 2] * it.M[6 + j]));
-            gR[3 * i + j] = gM * it.s[j];
-            gs[j] = __fmaf_rn(gM, it.R[3 * i + j], gs[j]);
+            const float gM = 2.0f * __fmaf_rn(Gs[3 * i], ac.M[j], __fmaf_rn(Gs[3 * i + 1], ac.M[3 + j], Gs[3 * i + 2] * ac.M[6 + j]));
+            gR[3 * i + j] = gM * ac.s[j];
+            gs[j] = __fmaf_rn(gM, ac.R[3 * i + j], gs[j]);
         }
-    const float w = it.qh[0], x = it.qh[1], y = it.qh[2], z = it.qh[3];
+    const float w = ac.qh[0], x = ac.qh[1], y = ac.qh[2], z = ac.qh[3];
     const float gw = 2.0f * (-z * gR[1] + y * gR[2] + z * gR[3] - x * gR[5] - y * gR[6] + x * gR[7]);
     const float gx = 2.0f * (y * gR[1] + z * gR[2] + y * gR[3] - 2.0f * x * gR[4] - w * gR[5] + z * gR[6] + w * gR[7] - 2.0f * x * gR[8]);
     const float gy = 2.0f * (-2.0f * y * gR[0] + x * gR[1] + w * gR[2] + x * gR[3] + z * gR[5] - w * gR[6] + z * gR[7] - 2.0f * y * gR[8]);
     const float gz = 2.0f * (-2.0f * z * gR[0] - w * gR[1] + x * gR[2] + w * gR[3] - 2.0f * z * gR[4] + y * gR[5] + x * gR[6] + y * gR[7]);
     const float dotq = w * gw + x * gx + y * gy + z * gz;
-    const float iqn = 1.0f / it.qn;
+    const float iqn = 1.0f / ac.qn;
     // T = J W
     float gj00 = 0.0f, gj02 = 0.0f, gj11 = 0.0f, gj12 = 0.0f;
 #pragma unroll
@@ -281,45 +287,48 @@ __device__ __forceinline__ void vjp_one(const GaussParams<DEG>& gp, const gs_cam
 #pragma unroll
     for (int j = 0; j < 3; ++j) gmu[j] = __fmaf_rn(W[j], gt[0], __fmaf_rn(W[3 + j], gt[1], W[6 + j] * gt[2]));
     if (DEG == 0) {
-        grad[11] += g2[6];
-        grad[12] += g2[7];
-        grad[13] += g2[8];
+        gcol_out[0] += g2[6];
+        gcol_out[1] += g2[7];
+        gcol_out[2] += g2[8];
     } else {
         const float X = it.dir[0], Yv = it.dir[1], Z = it.dir[2];
         float Y[16];
         sh_basis(X, Yv, Z, Y);
         // gradient of each basis polynomial w.r.t. (x, y, z)
         const float XX = X * X, YY = Yv * Yv, ZZ = Z * Z;
-        float dY[16][3];
-        dY[0][0] = 0.0f; dY[0][1] = 0.0f; dY[0][2] = 0.0f;
-        dY[1][0] = 0.0f; dY[1][1] = SH::K1; dY[1][2] = 0.0f;
-        dY[2][0] = 0.0f; dY[2][1] = 0.0f; dY[2][2] = SH::K1;
-        dY[3][0] = SH::K1; dY[3][1] = 0.0f; dY[3][2] = 0.0f;
-        dY[4][0] = SH::K2 * Yv; dY[4][1] = SH::K2 * X; dY[4][2] = 0.0f;
-        dY[5][0] = 0.0f; dY[5][1] = SH::K2 * Z; dY[5][2] = SH::K2 * Yv;
-        dY[6][0] = -2.0f * SH::K3 * X; dY[6][1] = -2.0f * SH::K3 * Yv; dY[6][2] = 4.0f * SH::K3 * Z;
-        dY[7][0] = SH::K2 * Z; dY[7][1] = 0.0f; dY[7][2] = SH::K2 * X;
-        dY[8][0] = 2.0f * SH::K4 * X; dY[8][1] = -2.0f * SH::K4 * Yv; dY[8][2] = 0.0f;
-        dY[9][0] = 6.0f * SH::K5 * X * Yv; dY[9][1] = SH::K5 * (3.0f * XX - 3.0f * YY); dY[9][2] = 0.0f;
-        dY[10][0] = SH::K6 * Yv * Z; dY[10][1] = SH::K6 * X * Z; dY[10][2] = SH::K6 * X * Yv;
-        dY[11][0] = -2.0f * SH::K7 * X * Yv; dY[11][1] = SH::K7 * (4.0f * ZZ - XX - 3.0f * YY); dY[11][2] = 8.0f * SH::K7 * Yv * Z;
-        dY[12][0] = -6.0f * SH::K8 * X * Z; dY[12][1] = -6.0f * SH::K8 * Yv * Z; dY[12][2] = SH::K8 * (6.0f * ZZ - 3.0f * XX - 3.0f * YY);
-        dY[13][0] = SH::K7 * (4.0f * ZZ - 3.0f * XX - YY); dY[13][1] = -2.0f * SH::K7 * X * Yv; dY[13][2] = 8.0f * SH::K7 * X * Z;
-        dY[14][0] = 2.0f * SH::K9 * X * Z; dY[14][1] = -2.0f * SH::K9 * Yv * Z; dY[14][2] = SH::K9 * (XX - YY);
-        dY[15][0] = SH::K5 * (3.0f * XX - 3.0f * YY); dY[15][1] = -6.0f * SH::K5 * X * Yv; dY[15][2] = 0.0f;
         float gd0 = 0.0f, gd1 = 0.0f, gd2 = 0.0f;
 #pragma unroll
-        for (int ch = 0; ch < 3; ++ch) {
-            if (clamp & (1u << ch)) continue;
-            const float gcol = g2[6 + ch];
+        for (int k = 0; k < 16; ++k) {
+            // gradient of basis polynomial k w.r.t. (x, y, z)
+            float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f;
+            switch (k) {
+                case 1: d1 = SH::K1; break;
+                case 2: d2 = SH::K1; break;
+                case 3: d0 = SH::K1; break;
+                case 4: d0 = SH::K2 * Yv; d1 = SH::K2 * X; break;
+                case 5: d1 = SH::K2 * Z; d2 = SH::K2 * Yv; break;
+                case 6: d0 = -2.0f * SH::K3 * X; d1 = -2.0f * SH::K3 * Yv; d2 = 4.0f * SH::K3 * Z; break;
+                case 7: d0 = SH::K2 * Z; d2 = SH::K2 * X; break;
+                case 8: d0 = 2.0f * SH::K4 * X; d1 = -2.0f * SH::K4 * Yv; break;
+                case 9: d0 = 6.0f * SH::K5 * X * Yv; d1 = SH::K5 * (3.0f * XX - 3.0f * YY); break;
+                case 10: d0 = SH::K6 * Yv * Z; d1 = SH::K6 * X * Z; d2 = SH::K6 * X * Yv; break;
+                case 11: d0 = -2.0f * SH::K7 * X * Yv; d1 = SH::K7 * (4.0f * ZZ - XX - 3.0f * YY); d2 = 8.0f * SH::K7 * Yv * Z; break;
+                case 12: d0 = -6.0f * SH::K8 * X * Z; d1 = -6.0f * SH::K8 * Yv * Z; d2 = SH::K8 * (6.0f * ZZ - 3.0f * XX - 3.0f * YY); break;
+                case 13: d0 = SH::K7 * (4.0f * ZZ - 3.0f * XX - YY); d1 = -2.0f * SH::K7 * X * Yv; d2 = 8.0f * SH::K7 * X * Z; break;
+                case 14: d0 = 2.0f * SH::K9 * X * Z; d1 = -2.0f * SH::K9 * Yv * Z; d2 = SH::K9 * (XX - YY); break;
+                case 15: d0 = SH::K5 * (3.0f * XX - 3.0f * YY); d1 = -6.0f * SH::K5 * X * Yv; break;
+                default: break;
+            }
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int row = 11 + 3 * k + ch;
-                grad[row] = __fmaf_rn(gcol, Y[k], grad[row]);
-                const float kc = gcol * gp.col[(3 * k + ch) % GaussParams<DEG>::kCol];
-                gd0 = __fmaf_rn(kc, dY[k][0], gd0);
-                gd1 = __fmaf_rn(kc, dY[k][1], gd1);
-                gd2 = __fmaf_rn(kc, dY[k][2], gd2);
+            for (int ch = 0; ch < 3; ++ch) {
+                if (clamp & (1u << ch)) continue;
+                const float gcol = g2[6 + ch];
+                const int row = 3 * k + ch;
+                gcol_out[row] = __fmaf_rn(gcol, Y[k], gcol_out[row]);
+                const float kc = gcol * gp.col[row % GP::kCol];
+                gd0 = __fmaf_rn(kc, d0, gd0);
+                gd1 = __fmaf_rn(kc, d1, gd1);
+                gd2 = __fmaf_rn(kc, d2, gd2);
             }
         }
         const float dd = X * gd0 + Yv * gd1 + Z * gd2;
@@ -328,13 +337,13 @@ __device__ __forceinline__ void vjp_one(const GaussParams<DEG>& gp, const gs_cam
         gmu[1] += (gd1 - Yv * dd) * inv;
         gmu[2] += (gd2 - Z * dd) * inv;
     }
-    grad[10] += g2[5] * it.o * (1.0f - it.o);
+    grad[10] += g2[5] * ac.o * (1.0f - ac.o);
     grad[0] += gmu[0];
     grad[1] += gmu[1];
     grad[2] += gmu[2];
-    grad[3] += gs[0] * it.s[0];
-    grad[4] += gs[1] * it.s[1];
-    grad[5] += gs[2] * it.s[2];
+    grad[3] += gs[0] * ac.s[0];
+    grad[4] += gs[1] * ac.s[1];
+    grad[5] += gs[2] * ac.s[2];
     grad[6] += (gw - w * dotq) * iqn;
     grad[7] += (gx - x * dotq) * iqn;
     grad[8] += (gy - y * dotq) * iqn;
