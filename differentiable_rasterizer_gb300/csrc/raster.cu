@@ -492,9 +492,10 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         }
     }
     // Warp sums of the loss and the evaluation counts go to shared memory; the
-    // block's are added to global memory once, at the end of the kernel (a block
-    // retires with its slowest warp anyway), so the warps go on to the backward
-    // without waiting for one another.
+    // block's are added to global memory once, after the barrier that ends the
+    // forward.  (Deferring that barrier to the end of the kernel, so that the
+    // warps start their backward without waiting for one another, measured
+    // slower on every workload.)
     int ml = last;
     if (kMode != kBwdState) {
         unsigned long long ef = (unsigned long long)nev, eb = (unsigned long long)(last + 1);
@@ -562,6 +563,10 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     // resident one is staged again only if some pixel of the tile composited an
     // entry at or after its start (one vote at the barrier that precedes it); the
     // chunk below it is copied in while the warps work on it.
+    if (kMode == kFused) {
+        __syncthreads();
+        flush_sums();
+    }
     const int last_fwd = kMode == kBwdState ? INT32_MAX / 2 : resident;
     const int c_top = kMode == kBwdState ? (len > 0 ? (len - 1) / kChunk : -1) : resident;
     // backward from a stored state: the chunk whose pass bits the forward kept
@@ -770,10 +775,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         }
     }
     cp_async_wait_all();   // no copy outlives the block
-    if (kMode == kFused) {
-        __syncthreads();
-        flush_sums();
-    }
     if (kCount) {
 #pragma unroll
         for (int k = 0; k < kWCount; ++k) {

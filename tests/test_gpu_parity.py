@@ -93,6 +93,38 @@ def test_sort_split_recursion_on_equal_depths():
     assert st["instances"] == n
 
 
+@pytest.mark.parametrize("n", [1500, 6000])
+def test_sort_slices_with_clustered_depths_fall_back_to_the_block_sort(n):
+    """One 16x16 tile holding n instances (a 257-2048 and a 2049-8192 bucket) whose
+    depths sit in two tight clusters plus a far outlier: the key-range slices put
+    most keys in a slice too large for a warp, so the bucket goes to the block's
+    bitonic network; equal depths are ordered by index."""
+    sc = scenes.random_small_scene(35, n=n, width=16, height=16, sh_degree=0, log_lo=-2.0, log_hi=-1.0,
+                                   logit_mu=-3.0, spread=0.3)
+    rng = np.random.default_rng(6)
+    z = np.where(rng.uniform(size=n) < 0.5, np.float32(3.0), np.float32(3.0001)).astype(np.float32)
+    z[: n // 10] = np.float32(3.0)            # ties broken by index
+    z[-1] = np.float32(50.0)                  # stretches the key interval
+    sc.params[2] = z
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] == n
+
+
+def test_sort_slices_spread_over_warps_and_threads():
+    """One tile of 1900 instances with depths spread over a wide interval but a
+    dense band holding ~200 of them: slices of one key (threads), of tens (warps)
+    and empty ones in one bucket."""
+    n = 1900
+    sc = scenes.random_small_scene(36, n=n, width=16, height=16, sh_degree=0, log_lo=-2.0, log_hi=-1.0,
+                                   logit_mu=-3.0, spread=0.3)
+    rng = np.random.default_rng(7)
+    z = rng.uniform(2.0, 40.0, n).astype(np.float32)
+    z[:200] = rng.uniform(10.0, 10.05, 200).astype(np.float32)
+    sc.params[2] = z
+    st = parity.run_stage_parity(sc)
+    assert st["instances"] == n
+
+
 def test_wide_view_bins_in_two_tile_row_bands():
     """An 8192x1296 view has 512 x 81 tiles, more than one block's shared-memory
     counters hold: the binning runs in two bands of tile rows (80 + 1).  The
