@@ -147,6 +147,7 @@ extern "C" gs_status gs_adam_deferred(float* params, float* grads, float* m, flo
                                       int32_t sh_degree, const uint32_t* idx, const int64_t* n_idx, int32_t t,
                                       const float* lr, float beta1, float beta2, float eps, int32_t flush, void* stream)
 {
+    GS_NVTX_RANGE("gs_adam_deferred");
     const int rows = param_rows(sh_degree);
     if (rows < 0 || !lr || n < 0 || n > INT32_MAX || t < 1) return GS_ERR_INVALID_ARG;
     for (int i = 0; i < 5; ++i)

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __rest
     // nothing when the count exceeds the caller's capacity
     if (kScatter && *total > capacity) return;
     const int b = blockIdx.x, band = blockIdx.y;
-    if (!kScatter && b == 0 && band == 0 && threadIdx.x < 4) stats[threadIdx.x] = 0u;   // for bucket_stats
+    if (!kScatter && b == 0 && band == 0 && threadIdx.x < 5) stats[threadIdx.x] = 0u;   // bucket_stats, error word
     const int row0 = band * G.band_rows;
     const int row1 = min(G.tiles_y, row0 + G.band_rows);
     const int nt = (row1 - row0) * G.tiles_x;
@@ -353,21 +353,16 @@ __global__ void __launch_bounds__(kSortWarps * 32) sort_warp_kernel(const uint2*
     warp_sort(tmp, r.x, c, (uint64_t)t << 32, keys, ids);
 }
 
-// One kRegThreads-thread CTA per listed bucket of kWarpCap < size <= kRegCap.
-// Launched before the host knows the class size: one block per possible bucket,
-// the ones past the device-held count (or all, if the capacity is short) exit.
-// The bucket is split by uniform slices of its [min, max] key interval into
-// kSlices sub-buckets (the monotone digit of the huge-bucket splitter below), a
-// counting scatter through shared memory puts the sub-buckets in digit order,
-// and each sub-bucket is sorted on its own: up to kThreadCap keys by one thread
-// (insertion), larger ones by a warp (register bitonic, as for small buckets).
-// That is O(c) work plus small sorts where the bitonic network over the whole
-// bucket needs O(c log^2 c).  Keys are unique within a bucket, so the result
-// does not depend on the scatter's order.  A bucket with a sub-bucket of more
-// than kWarpCap keys (a tight cluster of depths) is sorted by the block's
-// register bitonic network instead.
-constexpr int kSlices = kRegThreads;
+// Sort of one bucket by key-range slices.  The bucket is split by uniform
+// slices of its [min, max] key interval into kT sub-buckets (the monotone digit
+// of the huge-bucket splitter below), a counting scatter through shared memory
+// puts the sub-buckets in digit order, and each sub-bucket is sorted on its own:
+// up to kThreadCap keys by one thread (insertion), larger ones by a warp
+// (register bitonic, as for small buckets).  That is O(c) work plus small sorts
+// where a bitonic network over the whole bucket needs O(c log^2 c).  Keys are
+// unique within a bucket, so the result does not depend on the scatter's order.
 constexpr int kThreadCap = 8;
+constexpr int kSplitMidCap = 8192;   // mid-class buckets sorted by slices (larger: bitonic)
 
 // One warp sorts s[0, c), c <= 32 E, in place (shared memory).
 template <int E>
@@ -396,66 +391,62 @@ __device__ __forceinline__ void warp_sort_smem(uint64_t* s, int c)
     else warp_sort_smem_e<8>(s, c);
 }
 
-__global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* __restrict__ list,
-                                                               const uint2* __restrict__ ranges,
-                                                               const uint64_t* __restrict__ tmp,
-                                                               uint64_t* __restrict__ keys, uint32_t* __restrict__ ids,
-                                                               const unsigned int* __restrict__ count,
-                                                               const unsigned long long* __restrict__ total,
-                                                               unsigned long long capacity)
+template <int kT>
+struct SplitSmem {
+    uint32_t start[kT], cur[kT], big[kT];   // per slice: size, cursor / start, slices left to warps
+    uint64_t red[2][kT / 32];
+    uint32_t wsum[kT / 32], wmax[kT / 32];
+    uint32_t nbig;
+};
+
+// A kT-thread block sorts tmp[o, o + c) into keys / ids at o through s_in and
+// s_out (c keys each).  Returns false, having written nothing, when a slice
+// holds more than kWarpCap keys (a tight cluster of depths): the caller sorts
+// the bucket another way (after a barrier; s_in and s_out are free again).
+template <int kT>
+__device__ bool split_sort(const uint64_t* __restrict__ tmp, size_t o, int c, uint64_t hi,
+                           uint64_t* __restrict__ keys, uint32_t* __restrict__ ids, uint64_t* s_in,
+                           uint64_t* s_out, SplitSmem<kT>& S)
 {
-    __shared__ uint64_t s[kRegThreads * 9];          // the bucket's keys (the bitonic path's workspace)
-    __shared__ uint64_t s_out[kRegCap];              // ... scattered into sub-bucket order
-    __shared__ uint32_t s_start[kSlices], s_cur[kSlices], s_big[kSlices];
-    __shared__ uint32_t s_nbig;
-    __shared__ uint64_t s_red[2][kRegThreads / 32];
-    __shared__ uint32_t s_wsum[kRegThreads / 32], s_wmax[kRegThreads / 32];
-    if (*total > capacity || blockIdx.x >= *count) return;
-    const uint32_t t = list[blockIdx.x];
-    const uint2 r = ranges[t];
-    const int c = (int)(r.y - r.x);
-    const uint64_t hi = (uint64_t)t << 32;
+    constexpr int kW = kT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kW = kRegThreads / 32;
-    // keys and their interval
     uint64_t kmin = ~0ull, kmax = 0ull;
-    for (int i = tid; i < c; i += kRegThreads) {
-        const uint64_t k = tmp[(size_t)r.x + i];
-        s[i] = k;
+    for (int i = tid; i < c; i += kT) {
+        const uint64_t k = tmp[o + i];
+        s_in[i] = k;
         kmin = k < kmin ? k : kmin;
         kmax = k > kmax ? k : kmax;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t a = __shfl_xor_sync(0xffffffffu, kmin, o);
-        const uint64_t b = __shfl_xor_sync(0xffffffffu, kmax, o);
+    for (int d = 16; d > 0; d >>= 1) {
+        const uint64_t a = __shfl_xor_sync(0xffffffffu, kmin, d);
+        const uint64_t b = __shfl_xor_sync(0xffffffffu, kmax, d);
         kmin = a < kmin ? a : kmin;
         kmax = b > kmax ? b : kmax;
     }
     if (lane == 0) {
-        s_red[0][warp] = kmin;
-        s_red[1][warp] = kmax;
+        S.red[0][warp] = kmin;
+        S.red[1][warp] = kmax;
     }
-    s_start[tid] = 0u;
-    if (tid == 0) s_nbig = 0u;
+    S.start[tid] = 0u;
+    if (tid == 0) S.nbig = 0u;
     __syncthreads();
-#pragma unroll
     for (int w = 0; w < kW; ++w) {
-        kmin = s_red[0][w] < kmin ? s_red[0][w] : kmin;
-        kmax = s_red[1][w] > kmax ? s_red[1][w] : kmax;
+        kmin = S.red[0][w] < kmin ? S.red[0][w] : kmin;
+        kmax = S.red[1][w] > kmax ? S.red[1][w] : kmax;
     }
-    // digit(k) = floor((k - kmin) * scale / 2^64): non-decreasing in k, below kSlices
+    // digit(k) = floor((k - kmin) * scale / 2^64): non-decreasing in k, below kT
     const uint64_t range = kmax - kmin;
-    const bool direct = range < (uint64_t)kSlices;
-    const uint64_t scale = direct ? 0ull : (~0ull / (range + 1ull)) * (uint64_t)kSlices;
+    const bool direct = range < (uint64_t)kT;
+    const uint64_t scale = direct ? 0ull : (~0ull / (range + 1ull)) * (uint64_t)kT;
     auto digit = [&](uint64_t k) -> uint32_t {
         const uint64_t d = k - kmin;
         return direct ? (uint32_t)d : (uint32_t)__umul64hi(d, scale);
     };
-    for (int i = tid; i < c; i += kRegThreads) atomicAdd(&s_start[digit(s[i])], 1u);
+    for (int i = tid; i < c; i += kT) atomicAdd(&S.start[digit(s_in[i])], 1u);
     __syncthreads();
-    // exclusive scan of the sub-bucket sizes, and the largest
-    const uint32_t mine = s_start[tid];
+    // exclusive scan of the slice sizes, and the largest
+    const uint32_t mine = S.start[tid];
     uint32_t incl = mine, mx = mine;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -463,36 +454,28 @@ __global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* _
         if (lane >= d) incl += y;
         mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
     }
-    if (lane == 31) s_wsum[warp] = incl;
-    if (lane == 0) s_wmax[warp] = mx;
+    if (lane == 31) S.wsum[warp] = incl;
+    if (lane == 0) S.wmax[warp] = mx;
     __syncthreads();
     uint32_t wpre = 0, bmax = 0;
-#pragma unroll
     for (int w = 0; w < kW; ++w) {
-        wpre += w < warp ? s_wsum[w] : 0u;
-        bmax = max(bmax, s_wmax[w]);
+        wpre += w < warp ? S.wsum[w] : 0u;
+        bmax = max(bmax, S.wmax[w]);
     }
+    if (bmax > (uint32_t)kWarpCap) return false;   // block-uniform
     const uint32_t start = wpre + incl - mine;
-    if (bmax > (uint32_t)kWarpCap) {
-        // a tight cluster of keys: the bitonic network (it reloads the keys into s)
-        __syncthreads();
-        if (c <= 2 * kRegThreads) reg_sort<kRegThreads, 2, true>(tmp, r.x, c, hi, keys, ids, s);
-        else if (c <= 4 * kRegThreads) reg_sort<kRegThreads, 4, true>(tmp, r.x, c, hi, keys, ids, s);
-        else reg_sort<kRegThreads, 8, true>(tmp, r.x, c, hi, keys, ids, s);
-        return;
-    }
-    s_cur[tid] = start;
+    S.cur[tid] = start;
     __syncthreads();
-    for (int i = tid; i < c; i += kRegThreads) {
-        const uint64_t k = s[i];
-        s_out[atomicAdd(&s_cur[digit(k)], 1u)] = k;
+    for (int i = tid; i < c; i += kT) {
+        const uint64_t k = s_in[i];
+        s_out[atomicAdd(&S.cur[digit(k)], 1u)] = k;
     }
     __syncthreads();
     if (mine > (uint32_t)kThreadCap) {
-        s_big[atomicAdd(&s_nbig, 1u)] = tid;     // sub-bucket for a warp
-        s_cur[tid] = start;                      // its start (s_cur held its end)
+        S.big[atomicAdd(&S.nbig, 1u)] = tid;   // a slice for a warp
+        S.cur[tid] = start;                    // its start (the cursor ended at its end)
     } else {
-        // thread tid: insertion sort of its sub-bucket [start, start + mine)
+        // insertion sort of this thread's slice [start, start + mine)
         for (uint32_t a = start + 1; a < start + mine; ++a) {
             const uint64_t k = s_out[a];
             uint32_t b = a;
@@ -504,27 +487,64 @@ __global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* _
         }
     }
     __syncthreads();
-    for (uint32_t b = warp; b < s_nbig; b += kW) {
-        const uint32_t d = s_big[b];
-        warp_sort_smem(s_out + s_cur[d], (int)s_start[d]);   // s_start[d]: the size of sub-bucket d
+    for (uint32_t b = warp; b < S.nbig; b += kW) {
+        const uint32_t d = S.big[b];
+        warp_sort_smem(s_out + S.cur[d], (int)S.start[d]);   // S.start[d]: the slice's size
     }
     __syncthreads();
-    for (int i = tid; i < c; i += kRegThreads) emit_sorted(s_out[i], hi, keys, ids, (size_t)r.x + i);
+    for (int i = tid; i < c; i += kT) emit_sorted(s_out[i], hi, keys, ids, o + i);
+    return true;
+}
+
+// One kRegThreads-thread CTA per listed bucket of kWarpCap < size <= kRegCap,
+// sorted by key-range slices (the block's register bitonic network when a slice
+// is too large).  Launched before the host knows the class size: one block per
+// possible bucket, the ones past the device-held count (or all, if the capacity
+// is short) exit.
+__global__ void __launch_bounds__(kRegThreads) sort_reg_kernel(const uint32_t* __restrict__ list,
+                                                               const uint2* __restrict__ ranges,
+                                                               const uint64_t* __restrict__ tmp,
+                                                               uint64_t* __restrict__ keys, uint32_t* __restrict__ ids,
+                                                               const unsigned int* __restrict__ count,
+                                                               const unsigned long long* __restrict__ total,
+                                                               unsigned long long capacity)
+{
+    __shared__ uint64_t s[kRegThreads * 9];
+    __shared__ uint64_t s_out[kRegCap];
+    __shared__ SplitSmem<kRegThreads> S;
+    if (*total > capacity || blockIdx.x >= *count) return;
+    const uint32_t t = list[blockIdx.x];
+    const uint2 r = ranges[t];
+    const int c = (int)(r.y - r.x);
+    const uint64_t hi = (uint64_t)t << 32;
+    if (split_sort<kRegThreads>(tmp, r.x, c, hi, keys, ids, s, s_out, S)) return;
+    __syncthreads();
+    if (c <= 2 * kRegThreads) reg_sort<kRegThreads, 2, true>(tmp, r.x, c, hi, keys, ids, s);
+    else if (c <= 4 * kRegThreads) reg_sort<kRegThreads, 4, true>(tmp, r.x, c, hi, keys, ids, s);
+    else reg_sort<kRegThreads, 8, true>(tmp, r.x, c, hi, keys, ids, s);
 }
 
 // One kMidThreads-thread CTA per listed bucket of kRegCap < size <= kBigCap:
-// the same register / shuffle / shared-memory bitonic with 4, 8 or 16 keys per
-// thread (dynamic shared memory: kMidThreads * (E + 1) keys for the largest E).
+// up to kSplitMidCap instances by key-range slices (the first 2 c keys of the
+// dynamic buffer hold the keys and their slice order), otherwise --
+// and when a slice is too large -- the register / shuffle / shared-memory
+// bitonic with 4, 8 or 16 keys per thread (dynamic shared memory:
+// kMidThreads * (E + 1) keys for the largest E).
 __global__ void __launch_bounds__(kMidThreads) sort_mid_kernel(const uint32_t* __restrict__ list,
                                                                const uint2* __restrict__ ranges,
                                                                const uint64_t* __restrict__ tmp,
                                                                uint64_t* __restrict__ keys, uint32_t* __restrict__ ids)
 {
     extern __shared__ uint64_t s_mid[];
+    __shared__ SplitSmem<kMidThreads> S;
     const uint32_t t = list[blockIdx.x];
     const uint2 r = ranges[t];
     const int c = (int)(r.y - r.x);
     const uint64_t hi = (uint64_t)t << 32;
+    if (c <= kSplitMidCap) {
+        if (split_sort<kMidThreads>(tmp, r.x, c, hi, keys, ids, s_mid, s_mid + c, S)) return;
+        __syncthreads();
+    }
     if (c <= 4 * kMidThreads) reg_sort<kMidThreads, 4, false>(tmp, r.x, c, hi, keys, ids, s_mid);
     else if (c <= 8 * kMidThreads) reg_sort<kMidThreads, 8, false>(tmp, r.x, c, hi, keys, ids, s_mid);
     else reg_sort<kMidThreads, 16, false>(tmp, r.x, c, hi, keys, ids, s_mid);
@@ -598,7 +618,8 @@ struct HugeSmem {
 // 7 * (kSplit - 1) + 1 ranges.
 __global__ void __launch_bounds__(1024) sort_huge_kernel(const uint32_t* __restrict__ list,
                                                          const uint2* __restrict__ ranges, uint64_t* tmp,
-                                                         uint64_t* keys, uint32_t* __restrict__ ids)
+                                                         uint64_t* keys, uint32_t* __restrict__ ids,
+                                                         unsigned int* __restrict__ error)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
     HugeSmem& S = *reinterpret_cast<HugeSmem*>(s_raw);
@@ -662,9 +683,13 @@ __global__ void __launch_bounds__(1024) sort_huge_kernel(const uint32_t* __restr
             if (sc <= (uint32_t)kWarpCap) continue;
             if (sc <= (uint32_t)kBigCap) {
                 cta_sort(S.keys, dst, o + S.hist[d], (int)sc, hi_key, keys, ids);
-            } else if (threadIdx.x == 0 && S.sp < kStack) {   // the bound above keeps sp < kStack
-                S.stack[S.sp] = make_uint2((uint32_t)(o + S.hist[d]), sc | (in_keys ? 0u : 0x80000000u));
-                S.sp += 1;
+            } else if (threadIdx.x == 0) {
+                if (S.sp < kStack) {   // the bound above keeps sp < kStack
+                    S.stack[S.sp] = make_uint2((uint32_t)(o + S.hist[d]), sc | (in_keys ? 0u : 0x80000000u));
+                    S.sp += 1;
+                } else {
+                    atomicOr(error, 1u);   // a range left unsorted: reported, never silent
+                }
             }
         }
         __syncthreads();
@@ -709,9 +734,9 @@ inline WsLayout ws_layout(const BinGeom& G, int64_t ntile_ids, int64_t capacity)
     L.cnt = o;       o = align_up(o + sizeof(uint32_t) * (size_t)ncnt);
     L.off = o;       o = align_up(o + sizeof(uint32_t) * (size_t)ncnt);
     L.scan_sums = o; o = align_up(o + scan_ws_bytes(ncnt));
-    L.totals = o;    // instance total (u64) and the bucket stats (4 x u32), read back in one copy
-    L.stats = o + sizeof(unsigned long long);
-    o = align_up(o + sizeof(unsigned long long) + 4 * sizeof(unsigned int));
+    L.totals = o;    // instance total (u64) and the bucket stats (4 x u32), read back in one copy,
+    L.stats = o + sizeof(unsigned long long);   // then the huge-bucket splitter's error word (u32)
+    o = align_up(o + sizeof(unsigned long long) + 5 * sizeof(unsigned int));
     L.lists = o;     o = align_up(o + 3 * sizeof(uint32_t) * (size_t)ntile_ids);
     L.tmp = o;       o = align_up(o + sizeof(uint64_t) * (size_t)capacity);
     L.bytes = o;
@@ -726,6 +751,7 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
                                  int64_t capacity, uint64_t* keys, uint32_t* ids, uint32_t* tile_ranges,
                                  int64_t* n_instances, void* ws, size_t* ws_bytes, void* stream)
 {
+    GS_NVTX_RANGE("gs_bin_sort");
     if (!ws_bytes || n < 0 || n > INT32_MAX || n_views < 1 || n_views > GS_MAX_VIEWS) return GS_ERR_INVALID_ARG;
     if (width <= 0 || height <= 0 || width > 65535 * kTile || height > 65535 * kTile) return GS_ERR_INVALID_ARG;
     if (capacity < 0 || capacity > (int64_t)UINT32_MAX) return GS_ERR_INVALID_ARG;
@@ -766,7 +792,7 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
         GS_LAUNCH_CHECK();
     } else {
         GS_CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * (size_t)ncnt, s));
-        GS_CUDA_TRY(cudaMemsetAsync(stats, 0, 4 * sizeof(unsigned int), s));
+        GS_CUDA_TRY(cudaMemsetAsync(stats, 0, 5 * sizeof(unsigned int), s));
     }
     GS_CUDA_TRY((scan_launch<uint32_t, false>(cnt, ncnt, off, scan_sums, totals, s)));
     const int threads = 256;
@@ -825,7 +851,10 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (host.total == 0) return GS_OK;
     if (host.st[2] > 0) {
         const int e = host.st[0] <= 4u * kMidThreads ? 4 : (host.st[0] <= 8u * kMidThreads ? 8 : 16);
-        const size_t smem = sizeof(uint64_t) * (size_t)kMidThreads * (size_t)(e + 1);
+        // the bitonic network's kMidThreads * (e + 1) keys, or the slice sort's 2 c
+        const size_t split_keys = 2 * (size_t)(host.st[0] < (unsigned)kSplitMidCap ? host.st[0] : kSplitMidCap);
+        const size_t bitonic_keys = (size_t)kMidThreads * (size_t)(e + 1);
+        const size_t smem = sizeof(uint64_t) * (split_keys > bitonic_keys ? split_keys : bitonic_keys);
         GS_CUDA_TRY(cudaFuncSetAttribute(sort_mid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         sort_mid_kernel<<<host.st[2], kMidThreads, smem, s>>>(lists + ntile_ids, ranges, tmp, keys, ids);
         GS_LAUNCH_CHECK();
@@ -833,8 +862,13 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (host.st[3] > 0) {
         const size_t smem = sizeof(HugeSmem);
         GS_CUDA_TRY(cudaFuncSetAttribute(sort_huge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        sort_huge_kernel<<<host.st[3], 1024, smem, s>>>(lists + 2 * ntile_ids, ranges, tmp, keys, ids);
+        sort_huge_kernel<<<host.st[3], 1024, smem, s>>>(lists + 2 * ntile_ids, ranges, tmp, keys, ids, stats + 4);
         GS_LAUNCH_CHECK();
+        // the splitter's error word: a second read-back, only when a bucket of more
+        // than kBigCap instances exists
+        GS_CUDA_TRY(cudaMemcpyAsync(&host.st[0], stats + 4, sizeof(unsigned int), cudaMemcpyDeviceToHost, s));
+        GS_CUDA_TRY(cudaStreamSynchronize(s));
+        if (host.st[0] != 0u) return GS_ERR_DEVICE;
     }
     return GS_OK;
 }

@@ -107,6 +107,7 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
                                      const gs_render_opts* opts, uint32_t* idx, int64_t* n_idx, float* grads,
                                      void* ws, size_t* ws_bytes, void* stream)
 {
+    GS_NVTX_RANGE("gs_grad_compact");
     if (!ws_bytes || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
     const CompactWs L = compact_ws(n);
     if (!ws) {
@@ -248,6 +249,7 @@ extern "C" gs_status gs_grad_compact_static(float* grad2d, uint8_t* touched, con
                                             const gs_render_opts* opts, uint32_t* idx, int64_t* n_idx, float* grads,
                                             void* stream)
 {
+    GS_NVTX_RANGE("gs_grad_compact_static");
     if (n < 0 || n > kStaticMaxN) return GS_ERR_INVALID_ARG;
     if (gs::compact_ws(n).bytes > kStaticScratchBytes) return GS_ERR_INVALID_ARG;
     void* scratch = nullptr;

@@ -85,6 +85,7 @@ extern "C" gs_status gs_split_ranges(const uint64_t* keys, const uint32_t* tile_
                                      int32_t width, int32_t height, int32_t n_subsets, const float* depth_splits,
                                      uint32_t* sub_ranges, void* stream)
 {
+    GS_NVTX_RANGE("gs_split_ranges");
     if (!tile_ranges || !sub_ranges || n_subsets < 1 || n_subsets > kMaxSubsets) return GS_ERR_INVALID_ARG;
     if (n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 || height < 1) return GS_ERR_INVALID_ARG;
     if (n_subsets > 1 && (!depth_splits || !keys)) return GS_ERR_INVALID_ARG;
@@ -115,6 +116,7 @@ extern "C" gs_status gs_compose(const float* c_parts, const float* t_parts, int3
                                 int32_t width, int32_t height, const float* bg, float* image, float* t_final,
                                 void* stream)
 {
+    GS_NVTX_RANGE("gs_compose");
     if (!c_parts || !t_parts || !bg || !image || n_subsets < 1 || n_subsets > kMaxSubsets) return GS_ERR_INVALID_ARG;
     if (n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 || height < 1) return GS_ERR_INVALID_ARG;
     const int64_t hw = (int64_t)width * height, n_pix = hw * n_views;

@@ -389,6 +389,7 @@ using namespace gs;
 extern "C" gs_status gs_dssim_loss_grad(const float* image, const float* target, int32_t n_views, int32_t width,
                                         int32_t height, float lambda, double* loss, float* dldc, void* stream)
 {
+    GS_NVTX_RANGE("gs_dssim_loss_grad");
     using namespace ssim;
     if (!image || !target || !loss || !dldc) return GS_ERR_INVALID_ARG;
     if (n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 || height < 1) return GS_ERR_INVALID_ARG;

@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/gs.h"
@@ -129,6 +130,17 @@ struct CamSet {
     gs_camera cam[GS_MAX_VIEWS];
     int32_t n_views;
 };
+
+// One NVTX range per C-ABI call, named after the call (it groups the call's
+// kernels in Nsight Systems and in ncu's --nvtx range filters).  NVTX 3 is
+// header-only: with no tool attached, a push and a pop cost a pointer check.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define GS_NVTX_RANGE(name) ::gs::NvtxRange gs_nvtx_range_(name)
 
 // Status plumbing for host code.
 #define GS_CUDA_TRY(expr)                                      \

@@ -101,6 +101,7 @@ using namespace gs;
 extern "C" gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, const gs_camera* cams,
                                 int32_t n_views, const gs_render_opts* opts, const gs_proj* out, void* stream)
 {
+    GS_NVTX_RANGE("gs_project");
     if (!opts_ok(opts) || !out || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
     if (param_rows(sh_degree) < 0) return GS_ERR_INVALID_ARG;
     gs_status st = check_views(cams, n_views);

@@ -220,6 +220,7 @@ using namespace gs;
 extern "C" gs_status gs_prune_tiles(const gs_proj* proj, int64_t n, int32_t n_views, int32_t width, int32_t height,
                                     int32_t budget, uint32_t* ids, uint32_t* tile_ranges, void* stream)
 {
+    GS_NVTX_RANGE("gs_prune_tiles");
     if (!proj || !tile_ranges || budget < 1 || n < 0 || n > INT32_MAX) return GS_ERR_INVALID_ARG;
     if (n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 || height < 1) return GS_ERR_INVALID_ARG;
     if (n > 0 && (!proj->rec || !ids)) return GS_ERR_INVALID_ARG;

@@ -849,6 +849,7 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
                                              double* loss, float* grad2d, uint8_t* touched, uint64_t* eval_counts,
                                              void* stream)
 {
+    GS_NVTX_RANGE("gs_raster_fused_fwd_bwd");
     RasterArgs a;
     long long grid = 0;
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
@@ -876,6 +877,7 @@ extern "C" gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const
                                            double* loss, float* grad2d, uint8_t* touched, uint64_t* work,
                                            void* stream)
 {
+    GS_NVTX_RANGE("gs_raster_work_counts");
     RasterArgs a;
     long long grid = 0;
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
@@ -900,6 +902,7 @@ extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, con
                                              int32_t* last_idx, uint32_t* pass_bits, int32_t* bits_chunk,
                                              uint64_t* eval_counts, void* stream)
 {
+    GS_NVTX_RANGE("gs_raster_forward_state");
     RasterArgs a;
     long long grid = 0;
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
@@ -921,6 +924,7 @@ extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, co
                                               const int32_t* bits_chunk, const float* dldc, float* grad2d,
                                               uint8_t* touched, void* stream)
 {
+    GS_NVTX_RANGE("gs_raster_backward_state");
     RasterArgs a;
     long long grid = 0;
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);

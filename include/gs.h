@@ -78,7 +78,7 @@ typedef enum gs_status {
     GS_ERR_INVALID_ARG = 1, /* a pointer, size or option is out of range          */
     GS_ERR_CAPACITY = 2,    /* instance buffers too small; needed count reported  */
     GS_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed        */
-    GS_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out                 */
+    GS_ERR_TIMEOUT = 4,     /* reserved: no call waits on the device              */
     GS_ERR_DEVICE = 5       /* a kernel reported an error through the device word */
 } gs_status;
 
@@ -153,13 +153,17 @@ GS_API gs_status gs_project(const float* params, int64_t n, int32_t sh_degree, c
  * ws / ws_bytes: scratch (ws == NULL: query).  Synchronises the host once, on
  * the read-back of the instance count (an event after the copy, so the scatter
  * and the sorts of buckets up to 2048 instances, already queued, run
- * meanwhile).  The
+ * meanwhile), and a second time only when some tile holds more than 16384
+ * instances: the key-range splitter of such buckets reports a range it could
+ * not sort through a device error word, read back before returning.  The
  * count is read into a 24-byte pinned host buffer that each calling thread
  * allocates on its first call and keeps for its lifetime.
  * Errors: CAPACITY if n_instances > capacity (outputs untouched: the queued
  * kernels check the count on the device and write nothing);
  * INVALID_ARG for bad sizes (width above 655360, i.e. more than 40960 tiles in a
- * row) or a too small workspace. */
+ * row) or a too small workspace; DEVICE if the splitter's pending-range stack
+ * overflowed (impossible for unique keys: each split level narrows the key
+ * interval by at least 512, so at most seven levels are pending). */
 GS_API gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views, int32_t width, int32_t height,
                       int64_t capacity, uint64_t* keys, uint32_t* ids, uint32_t* tile_ranges,
                       int64_t* n_instances, void* ws, size_t* ws_bytes, void* stream);

@@ -121,3 +121,22 @@ def test_binding_raises_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(abi, "_lib", None)
     with pytest.raises(RuntimeError, match="CUDA library missing"):
         abi.lib()
+
+
+def test_every_entry_point_opens_an_nvtx_range_named_after_it():
+    """Each C-ABI call that does device work starts with GS_NVTX_RANGE("<its name>"),
+    so a profiler groups the kernels it launches under the call."""
+    import glob
+    csrc = os.path.join(ROOT, "differentiable_rasterizer_gb300", "csrc")
+    seen = set()
+    for path in glob.glob(os.path.join(csrc, "*.cu")):
+        text = open(path).read()
+        for m in re.finditer(r'extern "C" gs_status (gs_\w+)\(', text):
+            body = text[text.index("\n{\n", m.end()) + 3:]
+            first = body.lstrip().split("\n", 1)[0].strip()
+            assert first == f'GS_NVTX_RANGE("{m.group(1)}");', (m.group(1), first)
+            seen.add(m.group(1))
+    declared = {s for s in _declared_symbols()}
+    status_calls = {s for s in declared if s not in ("gs_error_string", "gs_param_rows", "gs_param_stride",
+                                                     "gs_num_tiles", "gs_version")}
+    assert status_calls <= seen, status_calls - seen
