@@ -205,7 +205,7 @@ def run_reference(args):
     from differentiable_rasterizer_gb300 import scenes
     import oracle
     oracle.build()
-    sc = scenes.make_scene(args.config)
+    sc = scenes.make_scene(args.config, seed=args.seed)
     rows = args.ref_rows
     targets = cpu_targets_band(sc, rows)
     state = dict(params=sc.params.copy(), m=np.zeros_like(sc.params), v=np.zeros_like(sc.params),
@@ -258,7 +258,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     gs_build.build()
 
-    sc = scenes.make_scene(args.config)
+    sc = scenes.make_scene(args.config, seed=args.seed)
     tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda",
                                   dssim_lambda=args.dssim, tile_budget=args.tile_budget)
     if sc.target_kind == "uniform":
@@ -332,6 +332,16 @@ def run_gpu(args):
     clocks = stop_clock_sampler(sampler, clock_path)
     total_ms = t_start.elapsed_time(t_end)
     stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in evs])
+    if args.log_steps and rank == 0:
+        with open(args.log_steps, "w") as f:
+            for k in range(args.steps):
+                f.write(json.dumps({"step": k, "ms": float(evs[k][0].elapsed_time(evs[k][5])),
+                                    "stage_ms": dict(zip(["project", "bin_sort", "raster", "grad_compact",
+                                                          "adam_deferred"], [float(x) for x in stage_ms[k]]))}) + "\n")
+            # the state after the last timed step
+            f.write(json.dumps({"after_steps": args.steps, "loss": [float(x) for x in tr.loss.cpu().tolist()],
+                                "instances": int(tr.n_instances), "union": int(tr.n_idx[tr.V].item()),
+                                "per_view_nonzero": [int(x) for x in tr.n_idx[:tr.V].cpu().tolist()]}) + "\n")
     counts = tr.eval_counts.cpu().numpy().astype(np.float64)
     e_fwd, e_bwd, e_comp = counts / args.steps
     evals_per_step = e_fwd + e_bwd
@@ -458,7 +468,7 @@ def run_partial(args):
     from differentiable_rasterizer_gb300 import build as gs_build, pipeline, scenes
     torch.cuda.set_device(0)
     gs_build.build()
-    sc = scenes.make_scene(args.config)
+    sc = scenes.make_scene(args.config, seed=args.seed)
     tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr, device="cuda")
     S = args.partial
     tr.project()
@@ -522,6 +532,10 @@ def main():
                     help="prune every tile list to its K most opaque entries before rasterizing")
     ap.add_argument("--dssim", type=float, default=None, metavar="LAMBDA",
                     help="train with (1 - LAMBDA) L1 + LAMBDA D-SSIM (three raster launches instead of the fused one)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="seed of the synthetic scene (default: the workload's own: tiny 0 ... batched 4)")
+    ap.add_argument("--log-steps", default=None, metavar="PATH",
+                    help="also write one JSON line per timed step (stage ms, loss, instances, union size) to PATH")
     ap.add_argument("--cpu-rows", type=int, default=1080)
     ap.add_argument("--ref-rows", type=int, default=68)
     args = ap.parse_args()

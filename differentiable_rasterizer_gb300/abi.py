@@ -15,6 +15,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libgs_gb300.so")
+CHECKED_LIB_PATH = os.path.join(_HERE, "_build", "libgs_gb300_checked.so")
 
 GS_OK, GS_ERR_INVALID_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA, GS_ERR_TIMEOUT, GS_ERR_DEVICE = range(6)
 GS_TILE = 16
@@ -24,7 +25,7 @@ GS_GRAD2D_STRIDE = 12
 
 EXPORTS = ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
            "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_grad_compact_static",
-           "gs_prune_tiles", "gs_split_ranges", "gs_compose", "gs_raster_work_counts",
+           "gs_prune_tiles", "gs_split_ranges", "gs_compose", "gs_raster_work_counts", "gs_check_report",
            "gs_error_string", "gs_param_rows", "gs_param_stride", "gs_num_tiles", "gs_version")
 
 
@@ -59,14 +60,21 @@ _I32 = ctypes.c_int32
 _F = ctypes.c_float
 
 
+def lib_path() -> str:
+    """The library lib() loads: the bounds-checked build when the environment sets
+    GS_CHECKED=1 (read once, at the first load), else the plain one."""
+    return CHECKED_LIB_PATH if os.environ.get("GS_CHECKED", "") == "1" else LIB_PATH
+
+
 def lib():
-    """Load libgs_gb300.so (raises if it has not been built)."""
+    """Load the CUDA library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"CUDA library missing: {LIB_PATH}; build it with "
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library missing: {path}; build it with "
                                "`python -m differentiable_rasterizer_gb300.build`")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         L.gs_project.argtypes = [_P, _I64, _I32, _P, _I32, _P, ctypes.POINTER(GsProj), _P]
         L.gs_bin_sort.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I64, _P, _P, _P,
                                   ctypes.POINTER(ctypes.c_int64), _P, ctypes.POINTER(ctypes.c_size_t), _P]
@@ -89,6 +97,8 @@ def lib():
                      "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_prune_tiles",
                      "gs_split_ranges", "gs_compose", "gs_raster_work_counts"):
             getattr(L, name).restype = ctypes.c_int
+        L.gs_check_report.argtypes = [_P, ctypes.POINTER(ctypes.c_int32)]
+        L.gs_check_report.restype = ctypes.c_int
         L.gs_error_string.argtypes = [ctypes.c_int]
         L.gs_error_string.restype = ctypes.c_char_p
         L.gs_param_rows.argtypes = [_I32]
@@ -175,6 +185,25 @@ def gs_raster_work_counts(proj, n, tile_ranges, ids, cams, n_views, opts, target
     _check("gs_raster_work_counts",
            lib().gs_raster_work_counts(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
                                        target, image, loss, grad2d, touched, work, stream))
+
+
+CHECK_SITES = ("none", "bin_rect", "bin_slot", "sort_slot", "sort_id", "range", "raster_id", "prune_id",
+               "compact_id", "adam_id")
+
+
+def gs_check_report() -> dict:
+    """Bounds-check report since the previous one (then reset): {"checked": bool,
+    "failures": count, "site": name, "index": i, "bound": n}.  A DEVICE status
+    (failed checks) is returned in the dict, not raised."""
+    rep = (ctypes.c_uint64 * 4)()
+    checked = ctypes.c_int32(0)
+    st = lib().gs_check_report(rep, ctypes.byref(checked))
+    if st not in (GS_OK, GS_ERR_DEVICE):
+        _check("gs_check_report", st)
+    idx = rep[2] - (1 << 64) if rep[2] >= (1 << 63) else rep[2]
+    site = CHECK_SITES[rep[1]] if rep[1] < len(CHECK_SITES) else str(rep[1])
+    return {"checked": bool(checked.value), "failures": int(rep[0]), "site": site, "index": int(idx),
+            "bound": int(rep[3])}
 
 
 def gs_prune_tiles(proj, n, n_views, width, height, budget, ids, tile_ranges, stream):

@@ -1,10 +1,14 @@
-"""Builds libgs_gb300.so (the C-ABI CUDA library) in-tree for sm_103a.
+"""Builds libgs_gb300.so (the C-ABI CUDA library) in-tree for sm_103a, and its
+bounds-checked twin libgs_gb300_checked.so (the same sources with -DGS_CHECKED:
+every index read from memory is tested before use, failures are counted and
+the access skipped, gs_check_report returns the count).
 
-Each translation unit is compiled by nvcc in parallel, then linked with the
-shared CUDA runtime.  Forward-decision code relies on IEEE rounding of every
-operation, so the whole library is compiled without fma contraction
-(-fmad=false), with IEEE division and square root and without flush-to-zero;
-fused multiply-adds appear only where the source spells __fmaf_rn.
+Each translation unit of both libraries is compiled by nvcc in parallel, then
+each library is linked with the shared CUDA runtime.  Forward-decision code
+relies on IEEE rounding of every operation, so both libraries are compiled
+without fma contraction (-fmad=false), with IEEE division and square root and
+without flush-to-zero; fused multiply-adds appear only where the source spells
+__fmaf_rn.
 
     python -m differentiable_rasterizer_gb300.build [--verbose]
 """
@@ -20,6 +24,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgs_gb300.so")
+CHECKED_LIB = os.path.join(OUT_DIR, "libgs_gb300_checked.so")
+# (library, object directory, extra flags)
+VARIANTS = ((LIB, OUT_DIR, []), (CHECKED_LIB, os.path.join(OUT_DIR, "checked"), ["-DGS_CHECKED"]))
 SOURCES = ["abi.cu", "project.cu", "binsort.cu", "prune.cu", "raster.cu", "dssim.cu", "compose.cu", "compact.cu", "adam.cu"]
 HEADERS = ["gs_common.cuh", "project_math.cuh", "scan.cuh"]
 
@@ -41,34 +48,41 @@ def _stale(target, deps):
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+    """Build both libraries (only what is stale); returns the plain library's path."""
     nvcc = _nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "gs.h")]
-    objs, jobs = [], []
-    for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        objs.append(o)
-        if force or _stale(o, [s] + hdrs):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", s, "-o", o]
-            if verbose:
-                cmd += ["-Xptxas", "-v"]
-            jobs.append(cmd)
+    jobs, links = [], []
+    for lib, obj_dir, extra in VARIANTS:
+        os.makedirs(obj_dir, exist_ok=True)
+        objs, fresh = [], False
+        for src in SOURCES:
+            s = os.path.join(CSRC, src)
+            o = os.path.join(obj_dir, src.replace(".cu", ".o"))
+            objs.append(o)
+            if force or _stale(o, [s] + hdrs):
+                cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", s, "-o", o]
+                if verbose:
+                    cmd += ["-Xptxas", "-v"]
+                jobs.append(cmd)
+                fresh = True
+        links.append((lib, objs, fresh))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
         return cmd, r
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, max(1, len(jobs)))) as ex:
+    workers = min(16, max(1, os.cpu_count() or 1), max(1, len(jobs)))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
         for cmd, r in ex.map(run, jobs):
             if verbose or r.returncode != 0:
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
+    for lib, objs, fresh in links:
+        if force or fresh or _stale(lib, objs):
+            tmp = lib + ".tmp%d" % os.getpid()
+            subprocess.check_call([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs])
+            os.replace(tmp, lib)
     return LIB
 
 

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(256, 5) adam_deferred_kernel(AdamArgs a)
         const int64_t e = i / kChunks;
         const int c = (int)(i - e * kChunks);
         const int64_t g = kFlush ? e : (int64_t)__ldg(a.idx + e);
+        if (!kFlush && !GS_IN_RANGE(g, a.n, GS_CHECK_ADAM_ID)) continue;
         const size_t off = (size_t)g * kStride + 4 * c;
         float4 p = *reinterpret_cast<const float4*>(a.params + off);
         float4 m = *reinterpret_cast<const float4*>(a.m + off);
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) stamp_kernel(AdamArgs a)
     const int64_t count = kFlush ? a.n : *a.n_idx;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t g = kFlush ? i : (int64_t)a.idx[i];
+        if (!kFlush && !GS_IN_RANGE(g, a.n, GS_CHECK_ADAM_ID)) continue;
         if (a.last_step[g] < a.t) a.last_step[g] = a.t;
     }
 }

@@ -107,12 +107,15 @@ __global__ void __launch_bounds__(kBinThreads) bin_kernel(const uint32_t* __rest
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (!tc[u]) continue;
+                if (!(GS_IN_RANGE(r[u].x, r[u].z, GS_CHECK_BIN_RECT) && GS_IN_RANGE(r[u].z - 1, G.tiles_x, GS_CHECK_BIN_RECT) &&
+                      GS_IN_RANGE(r[u].y, r[u].w, GS_CHECK_BIN_RECT) && GS_IN_RANGE(r[u].w - 1, G.tiles_y, GS_CHECK_BIN_RECT)))
+                    continue;
                 const int y0 = max((int)r[u].y, row0), y1 = min((int)r[u].w, row1);
                 for (int ty = y0; ty < y1; ++ty) {
                     uint32_t* row = s_cnt + (ty - row0) * G.tiles_x;
                     for (int tx = r[u].x; tx < r[u].z; ++tx) {
                         const uint32_t pos = atomicAdd(row + tx, 1u);
-                        if (kScatter) tmp[pos] = key[u];
+                        if (kScatter && GS_IN_RANGE(pos, capacity, GS_CHECK_BIN_SLOT)) tmp[pos] = key[u];
                     }
                 }
             }
@@ -145,10 +148,20 @@ __global__ void bucket_stats_kernel(const uint32_t* __restrict__ off, int32_t B,
 }
 
 // -------------------------------------------------------------------- sorts
+#ifdef GS_CHECKED
+// Gaussian count and instance capacity of the running gs_bin_sort call, for the
+// checks at the sorts' output (set by the host before the first launch).
+__device__ long long g_sort_limits[2];
+#endif
+
 // Sorted keys leave as key = (tile_lin << 32) | bits(depth), value = g.
 __device__ __forceinline__ void emit_sorted(uint64_t k, uint64_t hi, uint64_t* __restrict__ keys,
                                             uint32_t* __restrict__ ids, size_t pos)
 {
+#ifdef GS_CHECKED
+    if (!GS_IN_RANGE(pos, g_sort_limits[1], GS_CHECK_SORT_SLOT)) return;
+    (void)GS_IN_RANGE((uint32_t)k, g_sort_limits[0], GS_CHECK_SORT_ID);   // written all the same; the raster drops it
+#endif
     keys[pos] = hi | (k >> 32);
     ids[pos] = (uint32_t)k;
 }
@@ -770,6 +783,13 @@ extern "C" gs_status gs_bin_sort(const gs_proj* proj, int64_t n, int32_t n_views
     if (n > 0 && (!proj->depth || !proj->rect || !proj->tiles_touched)) return GS_ERR_INVALID_ARG;
     if (capacity > 0 && (!keys || !ids)) return GS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
+#ifdef GS_CHECKED
+    {
+        // pageable source: staged before the call returns; calls on two streams at once share it
+        const long long lim[2] = {(long long)n, (long long)capacity};
+        GS_CUDA_TRY(cudaMemcpyToSymbolAsync(g_sort_limits, lim, sizeof lim, 0, cudaMemcpyHostToDevice, s));
+    }
+#endif
     char* w = (char*)ws;
     uint32_t* cnt = (uint32_t*)(w + L.cnt);
     uint32_t* off = (uint32_t*)(w + L.off);

@@ -80,8 +80,10 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
 {
     const int64_t count = *a.n_union;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
-         i += (int64_t)gridDim.x * blockDim.x)
-        vjp_gaussian<DEG>(a, cs, (int64_t)a.idx_union[i]);
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = (int64_t)a.idx_union[i];
+        if (GS_IN_RANGE(g, a.n, GS_CHECK_COMPACT_ID)) vjp_gaussian<DEG>(a, cs, g);
+    }
 }
 
 struct CompactWs {

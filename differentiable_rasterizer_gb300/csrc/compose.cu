@@ -35,7 +35,8 @@ __global__ void split_ranges_kernel(SplitArgs a)
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.n_ranges) return;
     const int v = (int)(i / a.tiles);
-    const uint2 r = a.ranges[i];
+    uint2 r = a.ranges[i];
+    if (!GS_IN_RANGE((int64_t)r.y - (int64_t)r.x, 1ll << 32, GS_CHECK_RANGE)) r.y = r.x;
     uint32_t start = r.x;
     for (int s = 0; s < a.S; ++s) {
         uint32_t end = r.y;

@@ -142,6 +142,56 @@ struct NvtxRange {
 };
 #define GS_NVTX_RANGE(name) ::gs::NvtxRange gs_nvtx_range_(name)
 
+// ---------------------------------------------------------------------------
+// Bounds checks (-DGS_CHECKED).  GS_IN_RANGE(i, n, site) is true when
+// 0 <= i < n.  In the checked build a false result is counted in this
+// translation unit's check record -- failures, then the site, index and bound of
+// the first -- and the caller skips the access; in the plain build the macro is
+// the constant true and its arguments are not evaluated.  Each unit registers a
+// host reader of its record with the library (abi.cu), which gs_check_report
+// calls; the registration only stores a function pointer.
+// ---------------------------------------------------------------------------
+#ifdef GS_CHECKED
+using CheckReader = cudaError_t (*)(unsigned long long out[4]);   // copies the record out, then clears it
+void register_check_reader(CheckReader reader);
+
+namespace {
+__device__ unsigned long long g_check[4];
+
+__device__ __noinline__ void check_record(long long i, long long n, int site)
+{
+    if (atomicAdd(&g_check[0], 1ull) == 0ull) {
+        g_check[1] = (unsigned long long)site;
+        g_check[2] = (unsigned long long)i;
+        g_check[3] = (unsigned long long)n;
+    }
+}
+
+__device__ __forceinline__ bool in_range(long long i, long long n, int site)
+{
+    if (i >= 0 && i < n) return true;
+    check_record(i, n, site);
+    return false;
+}
+
+cudaError_t read_check_record(unsigned long long out[4])
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_check, sizeof(unsigned long long) * 4);
+    if (e != cudaSuccess) return e;
+    const unsigned long long zero[4] = {0ull, 0ull, 0ull, 0ull};
+    return cudaMemcpyToSymbol(g_check, zero, sizeof zero);
+}
+
+struct CheckRegistrar {
+    CheckRegistrar() { register_check_reader(&read_check_record); }
+};
+const CheckRegistrar g_check_registrar;
+}  // namespace
+#define GS_IN_RANGE(i, n, site) (::gs::in_range((long long)(i), (long long)(n), (site)))
+#else
+#define GS_IN_RANGE(i, n, site) true
+#endif
+
 // Status plumbing for host code.
 #define GS_CUDA_TRY(expr)                                      \
     do {                                                       \

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_tiles_kernel(const float4
     const size_t ri = (size_t)blockIdx.y * gridDim.x + blockIdx.x;   // ranges are [view][tile]
     const uint2 range = ranges[ri];
     const int64_t len = (int64_t)range.y - (int64_t)range.x;
+    if (!GS_IN_RANGE(len, 1ll << 32, GS_CHECK_RANGE)) return;
     if (len <= budget) return;
     const int v = blockIdx.y;
     const size_t lo = range.x;
@@ -85,7 +86,9 @@ __global__ void __launch_bounds__(kPruneThreads) prune_tiles_kernel(const float4
 #pragma unroll
         for (int i = 0; i < kPer; ++i) g[i] = i < nv ? ids[lo + k0 + i] : 0u;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) b[i] = i < nv ? __float_as_uint(__ldg(recv + (size_t)g[i] * 3 + 1).y) : 0u;
+        for (int i = 0; i < kPer; ++i)
+            b[i] = (i < nv && GS_IN_RANGE(g[i], n, GS_CHECK_PRUNE_ID)) ? __float_as_uint(__ldg(recv + (size_t)g[i] * 3 + 1).y)
+                                                                     : 0u;
         // largest T with #(o >= T) >= budget, one bit at a time (bit 31, the sign, is 0): T = o*
         uint32_t T = 0;
         for (int bit = 30; bit >= 0; --bit) {
@@ -127,6 +130,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_tiles_kernel(const float4
     // pass, gathering the opacities again each pass.
     auto obits = [&](int64_t k) -> uint32_t {
         const uint32_t gid = ids[lo + k];
+        if (!GS_IN_RANGE(gid, n, GS_CHECK_PRUNE_ID)) return 0u;
         return __float_as_uint(__ldg(recv + (size_t)gid * 3 + 1).y);
     };
     uint32_t prefix = 0, need = (uint32_t)budget;

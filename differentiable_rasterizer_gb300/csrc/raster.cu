@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     const float pxf = (float)px + 0.5f, pyf = (float)py + 0.5f;
     const uint2 range = a.ranges[tile_lin];
     const size_t lo = range.x;                      // list start: instance counts up to 2^32 - 1
-    const int len = (int)(range.y - range.x);
+    const int len = GS_IN_RANGE((int64_t)range.y - (int64_t)range.x, 1ll << 32, GS_CHECK_RANGE)
+                        ? (int)(range.y - range.x) : 0;
     const float4* __restrict__ recv = a.rec + (size_t)v * (size_t)a.n * 3;
     const float alpha_min = a.alpha_min, alpha_max = a.alpha_max;
     unsigned long long work[kCount ? kWCount : 1];
@@ -271,6 +272,12 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         return k < len ? __ldg(a.ids + lo + k) : kNone;
     };
     auto stage_copy = [&](uint32_t g, int b) {
+        if (g != kNone && !GS_IN_RANGE(g, a.n, GS_CHECK_RASTER_ID)) {
+            // dropped: an empty extent gives the entry an empty box, so it never
+            // passes a pixel and no later phase reads its record or index
+            s_r2[b][threadIdx.x] = make_float4(0.0f, 0.0f, -1.0f, -1.0f);
+            g = kNone;
+        }
         if (g != kNone) {
             const float4* r = recv + (size_t)g * 3;
             cp_async16(&s_r0[b][threadIdx.x], r);
@@ -676,8 +683,10 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
                     if (kCount && lane == 0) ++work[kWDenseSteps];
                     const float sum = warp_sum_terms(e, lane);
                     const uint32_t gid = s_id[b][j];
-                    if (red_term >= 0) atomicAdd(g2v + (size_t)gid * GS_GRAD2D_STRIDE + red_term, sum);
-                    if (lane == 1) touchv[gid] = 1;
+                    if (GS_IN_RANGE(gid, a.n, GS_CHECK_RASTER_ID)) {   // a dropped entry never has pass bits
+                        if (red_term >= 0) atomicAdd(g2v + (size_t)gid * GS_GRAD2D_STRIDE + red_term, sum);
+                        if (lane == 1) touchv[gid] = 1;
+                    }
                 }
             }
             continue;
@@ -754,11 +763,13 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
                     const EntryGrad e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb, dotc,
                                                       Sgs + Tst * (Y - da * P), rc);
                     const uint32_t gid = s_id[b][j];
-                    float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
-                    atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
-                    atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
-                    atomicAdd(dst + 8, e.gb);
-                    touchv[gid] = 1;
+                    if (GS_IN_RANGE(gid, a.n, GS_CHECK_RASTER_ID)) {
+                        float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
+                        atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
+                        atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
+                        atomicAdd(dst + 8, e.gb);
+                        touchv[gid] = 1;
+                    }
                 }
                 // carry each pixel's T and S past the part of its segment in this round
                 const int seg_lo = max(myoff, r), seg_hi = min(myend, r + 32);

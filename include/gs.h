@@ -381,6 +381,41 @@ GS_API gs_status gs_adam_deferred(float* params, float* grads, float* m, float* 
                            int32_t sh_degree, const uint32_t* idx, const int64_t* n_idx, int32_t t, const float* lr,
                            float beta1, float beta2, float eps, int32_t flush, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Bounds-checked build.  The same sources compiled with -DGS_CHECKED give
+ * libgs_gb300_checked.so, in which every kernel tests the indexes it reads from
+ * memory before it uses them: the Gaussian index of a sorted, listed or
+ * compacted entry against n, a projected tile rect against the tile grid, a
+ * scatter slot against the instance capacity, a tile range's end against its
+ * start.  A failing index is counted and the access it would make is skipped
+ * (the entry is dropped, the write not made), so a bad index never reaches
+ * memory; no kernel traps.  The plain library compiles the tests away.
+ * Sites, reported as the `site` word below: */
+typedef enum gs_check_site {
+    GS_CHECK_NONE = 0,
+    GS_CHECK_BIN_RECT = 1,    /* gs_bin_sort: a touched Gaussian's rect outside the grid (index: its end)  */
+    GS_CHECK_BIN_SLOT = 2,    /* gs_bin_sort: a scatter slot >= capacity                                     */
+    GS_CHECK_SORT_SLOT = 3,   /* gs_bin_sort: a sorted entry's position >= capacity                          */
+    GS_CHECK_SORT_ID = 4,     /* gs_bin_sort: a sorted entry's Gaussian index >= n                           */
+    GS_CHECK_RANGE = 5,       /* raster / prune / split: a tile range whose end precedes its start           */
+    GS_CHECK_RASTER_ID = 6,   /* raster kernels: a listed Gaussian index >= n (entry dropped)                */
+    GS_CHECK_PRUNE_ID = 7,    /* gs_prune_tiles: a listed Gaussian index >= n (read as opacity 0)            */
+    GS_CHECK_COMPACT_ID = 8,  /* gs_grad_compact: a union-list index >= n (entry skipped)                    */
+    GS_CHECK_ADAM_ID = 9      /* gs_adam_deferred: a listed index >= n (entry skipped)                       */
+} gs_check_site;
+
+/* Report of the bounds checks since the previous report, then reset.
+ * report: HOST [4] u64 out: number of failed checks; the site (gs_check_site),
+ *   index and bound of one of the first to fail (zeros when none failed).
+ *   An index read as a negative number is reported in two's complement.
+ * checked: HOST int32 out: 1 from the bounds-checked build, 0 from the plain
+ *   one (whose report is always zeros and which does no device work here).
+ * The checked build synchronizes the device first (all streams), so the report
+ * covers every kernel launched before the call.
+ * Errors: INVALID_ARG for NULL pointers; DEVICE when a check failed; CUDA when a
+ * copy of the records fails. */
+GS_API gs_status gs_check_report(uint64_t* report, int32_t* checked);
+
 /* Static helpers (no device work). */
 GS_API const char* gs_error_string(gs_status s);
 GS_API int32_t gs_param_rows(int32_t sh_degree);                     /* P: 14, 59, or -1 */

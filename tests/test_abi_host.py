@@ -140,3 +140,41 @@ def test_every_entry_point_opens_an_nvtx_range_named_after_it():
     status_calls = {s for s in declared if s not in ("gs_error_string", "gs_param_rows", "gs_param_stride",
                                                      "gs_num_tiles", "gs_version")}
     assert status_calls <= seen, status_calls - seen
+
+
+def test_checked_library_exports_every_declared_symbol(L):
+    from differentiable_rasterizer_gb300 import build
+    C = ctypes.CDLL(build.CHECKED_LIB)
+    for name in _declared_symbols():
+        assert hasattr(C, name), name
+
+
+def test_check_report_on_the_host(L):
+    """The plain build reports itself unchecked with a zero report and does no
+    device work; both builds reject NULL outputs before touching the device."""
+    from differentiable_rasterizer_gb300 import abi, build
+    rep = (ctypes.c_uint64 * 4)(1, 2, 3, 4)
+    chk = ctypes.c_int32(7)
+    assert L.gs_check_report(rep, ctypes.byref(chk)) == abi.GS_OK
+    assert chk.value == 0 and list(rep) == [0, 0, 0, 0]
+    C = ctypes.CDLL(build.CHECKED_LIB)
+    for lib in (L, C):
+        assert lib.gs_check_report(None, ctypes.byref(chk)) == abi.GS_ERR_INVALID_ARG
+        assert lib.gs_check_report(rep, None) == abi.GS_ERR_INVALID_ARG
+
+
+def test_check_sites_agree_between_header_binding_and_kernels():
+    """The binding's site names follow gs.h's gs_check_site enum in order, and every
+    declared site is tested somewhere in the kernels and only declared sites are."""
+    import glob
+    from differentiable_rasterizer_gb300 import abi
+    text = open(os.path.join(ROOT, "include", "gs.h")).read()
+    body = text[text.index("typedef enum gs_check_site"):]
+    body = body[:body.index("} gs_check_site;")]
+    decl = re.findall(r"GS_CHECK_(\w+)\s*=\s*(\d+)", body)
+    assert [int(v) for _, v in decl] == list(range(len(decl)))
+    assert tuple(name.lower() for name, _ in decl) == abi.CHECK_SITES
+    used = set()
+    for path in glob.glob(os.path.join(ROOT, "differentiable_rasterizer_gb300", "csrc", "*.cu")):
+        used |= set(re.findall(r"GS_IN_RANGE\([^;]*?GS_CHECK_(\w+)\)", open(path).read(), re.S))
+    assert used == {name for name, _ in decl if name != "NONE"}, used
