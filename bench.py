@@ -62,12 +62,13 @@ WORKLOADS = {
 #   pair exponential:    14  (portable exp 12: scale, round, 2-fma reduction,
 #                             7-fma Horner; alpha = min(0.99, o G) 2)
 #   composite walk:      33  (dx, dy, power, exp, alpha, T update, C += c w T)
-#   backward, queued:    74  + 1 SFU reciprocal (power, exp, alpha, 1 / (1 - alpha),
-#                             dL/dC . c, 5-step (product, sum) scan, 9 gradient terms)
-#   backward, per Gaussian: 56 + 1 SFU reciprocal per (entry, pixel), and 12 adds
+#   backward, per pixel: 56  + 1 SFU reciprocal (power, exp, alpha, 1 / (1 - alpha),
+#                             T before the entry, dL/dC . c, 9 gradient terms,
+#                             dL/dC . colour behind)
+#   backward, per Gaussian: the same 56 + 1 SFU per (entry, pixel), and 12 adds
 #                             per lane per warp step (recursive-halving warp sum)
 #   per pixel:           15  (background, L1 difference, signs, S init)
-W_OPS = {"pairs": 14, "pair_exps": 14, "composite_walks": 33, "sparse_entries": 74, "dense_entries": 56,
+W_OPS = {"pairs": 14, "pair_exps": 14, "composite_walks": 33, "sparse_entries": 56, "dense_entries": 56,
          "dense_steps": 12 * 32}
 W_OPS_PIXEL = 15
 # The per-evaluation model the metric's units suggest (kept beside it for

@@ -176,7 +176,7 @@ def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, targ
 
 
 GS_RASTER_WORK_COUNTERS = 10
-RASTER_WORK_NAMES = ("pairs", "pair_exps", "composite_walks", "sparse_entries", "sparse_rounds", "dense_entries",
+RASTER_WORK_NAMES = ("pairs", "pair_exps", "composite_walks", "sparse_entries", "sparse_steps", "dense_entries",
                      "dense_steps", "chunks", "restaged_chunks", "recomputed_chunks")
 
 

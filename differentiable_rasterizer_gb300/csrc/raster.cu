@@ -21,11 +21,10 @@
 // and evaluation counts are those of walking every list entry.  The entries a
 // pixel composited are exactly its passing bits up to its last index, so
 // backward needs no per-pixel list.  Backward walks the chunks last to first;
-// per chunk each warp queues its pixels' composited entries grouped by pixel,
-// newest first, and handles them 32 at a time: T before an entry is a
-// segmented product of 1 / (1 - alpha) from the pixel's current T, the colour
-// behind it a segmented sum, both by warp shuffles; each entry's 9 gradient
-// terms go to the Gaussian's grad2d row with vector atomics.  The pass bits of
+// per chunk each pixel walks its own composited entries newest first, with T
+// before an entry = T after it / (1 - alpha) and dL/dC . (colour behind it)
+// carried in registers; each (entry, pixel) pair's 9 gradient terms go to the
+// Gaussian's grad2d row with vector atomics.  The pass bits of
 // the last kRing chunks stay in shared memory (a ring), so backward re-gathers
 // only their records; older chunks also get their bits recomputed.  A chunk in
 // which the warp's pixels mostly composite the same entries (large Gaussians) is
@@ -50,7 +49,6 @@ namespace gs {
 constexpr int kChunk = 256;      // records per shared-memory stage
 constexpr int kWords = kChunk / 32;
 constexpr int kWarps = kTileThreads / 32;
-constexpr int kQueue = 256;      // queue window (entries) per warp
 constexpr int kRing = 3;         // chunks whose pass bits stay in shared memory
 constexpr int kDense = 12;       // backward: entries per distinct Gaussian from which a warp reduces per Gaussian
 
@@ -198,8 +196,8 @@ enum WorkCounter {
     kWPairs = 0,        // (Gaussian, pixel) pairs swept: power evaluated
     kWPairExp,          // ... of which reached the exponential (tau <= power <= 0)
     kWCompWalk,         // composite: passing entries walked (power, exp, alpha, T)
-    kWSparseEntries,    // backward, queued path: entries processed (valid lanes)
-    kWSparseRounds,     // ... warp rounds of 32 lanes
+    kWSparseEntries,    // backward, per-pixel walk: (entry, pixel) evaluations
+    kWSparseSteps,      // ... warp steps (the most entries any lane of the warp walked, per chunk)
     kWDenseEntries,     // backward, per-Gaussian path: (entry, pixel) evaluations
     kWDenseSteps,       // ... warp steps (one union entry for 32 lanes, one warp sum)
     kWChunks,           // chunks staged in the forward
@@ -217,7 +215,6 @@ struct RasterSmem {
     int max_last[kWarps];
     double red_loss[kWarps];                               // per warp: loss sum ...
     unsigned long long red_counts[3][kWarps];              // ... and evaluation counts
-    uint16_t q[kWarps][kQueue];                            // (owner lane << 8) | entry, grouped by pixel
     uint8_t nz[kWarps][32];                                // pair phase: lane of the r-th entry with a non-empty box
 };
 
@@ -234,7 +231,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     auto& s_bits = sm.bits;
     auto& s_skip = sm.skip;
     auto& s_nz = sm.nz;
-    auto& s_q = sm.q;
     auto& s_max_last = sm.max_last;
 
     // Views interleaved (CTA i: view i mod V, tile i / V) so the heavy central
@@ -262,10 +258,12 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
 #pragma unroll
         for (int k = 0; k < kWCount; ++k) work[k] = 0ull;
 
-    // Staging of a chunk, asynchronous: the instance id is loaded first (early,
-    // into a register), then the three record float4s are copied into buffer b
-    // with cp.async while the block works on the chunk before.  Waiting for them
-    // (cp_async_wait_all) and a block barrier make them visible.
+    // Staging of a chunk, asynchronous: the instance ids are loaded into a
+    // register one chunk before they are used, then the three record float4s
+    // are copied into buffer b with cp.async while the block works on the chunk
+    // before (forward: issued as that chunk starts, so the copy overlaps its
+    // pairs and composite).  Waiting for them (cp_async_wait_all) and a block
+    // barrier make them visible.
     constexpr uint32_t kNone = 0xffffffffu;        // no entry (ids are < 2^31)
     auto stage_id = [&](int base) -> uint32_t {
         const int k = base + (int)threadIdx.x;
@@ -362,29 +360,9 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         }
     };
 
-    // Queue window: this lane's entries (bits in `words`, in list order when
-    // ascending, newest first otherwise) whose position in the warp's queue
-    // (myoff + rank) falls in [wb, wb + kQueue), written grouped by pixel.
-    uint16_t* const q = s_q[warp];
-    auto fill_window = [&](const uint32_t (&words)[kWords], bool ascending, int myoff, int nmine, int wb) {
-        const int k0 = max(wb - myoff, 0), k1 = min(wb + kQueue - myoff, nmine);
-        if (k0 >= k1) return;
-        int k = 0;
-#pragma unroll
-        for (int i = 0; i < kWords; ++i) {
-            const int w = ascending ? i : kWords - 1 - i;
-            uint32_t word = words[w];
-            while (word && k < k1) {
-                const int b = ascending ? (__ffs(word) - 1) : (31 - __clz(word));
-                word &= ~(1u << b);
-                if (k >= k0) q[myoff + k - wb] = (uint16_t)((lane << 8) | (w << 5) | b);
-                ++k;
-            }
-        }
-    };
-    // This lane's entry bits (passing, up to lim), their count, the warp prefix;
-    // returns the warp total.
-    auto gather = [&](uint32_t (&words)[kWords], int lim, int sl, int& myoff, int& nmine) {
+    // This lane's entry bits (passing, up to lim) and their count; returns the
+    // warp total.
+    auto gather = [&](uint32_t (&words)[kWords], int lim, int sl, int& nmine) {
         nmine = 0;
 #pragma unroll
         for (int w = 0; w < kWords; ++w) {
@@ -394,14 +372,7 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             words[w] = word;
             nmine += __popc(word);
         }
-        int incl = nmine;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
-        }
-        myoff = incl - nmine;
-        return __shfl_sync(0xffffffffu, incl, 31);
+        return (int)__reduce_add_sync(0xffffffffu, (unsigned)nmine);
     };
 
 
@@ -418,6 +389,15 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         last = a.last_idx[spix];
     }
     const int nchunks = kMode == kBwdState ? 0 : (len + kChunk - 1) / kChunk;
+    uint32_t g_ahead = nchunks > 1 ? stage_id(kChunk) : kNone;   // ids of the chunk after the next
+    // the target, loaded before the forward so that its latency is hidden
+    float t0v = 0.0f, t1v = 0.0f, t2v = 0.0f;
+    if (kBackward && kMode != kBwdState && inside) {
+        const size_t tp = (size_t)v * 3 * HW + (size_t)py * a.W + px;
+        t0v = __ldg(a.target + tp);
+        t1v = __ldg(a.target + tp + HW);
+        t2v = __ldg(a.target + tp + 2 * HW);
+    }
     if (nchunks > 0) stage_copy(stage_id(0), 0);
     for (int c = 0; c < nchunks; ++c) {
         cp_async_wait_all();
@@ -431,10 +411,10 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         resident = c;
         if (kCount && threadIdx.x == 0) ++work[kWChunks];
         __syncthreads();
-        const uint32_t g_next = c + 1 < nchunks ? stage_id(base + kChunk) : kNone;
+        if (c + 1 < nchunks) stage_copy(g_ahead, b ^ 1);
+        g_ahead = c + 2 < nchunks ? stage_id(base + 2 * kChunk) : kNone;
         const int cnt = min(kChunk, len - base);
         pairs(cnt, sl, b);
-        if (c + 1 < nchunks) stage_copy(g_next, b ^ 1);
         __syncthreads();
         // Composite: each pixel applies its passing entries in list order.
         if (!done) {
@@ -470,7 +450,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     C2 = C2 + T * a.bg2;
     const size_t pix = (size_t)v * 3 * HW + (size_t)py * a.W + px;
     float g0 = 0.0f, g1 = 0.0f, g2c = 0.0f;
-    int gcode = 1 + 4 + 16;   // signs of dL/dC per channel, +1, two bits each
     double lsum = 0.0;
     if (kMode == kBwdState) {
         if (inside) {
@@ -487,15 +466,13 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             a.last_idx[spix] = last;
         }
         if (kBackward) {
-            const float d0 = C0 - __ldg(a.target + pix);
-            const float d1 = C1 - __ldg(a.target + pix + HW);
-            const float d2 = C2 - __ldg(a.target + pix + 2 * HW);
+            const float d0 = C0 - t0v;
+            const float d1 = C1 - t1v;
+            const float d2 = C2 - t2v;
             lsum = (double)fabsf(d0) + (double)fabsf(d1) + (double)fabsf(d2);
             g0 = d0 > 0.0f ? a.inv3hw : (d0 < 0.0f ? -a.inv3hw : 0.0f);
             g1 = d1 > 0.0f ? a.inv3hw : (d1 < 0.0f ? -a.inv3hw : 0.0f);
             g2c = d2 > 0.0f ? a.inv3hw : (d2 < 0.0f ? -a.inv3hw : 0.0f);
-            gcode = (int)(d0 > 0.0f) - (int)(d0 < 0.0f) + 1 + 4 * ((int)(d1 > 0.0f) - (int)(d1 < 0.0f) + 1) +
-                    16 * ((int)(d2 > 0.0f) - (int)(d2 < 0.0f) + 1);
         }
     }
     // Warp sums of the loss and the evaluation counts go to shared memory; the
@@ -587,11 +564,17 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         }
     }
     int fetched = -1;    // chunk whose records were last copied into buffer fetched & 1
+    uint32_t g_pre = kNone;   // ids of chunk pre_chunk, loaded a step before their copy
+    int pre_chunk = -1;
     if (resident >= 1) {
         // the chunk below the resident one, copied in speculatively; its buffer
         // held chunk resident + 1 (never read) or resident - 1 (finished)
         stage_copy(stage_id((resident - 1) * kChunk), (resident - 1) & 1);
         fetched = resident - 1;
+        if (resident >= 2) {
+            g_pre = stage_id((resident - 2) * kChunk);
+            pre_chunk = resident - 2;
+        }
     }
     // dL/dC . (colour composited behind the next entry to visit), per pixel
     float Sg = T * __fmaf_rn(g0, a.bg0, __fmaf_rn(g1, a.bg1, g2c * a.bg2));
@@ -613,8 +596,12 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             // barrier: the chunk above is finished by every warp, this one's records visible
             if (!__syncthreads_or(last >= base)) continue;   // no pixel composited anything here or after
             if (c >= 1) {
-                stage_copy(stage_id(base - kChunk), b ^ 1);
+                stage_copy(pre_chunk == c - 1 ? g_pre : stage_id(base - kChunk), b ^ 1);
                 fetched = c - 1;
+                if (c >= 2) {
+                    g_pre = stage_id(base - 2 * kChunk);
+                    pre_chunk = c - 2;
+                }
             }
             if (kCount && threadIdx.x == 0) ++work[kWRestaged];
             if (kMode == kBwdState ? c != c_kept : c <= last_fwd - kRing) {
@@ -631,15 +618,11 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             __syncthreads();
         }
         // This pixel's composited entries in the chunk are its passing bits up to
-        // last.  The warp queues them grouped by pixel, newest first, and handles
-        // them 32 at a time: T before each entry is a segmented product of
-        // 1/(1 - alpha) from the pixel's current T, the colour behind it a
-        // segmented exclusive sum of c * w from the pixel's current S.
+        // last.
         uint32_t words[kWords];
-        int myoff, nmine;
-        const int nq = gather(words, last - base, sl, myoff, nmine);
+        int nmine;
+        const int nq = gather(words, last - base, sl, nmine);
         if (nq == 0) continue;
-        const int myend = myoff + nmine;
         // Distinct entries composited by any of the warp's pixels in this chunk.
         uint32_t uni[kWords];
         int nu = 0;
@@ -691,98 +674,44 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             }
             continue;
         }
-        for (int wb = 0; wb < nq; wb += kQueue) {
-            fill_window(words, false, myoff, nmine, wb);
-            __syncwarp();
-            const int wend = min(nq, wb + kQueue);
-            for (int r = wb; r < wend; r += 32) {
-                const int qi = r + lane;
-                const bool valid = qi < wend;
-                const uint32_t ent = valid ? (uint32_t)q[qi - wb] : 0u;
-                const int owner = (int)(ent >> 8);
-                const int j = (int)(ent & 0xffu);
-                const int own_off = __shfl_sync(0xffffffffu, myoff, owner);
-                const float Tst = __shfl_sync(0xffffffffu, Tcur, owner);
-                const float Sgs = __shfl_sync(0xffffffffu, Sg, owner);
-                float go0, go1, go2;
-                if (kMode == kBwdState) {
-                    go0 = __shfl_sync(0xffffffffu, g0, owner);
-                    go1 = __shfl_sync(0xffffffffu, g1, owner);
-                    go2 = __shfl_sync(0xffffffffu, g2c, owner);
-                } else {
-                    const int gco = __shfl_sync(0xffffffffu, gcode, owner);
-                    go0 = (float)((gco & 3) - 1) * a.inv3hw;
-                    go1 = (float)(((gco >> 2) & 3) - 1) * a.inv3hw;
-                    go2 = (float)(((gco >> 4) & 3) - 1) * a.inv3hw;
-                }
-                const int pidx = warp * 32 + owner;
-                const float pxo = (float)(ox + (pidx & (kTile - 1))) + 0.5f;
-                const float pyo = (float)(oy + pidx / kTile) + 0.5f;
-                float4 r0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), r1 = r0;
-                float cb = 0.0f, dx = 0.0f, dy = 0.0f, G = 0.0f, araw = 0.0f, alpha = 0.0f;
-                if (valid) {
-                    r0 = s_r0[b][j];
-                    r1 = s_r1[b][j];
-                    cb = s_r2[b][j].x;
-                    dx = pxo - r0.x;
-                    dy = pyo - r0.y;
-                    const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                    G = pexp_neg(power);
-                    araw = r1.y * G;
-                    alpha = fminf(alpha_max, araw);
-                    if (kCount) ++work[kWSparseEntries];
-                }
-                if (kCount && lane == 0) ++work[kWSparseRounds];
-                const float rc = rcp_approx(1.0f - alpha);
-                // segments = pixels: a lane's segment starts at the nearest head at
-                // or below it (lane 0 always is one)
-                const uint32_t heads = __ballot_sync(0xffffffffu, !valid || lane == 0 || qi == own_off);
-                const int seg = 31 - __clz(heads & ((2u << lane) - 1u));
-                // One segmented scan gives both running quantities relative to the
-                // pixel's current T:  P = product of 1 / (1 - alpha) up to this
-                // entry (T before it = T * P) and Y = sum of dL/dC . c * alpha * P
-                // up to it (dL/dC . the colour composited behind an entry = T * the
-                // sum over the entries before it in the queue, after it in the
-                // list).  Pairs combine as (P1, Y1) then (P2, Y2) ->
-                // (P1 P2, Y1 + P1 Y2): five dependent steps instead of ten.
-                const float dotc = __fmaf_rn(go0, r1.z, __fmaf_rn(go1, r1.w, go2 * cb));
-                const float da = valid ? dotc * alpha : 0.0f;
-                float P = rc, Y = da * rc;
+        // Sparse chunk: each lane walks its own pixel's entries newest first,
+        // T and dL/dC . (colour behind) in registers (no exchange between lanes);
+        // each (entry, pixel) pair adds its terms with vector atomics.
+        if (kCount) {
+            const unsigned steps = __reduce_max_sync(0xffffffffu, (unsigned)nmine);
+            if (lane == 0) work[kWSparseSteps] += steps;
+        }
 #pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const float Pu = __shfl_up_sync(0xffffffffu, P, d);
-                    const float Yu = __shfl_up_sync(0xffffffffu, Y, d);
-                    if (lane - d >= seg) {
-                        Y = __fmaf_rn(Pu, Y, Yu);
-                        P = Pu * P;
-                    }
-                }
-                const float Tb = Tst * P;             // transmittance before this entry
-                const float y = Tst * Y;
-                if (valid) {
-                    const EntryGrad e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, go0, go1, go2, Tb, dotc,
-                                                      Sgs + Tst * (Y - da * P), rc);
-                    const uint32_t gid = s_id[b][j];
-                    if (GS_IN_RANGE(gid, a.n, GS_CHECK_RASTER_ID)) {
-                        float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
-                        atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
-                        atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
-                        atomicAdd(dst + 8, e.gb);
-                        touchv[gid] = 1;
-                    }
-                }
-                // carry each pixel's T and S past the part of its segment in this round
-                const int seg_lo = max(myoff, r), seg_hi = min(myend, r + 32);
-                const int k = seg_hi - 1 - r;
-                const int src = k < 0 ? 0 : (k > 31 ? 31 : k);
-                const float Tk = __shfl_sync(0xffffffffu, Tb, src);
-                const float Yk = __shfl_sync(0xffffffffu, y, src);
-                if (seg_lo < seg_hi) {
-                    Tcur = Tk;
-                    Sg += Yk;
+        for (int w = kWords - 1; w >= 0; --w) {
+            uint32_t word = words[w];
+            while (word) {
+                const int bt = 31 - __clz(word);
+                word &= ~(1u << bt);
+                const int j = (w << 5) | bt;
+                const float4 r0 = s_r0[b][j];
+                const float4 r1 = s_r1[b][j];
+                const float cb = s_r2[b][j].x;
+                const float dx = pxf - r0.x, dy = pyf - r0.y;
+                const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+                const float G = pexp_neg(power);
+                const float araw = r1.y * G;
+                const float alpha = fminf(alpha_max, araw);
+                const float rc = rcp_approx(1.0f - alpha);
+                const float Tb = Tcur * rc;
+                const float dotc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2c * cb));
+                const EntryGrad e = entry_grad_at(r0, r1, dx, dy, G, araw, alpha, alpha_max, g0, g1, g2c, Tb, dotc, Sg, rc);
+                Sg += dotc * alpha * Tb;
+                Tcur = Tb;
+                if (kCount) ++work[kWSparseEntries];
+                const uint32_t gid = s_id[b][j];
+                if (GS_IN_RANGE(gid, a.n, GS_CHECK_RASTER_ID)) {
+                    float* dst = g2v + (size_t)gid * GS_GRAD2D_STRIDE;
+                    atomicAdd(reinterpret_cast<float4*>(dst), make_float4(e.gm0, e.gm1, e.gA, e.gB));
+                    atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(e.gC, e.go, e.gr, e.gg));
+                    atomicAdd(dst + 8, e.gb);
+                    touchv[gid] = 1;
                 }
             }
-            __syncwarp();
         }
     }
     cp_async_wait_all();   // no copy outlives the block

@@ -171,7 +171,7 @@ class GaussianTrainer:
         """One fused raster launch in its counting variant (gs_raster_work_counts) on
         the current projection and lists: the same outputs as raster(target), plus
         what the kernel executed (pairs swept, exponentials, composite walks,
-        backward entries and rounds, chunks staged).  grad2d and touched are left
+        backward entries and warp steps, chunks staged).  grad2d and touched are left
         filled as after raster(); compact() consumes them."""
         work = torch.zeros(abi.GS_RASTER_WORK_COUNTERS, dtype=torch.int64, device=self.device)
         abi.gs_raster_work_counts(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,

@@ -491,4 +491,5 @@ def test_work_counting_variant_matches_the_fused_kernel(exclude):
     assert (lens > 256).any()
     assert 0 < w["chunks"] <= int(((lens + 255) // 256).sum())
     assert 0 < w["restaged_chunks"] and w["recomputed_chunks"] <= w["restaged_chunks"]
-    assert w["sparse_rounds"] * 32 >= w["sparse_entries"]
+    # a warp's walk takes as many steps as its busiest lane has entries
+    assert w["sparse_steps"] <= w["sparse_entries"] <= 32 * w["sparse_steps"]
