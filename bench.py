@@ -58,17 +58,17 @@ WORKLOADS = {
 # counting variant (gs_raster_work_counts) in one untimed launch, at the FP32
 # operations each item performs in the source (an fma counts once; compares,
 # integer and shared-memory work not counted):
-#   pair swept:          14  (pixel centre, dx, dy, power, the row/column split)
-#   pair exponential:    14  (portable exp 12: scale, round, 2-fma reduction,
+#   candidate tested:    10  (dx, dy, power)
+#   exponential:         14  (portable exp 12: scale, round, 2-fma reduction,
 #                             7-fma Horner; alpha = min(0.99, o G) 2)
-#   composite walk:      33  (dx, dy, power, exp, alpha, T update, C += c w T)
+#   composite:            9  (T update, weight, C += c w T)
 #   backward, per pixel: 56  + 1 SFU reciprocal (power, exp, alpha, 1 / (1 - alpha),
 #                             T before the entry, dL/dC . c, 9 gradient terms,
 #                             dL/dC . colour behind)
 #   backward, per Gaussian: the same 56 + 1 SFU per (entry, pixel), and 12 adds
 #                             per lane per warp step (recursive-halving warp sum)
 #   per pixel:           15  (background, L1 difference, signs, S init)
-W_OPS = {"pairs": 14, "pair_exps": 14, "composite_walks": 33, "sparse_entries": 56, "dense_entries": 56,
+W_OPS = {"pairs": 10, "pair_exps": 14, "composite_walks": 9, "sparse_entries": 56, "dense_entries": 56,
          "dense_steps": 12 * 32}
 W_OPS_PIXEL = 15
 # The per-evaluation model the metric's units suggest (kept beside it for

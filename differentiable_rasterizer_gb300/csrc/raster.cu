@@ -5,17 +5,15 @@
 //
 // One CTA per 16x16 tile; thread t owns pixel (t % 16, t / 16).  The tile's
 // sorted list is staged through shared memory in chunks of kChunk records
-// (gathered through the instance ids).  Each chunk is handled in two phases:
-//
-//  pairs      Gaussian-parallel: each warp lays the (Gaussian, pixel) pairs of
-//             its 32 staged Gaussians end to end -- the pixels of each
-//             Gaussian's alpha-support box inside the tile (the box comes from
-//             gs_project and provably contains every pixel whose fp32 power can
-//             reach the per-Gaussian cut tau) -- and sweeps them 32 at a time;
-//             every pixel whose alpha passes sets bit j in its 256-bit row.
-//  composite  pixel-parallel: each pixel walks its set bits in list order and
-//             composites them, with T, the colour, the stop index and dL/dC in
-//             registers.
+// (gathered through the instance ids).  Per chunk, thread t turns entry t's
+// alpha-support box (from gs_project; it provably contains every pixel whose
+// fp32 power can reach the entry's cut tau) into row and column spans, and the
+// warps transpose them by ballots into one 256-bit candidate mask per tile row
+// and per tile column.  Each pixel then ANDs its row and column masks and walks
+// its candidates in list order: the pass test (power, tau, exp, alpha) and, for
+// the entries that pass, compositing, with T, the colour, the stop index and
+// dL/dC in registers; the entries that passed set bits in the pixel's own
+// 256-bit row.
 //
 // Entries that do not pass are skipped by definition, so the image, stop index
 // and evaluation counts are those of walking every list entry.  The entries a
@@ -193,9 +191,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Executed-work counters of the counting variant (kCount): what the kernel
 // actually does, as opposed to the E_fwd / E_bwd evaluations the method defines.
 enum WorkCounter {
-    kWPairs = 0,        // (Gaussian, pixel) pairs swept: power evaluated
+    kWPairs = 0,        // (entry, pixel) candidates tested: power evaluated
     kWPairExp,          // ... of which reached the exponential (tau <= power <= 0)
-    kWCompWalk,         // composite: passing entries walked (power, exp, alpha, T)
+    kWCompWalk,         // ... of which passed and were composited (T, colour)
     kWSparseEntries,    // backward, per-pixel walk: (entry, pixel) evaluations
     kWSparseSteps,      // ... warp steps (the most entries any lane of the warp walked, per chunk)
     kWDenseEntries,     // backward, per-Gaussian path: (entry, pixel) evaluations
@@ -211,11 +209,11 @@ struct RasterSmem {
     float4 r0[2][kChunk], r1[2][kChunk], r2[2][kChunk];   // records of two chunks; r2: (blue, tau, hx, hy)
     uint32_t id[2][kChunk];                                // their instance ids
     uint32_t bits[kRing][kWords][kTileThreads];            // per ring slot: bit j of pixel p = entry j passes at p
-    uint32_t skip[kWarps];                                 // pixels that need no more pairs
+    uint32_t rowm[2][kTile][kWords];                       // per mask buffer: entries whose box covers tile row y
+    uint32_t colm[2][kTile][kWords + 1];                   // ... column x (padded: conflict-free reads)
     int max_last[kWarps];
     double red_loss[kWarps];                               // per warp: loss sum ...
     unsigned long long red_counts[3][kWarps];              // ... and evaluation counts
-    uint8_t nz[kWarps][32];                                // pair phase: lane of the r-th entry with a non-empty box
 };
 
 template <int kMode, bool kCount>
@@ -229,8 +227,8 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     auto& s_r2 = sm.r2;
     auto& s_id = sm.id;
     auto& s_bits = sm.bits;
-    auto& s_skip = sm.skip;
-    auto& s_nz = sm.nz;
+    auto& s_rowm = sm.rowm;
+    auto& s_colm = sm.colm;
     auto& s_max_last = sm.max_last;
 
     // Views interleaved (CTA i: view i mod V, tile i / V) so the heavy central
@@ -262,7 +260,7 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     // register one chunk before they are used, then the three record float4s
     // are copied into buffer b with cp.async while the block works on the chunk
     // before (forward: issued as that chunk starts, so the copy overlaps its
-    // pairs and composite).  Waiting for them (cp_async_wait_all) and a block
+    // candidate walk).  Waiting for them (cp_async_wait_all) and a block
     // barrier make them visible.
     constexpr uint32_t kNone = 0xffffffffu;        // no entry (ids are < 2^31)
     auto stage_id = [&](int base) -> uint32_t {
@@ -285,78 +283,66 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         s_id[b][threadIdx.x] = g;
         cp_async_commit();
     };
-    // Clear this pixel's bit row in ring slot sl.
-    auto clear_bits = [&](int sl) {
-#pragma unroll
-        for (int w = 0; w < kWords; ++w) s_bits[sl][w][threadIdx.x] = 0u;
-    };
-    // Pair phase on the chunk in buffer b, setting pass bits in slot sl.  The cnt
-    // staged entries are dealt out evenly, warp w owning [w E, w E + E) with
-    // E = ceil(cnt / 8) <= 32 (a partial chunk keeps every warp equally busy);
-    // the (entry, box pixel) pairs of a warp's entries are laid end to end
-    // (exclusive scan of the box areas) and swept 32 at a time, so a lane never
-    // idles on a small box.  A lane finds the entry owning its pair from the
-    // start positions inside the round and the count of entries started before
-    // it (s_nz maps that rank to the owning lane).  Entry j sets bit j & 31 of
-    // word j >> 5 of each pixel where it passes.
-    auto pairs = [&](int cnt, int sl, int b) {
-        const int per = (cnt + kWarps - 1) / kWarps;
-        const int j0 = warp * per;
-        const int jl = j0 + lane;
+    // Candidate masks of the chunk in buffer b, into mask buffer mb: bit j of
+    // row mask y (column mask x) is set when entry j's alpha-support box (from
+    // gs_project, clipped to the tile; it provably holds every pixel whose fp32
+    // power can reach the entry's cut tau) covers tile row y (column x), so
+    // pixel (x, y)'s candidates are the AND of its two masks -- exactly the
+    // (entry, box pixel) pairs.  Thread t reads entry t's record (copied by
+    // itself); each warp transposes its 32 entries' spans with ballots.
+    auto build_masks = [&](int cnt, int b, int mb) {
         uint32_t box = 0u;
-        if (lane < per && jl < cnt) {
-            const float4 q0 = s_r0[b][jl], q2 = s_r2[b][jl];
+        if ((int)threadIdx.x < cnt) {
+            const float4 q0 = s_r0[b][threadIdx.x], q2 = s_r2[b][threadIdx.x];
             box = tile_box(q0.x, q0.y, q2.z, q2.w, ox, oy);
         }
-        const int bx0 = box & 0xff, bw = (int)((box >> 8) & 0xff) - bx0;
-        const int by0 = (box >> 16) & 0xff, bh = (int)(box >> 24) - by0;
-        const int area = box ? bw * bh : 0;
-        int incl = area;
+        const int x0 = box & 0xff, x1 = (box >> 8) & 0xff;   // an empty box is all zero
+        const int y0 = (box >> 16) & 0xff, y1 = box >> 24;
+        uint32_t mine = 0u;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
+        for (int r = 0; r < kTile; ++r) {
+            const uint32_t br = __ballot_sync(0xffffffffu, r >= y0 && r < y1);
+            const uint32_t bc = __ballot_sync(0xffffffffu, r >= x0 && r < x1);
+            if (lane == r) mine = br;
+            if (lane == kTile + r) mine = bc;
         }
-        const int off = incl - area;
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total == 0) return;
-        const uint32_t nz = __ballot_sync(0xffffffffu, area > 0);
-        if (area > 0) s_nz[warp][__popc(nz & ((1u << lane) - 1u))] = (uint8_t)lane;
-        const float inv_w = area > 0 ? 1.0f / (float)bw : 0.0f;
-        __syncwarp();
-        int started = 0;   // entries whose pairs start before this round
-        for (int rb = 0; rb < total; rb += 32) {
-            const uint32_t mine = (area > 0 && off >= rb && off < rb + 32) ? (1u << (off - rb)) : 0u;
-            const uint32_t starts = __reduce_or_sync(0xffffffffu, mine);
-            const int rank = started + __popc(starts & ((2u << lane) - 1u)) - 1;
-            started += __popc(starts);
-            const int ol = s_nz[warp][rank];
-            const int o_off = __shfl_sync(0xffffffffu, off, ol);
-            const uint32_t o_box = __shfl_sync(0xffffffffu, box, ol);
-            const float o_inv = __shfl_sync(0xffffffffu, inv_w, ol);
-            const int pos = rb + lane;
-            if (pos >= total) continue;
-            const int q = pos - o_off;
-            const int ow = (int)((o_box >> 8) & 0xff) - (int)(o_box & 0xff);
-            const int ly = (int)(((float)q + 0.5f) * o_inv);   // exact: q < 256, box width <= 16
-            const int lx = q - ly * ow;
-            const int ix = (int)(o_box & 0xff) + lx, iy = (int)((o_box >> 16) & 0xff) + ly;
-            const int p = iy * kTile + ix;
-            if ((s_skip[p >> 5] >> (p & 31)) & 1u) continue;
-            const int j = j0 + ol;
-            const float4 r0 = s_r0[b][j];
-            const float4 r1 = s_r1[b][j];
-            const float dx = ((float)(ox + ix) + 0.5f) - r0.x;
-            const float dy = ((float)(oy + iy) + 0.5f) - r0.y;
-            // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
-            const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-            if (kCount) ++work[kWPairs];
-            // power > 0 is skipped by definition; power < tau has alpha < alpha_min
-            if (power > 0.0f || power < s_r2[b][j].y) continue;
-            if (kCount) ++work[kWPairExp];
-            const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
-            if (alpha < alpha_min) continue;
-            atomicOr(&s_bits[sl][j >> 5][p], 1u << (j & 31));
+        if (lane < kTile) s_rowm[mb][lane][warp] = mine;
+        else s_colm[mb][lane - kTile][warp] = mine;
+    };
+    // This pixel's candidates in word w of the chunk (masks in buffer mb).
+    const int tx_l = (int)(threadIdx.x & (kTile - 1)), ty_l = (int)(threadIdx.x / kTile);
+    auto candidates = [&](int mb, int w) -> uint32_t { return s_rowm[mb][ty_l][w] & s_colm[mb][tx_l][w]; };
+    // Pass test of entry j at this pixel: alpha from the same fp32 operations as
+    // the CPU definition; power > 0 is skipped by definition, power < tau has
+    // alpha < alpha_min.  Returns alpha, or -1 if the entry does not pass.
+    auto pass_alpha = [&](int b, int j, float4& r0, float4& r1) -> float {
+        r0 = s_r0[b][j];
+        r1 = s_r1[b][j];
+        const float dx = pxf - r0.x, dy = pyf - r0.y;
+        // power = -1/2 (A dx^2 + C dy^2) - B dx dy, with r0.z = -A/2, r1.x = -C/2
+        const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
+        if (kCount) ++work[kWPairs];
+        if (power > 0.0f || power < s_r2[b][j].y) return -1.0f;
+        if (kCount) ++work[kWPairExp];
+        const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
+        return alpha < alpha_min ? -1.0f : alpha;
+    };
+    // Pass bits of this pixel for the chunk in buffer b (masks in mb), entries
+    // up to lim only, into its row of ring slot sl (zero when lim < 0).
+    auto eval_bits = [&](int b, int mb, int sl, int lim) {
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            const int top = lim - (w << 5);
+            uint32_t cand = top >= 0 ? candidates(mb, w) : 0u;
+            if (top >= 0 && top < 31) cand &= (2u << top) - 1u;
+            uint32_t pass = 0u;
+            while (cand) {
+                const int bt = __ffs(cand) - 1;
+                cand &= cand - 1u;
+                float4 r0, r1;
+                if (pass_alpha(b, (w << 5) | bt, r0, r1) >= 0.0f) pass |= 1u << bt;
+            }
+            s_bits[sl][w][threadIdx.x] = pass;
         }
     };
 
@@ -400,47 +386,43 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     }
     if (nchunks > 0) stage_copy(stage_id(0), 0);
     for (int c = 0; c < nchunks; ++c) {
+        const int base = c * kChunk, b = c & 1, sl = c % kRing;
         cp_async_wait_all();
-        // one barrier: chunk c's records visible, chunk c - 1 no longer read
+        build_masks(min(kChunk, len - base), b, b);
+        // one barrier: chunk c's records and masks visible, chunk c - 1 finished
         if (__syncthreads_and(done)) break;
-        const int base = c * kChunk, b = c & 1;
-        const uint32_t skip = __ballot_sync(0xffffffffu, done);
-        if (lane == 0) s_skip[warp] = skip;
-        const int sl = c % kRing;
-        clear_bits(sl);
         resident = c;
         if (kCount && threadIdx.x == 0) ++work[kWChunks];
-        __syncthreads();
         if (c + 1 < nchunks) stage_copy(g_ahead, b ^ 1);
         g_ahead = c + 2 < nchunks ? stage_id(base + 2 * kChunk) : kNone;
-        const int cnt = min(kChunk, len - base);
-        pairs(cnt, sl, b);
-        __syncthreads();
-        // Composite: each pixel applies its passing entries in list order.
-        if (!done) {
-            for (int w = 0; w < kWords && !done; ++w) {
-                uint32_t word = s_bits[sl][w][threadIdx.x];
-                while (word) {
-                    const int j = (w << 5) | (__ffs(word) - 1);
-                    word &= word - 1u;
-                    const float4 r0 = s_r0[b][j];
-                    const float dx = pxf - r0.x, dy = pyf - r0.y;
-                    const float4 r1 = s_r1[b][j];
-                    const float power = ((r0.z * dx) * dx + (r1.x * dy) * dy) - (r0.w * dx) * dy;
-                    const float alpha = fminf(alpha_max, r1.y * pexp_neg(power));
-                    const float Tn = T * (1.0f - alpha);
-                    if (kCount) ++work[kWCompWalk];
-                    if (a.exclude_crossing && Tn < a.t_min) { done = true; stop = base + j; break; }
-                    const float wgt = alpha * T;
-                    C0 = C0 + r1.z * wgt;
-                    C1 = C1 + r1.w * wgt;
-                    C2 = C2 + s_r2[b][j].x * wgt;
-                    T = Tn;
-                    last = base + j;
-                    ++ncomp;
-                    if (!a.exclude_crossing && T < a.t_min) { done = true; stop = base + j; break; }
-                }
+        // Each pixel tests its candidates in list order and composites the ones
+        // that pass, with T, the colour, the stop index and dL/dC in registers;
+        // its pass bits go to its own row of ring slot sl for the backward.
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            uint32_t cand = done ? 0u : candidates(b, w);
+            uint32_t pass = 0u;
+            while (cand) {
+                const int bt = __ffs(cand) - 1;
+                cand &= cand - 1u;
+                const int j = (w << 5) | bt;
+                float4 r0, r1;
+                const float alpha = pass_alpha(b, j, r0, r1);
+                if (alpha < 0.0f) continue;
+                pass |= 1u << bt;
+                const float Tn = T * (1.0f - alpha);
+                if (kCount) ++work[kWCompWalk];
+                if (a.exclude_crossing && Tn < a.t_min) { done = true; stop = base + j; break; }
+                const float wgt = alpha * T;
+                C0 = C0 + r1.z * wgt;
+                C1 = C1 + r1.w * wgt;
+                C2 = C2 + s_r2[b][j].x * wgt;
+                T = Tn;
+                last = base + j;
+                ++ncomp;
+                if (!a.exclude_crossing && T < a.t_min) { done = true; stop = base + j; break; }
             }
+            s_bits[sl][w][threadIdx.x] = pass;
         }
     }
     cp_async_wait_all();   // a break above can leave the next chunk's copies in flight
@@ -605,17 +587,15 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             }
             if (kCount && threadIdx.x == 0) ++work[kWRestaged];
             if (kMode == kBwdState ? c != c_kept : c <= last_fwd - kRing) {
-                // pass bits no longer in the ring: recompute them for the pixels
-                // that composited an entry of this chunk
-                const uint32_t skip = __ballot_sync(0xffffffffu, last < base);
-                if (lane == 0) s_skip[warp] = skip;
-                clear_bits(sl);
+                // pass bits no longer in the ring: recompute them, each pixel up
+                // to its last composited entry (mask buffer 0: the forward is over)
+                build_masks(min(kChunk, len - base), b, 0);
                 __syncthreads();
-                pairs(min(kChunk, len - base), sl, b);
+                eval_bits(b, 0, sl, last - base);
                 if (kCount && threadIdx.x == 0) ++work[kWRecomputed];
             }
+            // (no barrier: a pixel reads back only its own row of pass bits)
             resident = c;
-            __syncthreads();
         }
         // This pixel's composited entries in the chunk are its passing bits up to
         // last.

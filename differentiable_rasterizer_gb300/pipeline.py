@@ -170,7 +170,7 @@ class GaussianTrainer:
     def work_counts(self, target) -> dict:
         """One fused raster launch in its counting variant (gs_raster_work_counts) on
         the current projection and lists: the same outputs as raster(target), plus
-        what the kernel executed (pairs swept, exponentials, composite walks,
+        what the kernel executed (candidates tested, exponentials, composites,
         backward entries and warp steps, chunks staged).  grad2d and touched are left
         filled as after raster(); compact() consumes them."""
         work = torch.zeros(abi.GS_RASTER_WORK_COUNTERS, dtype=torch.int64, device=self.device)

@@ -219,8 +219,8 @@ GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const u
  * same step as gs_raster_fused_fwd_bwd (target required; same outputs, eval
  * counts not taken) in a variant that also counts, into work[] (DEVICE u64,
  * accumulated +=), in this order:
- *   0 pairs swept (power evaluated)      1 of which reached the exponential
- *   2 composite entries walked            3 backward per-pixel walk entries
+ *   0 candidates tested (power)          1 of which reached the exponential
+ *   2 of which were composited            3 backward per-pixel walk entries
  *   4 ... walk steps (per warp)           5 backward per-Gaussian evaluations
  *   6 backward per-Gaussian steps (warp)  7 chunks staged in the forward
  *   8 chunks staged again in the backward 9 of which had pass bits recomputed
