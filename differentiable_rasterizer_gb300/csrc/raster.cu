@@ -3,7 +3,9 @@
 // rasterization passes are one kernel whose intermediate results stay on chip
 // instead of going through off-chip memory).
 //
-// One CTA per 16x16 tile; thread t owns pixel (t % 16, t / 16).  The tile's
+// One CTA per 16x16 tile, one pixel per thread; warp w owns the 8x4 pixel block
+// (w % 2, w / 2) of the tile (compact blocks: their pixels' walks are of more
+// similar length than those of two tile rows).  The tile's
 // sorted list is staged through shared memory in chunks of kChunk records
 // (gathered through the instance ids).  Per chunk, thread t turns entry t's
 // alpha-support box (from gs_project; it provably contains every pixel whose
@@ -241,8 +243,8 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int red_term = reduce_term(lane);   // dense backward: the gradient term this lane adds
     const int ox = tx * kTile, oy = ty * kTile;
-    const int px = ox + (threadIdx.x & (kTile - 1));
-    const int py = oy + (threadIdx.x / kTile);
+    const int px = ox + ((warp & 1) << 3) + (lane & 7);   // warp w: the 8 x 4 block (w % 2, w / 2)
+    const int py = oy + ((warp >> 1) << 2) + (lane >> 3);
     const bool inside = px < a.W && py < a.H;
     const float pxf = (float)px + 0.5f, pyf = (float)py + 0.5f;
     const uint2 range = a.ranges[tile_lin];
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         else s_colm[mb][lane - kTile][warp] = mine;
     };
     // This pixel's candidates in word w of the chunk (masks in buffer mb).
-    const int tx_l = (int)(threadIdx.x & (kTile - 1)), ty_l = (int)(threadIdx.x / kTile);
+    const int tx_l = px - ox, ty_l = py - oy;
     auto candidates = [&](int mb, int w) -> uint32_t { return s_rowm[mb][ty_l][w] & s_colm[mb][tx_l][w]; };
     // Pass test of entry j at this pixel: alpha from the same fp32 operations as
     // the CPU definition; power > 0 is skipped by definition, power < tau has
