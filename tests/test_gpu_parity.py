@@ -57,6 +57,58 @@ def test_dense_lists_span_several_chunks_and_stop_early():
     assert st["e_fwd"] < st["instances"] * 256   # early stops happened
 
 
+def _border_scene(seed, sh_degree):
+    """Gaussians placed where the per-tile candidate masks have their edge cases:
+    tiny ones centred on tile-border pixel centres and tile corners (boxes that
+    start or end exactly at a tile edge, or cover a single pixel), ones whose
+    support spans a whole tile or the whole view (boxes 0..16 in both axes), thin
+    rotated ones crossing borders diagonally, and opacities from just above the
+    1/255 cut to the 0.99 clamp."""
+    rng = np.random.default_rng(seed)
+    W = H = 64
+    fx, z = 64.0, 2.0
+    groups = []
+    # tiny: centre u = 16 k + {-0.5, 0, 0.5} on one axis or both (tile corners)
+    for _ in range(300):
+        k = rng.integers(1, 4, size=2)
+        off = rng.choice([-0.5, 0.0, 0.5], size=2)
+        u = np.where(rng.random(2) < 0.7, 16.0 * k + off, rng.uniform(0.5, 63.5, 2))
+        groups.append((u, rng.uniform(-7.5, -5.5, 3), rng.normal(size=4)))
+    # spanning a tile or the view
+    for _ in range(40):
+        groups.append((rng.uniform(0, 64, 2), rng.uniform(-1.8, -0.8, 3), rng.normal(size=4)))
+    # thin and rotated
+    for _ in range(160):
+        ls = np.array([rng.uniform(-2.6, -2.0), rng.uniform(-6.5, -5.5), rng.uniform(-6.5, -5.5)])
+        groups.append((16.0 * rng.integers(1, 4, size=2) + rng.uniform(-3, 3, 2), ls, rng.normal(size=4)))
+    n = len(groups)
+    P = 14 if sh_degree == 0 else 59
+    params = np.zeros((P, n), np.float32)
+    for i, (u, ls, q) in enumerate(groups):
+        zi = z + rng.uniform(0.0, 1.5)
+        params[0, i] = (u[0] - 32.0) * zi / fx
+        params[1, i] = (u[1] - 32.0) * zi / fx
+        params[2, i] = zi
+        params[3:6, i] = ls
+        params[6:10, i] = q / np.linalg.norm(q)
+    params[10] = rng.choice([-5.4, -2.0, 0.0, 2.0, 6.0], size=n) + rng.normal(0, 0.05, n)
+    if sh_degree == 0:
+        params[11:14] = rng.uniform(0, 1, (3, n))
+    else:
+        params[11:14] = rng.uniform(-1.7, 1.7, (3, n))
+        params[14:59] = rng.normal(0, 0.2, (45, n))
+    cam = scenes.Camera(np.eye(3, dtype=np.float32), np.zeros(3, np.float32), fx, fx, 32.0, 32.0, W, H)
+    target = rng.uniform(0, 1, (1, 3, H, W)).astype(np.float32)
+    return scenes.Scene("tile-borders", params, sh_degree, [cam], "uniform", target, None, scenes.DEFAULT_LR,
+                        dict(scenes.DEFAULT_OPTS))
+
+
+@pytest.mark.parametrize("sh", [0, 3])
+def test_gaussians_on_tile_borders_corners_and_spanning_tiles(sh):
+    st = parity.run_stage_parity(_border_scene(40 + sh, sh))
+    assert st["instances"] > 500
+
+
 def test_sort_bucket_sizes_over_2048_use_the_large_block_sort():
     """~6000 wide Gaussians on a 32x32 view: 4 tile buckets of ~6000 instances."""
     sc = scenes.random_small_scene(31, n=6000, width=32, height=32, sh_degree=0, log_lo=-1.5, log_hi=-1.0,
