@@ -1,7 +1,8 @@
 // scan.cuh -- device-wide exclusive scan and stream compaction (three launches:
 // per-block sums, one-block scan of the sums, per-block rescan with the block
 // prefix).  Blocks of 256 threads own 16 consecutive items per thread, so each
-// block covers kScanItems consecutive items and no inter-block waiting is needed.
+// block covers kScanItems consecutive items and no inter-block waiting is needed;
+// a thread reads its items with 16-byte loads where the input is aligned.
 #pragma once
 
 #include "gs_common.cuh"
@@ -26,6 +27,39 @@ __device__ __forceinline__ unsigned long long item_value(const T* in, int64_t i,
     if (i >= n) return 0ull;
     const T x = in[i];
     return kFlag ? (x != 0 ? 1ull : 0ull) : (unsigned long long)x;
+}
+
+// The kScanPerThread items of one thread, from base: 16-byte vector loads when
+// the input is 16-byte aligned and all the items are in range (one load for
+// bytes, four for 32-bit words), else one item at a time.
+template <typename T, bool kFlag>
+__device__ __forceinline__ void load_items(const T* in, int64_t base, int64_t n, bool vec, uint32_t (&v)[kScanPerThread])
+{
+    static_assert(sizeof(T) == 1 || sizeof(T) == 4, "bytes or 32-bit words");
+    if (vec && base + kScanPerThread <= n) {
+        constexpr int kQ = kScanPerThread * (int)sizeof(T) / 16;   // uint4 loads
+        const uint4* q = reinterpret_cast<const uint4*>(in + base);
+#pragma unroll
+        for (int l = 0; l < kQ; ++l) {
+            const uint4 u = q[l];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (sizeof(T) == 1) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const uint32_t x = (w[e] >> (8 * b)) & 0xffu;
+                        v[16 * l + 4 * e + b] = kFlag ? (x != 0u ? 1u : 0u) : x;
+                    }
+                } else {
+                    v[4 * l + e] = kFlag ? (w[e] != 0u ? 1u : 0u) : w[e];
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kScanPerThread; ++k) v[k] = (uint32_t)item_value<T, kFlag>(in, base + k, n);
+    }
 }
 
 // Block-wide exclusive scan of one u64 per thread; returns the exclusive prefix,
@@ -55,12 +89,15 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long
 }
 
 template <typename T, bool kFlag>
-__global__ void __launch_bounds__(kScanThreads) scan_block_sums(const T* in, int64_t n, unsigned long long* sums)
+__global__ void __launch_bounds__(kScanThreads) scan_block_sums(const T* in, int64_t n, unsigned long long* sums,
+                                                                bool vec)
 {
     const int64_t base = (int64_t)blockIdx.x * kScanItems + (int64_t)threadIdx.x * kScanPerThread;
+    uint32_t v[kScanPerThread];
+    load_items<T, kFlag>(in, base, n, vec, v);
     unsigned long long s = 0;
 #pragma unroll
-    for (int k = 0; k < kScanPerThread; ++k) s += item_value<T, kFlag>(in, base + k, n);
+    for (int k = 0; k < kScanPerThread; ++k) s += v[k];
     unsigned long long tot;
     block_exclusive_scan(s, &tot);
     if (threadIdx.x == 0) sums[blockIdx.x] = tot;
@@ -85,16 +122,15 @@ __global__ void __launch_bounds__(kScanThreads) scan_sums_kernel(unsigned long l
 // Value mode: out[i] = exclusive prefix (u32).  Flag mode: out[prefix] = i for nonzero in[i].
 template <typename T, bool kFlag>
 __global__ void __launch_bounds__(kScanThreads) scan_block_apply(const T* in, int64_t n,
-                                                                 const unsigned long long* sums, uint32_t* out)
+                                                                 const unsigned long long* sums, uint32_t* out,
+                                                                 bool vec)
 {
     const int64_t base = (int64_t)blockIdx.x * kScanItems + (int64_t)threadIdx.x * kScanPerThread;
-    unsigned long long vals[kScanPerThread];
+    uint32_t vals[kScanPerThread];
+    load_items<T, kFlag>(in, base, n, vec, vals);
     unsigned long long s = 0;
 #pragma unroll
-    for (int k = 0; k < kScanPerThread; ++k) {
-        vals[k] = item_value<T, kFlag>(in, base + k, n);
-        s += vals[k];
-    }
+    for (int k = 0; k < kScanPerThread; ++k) s += vals[k];
     unsigned long long tot;
     unsigned long long run = sums[blockIdx.x] + block_exclusive_scan(s, &tot);
 #pragma unroll
@@ -124,9 +160,10 @@ inline cudaError_t scan_launch(const T* in, int64_t n, uint32_t* out, unsigned l
 {
     const int64_t nb = scan_blocks(n);
     if (nb == 0) return cudaMemsetAsync(d_total, 0, sizeof(unsigned long long), s);
-    scan_block_sums<T, kFlag><<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, ws);
+    const bool vec = ((uintptr_t)in & 15u) == 0;   // 16-byte loads need an aligned start
+    scan_block_sums<T, kFlag><<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, ws, vec);
     scan_sums_kernel<<<1, kScanThreads, 0, s>>>(ws, nb, d_total);
-    scan_block_apply<T, kFlag><<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, ws, out);
+    scan_block_apply<T, kFlag><<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, ws, out, vec);
     return cudaPeekAtLastError();
 }
 
