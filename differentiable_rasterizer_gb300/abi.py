@@ -79,7 +79,7 @@ def lib():
         L.gs_bin_sort.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I64, _P, _P, _P,
                                   ctypes.POINTER(ctypes.c_int64), _P, ctypes.POINTER(ctypes.c_size_t), _P]
         L.gs_raster_fused_fwd_bwd.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P,
-                                              _P, _P]
+                                              _P, _P, _I64, _P]
         L.gs_grad_compact.argtypes = [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P,
                                       ctypes.POINTER(ctypes.c_size_t), _P]
         L.gs_adam_deferred.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _P, _P, _I32, _P, _F, _F, _F, _I32, _P]
@@ -92,7 +92,7 @@ def lib():
         L.gs_split_ranges.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.gs_compose.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
         L.gs_raster_work_counts.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P,
-                                            _P, _P]
+                                            _P, _P, _I64, _P]
         for name in ("gs_project", "gs_bin_sort", "gs_raster_fused_fwd_bwd", "gs_grad_compact", "gs_adam_deferred",
                      "gs_raster_forward_state", "gs_dssim_loss_grad", "gs_raster_backward_state", "gs_prune_tiles",
                      "gs_split_ranges", "gs_compose", "gs_raster_work_counts"):
@@ -168,11 +168,18 @@ def gs_bin_sort(proj, n, n_views, width, height, capacity, keys, ids, tile_range
     return st, cnt.value
 
 
+def raster_bits_ws_words(n_instances) -> int:
+    """GS_RASTER_BITS_WS_WORDS: scratch words that cover lists of n_instances entries."""
+    return (int(n_instances) + 256) * 8
+
+
 def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, target, image, loss, grad2d, touched,
-                            eval_counts, stream):
+                            eval_counts, stream, bits_ws=None, bits_ws_words=0):
+    """bits_ws: None or a device pointer to bits_ws_words u32 of saved-pass-bits scratch."""
     _check("gs_raster_fused_fwd_bwd",
            lib().gs_raster_fused_fwd_bwd(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
-                                         target, image, loss, grad2d, touched, eval_counts, stream))
+                                         target, image, loss, grad2d, touched, eval_counts, bits_ws,
+                                         int(bits_ws_words), stream))
 
 
 GS_RASTER_WORK_COUNTERS = 10
@@ -181,10 +188,11 @@ RASTER_WORK_NAMES = ("pairs", "pair_exps", "composite_walks", "sparse_entries", 
 
 
 def gs_raster_work_counts(proj, n, tile_ranges, ids, cams, n_views, opts, target, image, loss, grad2d, touched, work,
-                          stream):
+                          stream, bits_ws=None, bits_ws_words=0):
     _check("gs_raster_work_counts",
            lib().gs_raster_work_counts(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
-                                       target, image, loss, grad2d, touched, work, stream))
+                                       target, image, loss, grad2d, touched, work, bits_ws, int(bits_ws_words),
+                                       stream))
 
 
 CHECK_SITES = ("none", "bin_rect", "bin_slot", "sort_slot", "sort_id", "range", "raster_id", "prune_id",

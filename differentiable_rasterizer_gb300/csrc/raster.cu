@@ -66,6 +66,8 @@ struct RasterArgs {
     float* t_final;                     // [V][H][W]: final transmittance per pixel, or null
     int32_t* last_idx;                  // [V][H][W]: last composited list index per pixel (-1: none)
     uint32_t* bits;                     // [V * tiles][kWords][256]: pass bits of one chunk per tile, or null
+    uint32_t* bits_ws;                  // fused: pass bits of the chunks the ring evicts, by list position, or null
+    int64_t bits_ws_words;              // its size in 32-bit words
     int32_t* bits_chunk;                // [V * tiles]: the chunk those bits belong to (-1: none)
     float* image;                       // [V][3][H][W]
     double* loss;                       // [V]
@@ -285,6 +287,17 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         s_id[b][threadIdx.x] = g;
         cp_async_commit();
     };
+    // Chunk c's slot in the saved-bits scratch: the kWords x 256 words from word
+    // (lo + c kChunk) kWords on (8 KB a chunk, 32 bytes per list entry); a
+    // chunk past the scratch's end has none and is recomputed instead.
+    auto saved = [&](int c) -> bool {
+        return a.bits_ws != nullptr &&
+               (int64_t)((lo + (size_t)(c + 1) * kChunk) * kWords) <= a.bits_ws_words;
+    };
+    auto saved_row = [&](int c) -> uint32_t* {
+        return a.bits_ws + (lo + (size_t)c * kChunk) * kWords + threadIdx.x;
+    };
+
     // Candidate masks of the chunk in buffer b, into mask buffer mb: bit j of
     // row mask y (column mask x) is set when entry j's alpha-support box (from
     // gs_project, clipped to the tile; it provably holds every pixel whose fp32
@@ -397,6 +410,13 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         if (kCount && threadIdx.x == 0) ++work[kWChunks];
         if (c + 1 < nchunks) stage_copy(g_ahead, b ^ 1);
         g_ahead = c + 2 < nchunks ? stage_id(base + 2 * kChunk) : kNone;
+        if (kMode == kFused && c >= kRing && saved(c - kRing)) {
+            // slot sl still holds chunk c - kRing, which the ring now evicts: its
+            // rows go to the scratch, where the backward reads them back
+            uint32_t* dst = saved_row(c - kRing);
+#pragma unroll
+            for (int w = 0; w < kWords; ++w) dst[w * kTileThreads] = s_bits[sl][w][threadIdx.x];
+        }
         // Each pixel tests its candidates in list order and composites the ones
         // that pass, with T, the colour, the stop index and dL/dC in registers;
         // its pass bits go to its own row of ring slot sl for the backward.
@@ -589,12 +609,19 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             }
             if (kCount && threadIdx.x == 0) ++work[kWRestaged];
             if (kMode == kBwdState ? c != c_kept : c <= last_fwd - kRing) {
-                // pass bits no longer in the ring: recompute them, each pixel up
-                // to its last composited entry (mask buffer 0: the forward is over)
-                build_masks(min(kChunk, len - base), b, 0);
-                __syncthreads();
-                eval_bits(b, 0, sl, last - base);
-                if (kCount && threadIdx.x == 0) ++work[kWRecomputed];
+                if (kMode == kFused && saved(c)) {
+                    // pass bits evicted from the ring and saved by the forward
+                    const uint32_t* src = saved_row(c);
+#pragma unroll
+                    for (int w = 0; w < kWords; ++w) s_bits[sl][w][threadIdx.x] = src[w * kTileThreads];
+                } else {
+                    // pass bits no longer in the ring: recompute them, each pixel up
+                    // to its last composited entry (mask buffer 0: the forward is over)
+                    build_masks(min(kChunk, len - base), b, 0);
+                    __syncthreads();
+                    eval_bits(b, 0, sl, last - base);
+                    if (kCount && threadIdx.x == 0) ++work[kWRecomputed];
+                }
             }
             // (no barrier: a pixel reads back only its own row of pass bits)
             resident = c;
@@ -769,7 +796,7 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
                                              const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                              const gs_render_opts* opts, const float* target, float* image,
                                              double* loss, float* grad2d, uint8_t* touched, uint64_t* eval_counts,
-                                             void* stream)
+                                             uint32_t* bits_ws, int64_t bits_ws_words, void* stream)
 {
     GS_NVTX_RANGE("gs_raster_fused_fwd_bwd");
     RasterArgs a;
@@ -779,12 +806,15 @@ extern "C" gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, con
     if (!image) return GS_ERR_INVALID_ARG;
     if (target && (!loss || (n > 0 && (!grad2d || !touched)))) return GS_ERR_INVALID_ARG;
     if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    if (bits_ws_words < 0 || (bits_ws && bits_ws_words == 0)) return GS_ERR_INVALID_ARG;
     a.target = target;
     a.image = image;
     a.loss = loss;
     a.grad2d = grad2d;
     a.touched = touched;
     a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
+    a.bits_ws = bits_ws;
+    a.bits_ws_words = bits_ws ? bits_ws_words : 0;
     cudaStream_t s = (cudaStream_t)stream;
     if (target) {
         GS_CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(double) * (size_t)n_views, s));
@@ -797,7 +827,7 @@ extern "C" gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const
                                            const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                            const gs_render_opts* opts, const float* target, float* image,
                                            double* loss, float* grad2d, uint8_t* touched, uint64_t* work,
-                                           void* stream)
+                                           uint32_t* bits_ws, int64_t bits_ws_words, void* stream)
 {
     GS_NVTX_RANGE("gs_raster_work_counts");
     RasterArgs a;
@@ -806,7 +836,10 @@ extern "C" gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const
     if (st != GS_OK) return st;
     if (!image || !target || !loss || !work || (n > 0 && (!grad2d || !touched))) return GS_ERR_INVALID_ARG;
     if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
+    if (bits_ws_words < 0 || (bits_ws && bits_ws_words == 0)) return GS_ERR_INVALID_ARG;
     static_assert(kWCount == GS_RASTER_WORK_COUNTERS, "counter layout");
+    a.bits_ws = bits_ws;
+    a.bits_ws_words = bits_ws ? bits_ws_words : 0;
     a.target = target;
     a.image = image;
     a.loss = loss;

@@ -112,6 +112,8 @@ class GaussianTrainer:
         self.capacity = capacity
         self.keys = torch.empty(capacity, dtype=torch.int64, device=self.device)
         self.ids = torch.empty(capacity, dtype=torch.int32, device=self.device)
+        # the fused raster's saved-pass-bits scratch (32 B per instance)
+        self.bits_ws = torch.empty(abi.raster_bits_ws_words(capacity), dtype=torch.int32, device=self.device)
         nbytes = abi.gs_bin_sort_ws_bytes(self.n, self.V, self.W, self.H, capacity)
         self.sort_ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
@@ -165,7 +167,7 @@ class GaussianTrainer:
                                     self.opts, target.data_ptr() if target is not None else None,
                                     self.image.data_ptr(), self.loss.data_ptr(), self.grad2d.data_ptr(),
                                     self.touched.data_ptr(), self.eval_counts.data_ptr() if count_evals else None,
-                                    self.stream_handle())
+                                    self.stream_handle(), self.bits_ws.data_ptr(), self.bits_ws.numel())
 
     def work_counts(self, target) -> dict:
         """One fused raster launch in its counting variant (gs_raster_work_counts) on
@@ -177,7 +179,7 @@ class GaussianTrainer:
         abi.gs_raster_work_counts(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,
                                   self.opts, target.data_ptr(), self.image.data_ptr(), self.loss.data_ptr(),
                                   self.grad2d.data_ptr(), self.touched.data_ptr(), work.data_ptr(),
-                                  self.stream_handle())
+                                  self.stream_handle(), self.bits_ws.data_ptr(), self.bits_ws.numel())
         return dict(zip(abi.RASTER_WORK_NAMES, (int(x) for x in work.cpu().tolist())))
 
     def raster_dssim(self, target, count_evals=True, events=None):

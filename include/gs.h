@@ -188,14 +188,17 @@ GS_API gs_status gs_prune_tiles(const gs_proj* proj, int64_t n, int32_t n_views,
  * power > 0 or alpha < alpha_min, C += c * alpha * T, T *= 1 - alpha, stop at
  * T < t_min; C += T * bg.  The list's records pass through shared memory in
  * chunks of 256, the next chunk copied in (cp.async) while the block works on
- * the current one.  The per-pixel T, colour and last index stay in
- * registers.  With a target: L1 loss per view, mean over 3*H*W values, summed in
- * fp64, and its gradient sign(C - target) / (3HW) on chip; backward walks each
- * pixel's composited entries back to front (transmittance recovered by
- * division): a warp queues its pixels' entries grouped by pixel and takes them
- * 32 at a time, with T and dL/dC . (colour behind) from segmented warp scans,
- * and adds each entry's 9 gradient terms to the Gaussian's grad2d row with
- * vector atomics (their order varies from run to run).
+ * the current one; each pixel walks the entries whose support box covers it
+ * (per-chunk row and column candidate masks) in list order.  The per-pixel T,
+ * colour and last index stay in registers, and the entries that pass set bits
+ * in the pixel's row of an on-chip ring that keeps the last three chunks.  With
+ * a target: L1 loss per view, mean over 3*H*W values, summed in fp64, and its
+ * gradient sign(C - target) / (3HW) on chip; backward walks each pixel's
+ * composited entries back to front, T recovered by division and
+ * dL/dC . (colour behind) carried in registers, and adds each entry's 9
+ * gradient terms to the Gaussian's grad2d row with vector atomics (their order
+ * varies from run to run); where most of a warp's pixels share the entries it
+ * sums the terms over the warp first.
  * target: [V][3][H][W] or NULL (forward only: no loss, gradients or touched).
  * image: [V][3][H][W] out.  loss: [V] fp64 out (overwritten).
  * grad2d: [V][n][GS_GRAD2D_STRIDE] accumulated (+=): d/d mean2d (x, y),
@@ -206,18 +209,27 @@ GS_API gs_status gs_prune_tiles(const gs_proj* proj, int64_t n, int32_t n_views,
  * eval_counts: NULL or [3] u64 accumulated (+=): E_fwd = list entries evaluated
  *   up to the stop (skipped ones included), E_bwd = sum of (last index + 1),
  *   E_comp = entries composited (alpha >= alpha_min and not stopped).
+ * bits_ws, bits_ws_words: NULL and 0, or a DEVICE u32 scratch and its size in
+ *   words.  The pass bits of the chunks the on-chip ring evicts are saved there
+ *   in the forward (8 words per list entry, at the entry's list position) and
+ *   read back by the backward instead of being recomputed; a chunk whose slot
+ *   lies past the scratch's end is recomputed.  GS_RASTER_BITS_WS_WORDS(I)
+ *   words cover lists of I instances.  Contents on entry are ignored and left
+ *   undefined; results do not depend on the scratch.
  * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
+#define GS_RASTER_BITS_WS_WORDS(n_instances) (((int64_t)(n_instances) + 256) * 8)
 GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges, const uint32_t* ids,
                                   const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
                                   const float* target, float* image, double* loss, float* grad2d, uint8_t* touched,
-                                  uint64_t* eval_counts, void* stream);
+                                  uint64_t* eval_counts, uint32_t* bits_ws, int64_t bits_ws_words, void* stream);
 
 /* Executed-work counters of the fused kernel -- a measurement aid with no
  * counterpart on the pages: the kernel skips, with results unchanged, the
  * (entry, pixel) pairs its per-Gaussian support box and alpha cut prove
  * cannot pass, so the work it executes is far below E_fwd + E_bwd.  Runs the
  * same step as gs_raster_fused_fwd_bwd (target required; same outputs, eval
- * counts not taken) in a variant that also counts, into work[] (DEVICE u64,
+ * counts not taken; bits_ws as there) in a variant that also counts, into
+ * work[] (DEVICE u64,
  * accumulated +=), in this order:
  *   0 candidates tested (power)          1 of which reached the exponential
  *   2 of which were composited            3 backward per-pixel walk entries
@@ -230,7 +242,8 @@ GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const u
 GS_API gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                        const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                        const gs_render_opts* opts, const float* target, float* image, double* loss,
-                                       float* grad2d, uint8_t* touched, uint64_t* work, void* stream);
+                                       float* grad2d, uint8_t* touched, uint64_t* work, uint32_t* bits_ws,
+                                       int64_t bits_ws_words, void* stream);
 
 /* ---- L1 + D-SSIM loss (the standard 3DGS loss: On Scaling Up 3D Gaussian
  * Splatting Training, summary of the loss) ----

@@ -86,7 +86,11 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
                                   ctypes.c_float(e), 0, None) == abi.GS_ERR_INVALID_ARG
     # raster with a target but no gradient buffers
     assert L.gs_raster_fused_fwd_bwd(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None, None,
-                                     None, None, None) == abi.GS_ERR_INVALID_ARG
+                                     None, None, None, 0, None) == abi.GS_ERR_INVALID_ARG
+    # saved-bits scratch: a pointer needs a positive size, a size is never negative
+    for ws, words in ((16, 0), (None, -1), (16, -8)):
+        assert L.gs_raster_fused_fwd_bwd(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), None, 16, None,
+                                         None, None, None, ws, words, None) == abi.GS_ERR_INVALID_ARG
     # forward with state: state buffers required; backward from state: dL/dC and gradient buffers required
     assert L.gs_raster_forward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, None, 16, None,
                                      None, None, None) == abi.GS_ERR_INVALID_ARG

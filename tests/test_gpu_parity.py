@@ -109,6 +109,53 @@ def test_gaussians_on_tile_borders_corners_and_spanning_tiles(sh):
     assert st["instances"] > 500
 
 
+def test_saved_pass_bits_scratch_gives_the_recomputed_results():
+    """The fused raster with its saved-pass-bits scratch -- covering every list,
+    covering half of the list positions, absent -- renders the same image and
+    gives the same E counts and touched sets, and grad2d up to the atomics'
+    summation order; with the whole scratch no chunk's bits are recomputed."""
+    from differentiable_rasterizer_gb300 import abi
+    sc = scenes.random_small_scene(23, n=6000, width=64, height=64, sh_degree=0, log_lo=-3.0, log_hi=-1.8,
+                                   logit_mu=-2.0, spread=1.2)
+    tr = pipeline.GaussianTrainer(sc.params, sc.sh_degree, sc.cameras, sc.opts, sc.lr)
+    target = torch.from_numpy(sc.target_uniform).cuda()
+    tr.project()
+    tr.bin_sort()
+    lens = np.diff(tr.ranges.cpu().numpy().view(np.uint32).reshape(-1, 2), axis=1)
+    assert lens.max() > 4 * 256   # chunks evicted from the three-chunk ring
+    n_inst = tr.n_instances
+
+    def run(ws, words):
+        tr.grad2d.zero_()
+        tr.touched.zero_()
+        tr.eval_counts.zero_()
+        abi.gs_raster_fused_fwd_bwd(tr.proj, tr.n, tr.ranges.data_ptr(), tr.ids.data_ptr(), tr.cams, tr.V, tr.opts,
+                                    target.data_ptr(), tr.image.data_ptr(), tr.loss.data_ptr(),
+                                    tr.grad2d.data_ptr(), tr.touched.data_ptr(), tr.eval_counts.data_ptr(),
+                                    tr.stream_handle(), ws, words)
+        torch.cuda.synchronize()
+        out = {k: getattr(tr, k).clone() for k in ("image", "loss", "grad2d", "touched", "eval_counts")}
+        work = torch.zeros(abi.GS_RASTER_WORK_COUNTERS, dtype=torch.int64, device="cuda")
+        tr.grad2d.zero_()
+        tr.touched.zero_()
+        abi.gs_raster_work_counts(tr.proj, tr.n, tr.ranges.data_ptr(), tr.ids.data_ptr(), tr.cams, tr.V, tr.opts,
+                                  target.data_ptr(), tr.image.data_ptr(), tr.loss.data_ptr(), tr.grad2d.data_ptr(),
+                                  tr.touched.data_ptr(), work.data_ptr(), tr.stream_handle(), ws, words)
+        out["work"] = dict(zip(abi.RASTER_WORK_NAMES, work.cpu().tolist()))
+        return out
+
+    full = run(tr.bits_ws.data_ptr(), abi.raster_bits_ws_words(n_inst))
+    half = run(tr.bits_ws.data_ptr(), abi.raster_bits_ws_words(n_inst // 2))
+    none = run(None, 0)
+    assert none["work"]["recomputed_chunks"] > half["work"]["recomputed_chunks"] > full["work"]["recomputed_chunks"] == 0
+    for got in (half, none):
+        for k in ("image", "touched", "eval_counts"):
+            assert torch.equal(got[k], full[k]), k
+        g, f = got["grad2d"].double(), full["grad2d"].double()
+        assert float((g - f).abs().max()) <= 1e-5 * float(f.abs().max())
+        assert abs(float(got["loss"][0]) - float(full["loss"][0])) <= 1e-12 * abs(float(full["loss"][0]))
+
+
 def test_sort_bucket_sizes_over_2048_use_the_large_block_sort():
     """~6000 wide Gaussians on a 32x32 view: 4 tile buckets of ~6000 instances."""
     sc = scenes.random_small_scene(31, n=6000, width=32, height=32, sh_degree=0, log_lo=-1.5, log_hi=-1.0,
