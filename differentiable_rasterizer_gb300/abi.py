@@ -83,10 +83,10 @@ def lib():
         L.gs_grad_compact.argtypes = [_P, _P, _P, _I64, _I32, _P, _I32, _P, _P, _P, _P, _P,
                                       ctypes.POINTER(ctypes.c_size_t), _P]
         L.gs_adam_deferred.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _P, _P, _I32, _P, _F, _F, _F, _I32, _P]
-        L.gs_raster_forward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P,
+        L.gs_raster_forward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _I64,
                                               _P, _P]
         L.gs_dssim_loss_grad.argtypes = [_P, _P, _I32, _I32, _I32, _F, _P, _P, _P]
-        L.gs_raster_backward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
+        L.gs_raster_backward_state.argtypes = [ctypes.POINTER(GsProj), _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _I64,
                                                _P, _P, _P, _P]
         L.gs_prune_tiles.argtypes = [ctypes.POINTER(GsProj), _I64, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.gs_split_ranges.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
@@ -168,9 +168,9 @@ def gs_bin_sort(proj, n, n_views, width, height, capacity, keys, ids, tile_range
     return st, cnt.value
 
 
-def raster_bits_ws_words(n_instances) -> int:
-    """GS_RASTER_BITS_WS_WORDS: scratch words that cover lists of n_instances entries."""
-    return (int(n_instances) + 256) * 8
+def raster_bits_ws_words(n_instances, n_lists) -> int:
+    """GS_RASTER_BITS_WS_WORDS: scratch words that cover n_instances entries in n_lists tile lists."""
+    return (int(n_instances) + 32 * int(n_lists)) * 8
 
 
 def gs_raster_fused_fwd_bwd(proj, n, tile_ranges, ids, cams, n_views, opts, target, image, loss, grad2d, touched,
@@ -233,11 +233,12 @@ def gs_compose(c_parts, t_parts, n_subsets, n_views, width, height, bg, image, t
                                           stream))
 
 
-def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, pass_bits,
-                            bits_chunk, eval_counts, stream):
+def gs_raster_forward_state(proj, n, tile_ranges, ids, cams, n_views, opts, image, t_final, last_idx, bits_ws,
+                            bits_ws_words, eval_counts, stream):
+    """bits_ws: None or a device pointer to bits_ws_words u32 (every chunk's pass bits are stored there)."""
     _check("gs_raster_forward_state",
            lib().gs_raster_forward_state(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
-                                         image, t_final, last_idx, pass_bits, bits_chunk, eval_counts, stream))
+                                         image, t_final, last_idx, bits_ws, int(bits_ws_words), eval_counts, stream))
 
 
 def gs_dssim_loss_grad(image, target, n_views, width, height, lam, loss, dldc, stream):
@@ -245,11 +246,12 @@ def gs_dssim_loss_grad(image, target, n_views, width, height, lam, loss, dldc, s
                                                           stream))
 
 
-def gs_raster_backward_state(proj, n, tile_ranges, ids, cams, n_views, opts, t_final, last_idx, pass_bits, bits_chunk,
-                             dldc, grad2d, touched, stream):
+def gs_raster_backward_state(proj, n, tile_ranges, ids, cams, n_views, opts, t_final, last_idx, bits_ws,
+                             bits_ws_words, dldc, grad2d, touched, stream):
     _check("gs_raster_backward_state",
            lib().gs_raster_backward_state(ctypes.byref(proj), n, tile_ranges, ids, cams, n_views, ctypes.byref(opts),
-                                          t_final, last_idx, pass_bits, bits_chunk, dldc, grad2d, touched, stream))
+                                          t_final, last_idx, bits_ws, int(bits_ws_words), dldc, grad2d, touched,
+                                          stream))
 
 
 def gs_grad_compact_ws_bytes(n) -> int:

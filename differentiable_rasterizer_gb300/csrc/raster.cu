@@ -65,10 +65,8 @@ struct RasterArgs {
     const float* __restrict__ dldc;     // [V][3][H][W]: dL/dC (backward from stored state)
     float* t_final;                     // [V][H][W]: final transmittance per pixel, or null
     int32_t* last_idx;                  // [V][H][W]: last composited list index per pixel (-1: none)
-    uint32_t* bits;                     // [V * tiles][kWords][256]: pass bits of one chunk per tile, or null
-    uint32_t* bits_ws;                  // fused: pass bits of the chunks the ring evicts, by list position, or null
+    uint32_t* bits_ws;                  // saved pass bits by list position (kWords words per entry), or null
     int64_t bits_ws_words;              // its size in 32-bit words
-    int32_t* bits_chunk;                // [V * tiles]: the chunk those bits belong to (-1: none)
     float* image;                       // [V][3][H][W]
     double* loss;                       // [V]
     float* grad2d;                      // [V][n][12]
@@ -215,7 +213,6 @@ struct RasterSmem {
     uint32_t bits[kRing][kWords][kTileThreads];            // per ring slot: bit j of pixel p = entry j passes at p
     uint32_t rowm[2][kTile][kWords];                       // per mask buffer: entries whose box covers tile row y
     uint32_t colm[2][kTile][kWords + 1];                   // ... column x (padded: conflict-free reads)
-    int max_last[kWarps];
     double red_loss[kWarps];                               // per warp: loss sum ...
     unsigned long long red_counts[3][kWarps];              // ... and evaluation counts
 };
@@ -233,7 +230,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     auto& s_bits = sm.bits;
     auto& s_rowm = sm.rowm;
     auto& s_colm = sm.colm;
-    auto& s_max_last = sm.max_last;
 
     // Views interleaved (CTA i: view i mod V, tile i / V) so the heavy central
     // tiles of all views are spread over the launch instead of queued view by
@@ -287,16 +283,19 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         s_id[b][threadIdx.x] = g;
         cp_async_commit();
     };
-    // Chunk c's slot in the saved-bits scratch: the kWords x 256 words from word
-    // (lo + c kChunk) kWords on (8 KB a chunk, 32 bytes per list entry); a
-    // chunk past the scratch's end has none and is recomputed instead.
+    // Chunk c's slot in the saved-bits scratch: its rows (word w of every pixel
+    // = 256 words, 32 list entries' bits) for the words that hold entries, from
+    // word (lo + 32 l + c kChunk) kWords on, l = the list's index.  32 bytes
+    // per list entry plus 32 entries' worth per list keep a list's partial last
+    // chunk clear of the next list.  A chunk past the scratch's end has no slot
+    // and is recomputed instead.
+    auto saved_words = [&](int c) -> int { return (min(kChunk, len - c * kChunk) + 31) >> 5; };
+    auto saved_base = [&](int c) -> size_t { return lo + (size_t)tile_lin * 32 + (size_t)c * kChunk; };
     auto saved = [&](int c) -> bool {
         return a.bits_ws != nullptr &&
-               (int64_t)((lo + (size_t)(c + 1) * kChunk) * kWords) <= a.bits_ws_words;
+               (int64_t)((saved_base(c) + (size_t)saved_words(c) * 32) * kWords) <= a.bits_ws_words;
     };
-    auto saved_row = [&](int c) -> uint32_t* {
-        return a.bits_ws + (lo + (size_t)c * kChunk) * kWords + threadIdx.x;
-    };
+    auto saved_row = [&](int c) -> uint32_t* { return a.bits_ws + saved_base(c) * kWords + threadIdx.x; };
 
     // Candidate masks of the chunk in buffer b, into mask buffer mb: bit j of
     // row mask y (column mask x) is set when entry j's alpha-support box (from
@@ -410,12 +409,12 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         if (kCount && threadIdx.x == 0) ++work[kWChunks];
         if (c + 1 < nchunks) stage_copy(g_ahead, b ^ 1);
         g_ahead = c + 2 < nchunks ? stage_id(base + 2 * kChunk) : kNone;
-        if (kMode == kFused && c >= kRing && saved(c - kRing)) {
+        if (kMode != kBwdState && c >= kRing && saved(c - kRing)) {
             // slot sl still holds chunk c - kRing, which the ring now evicts: its
             // rows go to the scratch, where the backward reads them back
             uint32_t* dst = saved_row(c - kRing);
 #pragma unroll
-            for (int w = 0; w < kWords; ++w) dst[w * kTileThreads] = s_bits[sl][w][threadIdx.x];
+            for (int w = 0; w < kWords; ++w) dst[w * kTileThreads] = s_bits[sl][w][threadIdx.x];   // a full chunk
         }
         // Each pixel tests its candidates in list order and composites the ones
         // that pass, with T, the colour, the stop index and dL/dC in registers;
@@ -484,7 +483,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     // forward.  (Deferring that barrier to the end of the kernel, so that the
     // warps start their backward without waiting for one another, measured
     // slower on every workload.)
-    int ml = last;
     if (kMode != kBwdState) {
         unsigned long long ef = (unsigned long long)nev, eb = (unsigned long long)(last + 1);
         unsigned long long ec = (unsigned long long)ncomp;
@@ -494,7 +492,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
             ef += __shfl_xor_sync(0xffffffffu, ef, o);
             eb += __shfl_xor_sync(0xffffffffu, eb, o);
             ec += __shfl_xor_sync(0xffffffffu, ec, o);
-            ml = max(ml, __shfl_xor_sync(0xffffffffu, ml, o));
         }
         if (lane == 0) {
             sm.red_loss[warp] = lsum;
@@ -524,30 +521,26 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
         }
     };
     if (kMode == kFwd) {
-        if (lane == 0) s_max_last[warp] = ml;
         __syncthreads();
         flush_sums();
-        if (!a.bits) return;
-        // Keep the pass bits of the chunk holding the tile's last composited entry
-        // (where a backward from this state starts), if the ring still has them.
-        int tl = -1;
+        // the chunks still in the ring go to the scratch as well (the evicted ones
+        // went there during the forward), for a backward from this state
+        for (int cc = max(0, resident - kRing + 1); cc <= resident; ++cc) {
+            if (!saved(cc)) continue;
+            uint32_t* dst = saved_row(cc);
+            const int nw = saved_words(cc);
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) tl = max(tl, s_max_last[w]);
-        const int cl = tl >= 0 ? tl / kChunk : -1;
-        const bool keep = cl >= 0 && cl >= resident - kRing + 1;
-        uint32_t* dst = a.bits + (size_t)tile_lin * kWords * kTileThreads;
-        if (keep) {
-#pragma unroll
-            for (int w = 0; w < kWords; ++w) dst[w * kTileThreads + threadIdx.x] = s_bits[cl % kRing][w][threadIdx.x];
+            for (int w = 0; w < kWords; ++w)
+                if (w < nw) dst[w * kTileThreads] = s_bits[cc % kRing][w][threadIdx.x];
         }
-        if (threadIdx.x == 0) a.bits_chunk[tile_lin] = keep ? cl : -1;
         return;
     }
 
     // ------------------------------------------------------------- backward
     // The chunks are visited from the forward's last (still in shared memory) down
     // to 0; the ring holds the pass bits of chunks last_fwd - kRing + 1 .. last_fwd
-    // (none when the forward ran in an earlier launch).  A chunk other than the
+    // (none when the forward ran in an earlier launch: then every chunk's bits
+    // come from the scratch, or are recomputed).  A chunk other than the
     // resident one is staged again only if some pixel of the tile composited an
     // entry at or after its start (one vote at the barrier that precedes it); the
     // chunk below it is copied in while the warps work on it.
@@ -557,16 +550,6 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
     }
     const int last_fwd = kMode == kBwdState ? INT32_MAX / 2 : resident;
     const int c_top = kMode == kBwdState ? (len > 0 ? (len - 1) / kChunk : -1) : resident;
-    // backward from a stored state: the chunk whose pass bits the forward kept
-    int c_kept = -1;
-    if (kMode == kBwdState && a.bits) {
-        c_kept = a.bits_chunk[tile_lin];
-        if (c_kept >= 0) {
-            const uint32_t* src = a.bits + (size_t)tile_lin * kWords * kTileThreads;
-#pragma unroll
-            for (int w = 0; w < kWords; ++w) s_bits[c_kept % kRing][w][threadIdx.x] = src[w * kTileThreads + threadIdx.x];
-        }
-    }
     int fetched = -1;    // chunk whose records were last copied into buffer fetched & 1
     uint32_t g_pre = kNone;   // ids of chunk pre_chunk, loaded a step before their copy
     int pre_chunk = -1;
@@ -608,12 +591,14 @@ __global__ void __launch_bounds__(kTileThreads, kCount ? 1 : 4) raster_fused_ker
                 }
             }
             if (kCount && threadIdx.x == 0) ++work[kWRestaged];
-            if (kMode == kBwdState ? c != c_kept : c <= last_fwd - kRing) {
-                if (kMode == kFused && saved(c)) {
-                    // pass bits evicted from the ring and saved by the forward
+            if (c <= last_fwd - kRing) {
+                if (saved(c)) {
+                    // pass bits saved by the forward (evicted from the ring, or all
+                    // of them for a backward from a stored state)
                     const uint32_t* src = saved_row(c);
+                    const int nw = saved_words(c);
 #pragma unroll
-                    for (int w = 0; w < kWords; ++w) s_bits[sl][w][threadIdx.x] = src[w * kTileThreads];
+                    for (int w = 0; w < kWords; ++w) s_bits[sl][w][threadIdx.x] = w < nw ? src[w * kTileThreads] : 0u;
                 } else {
                     // pass bits no longer in the ring: recompute them, each pixel up
                     // to its last composited entry (mask buffer 0: the forward is over)
@@ -854,7 +839,7 @@ extern "C" gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const
 extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                              const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                              const gs_render_opts* opts, float* image, float* t_final,
-                                             int32_t* last_idx, uint32_t* pass_bits, int32_t* bits_chunk,
+                                             int32_t* last_idx, uint32_t* bits_ws, int64_t bits_ws_words,
                                              uint64_t* eval_counts, void* stream)
 {
     GS_NVTX_RANGE("gs_raster_forward_state");
@@ -862,12 +847,13 @@ extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, con
     long long grid = 0;
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
     if (st != GS_OK) return st;
-    if (!image || !t_final || !last_idx || (pass_bits && !bits_chunk)) return GS_ERR_INVALID_ARG;
+    if (!image || !t_final || !last_idx) return GS_ERR_INVALID_ARG;
+    if (bits_ws_words < 0 || (bits_ws && bits_ws_words == 0)) return GS_ERR_INVALID_ARG;
     a.image = image;
     a.t_final = t_final;
     a.last_idx = last_idx;
-    a.bits = pass_bits;
-    a.bits_chunk = bits_chunk;
+    a.bits_ws = bits_ws;
+    a.bits_ws_words = bits_ws ? bits_ws_words : 0;
     a.counts = reinterpret_cast<unsigned long long*>(eval_counts);
     return launch_raster<kFwd, false>(a, grid, (cudaStream_t)stream);
 }
@@ -875,8 +861,8 @@ extern "C" gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, con
 extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                               const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                               const gs_render_opts* opts, const float* t_final,
-                                              const int32_t* last_idx, const uint32_t* pass_bits,
-                                              const int32_t* bits_chunk, const float* dldc, float* grad2d,
+                                              const int32_t* last_idx, const uint32_t* bits_ws,
+                                              int64_t bits_ws_words, const float* dldc, float* grad2d,
                                               uint8_t* touched, void* stream)
 {
     GS_NVTX_RANGE("gs_raster_backward_state");
@@ -885,9 +871,9 @@ extern "C" gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, co
     gs_status st = raster_args(a, proj, n, tile_ranges, ids, cams, n_views, opts, grid);
     if (st != GS_OK) return st;
     if (!t_final || !last_idx || !dldc || (n > 0 && (!grad2d || !touched))) return GS_ERR_INVALID_ARG;
-    if (pass_bits && !bits_chunk) return GS_ERR_INVALID_ARG;
-    a.bits = const_cast<uint32_t*>(pass_bits);
-    a.bits_chunk = const_cast<int32_t*>(bits_chunk);
+    if (bits_ws_words < 0 || (bits_ws && bits_ws_words == 0)) return GS_ERR_INVALID_ARG;
+    a.bits_ws = const_cast<uint32_t*>(bits_ws);   // only read in this mode
+    a.bits_ws_words = bits_ws ? bits_ws_words : 0;
     if (grad2d && !aligned16(grad2d)) return GS_ERR_INVALID_ARG;
     a.t_final = const_cast<float*>(t_final);
     a.last_idx = const_cast<int32_t*>(last_idx);

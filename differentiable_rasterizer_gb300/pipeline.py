@@ -23,7 +23,7 @@ Buffer layout in HBM (fp32 unless stated):
     touched                         [V, n] u8   (kept all-zero between steps)
     idx, n_idx                      [V + 1, n] u32, [V + 1] int64 (per-view lists + union)
     t_final, last_idx, dldc         [V, H, W], [V, H, W] int32, [V, 3, H, W]  (D-SSIM loss only)
-    pass_bits, bits_chunk           [V * tiles, 8, 256] u32, [V * tiles] int32  (D-SSIM loss only)
+    bits_ws                         [(capacity + 32 V tiles) * 8] u32: saved pass bits (the raster's scratch)
 The sizes follow the workload: nothing is allocated per step once the instance
 capacity has been reached (it grows by 25 % headroom when a step needs more).
 """
@@ -86,8 +86,6 @@ class GaussianTrainer:
             self.t_final = torch.empty((V, self.H, self.W), dtype=torch.float32, device=dev)
             self.last_idx = torch.empty((V, self.H, self.W), dtype=torch.int32, device=dev)
             self.dldc = torch.empty((V, 3, self.H, self.W), dtype=torch.float32, device=dev)
-            self.pass_bits = torch.empty((V * self.tiles, 8, 256), dtype=torch.int32, device=dev)
-            self.bits_chunk = torch.empty(V * self.tiles, dtype=torch.int32, device=dev)
         self.proj = abi.proj_struct(self.rec.data_ptr(), self.depth.data_ptr(), self.rect.data_ptr(),
                                     self.tiles_touched.data_ptr())
         self.capacity = 0
@@ -113,7 +111,8 @@ class GaussianTrainer:
         self.keys = torch.empty(capacity, dtype=torch.int64, device=self.device)
         self.ids = torch.empty(capacity, dtype=torch.int32, device=self.device)
         # the fused raster's saved-pass-bits scratch (32 B per instance)
-        self.bits_ws = torch.empty(abi.raster_bits_ws_words(capacity), dtype=torch.int32, device=self.device)
+        self.bits_ws = torch.empty(abi.raster_bits_ws_words(capacity, self.V * self.tiles), dtype=torch.int32,
+                                   device=self.device)
         nbytes = abi.gs_bin_sort_ws_bytes(self.n, self.V, self.W, self.H, capacity)
         self.sort_ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
@@ -188,7 +187,7 @@ class GaussianTrainer:
         sh = self.stream_handle()
         abi.gs_raster_forward_state(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams, self.V,
                                     self.opts, self.image.data_ptr(), self.t_final.data_ptr(),
-                                    self.last_idx.data_ptr(), self.pass_bits.data_ptr(), self.bits_chunk.data_ptr(),
+                                    self.last_idx.data_ptr(), self.bits_ws.data_ptr(), self.bits_ws.numel(),
                                     self.eval_counts.data_ptr() if count_evals else None, sh)
         if events is not None:
             events[0].record(torch.cuda.current_stream(self.device))
@@ -198,7 +197,7 @@ class GaussianTrainer:
             events[1].record(torch.cuda.current_stream(self.device))
         abi.gs_raster_backward_state(self.proj, self.n, self.ranges.data_ptr(), self.ids.data_ptr(), self.cams,
                                      self.V, self.opts, self.t_final.data_ptr(), self.last_idx.data_ptr(),
-                                     self.pass_bits.data_ptr(), self.bits_chunk.data_ptr(), self.dldc.data_ptr(),
+                                     self.bits_ws.data_ptr(), self.bits_ws.numel(), self.dldc.data_ptr(),
                                      self.grad2d.data_ptr(), self.touched.data_ptr(), sh)
 
     def compact(self):
@@ -306,7 +305,7 @@ class GaussianTrainer:
         for s in range(S):
             abi.gs_raster_forward_state(self.proj, self.n, self.sub_ranges[s].data_ptr(), self.ids.data_ptr(),
                                         self.cams, V, zero_bg, self.c_parts[s].data_ptr(),
-                                        self.t_parts[s].data_ptr(), self.l_parts[s].data_ptr(), None, None, None, sh)
+                                        self.t_parts[s].data_ptr(), self.l_parts[s].data_ptr(), None, 0, None, sh)
         abi.gs_compose(self.c_parts.data_ptr(), self.t_parts.data_ptr(), S, V, W, H, self._opts_dict["bg"],
                        self.image.data_ptr(), self.t_composed.data_ptr(), sh)
         return self.image

@@ -211,13 +211,16 @@ GS_API gs_status gs_prune_tiles(const gs_proj* proj, int64_t n, int32_t n_views,
  *   E_comp = entries composited (alpha >= alpha_min and not stopped).
  * bits_ws, bits_ws_words: NULL and 0, or a DEVICE u32 scratch and its size in
  *   words.  The pass bits of the chunks the on-chip ring evicts are saved there
- *   in the forward (8 words per list entry, at the entry's list position) and
- *   read back by the backward instead of being recomputed; a chunk whose slot
- *   lies past the scratch's end is recomputed.  GS_RASTER_BITS_WS_WORDS(I)
- *   words cover lists of I instances.  Contents on entry are ignored and left
- *   undefined; results do not depend on the scratch.
+ *   in the forward and read back by the backward instead of being recomputed.
+ *   Layout: list l's chunk c (256 entries) from word (start of l + 32 l +
+ *   256 c) * 8 on, word w of pixel p at 256 w + p (bit j: entry 32 w + j of the
+ *   chunk passes at p), only the words that hold entries; a chunk whose slot
+ *   lies past the scratch's end is recomputed.  GS_RASTER_BITS_WS_WORDS(I, L)
+ *   words cover I instances in L = n_views * tiles lists laid out in tile order
+ *   (as gs_bin_sort and gs_prune_tiles leave them).  Contents on entry are
+ *   ignored and left undefined; results do not depend on the scratch.
  * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
-#define GS_RASTER_BITS_WS_WORDS(n_instances) (((int64_t)(n_instances) + 256) * 8)
+#define GS_RASTER_BITS_WS_WORDS(n_instances, n_lists) (((int64_t)(n_instances) + 32 * (int64_t)(n_lists)) * 8)
 GS_API gs_status gs_raster_fused_fwd_bwd(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges, const uint32_t* ids,
                                   const gs_camera* cams, int32_t n_views, const gs_render_opts* opts,
                                   const float* target, float* image, double* loss, float* grad2d, uint8_t* touched,
@@ -253,25 +256,26 @@ GS_API gs_status gs_raster_work_counts(const gs_proj* proj, int64_t n, const uin
  *   gs_raster_forward_state   image + per-pixel final T and last index
  *   gs_dssim_loss_grad        loss and dL/dC from image and target
  *   gs_raster_backward_state  backward from the stored state and dL/dC
- * The backward reuses the pass bits of the chunk it starts in (stored by the
- * forward) and recomputes older chunks' (the fused kernel keeps the last three
- * on chip); otherwise it is the fused kernel's backward. */
+ * The forward saves every chunk's pass bits to a scratch (as the fused kernel
+ * saves the chunks its on-chip ring evicts) and the backward reads them back
+ * instead of recomputing them; otherwise it is the fused kernel's backward. */
 
 /* Forward rasterization as in gs_raster_fused_fwd_bwd without a target, that
  * also stores per pixel the final transmittance and the last composited list
- * index (-1 if none), and optionally, per tile, the pass bits of the chunk of
- * 256 list entries that holds the tile's last composited entry (the backward
- * starts there and reuses them instead of recomputing them).
+ * index (-1 if none), and optionally the pass bits of every chunk of 256 list
+ * entries it works on (the backward reads them instead of recomputing them).
  * image: [V][3][H][W] out.  t_final: [V][H][W] fp32 out.  last_idx: [V][H][W]
- * int32 out.  pass_bits: NULL or [V * tiles][8][256] u32 out (bit j of word w of
- * pixel p: entry 32 w + j of that chunk passes at p); bits_chunk: [V * tiles]
- * int32 out, the chunk they belong to, -1 if none (required with pass_bits).
- * eval_counts: NULL or [3] u64 accumulated (+=), as for the fused call.
+ * int32 out.  bits_ws, bits_ws_words: NULL and 0, or a DEVICE u32 scratch and
+ * its size in words, laid out as for gs_raster_fused_fwd_bwd (8 words per list
+ * entry at its list position: word w of pixel p of a chunk at 256 w + p, bit j
+ * set when entry 32 w + j of the chunk passes at p); chunks whose slot lies past
+ * the scratch's end are not stored.  eval_counts: NULL or [3] u64 accumulated
+ * (+=), as for the fused call.
  * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
 GS_API gs_status gs_raster_forward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                          const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                          const gs_render_opts* opts, float* image, float* t_final, int32_t* last_idx,
-                                         uint32_t* pass_bits, int32_t* bits_chunk, uint64_t* eval_counts,
+                                         uint32_t* bits_ws, int64_t bits_ws_words, uint64_t* eval_counts,
                                          void* stream);
 
 /* Loss (1 - lambda) L1 + lambda (1 - SSIM) per view and its gradient
@@ -290,14 +294,15 @@ GS_API gs_status gs_dssim_loss_grad(const float* image, const float* target, int
  * entries are walked back to front exactly as in gs_raster_fused_fwd_bwd, with
  * dL/dC taken from dldc instead of the L1 sign.  proj, tile lists, cams and
  * opts must be those of the gs_raster_forward_state call that wrote t_final,
- * last_idx and (if given) pass_bits / bits_chunk; without them every chunk's
- * pass bits are recomputed.  dldc: [V][3][H][W].  grad2d, touched: as for the
- * fused call (accumulated; zero on entry).
+ * last_idx and (if given) the scratch bits_ws / bits_ws_words, read here; a
+ * chunk without a slot in it (or all, without a scratch) has its pass bits
+ * recomputed.  dldc: [V][3][H][W].  grad2d, touched: as for the fused call
+ * (accumulated; zero on entry).
  * Errors: INVALID_ARG for bad pointers or sizes; CUDA on launch failure. */
 GS_API gs_status gs_raster_backward_state(const gs_proj* proj, int64_t n, const uint32_t* tile_ranges,
                                           const uint32_t* ids, const gs_camera* cams, int32_t n_views,
                                           const gs_render_opts* opts, const float* t_final, const int32_t* last_idx,
-                                          const uint32_t* pass_bits, const int32_t* bits_chunk, const float* dldc,
+                                          const uint32_t* bits_ws, int64_t bits_ws_words, const float* dldc,
                                           float* grad2d, uint8_t* touched, void* stream);
 
 /* ---- Partial render + compose (Splaxel, English abstract: each part renders

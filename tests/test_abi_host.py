@@ -93,13 +93,16 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
                                          None, None, None, ws, words, None) == abi.GS_ERR_INVALID_ARG
     # forward with state: state buffers required; backward from state: dL/dC and gradient buffers required
     assert L.gs_raster_forward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, None, 16, None,
-                                     None, None, None) == abi.GS_ERR_INVALID_ARG
-    assert L.gs_raster_forward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, 16, 16,
-                                     None, None, None) == abi.GS_ERR_INVALID_ARG       # bits without their chunk
+                                     0, None, None) == abi.GS_ERR_INVALID_ARG
+    for ws, words in ((16, 0), (None, -1)):   # the scratch: a pointer needs a size, no size is negative
+        assert L.gs_raster_forward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, 16,
+                                         ws, words, None, None) == abi.GS_ERR_INVALID_ARG
+        assert L.gs_raster_backward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, ws,
+                                          words, 16, 16, 16, None) == abi.GS_ERR_INVALID_ARG
     assert L.gs_raster_backward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None,
-                                      None, None, 16, 16, None) == abi.GS_ERR_INVALID_ARG
+                                      0, None, 16, 16, None) == abi.GS_ERR_INVALID_ARG
     assert L.gs_raster_backward_state(ctypes.byref(proj), 10, 16, 16, cams, 1, ctypes.byref(opts), 16, 16, None,
-                                      None, 16, None, 16, None) == abi.GS_ERR_INVALID_ARG
+                                      0, 16, None, 16, None) == abi.GS_ERR_INVALID_ARG
     # pruning: budget >= 1
     assert L.gs_prune_tiles(ctypes.byref(proj), 10, 1, 64, 64, 0, 16, 16, None) == abi.GS_ERR_INVALID_ARG
     assert L.gs_prune_tiles(ctypes.byref(proj), 10, 1, 64, 64, 8, 16, None, None) == abi.GS_ERR_INVALID_ARG

@@ -144,8 +144,9 @@ def test_saved_pass_bits_scratch_gives_the_recomputed_results():
         out["work"] = dict(zip(abi.RASTER_WORK_NAMES, work.cpu().tolist()))
         return out
 
-    full = run(tr.bits_ws.data_ptr(), abi.raster_bits_ws_words(n_inst))
-    half = run(tr.bits_ws.data_ptr(), abi.raster_bits_ws_words(n_inst // 2))
+    lists = tr.V * tr.tiles
+    full = run(tr.bits_ws.data_ptr(), abi.raster_bits_ws_words(n_inst, lists))
+    half = run(tr.bits_ws.data_ptr(), abi.raster_bits_ws_words(n_inst // 2, lists // 2))
     none = run(None, 0)
     assert none["work"]["recomputed_chunks"] > half["work"]["recomputed_chunks"] > full["work"]["recomputed_chunks"] == 0
     for got in (half, none):
