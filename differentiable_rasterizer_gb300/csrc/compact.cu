@@ -9,7 +9,10 @@
 //               touching view is summed in view order in registers and written
 //               as the Gaussian's dense gradient block ([n][stride] layout,
 //               float4 stores; other blocks are not touched); the consumed
-//               grad2d / touched entries are cleared.
+//               grad2d / touched entries are cleared.  (SH degree 3 with
+//               several views: the geometry and colour halves run in
+//               different warps, each summed in view order, and the two
+//               mean terms are added at the end.)
 // With one owner (this GPU) no record leaves the device, so the "send" of the
 // encoded list is the list itself.
 #include "gs_common.cuh"
@@ -83,6 +86,128 @@ __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t g = (int64_t)a.idx_union[i];
         if (GS_IN_RANGE(g, a.n, GS_CHECK_COMPACT_ID)) vjp_gaussian<DEG>(a, cs, g);
+    }
+}
+
+// SH degree 3 with several views: the decode with its two halves in different
+// warps.  A block of 128 threads takes 64 Gaussians of the union list at a
+// time: warps 0-1 run their geometry VJP (mean through the projection, scale,
+// rotation, opacity) and warps 2-3 their colour VJP (48 coefficients, and the
+// mean through the viewing direction), so each (Gaussian, view)'s dependent
+// chain is about half as long.  Warp w + 2 serves the same 32 Gaussians as
+// warp w, and the pair meets at a 64-thread named barrier: the colour warp
+// passes its direction term and the gradient of the first coefficient row
+// through shared memory; the geometry warp writes the first three float4 of
+// the gradient block and clears the consumed grad2d / touched entries, the
+// colour warp writes the rest.  (With one view the one-thread-per-Gaussian
+// vjp_kernel keeps more Gaussians in flight per SM and is the faster of the
+// two.)
+constexpr int kSplitThreads = 128;
+constexpr int kSplitGaussians = kSplitThreads / 2;
+
+// Barrier of the warp pair (w, w + 2): ids 1 and 2, 64 threads each.
+__device__ __forceinline__ void pair_sync(int warp)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 1)) : "memory");
+}
+
+struct GaussGeom {
+    float mu[3], ls[3], q[4], logit;
+};
+
+__global__ void __launch_bounds__(kSplitThreads) vjp_split_kernel(VjpArgs a, CamSet cs)
+{
+    __shared__ float4 s_x[kSplitGaussians];   // per Gaussian: (d/d coefficient row 0, d/d mean via the direction)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool geom = warp < 2;
+    const int slot = ((warp & 1) << 5) | lane;
+    const int64_t count = *a.n_union;
+    // block-uniform loop: every thread reaches both pair barriers of every iteration
+    for (int64_t base = (int64_t)blockIdx.x * kSplitGaussians; base < count;
+         base += (int64_t)gridDim.x * kSplitGaussians) {
+        const int64_t i = base + slot;
+        int64_t g = -1;
+        if (i < count) {
+            const int64_t gi = (int64_t)a.idx_union[i];
+            if (GS_IN_RANGE(gi, a.n, GS_CHECK_COMPACT_ID)) g = gi;
+        }
+        uint32_t vm = 0u;   // the views that composited g
+        if (g >= 0)
+            for (int v = 0; v < cs.n_views; ++v)
+                if (a.touched[(size_t)v * (size_t)a.n + (size_t)g]) vm |= 1u << v;
+        const float4* src = reinterpret_cast<const float4*>(a.params + (size_t)(g >= 0 ? g : 0) * 64);
+        if (geom) {
+            float grad[11];
+#pragma unroll
+            for (int k = 0; k < 11; ++k) grad[k] = 0.0f;
+            if (g >= 0) {
+                const float4 p0 = __ldg(src), p1 = __ldg(src + 1), p2 = __ldg(src + 2);
+                const GaussGeom gp = {{p0.x, p0.y, p0.z}, {p0.w, p1.x, p1.y}, {p1.z, p1.w, p2.x, p2.y}, p2.z};
+                GaussAct ac;
+                activate<3>(gp, ac);
+                for (uint32_t m = vm; m; m &= m - 1u) {
+                    const int v = __ffs(m) - 1;
+                    ProjInter it;
+                    project_geom(gp, ac, cs.cam[v], a.lowpass, it);
+                    const float4* g2s = reinterpret_cast<const float4*>(
+                        a.grad2d + ((size_t)v * (size_t)a.n + (size_t)g) * GS_GRAD2D_STRIDE);
+                    const float4 x0 = g2s[0], x1 = g2s[1];
+                    const float g2[6] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y};
+                    vjp_geom(gp, cs.cam[v], ac, it, g2, grad);
+                }
+            }
+            pair_sync(warp);   // the colour warp's hand-over is in s_x, and it has read its grad2d rows
+            if (g >= 0) {
+                const float4 x = s_x[slot];
+                float4* dst = reinterpret_cast<float4*>(a.grads + (size_t)g * 64);
+                dst[0] = make_float4(grad[0] + x.y, grad[1] + x.z, grad[2] + x.w, grad[3]);
+                dst[1] = make_float4(grad[4], grad[5], grad[6], grad[7]);
+                dst[2] = make_float4(grad[8], grad[9], grad[10], x.x);
+                const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (uint32_t m = vm; m; m &= m - 1u) {
+                    const size_t o = (size_t)(__ffs(m) - 1) * (size_t)a.n + (size_t)g;
+                    float4* g2s = reinterpret_cast<float4*>(a.grad2d + o * GS_GRAD2D_STRIDE);
+                    g2s[0] = z; g2s[1] = z; g2s[2] = z;
+                    a.touched[o] = 0;
+                }
+            }
+        } else {
+            if (g >= 0) {
+                float mu[3], col[48];
+                {
+                    const float4 p0 = __ldg(src), p2 = __ldg(src + 2);
+                    mu[0] = p0.x; mu[1] = p0.y; mu[2] = p0.z;
+                    col[0] = p2.w;
+#pragma unroll
+                    for (int k = 0; k < 12; ++k) {   // floats 12 .. 59 of the block (59: padding)
+                        const float4 p = __ldg(src + 3 + k);
+                        col[1 + 4 * k] = p.x;
+                        col[2 + 4 * k] = p.y;
+                        col[3 + 4 * k] = p.z;
+                        if (k < 11) col[4 + 4 * k] = p.w;
+                    }
+                }
+                float gcol[48], gmu[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int k = 0; k < 48; ++k) gcol[k] = 0.0f;
+                for (uint32_t m = vm; m; m &= m - 1u) {
+                    const int v = __ffs(m) - 1;
+                    const float4* g2s = reinterpret_cast<const float4*>(
+                        a.grad2d + ((size_t)v * (size_t)a.n + (size_t)g) * GS_GRAD2D_STRIDE);
+                    const float4 x1 = g2s[1], x2 = g2s[2];
+                    const float gc[3] = {x1.z, x1.w, x2.x};
+                    vjp_colour3(mu, col, cs.cam[v], gc, gcol, gmu);
+                }
+                float4* dst = reinterpret_cast<float4*>(a.grads + (size_t)g * 64);
+#pragma unroll
+                for (int k = 0; k < 12; ++k)
+                    dst[3 + k] = make_float4(gcol[1 + 4 * k], gcol[2 + 4 * k], gcol[3 + 4 * k],
+                                             k < 11 ? gcol[4 + 4 * k] : 0.0f);
+                s_x[slot] = make_float4(gcol[0], gmu[0], gmu[1], gmu[2]);
+            }
+            pair_sync(warp);   // meets the geometry warp's first barrier
+        }
+        pair_sync(warp);   // s_x is rewritten in the next iteration
     }
 }
 
@@ -160,17 +285,20 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
     int dev = 0, sms = 0, per_sm = 0;
     GS_CUDA_TRY(cudaGetDevice(&dev));
     GS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    if (sh_degree == 0)
-        GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vjp_kernel<0>, threads, 0));
-    else
-        GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vjp_kernel<3>, threads, 0));
-    int64_t blocks = (n + threads - 1) / threads;
-    const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
-    if (blocks > resident) blocks = resident;
-    if (sh_degree == 0)
-        vjp_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(a, cs);
-    else
-        vjp_kernel<3><<<(unsigned)blocks, threads, 0, s>>>(a, cs);
+    if (sh_degree == 0 || n_views == 1) {
+        auto kernel = sh_degree == 0 ? vjp_kernel<0> : vjp_kernel<3>;
+        GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0));
+        int64_t blocks = (n + threads - 1) / threads;
+        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > resident) blocks = resident;
+        kernel<<<(unsigned)blocks, threads, 0, s>>>(a, cs);
+    } else {
+        GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vjp_split_kernel, kSplitThreads, 0));
+        int64_t blocks = (n + kSplitGaussians - 1) / kSplitGaussians;
+        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > resident) blocks = resident;
+        vjp_split_kernel<<<(unsigned)blocks, kSplitThreads, 0, s>>>(a, cs);
+    }
     GS_LAUNCH_CHECK();
     return GS_OK;
 }

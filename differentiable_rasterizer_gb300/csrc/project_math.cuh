@@ -350,4 +350,195 @@ __device__ __forceinline__ void vjp_one(const GP& gp, const gs_camera& cam, cons
     grad[9] += (gz - z * dotq) * iqn;
 }
 
+// ---------------------------------------------------------------------------
+// The VJP of one (Gaussian, view) split in two independent halves, for a
+// decoder that runs them in different warps: the geometry (mean through the
+// projection, scale, rotation, opacity) and the SH-3 colour (coefficients, and
+// the mean through the viewing direction).  Both recompute their forward
+// intermediates with the operations of project_view, so the colour's clamp
+// decisions are the forward's; a composited (Gaussian, view) is always visible,
+// so no culling test is repeated.
+// ---------------------------------------------------------------------------
+
+// Geometry intermediates of project_view (t, T0, T1, the 2D covariance).
+template <class GP>
+__device__ __forceinline__ void project_geom(const GP& gp, const GaussAct& ac, const gs_camera& cam, float lowpass,
+                                             ProjInter& it)
+{
+    const float* W = cam.R;
+    float t[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        t[i] = ((W[3 * i + 0] * gp.mu[0] + W[3 * i + 1] * gp.mu[1]) + W[3 * i + 2] * gp.mu[2]) + cam.t[i];
+    const float* S = ac.S;
+    const float fx = cam.fx, fy = cam.fy;
+    const float tz2 = t[2] * t[2];
+    const float j00 = fx / t[2], j11 = fy / t[2];
+    const float j02 = -(fx * t[0]) / tz2, j12 = -(fy * t[1]) / tz2;
+    float T0[3], T1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        T0[k] = j00 * W[0 + k] + j02 * W[6 + k];
+        T1[k] = j11 * W[3 + k] + j12 * W[6 + k];
+    }
+    float u[3], v[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        u[k] = (T0[0] * S[0 + k] + T0[1] * S[3 + k]) + T0[2] * S[6 + k];
+        v[k] = (T1[0] * S[0 + k] + T1[1] * S[3 + k]) + T1[2] * S[6 + k];
+    }
+    it.a = ((u[0] * T0[0] + u[1] * T0[1]) + u[2] * T0[2]) + lowpass;
+    it.b = (u[0] * T1[0] + u[1] * T1[1]) + u[2] * T1[2];
+    it.c = ((v[0] * T1[0] + v[1] * T1[1]) + v[2] * T1[2]) + lowpass;
+    it.det = it.a * it.c - it.b * it.b;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) { it.t[i] = t[i]; it.T0[i] = T0[i]; it.T1[i] = T1[i]; }
+}
+
+// Geometry half of vjp_one: grad[0..10] += d loss / d (mean through the
+// projection, log-scale, quaternion, opacity logit).
+template <class GP>
+__device__ __forceinline__ void vjp_geom(const GP& gp, const gs_camera& cam, const GaussAct& ac, const ProjInter& it,
+                                         const float g2[6], float* grad)
+{
+    const float* W = cam.R;
+    const float fx = cam.fx, fy = cam.fy;
+    const float a = it.a, b = it.b, c = it.c;
+    const float id = 1.0f / it.det;
+    const float gA = g2[2], gB = g2[3], gC = g2[4];
+    const float g_id = __fmaf_rn(gA, c, __fmaf_rn(-gB, b, gC * a));
+    const float g_det = -g_id * id * id;
+    const float ga = __fmaf_rn(gC, id, g_det * c);
+    const float gc = __fmaf_rn(gA, id, g_det * a);
+    const float gb = __fmaf_rn(-gB, id, g_det * (-2.0f * b));
+    float ST0[3], ST1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        ST0[k] = __fmaf_rn(ac.S[3 * k], it.T0[0], __fmaf_rn(ac.S[3 * k + 1], it.T0[1], ac.S[3 * k + 2] * it.T0[2]));
+        ST1[k] = __fmaf_rn(ac.S[3 * k], it.T1[0], __fmaf_rn(ac.S[3 * k + 1], it.T1[1], ac.S[3 * k + 2] * it.T1[2]));
+    }
+    float gT0[3], gT1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        gT0[k] = __fmaf_rn(2.0f * ga, ST0[k], gb * ST1[k]);
+        gT1[k] = __fmaf_rn(gb, ST0[k], 2.0f * gc * ST1[k]);
+    }
+    float Gs[9];
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+        for (int l = 0; l < 3; ++l)
+            Gs[3 * k + l] = __fmaf_rn(ga * it.T0[k], it.T0[l],
+                                      __fmaf_rn(0.5f * gb, __fmaf_rn(it.T0[k], it.T1[l], it.T1[k] * it.T0[l]),
+                                                gc * it.T1[k] * it.T1[l]));
+    float gR[9], gs[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const float gM = 2.0f * __fmaf_rn(Gs[3 * i], ac.M[j], __fmaf_rn(Gs[3 * i + 1], ac.M[3 + j], Gs[3 * i + 2] * ac.M[6 + j]));
+            gR[3 * i + j] = gM * ac.s[j];
+            gs[j] = __fmaf_rn(gM, ac.R[3 * i + j], gs[j]);
+        }
+    const float w = ac.qh[0], x = ac.qh[1], y = ac.qh[2], z = ac.qh[3];
+    const float gw = 2.0f * (-z * gR[1] + y * gR[2] + z * gR[3] - x * gR[5] - y * gR[6] + x * gR[7]);
+    const float gx = 2.0f * (y * gR[1] + z * gR[2] + y * gR[3] - 2.0f * x * gR[4] - w * gR[5] + z * gR[6] + w * gR[7] - 2.0f * x * gR[8]);
+    const float gy = 2.0f * (-2.0f * y * gR[0] + x * gR[1] + w * gR[2] + x * gR[3] + z * gR[5] - w * gR[6] + z * gR[7] - 2.0f * y * gR[8]);
+    const float gz = 2.0f * (-2.0f * z * gR[0] - w * gR[1] + x * gR[2] + w * gR[3] - 2.0f * z * gR[4] + y * gR[5] + x * gR[6] + y * gR[7]);
+    const float dotq = w * gw + x * gx + y * gy + z * gz;
+    const float iqn = 1.0f / ac.qn;
+    float gj00 = 0.0f, gj02 = 0.0f, gj11 = 0.0f, gj12 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        gj00 = __fmaf_rn(gT0[k], W[k], gj00);
+        gj02 = __fmaf_rn(gT0[k], W[6 + k], gj02);
+        gj11 = __fmaf_rn(gT1[k], W[3 + k], gj11);
+        gj12 = __fmaf_rn(gT1[k], W[6 + k], gj12);
+    }
+    const float tx = it.t[0], ty = it.t[1], tz = it.t[2];
+    const float itz = 1.0f / tz, itz2 = itz * itz, itz3 = itz2 * itz;
+    const float gmx = g2[0], gmy = g2[1];
+    float gt[3];
+    gt[0] = gj02 * (-fx * itz2) + gmx * (fx * itz);
+    gt[1] = gj12 * (-fy * itz2) + gmy * (fy * itz);
+    gt[2] = gj00 * (-fx * itz2) + gj02 * (2.0f * fx * tx * itz3) + gj11 * (-fy * itz2) + gj12 * (2.0f * fy * ty * itz3)
+          + gmx * (-fx * tx * itz2) + gmy * (-fy * ty * itz2);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) grad[j] += __fmaf_rn(W[j], gt[0], __fmaf_rn(W[3 + j], gt[1], W[6 + j] * gt[2]));
+    grad[10] += g2[5] * ac.o * (1.0f - ac.o);
+    grad[3] += gs[0] * ac.s[0];
+    grad[4] += gs[1] * ac.s[1];
+    grad[5] += gs[2] * ac.s[2];
+    grad[6] += (gw - w * dotq) * iqn;
+    grad[7] += (gx - x * dotq) * iqn;
+    grad[8] += (gy - y * dotq) * iqn;
+    grad[9] += (gz - z * dotq) * iqn;
+}
+
+// Colour half of vjp_one for SH degree 3: the view's colour forward (the
+// operations of project_view, so the same clamp decisions), then gcol[48] +=
+// d loss / d coefficients and gmu[3] += d loss / d mean through the viewing
+// direction.  gc: d loss / d (r, g, b) of the view.
+__device__ __forceinline__ void vjp_colour3(const float mu[3], const float col[48], const gs_camera& cam,
+                                            const float gc[3], float gcol[48], float gmu[3])
+{
+    const float* W = cam.R;
+    float cc[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) cc[j] = -((W[0 + j] * cam.t[0] + W[3 + j] * cam.t[1]) + W[6 + j] * cam.t[2]);
+    const float dv0 = mu[0] - cc[0], dv1 = mu[1] - cc[1], dv2 = mu[2] - cc[2];
+    const float nv = sqrtf((dv0 * dv0 + dv1 * dv1) + dv2 * dv2);
+    const float X = dv0 / nv, Yv = dv1 / nv, Z = dv2 / nv;
+    float Y[16];
+    sh_basis(X, Yv, Z, Y);
+    uint32_t clamp = 0;
+#pragma unroll
+    for (int ch = 0; ch < 3; ++ch) {
+        float acc = col[ch] * Y[0];
+#pragma unroll
+        for (int k = 1; k < 16; ++k) acc = acc + col[3 * k + ch] * Y[k];
+        acc = acc + 0.5f;
+        if (acc < 0.0f) clamp |= 1u << ch;
+    }
+    const float XX = X * X, YY = Yv * Yv, ZZ = Z * Z;
+    float gd0 = 0.0f, gd1 = 0.0f, gd2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f;
+        switch (k) {
+            case 1: d1 = SH::K1; break;
+            case 2: d2 = SH::K1; break;
+            case 3: d0 = SH::K1; break;
+            case 4: d0 = SH::K2 * Yv; d1 = SH::K2 * X; break;
+            case 5: d1 = SH::K2 * Z; d2 = SH::K2 * Yv; break;
+            case 6: d0 = -2.0f * SH::K3 * X; d1 = -2.0f * SH::K3 * Yv; d2 = 4.0f * SH::K3 * Z; break;
+            case 7: d0 = SH::K2 * Z; d2 = SH::K2 * X; break;
+            case 8: d0 = 2.0f * SH::K4 * X; d1 = -2.0f * SH::K4 * Yv; break;
+            case 9: d0 = 6.0f * SH::K5 * X * Yv; d1 = SH::K5 * (3.0f * XX - 3.0f * YY); break;
+            case 10: d0 = SH::K6 * Yv * Z; d1 = SH::K6 * X * Z; d2 = SH::K6 * X * Yv; break;
+            case 11: d0 = -2.0f * SH::K7 * X * Yv; d1 = SH::K7 * (4.0f * ZZ - XX - 3.0f * YY); d2 = 8.0f * SH::K7 * Yv * Z; break;
+            case 12: d0 = -6.0f * SH::K8 * X * Z; d1 = -6.0f * SH::K8 * Yv * Z; d2 = SH::K8 * (6.0f * ZZ - 3.0f * XX - 3.0f * YY); break;
+            case 13: d0 = SH::K7 * (4.0f * ZZ - 3.0f * XX - YY); d1 = -2.0f * SH::K7 * X * Yv; d2 = 8.0f * SH::K7 * X * Z; break;
+            case 14: d0 = 2.0f * SH::K9 * X * Z; d1 = -2.0f * SH::K9 * Yv * Z; d2 = SH::K9 * (XX - YY); break;
+            case 15: d0 = SH::K5 * (3.0f * XX - 3.0f * YY); d1 = -6.0f * SH::K5 * X * Yv; break;
+            default: break;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 3; ++ch) {
+            if (clamp & (1u << ch)) continue;
+            const int row = 3 * k + ch;
+            gcol[row] = __fmaf_rn(gc[ch], Y[k], gcol[row]);
+            const float kc = gc[ch] * col[row];
+            gd0 = __fmaf_rn(kc, d0, gd0);
+            gd1 = __fmaf_rn(kc, d1, gd1);
+            gd2 = __fmaf_rn(kc, d2, gd2);
+        }
+    }
+    const float dd = X * gd0 + Yv * gd1 + Z * gd2;
+    const float inv = 1.0f / nv;
+    gmu[0] += (gd0 - X * dd) * inv;
+    gmu[1] += (gd1 - Yv * dd) * inv;
+    gmu[2] += (gd2 - Z * dd) * inv;
+}
+
 }  // namespace gs

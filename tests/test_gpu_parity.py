@@ -367,10 +367,12 @@ def test_three_training_steps_track_the_oracle():
     assert (tr.last_step.cpu().numpy() == 3).all()
 
 
-def test_maximum_view_count():
+@pytest.mark.parametrize("sh_degree", [0, 3])
+def test_maximum_view_count(sh_degree):
     """GS_MAX_VIEWS (32) views of a small scene in one step: every per-view
-    stage and the union over all of them."""
-    sc = scenes.random_small_scene(51, n=400, width=40, height=24, sh_degree=0, log_lo=-3.0, log_hi=-2.0)
+    stage and the union over all of them (SH 3: the decode whose geometry and
+    colour halves run in different warps, with every view bit in use)."""
+    sc = scenes.random_small_scene(51, n=400, width=40, height=24, sh_degree=sh_degree, log_lo=-3.0, log_hi=-2.0)
     cams = []
     for k in range(32):
         ang = -0.3 + 0.6 * k / 31
