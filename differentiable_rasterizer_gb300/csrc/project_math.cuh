@@ -541,4 +541,90 @@ __device__ __forceinline__ void vjp_colour3(const float mu[3], const float col[4
     gmu[2] += (gd2 - Z * dd) * inv;
 }
 
+// Colour half for SH degree 3 and ONE view, streaming the 48 coefficients from
+// the Gaussian's parameter block (global or shared memory; src may be dst: every
+// read comes before the first write) instead of holding them: coefficient i = 3 k + c
+// (float 11 + i of the block) adds to channel c's forward colour sum (in the
+// order of project_view, so the clamp decisions are the forward's) and to its
+// three sums col * dY_k / d(direction); once the clamps are known, the mean's
+// direction term is gmu += (gd - dir (dir . gd)) / |mu - C| with
+// gd = sum over unclamped c of gc[c] (channel c's sums).  With one view a
+// coefficient's gradient is gc[c] Y_k (0 if c clamped): written straight to
+// floats 12 .. 59 of dst (float4 3 .. 14; 59 is padding); the gradient of
+// coefficient 0 (float 11) is returned for the caller's float4 2.
+__device__ __forceinline__ float vjp_colour3_stream(const float4* src, const float mu[3], const gs_camera& cam,
+                                                    const float gc[3], float4* dst, float gmu[3])
+{
+    const float* W = cam.R;
+    float cc[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) cc[j] = -((W[0 + j] * cam.t[0] + W[3 + j] * cam.t[1]) + W[6 + j] * cam.t[2]);
+    const float dv0 = mu[0] - cc[0], dv1 = mu[1] - cc[1], dv2 = mu[2] - cc[2];
+    const float nv = sqrtf((dv0 * dv0 + dv1 * dv1) + dv2 * dv2);
+    const float X = dv0 / nv, Yv = dv1 / nv, Z = dv2 / nv;
+    float Y[16];
+    sh_basis(X, Yv, Z, Y);
+    const float XX = X * X, YY = Yv * Yv, ZZ = Z * Z;
+    float fwd[3] = {0.0f, 0.0f, 0.0f}, sd0[3] = {0.0f, 0.0f, 0.0f}, sd1[3] = {0.0f, 0.0f, 0.0f}, sd2[3] = {0.0f, 0.0f, 0.0f};
+    // coefficient i: forward sum and direction-derivative sums of its channel
+    auto take = [&](int i, float col) {
+        const int k = i / 3, ch = i - 3 * (i / 3);
+        fwd[ch] = k == 0 ? col * Y[0] : fwd[ch] + col * Y[k];
+        float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f;
+        switch (k) {
+            case 1: d1 = SH::K1; break;
+            case 2: d2 = SH::K1; break;
+            case 3: d0 = SH::K1; break;
+            case 4: d0 = SH::K2 * Yv; d1 = SH::K2 * X; break;
+            case 5: d1 = SH::K2 * Z; d2 = SH::K2 * Yv; break;
+            case 6: d0 = -2.0f * SH::K3 * X; d1 = -2.0f * SH::K3 * Yv; d2 = 4.0f * SH::K3 * Z; break;
+            case 7: d0 = SH::K2 * Z; d2 = SH::K2 * X; break;
+            case 8: d0 = 2.0f * SH::K4 * X; d1 = -2.0f * SH::K4 * Yv; break;
+            case 9: d0 = 6.0f * SH::K5 * X * Yv; d1 = SH::K5 * (3.0f * XX - 3.0f * YY); break;
+            case 10: d0 = SH::K6 * Yv * Z; d1 = SH::K6 * X * Z; d2 = SH::K6 * X * Yv; break;
+            case 11: d0 = -2.0f * SH::K7 * X * Yv; d1 = SH::K7 * (4.0f * ZZ - XX - 3.0f * YY); d2 = 8.0f * SH::K7 * Yv * Z; break;
+            case 12: d0 = -6.0f * SH::K8 * X * Z; d1 = -6.0f * SH::K8 * Yv * Z; d2 = SH::K8 * (6.0f * ZZ - 3.0f * XX - 3.0f * YY); break;
+            case 13: d0 = SH::K7 * (4.0f * ZZ - 3.0f * XX - YY); d1 = -2.0f * SH::K7 * X * Yv; d2 = 8.0f * SH::K7 * X * Z; break;
+            case 14: d0 = 2.0f * SH::K9 * X * Z; d1 = -2.0f * SH::K9 * Yv * Z; d2 = SH::K9 * (XX - YY); break;
+            case 15: d0 = SH::K5 * (3.0f * XX - 3.0f * YY); d1 = -6.0f * SH::K5 * X * Yv; break;
+            default: break;
+        }
+        sd0[ch] = __fmaf_rn(col, d0, sd0[ch]);
+        sd1[ch] = __fmaf_rn(col, d1, sd1[ch]);
+        sd2[ch] = __fmaf_rn(col, d2, sd2[ch]);
+    };
+    take(0, src[2].w);
+#pragma unroll
+    for (int m = 0; m < 12; ++m) {   // floats 12 .. 59 = coefficients 1 .. 47 (+ padding)
+        const float4 p = src[3 + m];
+        take(1 + 4 * m, p.x);
+        take(2 + 4 * m, p.y);
+        take(3 + 4 * m, p.z);
+        if (m < 11) take(4 + 4 * m, p.w);
+    }
+    // (a clamped channel's sums are never used: a visible Gaussian may hold an
+    // infinite coefficient in a channel that the clamp zeroes)
+    float gm[3], gd0 = 0.0f, gd1 = 0.0f, gd2 = 0.0f;
+#pragma unroll
+    for (int ch = 0; ch < 3; ++ch) {
+        const bool clamped = fwd[ch] + 0.5f < 0.0f;
+        gm[ch] = clamped ? 0.0f : gc[ch];
+        if (!clamped) {
+            gd0 = __fmaf_rn(gc[ch], sd0[ch], gd0);
+            gd1 = __fmaf_rn(gc[ch], sd1[ch], gd1);
+            gd2 = __fmaf_rn(gc[ch], sd2[ch], gd2);
+        }
+    }
+    auto gcol = [&](int i) -> float { return gm[i - 3 * (i / 3)] * Y[i / 3]; };
+#pragma unroll
+    for (int m = 0; m < 12; ++m)
+        dst[3 + m] = make_float4(gcol(1 + 4 * m), gcol(2 + 4 * m), gcol(3 + 4 * m), m < 11 ? gcol(4 + 4 * m) : 0.0f);
+    const float dd = X * gd0 + Yv * gd1 + Z * gd2;
+    const float inv = 1.0f / nv;
+    gmu[0] += (gd0 - X * dd) * inv;
+    gmu[1] += (gd1 - Yv * dd) * inv;
+    gmu[2] += (gd2 - Z * dd) * inv;
+    return gcol(0);
+}
+
 }  // namespace gs
