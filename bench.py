@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -92,11 +93,20 @@ def peaks():
                 sfu_tops=SMS * SFU_LANES * mhz * 1e6 / 1e12)
 
 
+def _code_only(text: str) -> str:
+    """Source text without its comments and blank lines: an edit of a comment does
+    not change the kernel the counters were taken of."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_sha():
+    """sha256 of the fused kernel's code (raster.cu + gs_common.cuh, comments removed)."""
     h = hashlib.sha256()
     for p in ("differentiable_rasterizer_gb300/csrc/raster.cu", "differentiable_rasterizer_gb300/csrc/gs_common.cuh"):
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -26,7 +26,9 @@
 // carried in registers; each (entry, pixel) pair's 9 gradient terms go to the
 // Gaussian's grad2d row with vector atomics.  The pass bits of
 // the last kRing chunks stay in shared memory (a ring), so backward re-gathers
-// only their records; older chunks also get their bits recomputed.  A chunk in
+// only their records; the bits of older chunks, written to a scratch buffer by
+// the forward as the ring evicts them, are read back from it (recomputed when
+// no scratch is given or it is too small).  A chunk in
 // which the warp's pixels mostly composite the same entries (large Gaussians) is
 // walked one entry at a time for all 32 pixels instead, its gradient terms summed
 // over the warp by shuffles before one atomic per component.
@@ -37,9 +39,9 @@
 //
 // Modes (template argument): kFused -- forward, L1 loss and backward in one
 // pass; kFwd -- forward only, optionally storing per pixel the final T and last
-// index and per tile the pass bits of the chunk holding the last composited
-// entry; kBwdState -- the backward alone, started from that stored state with
-// dL/dC given per pixel (for losses whose gradient needs other tiles' colours).
+// index, and the pass bits of every chunk in the scratch; kBwdState -- the
+// backward alone, started from that stored state with dL/dC given per pixel
+// (for losses whose gradient needs other tiles' colours).
 // Views are interleaved over the grid (CTA i: view i mod V, tile i / V) so the
 // heavy central tiles of all views spread over the launch.
 #include "gs_common.cuh"

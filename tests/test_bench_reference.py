@@ -36,3 +36,16 @@ def test_reference_arm_prints_one_contract_line():
 
 def test_reference_arm_other_ranks_print_nothing():
     assert _run({"RANK": "1"}) == []
+
+
+def test_capture_hash_ignores_comments_and_sees_code():
+    """The committed ncu capture's figures are reported only while the fused
+    kernel's code is the one captured: its hash drops comments and blank lines
+    (an edited comment keeps the figures) and changes with any code token."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int a = 1; // one\n/* block\n comment */\n\nfloat b = 2.0f;  \n'
+    assert bench._code_only(src) == "int a = 1;\nfloat b = 2.0f;"
+    assert bench._code_only(src.replace("// one", "// uno")) == bench._code_only(src)
+    assert bench._code_only(src.replace("1;", "2;")) != bench._code_only(src)
+    assert len(bench.source_sha()) == 64
