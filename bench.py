@@ -429,18 +429,21 @@ def run_gpu(args):
 
 def raster_roofline(tr, target, args, pk, prof, t_raster, e_fwd, e_bwd):
     """Roofline of the fused raster kernel against its executed work (see W_OPS),
-    counted in one untimed launch of the counting variant on a fresh step's lists."""
-    work, ops, sfu = None, None, None
-    if args.dssim is None:
-        tr.project()
-        tr.bin_sort()
-        work = tr.work_counts(target)
-        tr.compact()                      # consumes grad2d / touched as a step would
-        import torch
-        torch.cuda.synchronize()
-        pixels = tr.V * tr.W * tr.H
-        ops = sum(W_OPS[k] * work[k] for k in W_OPS) + W_OPS_PIXEL * pixels
-        sfu = work["sparse_entries"] + work["dense_entries"]
+    counted in one untimed launch of the counting variant on a fresh step's lists.
+    With the L1 + D-SSIM loss the raster runs as two launches (forward storing its
+    state, backward from it) that test the same candidates, composite the same
+    entries and walk the same backward entries (chunk by chunk, dense or sparse
+    by the same pass bits) as the fused kernel on those lists: the counting
+    variant's counts are theirs."""
+    tr.project()
+    tr.bin_sort()
+    work = tr.work_counts(target)
+    tr.compact()                      # consumes grad2d / touched as a step would
+    import torch
+    torch.cuda.synchronize()
+    pixels = tr.V * tr.W * tr.H
+    ops = sum(W_OPS[k] * work[k] for k in W_OPS) + W_OPS_PIXEL * pixels
+    sfu = work["sparse_entries"] + work["dense_entries"]
     t_model = e_fwd * (OPS_FWD + OPS_EXP) + e_bwd * (OPS_BWD + OPS_EXP)
     fp32 = pk["fp32_tops"] * 1e12
     r = {"bound": "alu", "peak": pk["fp32_tops"], "unit": "TFLOP/s",
@@ -450,16 +453,14 @@ def raster_roofline(tr, target, args, pk, prof, t_raster, e_fwd, e_bwd):
          "peak_basis": f"FP32 pipe: 152 SMs x 128 lanes x {pk['sm_max_mhz']:.0f} MHz (sm_max_mhz, {pk['src']}; "
                        f"an fma counts once); SFU: 152 x 16 lanes",
          "frac_per_evaluation_model": (t_model / fp32) / t_raster}
-    if work is not None:
-        t_work = max(ops / fp32, sfu / (pk["sfu_tops"] * 1e12))
-        r.update(achieved=ops / t_raster / 1e12, frac=t_work / t_raster, executed=work,
-                 ops_per_launch=ops, sfu_per_launch=sfu,
-                 work="executed FP32 ops: " + ", ".join(f"{v} per {k}" for k, v in W_OPS.items()) +
-                      f", {W_OPS_PIXEL} per pixel (counting variant, one untimed launch); SFU: one reciprocal "
-                      "per backward entry")
-    else:
-        r.update(achieved=t_model / t_raster / 1e12, frac=(t_model / fp32) / t_raster,
-                 work="per-evaluation model (no counting variant for the split D-SSIM launches)")
+    t_work = max(ops / fp32, sfu / (pk["sfu_tops"] * 1e12))
+    r.update(achieved=ops / t_raster / 1e12, frac=t_work / t_raster, executed=work,
+             ops_per_launch=ops, sfu_per_launch=sfu,
+             work="executed FP32 ops: " + ", ".join(f"{v} per {k}" for k, v in W_OPS.items()) +
+                  f", {W_OPS_PIXEL} per pixel (counting variant, one untimed launch); SFU: one reciprocal "
+                  "per backward entry" + ("" if args.dssim is None else
+                                          "; counted on the fused kernel, whose candidates, composites and "
+                                          "backward entries are those of the two D-SSIM launches"))
     for key, src in (("issue_active_ncu", "issue_active_pct"), ("pipe_fma_ncu", "pipe_fma_pct"),
                      ("pipe_alu_ncu", "pipe_alu_pct"), ("pipe_xu_ncu", "pipe_xu_pct"),
                      ("pipe_lsu_ncu", "pipe_lsu_pct")):

@@ -77,7 +77,8 @@ __device__ __forceinline__ void vjp_gaussian(const VjpArgs& a, const CamSet& cs,
 }
 
 // One thread per Gaussian of the union list; the list length lives on the
-// device, so a grid of resident blocks strides over it.
+// device, so a grid of resident blocks strides over it.  Used for SH degree 0
+// (a 64-byte block per Gaussian; degree 3 has the two kernels below).
 template <int DEG>
 __global__ void __launch_bounds__(128) vjp_kernel(VjpArgs a, CamSet cs)
 {
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kSplitThreads) vjp_split_kernel(VjpArgs a, Cam
 // blocks, 16 bytes a lane, where a thread reading its own block would touch 32
 // blocks per instruction -- the L1 and the load-store queues, not DRAM, held
 // that form back (long-scoreboard and LSU-throttle stalls at 42 % of the HBM
-// peak).  kStream: the 48 colour coefficients are streamed from the staged row
+// peak).  The 48 colour coefficients are streamed from the staged row
 // (vjp_colour3_stream) instead of held in registers, and the view's forward is
 // recomputed only as far as the VJP needs it (a composited Gaussian is visible:
 // no culling tests, radius or tile rectangle).
@@ -243,14 +244,13 @@ __device__ __forceinline__ void stage_rows(float* rows, int g, float* glob, int 
     }
 }
 
-template <bool kStream>
 __global__ void __launch_bounds__(kStageWarps * 32) vjp_staged3_kernel(VjpArgs a, CamSet cs)
 {
     __shared__ __align__(16) float s_rows[kStageWarps][32 * kRowF];
     const gs_camera& cam = cs.cam[0];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* rows = s_rows[warp];
-    float* row = rows + lane * kRowF;
+    float4* r4 = reinterpret_cast<float4*>(rows + lane * kRowF);
     const int64_t count = *a.n_union;
     const int64_t nwarps = (int64_t)gridDim.x * kStageWarps;
     // warp-uniform loop: all lanes take part in every staging step
@@ -264,73 +264,34 @@ __global__ void __launch_bounds__(kStageWarps * 32) vjp_staged3_kernel(VjpArgs a
         stage_rows<true>(rows, g, const_cast<float*>(a.params), lane);
         __syncwarp();
         if (g >= 0) {
-            float4* r4 = reinterpret_cast<float4*>(row);
             float grad[11];
 #pragma unroll
             for (int k = 0; k < 11; ++k) grad[k] = 0.0f;
             float gmu[3] = {0.0f, 0.0f, 0.0f};
             float gcol0 = 0.0f;
-            const bool hit = a.touched[g] != 0;   // the one view's union is its touched set
-            float4* g2s = reinterpret_cast<float4*>(a.grad2d + (size_t)g * GS_GRAD2D_STRIDE);
-            if (kStream) {
-                if (hit) {
-                    const float4 p0 = r4[0], p1 = r4[1], p2 = r4[2];
-                    const GaussGeom gp = {{p0.x, p0.y, p0.z}, {p0.w, p1.x, p1.y}, {p1.z, p1.w, p2.x, p2.y}, p2.z};
-                    const float4 x0 = g2s[0], x1 = g2s[1], x2 = g2s[2];
-                    GaussAct ac;
-                    activate<3>(gp, ac);
-                    ProjInter it;
-                    project_geom(gp, ac, cam, a.lowpass, it);
-                    const float g2[6] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y};
-                    vjp_geom(gp, cam, ac, it, g2, grad);
-                    const float gc[3] = {x1.z, x1.w, x2.x};
-                    gcol0 = vjp_colour3_stream(r4, gp.mu, cam, gc, r4, gmu);
-                } else {
-#pragma unroll
-                    for (int k = 3; k < 15; ++k) r4[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                }
-                r4[0] = make_float4(grad[0] + gmu[0], grad[1] + gmu[1], grad[2] + gmu[2], grad[3]);
-                r4[1] = make_float4(grad[4], grad[5], grad[6], grad[7]);
-                r4[2] = make_float4(grad[8], grad[9], grad[10], gcol0);
-            } else {
-                GaussParams<3> gp;
-                {
-                    float v[60];
-#pragma unroll
-                    for (int k = 0; k < 15; ++k) {
-                        const float4 t = r4[k];
-                        v[4 * k] = t.x; v[4 * k + 1] = t.y; v[4 * k + 2] = t.z; v[4 * k + 3] = t.w;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 3; ++k) { gp.mu[k] = v[k]; gp.ls[k] = v[3 + k]; }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) gp.q[k] = v[6 + k];
-                    gp.logit = v[10];
-#pragma unroll
-                    for (int k = 0; k < 48; ++k) gp.col[k] = v[11 + k];
-                }
-                float gall[60];
-#pragma unroll
-                for (int k = 0; k < 60; ++k) gall[k] = 0.0f;
-                if (hit) {
-                    GaussAct ac;
-                    activate<3>(gp, ac);
-                    ProjOut po;
-                    ProjInter it;
-                    if (project_view<3>(gp, ac, cam, a.near_z, a.lowpass, a.tiles_x, a.tiles_y, po, &it)) {
-                        const float4 x0 = g2s[0], x1 = g2s[1], x2 = g2s[2];
-                        const float g2[9] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x};
-                        vjp_one<3>(gp, cam, ac, it, po.clamp, g2, gall, gall + 11);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 15; ++k) r4[k] = make_float4(gall[4 * k], gall[4 * k + 1], gall[4 * k + 2], gall[4 * k + 3]);
-            }
-            if (hit) {
+            if (a.touched[g]) {   // the one view's union is its touched set
+                const float4 p0 = r4[0], p1 = r4[1], p2 = r4[2];
+                const GaussGeom gp = {{p0.x, p0.y, p0.z}, {p0.w, p1.x, p1.y}, {p1.z, p1.w, p2.x, p2.y}, p2.z};
+                float4* g2s = reinterpret_cast<float4*>(a.grad2d + (size_t)g * GS_GRAD2D_STRIDE);
+                const float4 x0 = g2s[0], x1 = g2s[1], x2 = g2s[2];
+                GaussAct ac;
+                activate<3>(gp, ac);
+                ProjInter it;
+                project_geom(gp, ac, cam, a.lowpass, it);
+                const float g2[6] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y};
+                vjp_geom(gp, cam, ac, it, g2, grad);
+                const float gc[3] = {x1.z, x1.w, x2.x};
+                gcol0 = vjp_colour3_stream(r4, gp.mu, cam, gc, r4, gmu);
                 const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 g2s[0] = z; g2s[1] = z; g2s[2] = z;
                 a.touched[g] = 0;
+            } else {
+#pragma unroll
+                for (int k = 3; k < 15; ++k) r4[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
+            r4[0] = make_float4(grad[0] + gmu[0], grad[1] + gmu[1], grad[2] + gmu[2], grad[3]);
+            r4[1] = make_float4(grad[4], grad[5], grad[6], grad[7]);
+            r4[2] = make_float4(grad[8], grad[9], grad[10], gcol0);
         }
         __syncwarp();
         stage_rows<false>(rows, g, a.grads, lane);
@@ -413,7 +374,7 @@ extern "C" gs_status gs_grad_compact(float* grad2d, uint8_t* touched, const floa
     GS_CUDA_TRY(cudaGetDevice(&dev));
     GS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (sh_degree == 0 || n_views == 1) {
-        auto kernel = sh_degree == 0 ? vjp_kernel<0> : vjp_staged3_kernel<true>;
+        auto kernel = sh_degree == 0 ? vjp_kernel<0> : vjp_staged3_kernel;
         GS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0));
         int64_t blocks = (n + threads - 1) / threads;
         const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
