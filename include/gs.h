@@ -345,6 +345,12 @@ GS_API gs_status gs_compose(const float* c_parts, const float* t_parts, int32_t 
  * and written as its gradient block (write only; the blocks of Gaussians
  * outside the union are not touched, so they keep whatever an earlier step
  * left there).  grad2d and touched are cleared for the entries consumed.
+ * touched and grad2d are those a gs_raster_* call left for the same params,
+ * cams and opts: a touched (Gaussian, view) was composited, hence visible, and
+ * for SH degree 3 the VJP recomputes the projection without repeating the
+ * culling tests (it differentiates the projection a composited record came
+ * from).  With SH degree 3 and several views the geometry and colour terms are
+ * each summed in view order and then added.
  * idx: [(n_views + 1) * n] u32 out; n_idx: [n_views + 1] int64 DEVICE out.
  * grads: [n][stride] fp32 out (union blocks only).  cams/opts: HOST, as given to gs_project.
  * Errors: INVALID_ARG for bad pointers, sizes or a too small workspace. */
