@@ -2,7 +2,7 @@
 lists, then the whole step on those lists: dense lists with distinct and with
 quantised (tied) opacities, a single tile list long enough for the re-gathering
 path, several views, and a budget that covers every list (nothing changes).
-Rendering quality is judged against the unpruned oracle render."""
+Rendering quality is measured against the unpruned oracle render."""
 import math
 
 import numpy as np
